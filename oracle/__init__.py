@@ -1,0 +1,207 @@
+"""CPU oracle for the W4A16 GEMV: ctypes binding to the plain C implementation.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's
+cpu_baseline / reference leg may import this package.  The GPU library in
+int4_weight_only_gemv_gb300/ never imports it and shares no code with it.
+
+Every function takes and returns numpy arrays.  fp16 data travels as uint16 bit
+patterns so that no conversion happens outside the C code.  The semantics of
+each function are documented in w4a16_oracle.c; the tolerance check follows the
+bound stated for the GEMV (maximum error and relative L2 error, below).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+ORC_OK = 0
+ORC_ERR_SHAPE = 1
+ORC_ERR_NONFINITE = 2
+ORC_ERR_SCALE_OVERFLOW = 3
+
+# Tolerances of the GEMV check: per activation row m,
+#   max_n |y - y_ref| <= ABS_SLOPE * ||x_m||_2 * max_n ||w_hat_n||_2 + ABS_FLOOR
+# and over the whole output ||y - y_ref||_2 / ||y_ref||_2 <= REL_L2.
+ABS_SLOPE = 2e-3
+ABS_FLOOR = 1e-3
+REL_L2 = 1e-3
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) the oracle library."""
+    global _LIB
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _LIB is None:
+        _LIB = _bind(ctypes.CDLL(_build.build()))
+    return _LIB
+
+
+def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
+    p, i64, u16 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint16
+    L.orc_half_to_double.argtypes = [u16]
+    L.orc_half_to_double.restype = ctypes.c_double
+    L.orc_double_to_half.argtypes = [ctypes.c_double]
+    L.orc_double_to_half.restype = u16
+    L.orc_float_to_half.argtypes = [ctypes.c_float]
+    L.orc_float_to_half.restype = u16
+    L.orc_double_to_half_array.argtypes = [p, i64, p]
+    L.orc_double_to_half_array.restype = None
+    L.orc_half_to_double_array.argtypes = [p, i64, p]
+    L.orc_half_to_double_array.restype = None
+    L.orc_quantize.argtypes = [p, i64, i64, i64, p, p]
+    L.orc_unpack.argtypes = [p, i64, i64, p]
+    L.orc_dequant.argtypes = [p, p, i64, i64, i64, p]
+    L.orc_dequant_f64.argtypes = [p, p, i64, i64, i64, p]
+    L.orc_gemv.argtypes = [p, p, p, i64, i64, i64, i64, p]
+    L.orc_gemv_rows.argtypes = [p, p, p, i64, i64, i64, i64, p, i64, p]
+    for f in ("orc_quantize", "orc_unpack", "orc_dequant", "orc_dequant_f64", "orc_gemv",
+              "orc_gemv_rows"):
+        getattr(L, f).restype = ctypes.c_int
+    return L
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != ORC_OK:
+        raise OracleError(f"{what} failed with oracle status {rc}")
+
+
+def half_to_double(h: np.ndarray, L=None) -> np.ndarray:
+    L = L or lib()
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, np.float64)
+    L.orc_half_to_double_array(_ptr(h), h.size, _ptr(out))
+    return out
+
+
+def double_to_half(v: np.ndarray, L=None) -> np.ndarray:
+    L = L or lib()
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, np.uint16)
+    L.orc_double_to_half_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def quantize(w: np.ndarray, group: int = 128, L=None) -> tuple[np.ndarray, np.ndarray]:
+    """fp32 W[N][K] -> (qweight uint32[N][K/8], scales uint16(fp16 bits)[N][K/G])."""
+    L = L or lib()
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    qw = np.zeros((N, K // 8), np.uint32)
+    sc = np.zeros((N, K // group), np.uint16)
+    _check(L.orc_quantize(_ptr(w), N, K, group, _ptr(qw), _ptr(sc)), "quantize")
+    return qw, sc
+
+
+def unpack(qweight: np.ndarray, L=None) -> np.ndarray:
+    L = L or lib()
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint32)
+    N, K8 = qweight.shape
+    q = np.empty((N, K8 * 8), np.int8)
+    _check(L.orc_unpack(_ptr(qweight), N, K8 * 8, _ptr(q)), "unpack")
+    return q
+
+
+def dequant(qweight: np.ndarray, scales: np.ndarray, group: int = 128, L=None) -> np.ndarray:
+    """fp16 bits [N][K] = fp16_RN(q * s)."""
+    L = L or lib()
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    N, K8 = qweight.shape
+    out = np.empty((N, K8 * 8), np.uint16)
+    _check(L.orc_dequant(_ptr(qweight), _ptr(scales), N, K8 * 8, group, _ptr(out)), "dequant")
+    return out
+
+
+def dequant_f64(qweight: np.ndarray, scales: np.ndarray, group: int = 128, L=None) -> np.ndarray:
+    """Exact q * s as float64 [N][K]."""
+    L = L or lib()
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    N, K8 = qweight.shape
+    out = np.empty((N, K8 * 8), np.float64)
+    _check(L.orc_dequant_f64(_ptr(qweight), _ptr(scales), N, K8 * 8, group, _ptr(out)),
+           "dequant_f64")
+    return out
+
+
+def gemv(qweight: np.ndarray, scales: np.ndarray, x: np.ndarray, group: int = 128,
+         L=None) -> np.ndarray:
+    """FP64 y[M][N] = x[M][K] . w_hat[N][K]^T; x given as fp16 bit patterns (uint16)."""
+    L = L or lib()
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    N, K8 = qweight.shape
+    M = x.shape[0]
+    assert x.shape[1] == K8 * 8
+    y = np.empty((M, N), np.float64)
+    _check(L.orc_gemv(_ptr(qweight), _ptr(scales), _ptr(x), M, N, K8 * 8, group, _ptr(y)), "gemv")
+    return y
+
+
+def gemv_rows(qweight: np.ndarray, scales: np.ndarray, x: np.ndarray, rows: np.ndarray,
+              group: int = 128, L=None) -> np.ndarray:
+    """FP64 y[M][len(rows)] for the selected output rows only."""
+    L = L or lib()
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    N, K8 = qweight.shape
+    M = x.shape[0]
+    y = np.empty((M, rows.size), np.float64)
+    _check(L.orc_gemv_rows(_ptr(qweight), _ptr(scales), _ptr(x), M, N, K8 * 8, group,
+                           _ptr(rows), rows.size, _ptr(y)), "gemv_rows")
+    return y
+
+
+def row_norms(qweight: np.ndarray, scales: np.ndarray, group: int = 128, L=None) -> np.ndarray:
+    """||w_hat_n||_2 for every output row n (exact dequantised weights)."""
+    w = dequant_f64(qweight, scales, group, L)
+    return np.sqrt(np.sum(w * w, axis=1))
+
+
+def check_gemv(y: np.ndarray, y_ref: np.ndarray, x_f64: np.ndarray, max_row_norm: float,
+               rel_l2: float = REL_L2, abs_slope: float = ABS_SLOPE,
+               abs_floor: float = ABS_FLOOR) -> dict:
+    """The GEMV tolerance.
+
+    y      -- the result under test, float64 [M][n] (fp16 values widened)
+    y_ref  -- the oracle's FP64 result, same shape
+    x_f64  -- the activations as float64 [M][K]
+    max_row_norm -- max_n ||w_hat_n||_2 over the rows of the weight matrix
+    Returns a report dict with 'ok' and the measured figures.
+    """
+    y = np.atleast_2d(np.asarray(y, np.float64))
+    y_ref = np.atleast_2d(np.asarray(y_ref, np.float64))
+    x_f64 = np.atleast_2d(np.asarray(x_f64, np.float64))
+    assert y.shape == y_ref.shape and x_f64.shape[0] == y.shape[0]
+    err = np.abs(y - y_ref)
+    bound = abs_slope * np.sqrt(np.sum(x_f64 * x_f64, axis=1)) * max_row_norm + abs_floor
+    max_err = err.max(axis=1) if err.size else np.zeros(y.shape[0])
+    denom = np.sqrt(np.sum(y_ref * y_ref))
+    rel = float(np.sqrt(np.sum(err * err)) / denom) if denom > 0 else float(np.sqrt(np.sum(err * err)))
+    finite = bool(np.all(np.isfinite(y)))
+    ok = finite and bool(np.all(max_err <= bound)) and rel <= rel_l2
+    return {"ok": ok, "finite": finite, "rel_l2": rel, "max_err": max_err.tolist(),
+            "bound": bound.tolist()}

@@ -1,0 +1,252 @@
+/*
+ * w4a16_oracle.c -- the CPU oracle for the INT4 weight-only (W4A16) GEMV.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain, single-threaded
+ * statement of what the GPU library computes.  Only the test suite, the smoke
+ * check in __graft_entry__ and the cpu_baseline / reference leg of bench.py may
+ * load it.  It shares no code, header, table or helper with the CUDA library in
+ * int4_weight_only_gemv_gb300/, and the CUDA library never calls it.
+ *
+ * What it follows.  The format is the one of the page "Costruire un runtime di
+ * inference LLM da zero" (datastack.it, summary of "How To Build Your Own LLM
+ * Runtime From Scratch"), section "Tre bug che insegnano":
+ *   - last paragraph: INT4 weights, symmetric, group-wise with group 128, on
+ *     the seven per-layer projections (embedding, rms_norm, lm_head stay FP16);
+ *   - third bug: the gate/up/down GEMVs unpack the INT4 nibbles inside the
+ *     kernel and multiply FP16 activations.
+ * The pages print no packing layout, no scale formula and no rounding rule.
+ * The numeric details used here are the workload definition's: per-group
+ * scale = max|w| / 7 stored as fp16, q = clamp(round(w / s), -8, 7), and eight
+ * nibbles per uint32, little-endian.  Where that is silent too, the readings
+ * are: nibble i (bits 4i..4i+3) of word j of row n holds k = 8j + i; scales
+ * are fp16[N][K/G] row-major; max|w| / 7 is divided in fp32 and rounded to
+ * fp16 to nearest-even; round() is half away from zero on the exact quotient
+ * w / s (computed in double, which decides every case exactly, see
+ * orc_quantize); a group whose max|w| is 0 gets s = 0 and q = 0.
+ *
+ * Every floating-point result that has a plain definition is that definition:
+ * the GEMV is y[m][n] = sum_k x[m][k] * (q[n][k] * s[n][k/G]) accumulated in
+ * FP64 in ascending k (each product is exact in FP64: 11 + 4 + 11 significand
+ * bits), and the dequant is fp16_RN(q * s) (q * s is exact, so this is one
+ * rounding).
+ *
+ * binary16 conversions are written from the IEEE 754 definition of the format
+ * (1 sign bit, 5 exponent bits with bias 15, 10 fraction bits, subnormals with
+ * exponent 2^-14, round to nearest with ties to even); they do not use any
+ * compiler or library half-precision type.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -shared -fPIC (see build.py).
+ * -ffp-contract=off keeps every a*b+c as two roundings on both x86-64 and
+ * aarch64, so the oracle gives the same bits on both hosts.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_SHAPE 1
+#define ORC_ERR_NONFINITE 2
+#define ORC_ERR_SCALE_OVERFLOW 3
+
+/* ---------------------------------------------------------------------------
+ * IEEE 754 binary16
+ * ------------------------------------------------------------------------- */
+
+/* Value of a binary16 bit pattern, exactly, as a double. */
+double orc_half_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int f = h & 0x3ff;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -24); /* subnormal: f * 2^-14 * 2^-10 */
+  } else if (e == 31) {
+    v = f ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+  }
+  return sign ? -v : v;
+}
+
+/* Round a non-negative double that is exact (an integer plus a fraction
+ * representable in double) to the nearest integer, ties to even. */
+static double round_half_even(double r) {
+  double fl = floor(r);
+  double d = r - fl; /* exact: r < 2^53 in every caller */
+  if (d > 0.5) return fl + 1.0;
+  if (d < 0.5) return fl;
+  return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/* binary16 nearest to v, ties to even; overflow goes to infinity. */
+uint16_t orc_double_to_half(double v) {
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  if (isnan(v)) return (uint16_t)(sign | 0x7e00);
+  double a = fabs(v);
+  /* Largest finite is 65504 = 2047 * 2^5; the next step would be 65536, so
+   * the midpoint 65520 and everything above rounds to infinity (65520 is a
+   * tie between 65504 (odd fraction 1023) and 65536 (even): goes to 65536). */
+  if (a >= 65520.0) return (uint16_t)(sign | 0x7c00);
+  if (a < ldexp(1.0, -14)) {
+    /* subnormal range: multiples of 2^-24 */
+    double m = round_half_even(ldexp(a, 24));
+    return (uint16_t)(sign | (uint16_t)m); /* m == 1024 is the smallest normal */
+  }
+  int E;
+  frexp(a, &E);      /* a = f * 2^E, f in [0.5, 1) */
+  int e = E - 1;     /* a in [2^e, 2^(e+1)), e in [-14, 15] */
+  double m = round_half_even(ldexp(a, 10 - e)); /* in [1024, 2048] */
+  if (m == 2048.0) {
+    m = 1024.0;
+    e += 1;
+  }
+  if (e > 15) return (uint16_t)(sign | 0x7c00);
+  return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(m - 1024.0));
+}
+
+/* float -> binary16: float -> double is exact, so this is a single rounding. */
+uint16_t orc_float_to_half(float v) { return orc_double_to_half((double)v); }
+
+void orc_double_to_half_array(const double* v, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_double_to_half(v[i]);
+}
+
+void orc_half_to_double_array(const uint16_t* h, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_half_to_double(h[i]);
+}
+
+/* ---------------------------------------------------------------------------
+ * The INT4 group-wise format
+ * ------------------------------------------------------------------------- */
+
+/* Signed value of one 4-bit two's-complement nibble. */
+static int nibble_value(uint32_t nib) {
+  int v = (int)(nib & 0xf);
+  if (v >= 8) v -= 16;
+  return v;
+}
+
+static int shape_ok(int64_t N, int64_t K, int64_t G) {
+  return N >= 0 && K > 0 && G > 0 && G % 8 == 0 && K % G == 0;
+}
+
+/*
+ * Quantise fp32 W[N][K] into qweight uint32[N][K/8] and scales fp16[N][K/G].
+ * Per (row n, group g):
+ *   s = fp16_RN( float( max_{k in g} |w[n][k]| / 7 ) )   -- fp32 division
+ *   q = clamp( round_half_away( w / s ), -8, 7 )          -- s == 0 -> q = 0
+ * The quotient is taken in double.  w has 24 significand bits and s 11, so a
+ * non-tie quotient w / s differs from every half-integer by far more than
+ * double's 2^-53 relative spacing: the double division therefore makes the
+ * same rounding decision as the exact real quotient.
+ * Nibble i of word j of row n holds k = 8j + i, as q & 0xF.
+ * Returns ORC_OK, ORC_ERR_SHAPE, ORC_ERR_NONFINITE or ORC_ERR_SCALE_OVERFLOW.
+ */
+int orc_quantize(const float* w, int64_t N, int64_t K, int64_t G, uint32_t* qweight,
+                 uint16_t* scales) {
+  if (!shape_ok(N, K, G)) return ORC_ERR_SHAPE;
+  for (int64_t i = 0; i < N * K; ++i)
+    if (!isfinite(w[i])) return ORC_ERR_NONFINITE;
+  memset(qweight, 0, (size_t)(N * (K / 8)) * sizeof(uint32_t));
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t g = 0; g < K / G; ++g) {
+      const float* wg = w + n * K + g * G;
+      float amax = 0.0f;
+      for (int64_t k = 0; k < G; ++k) {
+        float a = fabsf(wg[k]);
+        if (a > amax) amax = a;
+      }
+      float d = amax / 7.0f;
+      uint16_t sbits = orc_float_to_half(d);
+      if ((sbits & 0x7c00) == 0x7c00) return ORC_ERR_SCALE_OVERFLOW;
+      scales[n * (K / G) + g] = sbits;
+      double s = orc_half_to_double(sbits);
+      for (int64_t k = 0; k < G; ++k) {
+        int q = 0;
+        if (s != 0.0) {
+          double r = round((double)wg[k] / s); /* C round(): half away from zero */
+          if (r > 7.0) r = 7.0;
+          if (r < -8.0) r = -8.0;
+          q = (int)r;
+        }
+        int64_t kk = g * G + k;
+        qweight[n * (K / 8) + kk / 8] |= ((uint32_t)q & 0xfu) << (4 * (kk % 8));
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+/* q[n][k] in [-8, 7] from the packed words. */
+int orc_unpack(const uint32_t* qweight, int64_t N, int64_t K, int8_t* q) {
+  if (N < 0 || K <= 0 || K % 8 != 0) return ORC_ERR_SHAPE;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k) {
+      uint32_t word = qweight[n * (K / 8) + k / 8];
+      q[n * K + k] = (int8_t)nibble_value(word >> (4 * (k % 8)));
+    }
+  return ORC_OK;
+}
+
+/* w_hat[n][k] = q[n][k] * s[n][k/G], exact, as a double. */
+static double w_hat(const uint32_t* qweight, const uint16_t* scales, int64_t K, int64_t G,
+                    int64_t n, int64_t k) {
+  uint32_t word = qweight[n * (K / 8) + k / 8];
+  int q = nibble_value(word >> (4 * (k % 8)));
+  double s = orc_half_to_double(scales[n * (K / G) + k / G]);
+  return (double)q * s;
+}
+
+/* Debug dequantisation: w_out fp16[N][K] = fp16_RN(q * s). */
+int orc_dequant(const uint32_t* qweight, const uint16_t* scales, int64_t N, int64_t K,
+                int64_t G, uint16_t* w_out) {
+  if (!shape_ok(N, K, G)) return ORC_ERR_SHAPE;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k)
+      w_out[n * K + k] = orc_double_to_half(w_hat(qweight, scales, K, G, n, k));
+  return ORC_OK;
+}
+
+/* Exact dequantised weights as doubles (used for row norms in the tolerance). */
+int orc_dequant_f64(const uint32_t* qweight, const uint16_t* scales, int64_t N, int64_t K,
+                    int64_t G, double* w_out) {
+  if (!shape_ok(N, K, G)) return ORC_ERR_SHAPE;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k) w_out[n * K + k] = w_hat(qweight, scales, K, G, n, k);
+  return ORC_OK;
+}
+
+/* y[m][i] = sum_k x[m][k] * w_hat[rows[i]][k], FP64, ascending k.
+ * x is fp16 [M][K] (bit patterns); y is double [M][nrows]. */
+int orc_gemv_rows(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
+                  int64_t M, int64_t N, int64_t K, int64_t G, const int64_t* rows,
+                  int64_t nrows, double* y) {
+  if (!shape_ok(N, K, G) || M < 0) return ORC_ERR_SHAPE;
+  for (int64_t i = 0; i < nrows; ++i)
+    if (rows[i] < 0 || rows[i] >= N) return ORC_ERR_SHAPE;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t i = 0; i < nrows; ++i) {
+      int64_t n = rows[i];
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += orc_half_to_double(x[m * K + k]) * w_hat(qweight, scales, K, G, n, k);
+      y[m * nrows + i] = acc;
+    }
+  }
+  return ORC_OK;
+}
+
+/* The whole GEMV: y double [M][N]. */
+int orc_gemv(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x, int64_t M,
+             int64_t N, int64_t K, int64_t G, double* y) {
+  if (!shape_ok(N, K, G) || M < 0) return ORC_ERR_SHAPE;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += orc_half_to_double(x[m * K + k]) * w_hat(qweight, scales, K, G, n, k);
+      y[m * N + n] = acc;
+    }
+  }
+  return ORC_OK;
+}

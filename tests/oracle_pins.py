@@ -1,0 +1,331 @@
+"""Pins for the CPU oracle: checks against facts fixed outside the oracle.
+
+Each pin takes an oracle library handle (so the same pins can be run against
+deliberately broken builds of the oracle, see test_oracle_mutants.py) and
+raises AssertionError when the oracle disagrees with:
+  - the IEEE 754 binary16 definition (exhaustive over all 65,536 patterns,
+    every midpoint between neighbours, and numpy's float16 conversion);
+  - the hand-decoded words and hand-computed GEMVs under tests/golden/;
+  - the quantiser's closed-form properties (scale = fp16_RN(max|w| / 7),
+    q in [-8, 7], |w - q s| <= s / 2, exact recovery of w = q s);
+  - numpy's float64 matmul on a dense matrix built directly from chosen (q, s).
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# --------------------------------------------------------------------------- fp16
+
+def pin_half_to_double_exhaustive(L):
+    """All 65,536 binary16 patterns decode to numpy's float16 value."""
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.half_to_double(h, L)
+    want = h.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    # the sign of zero is kept
+    assert np.signbit(got[0x8000]) and not np.signbit(got[0])
+
+
+def pin_half_roundtrip(L):
+    """double(h) -> half gives back h for every non-NaN pattern."""
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    v = h.view(np.float16).astype(np.float64)
+    keep = ~np.isnan(v)
+    back = oracle.double_to_half(v[keep], L)
+    assert np.array_equal(back, h[keep])
+
+
+def pin_half_midpoints_ties_to_even(L):
+    """The exact midpoint between two neighbouring finite halves rounds to the
+    one with the even fraction (IEEE 754 ties-to-even); a hair above/below
+    rounds up/down."""
+    h = np.arange(0, 0x7bff, dtype=np.uint32).astype(np.uint16)  # 0 .. 65504's predecessor
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    mid = (lo + hi) / 2.0  # exact in double
+    got = oracle.double_to_half(mid, L)
+    even = np.where(h % 2 == 0, h, h + 1).astype(np.uint16)
+    assert np.array_equal(got, even)
+    up = oracle.double_to_half(np.nextafter(mid, np.inf), L)
+    down = oracle.double_to_half(np.nextafter(mid, -np.inf), L)
+    assert np.array_equal(up, (h + 1).astype(np.uint16))
+    assert np.array_equal(down, h)
+    # negative side mirrors
+    gotn = oracle.double_to_half(-mid, L)
+    assert np.array_equal(gotn, (even | 0x8000).astype(np.uint16))
+
+
+def pin_half_overflow_and_specials(L):
+    cases = [
+        (65504.0, 0x7BFF), (65519.99, 0x7BFF), (65520.0, 0x7C00), (1e9, 0x7C00),
+        (-65520.0, 0xFC00), (2.0 ** -24, 0x0001), (2.0 ** -25, 0x0000),
+        (1.5 * 2.0 ** -24, 0x0002), (2.0 ** -14, 0x0400), (1.0, 0x3C00), (-2.0, 0xC000),
+        (0.0, 0x0000), (-0.0, 0x8000), (float("inf"), 0x7C00), (float("-inf"), 0xFC00),
+        (1.0 + 2.0 ** -11, 0x3C00), (1.0 + 3 * 2.0 ** -11, 0x3C02),
+    ]
+    v = np.array([c[0] for c in cases], np.float64)
+    got = oracle.double_to_half(v, L)
+    want = [c[1] for c in cases]
+    assert [int(g) for g in got] == want, (got, want)
+    nan = oracle.double_to_half(np.array([np.nan]), L)
+    assert (int(nan[0]) & 0x7C00) == 0x7C00 and (int(nan[0]) & 0x3FF) != 0
+
+
+def pin_half_vs_numpy_random(L):
+    """Random doubles and floats over the whole binary16 range agree with numpy."""
+    rng = np.random.default_rng(12345)
+    mag = np.exp2(rng.uniform(-30, 17, 200000))
+    v = mag * rng.choice([-1.0, 1.0], mag.size)
+    got = oracle.double_to_half(v, L)
+    with np.errstate(over="ignore"):  # values past 65520 become inf, as they should
+        want = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+    f = v.astype(np.float32)
+    got32 = np.array([L.orc_float_to_half(float(t)) for t in f[:5000]], np.uint16)
+    with np.errstate(over="ignore"):
+        want32 = f[:5000].astype(np.float16).view(np.uint16)
+    assert np.array_equal(got32, want32)
+
+
+# --------------------------------------------------------------------------- format
+
+def read_hand_words():
+    rows = []
+    with open(os.path.join(GOLDEN, "hand_words.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            rows.append((int(parts[0], 16), [int(t) for t in parts[1:]]))
+    return rows
+
+
+def pin_hand_words(L):
+    for word, q in read_hand_words():
+        got = oracle.unpack(np.array([[word]], np.uint32), L)
+        assert got.tolist() == [q], (hex(word), got.tolist(), q)
+
+
+def pin_dequant_half_scale(L):
+    """s = 0.5: w_hat = q / 2, exact in fp16."""
+    for word, q in read_hand_words():
+        qw = np.full((1, 16), word, np.uint32)
+        sc = np.array([[0x3800]], np.uint16)  # 0.5
+        got = oracle.dequant(qw, sc, 128, L)
+        want = np.tile(np.array(q, np.float64) * 0.5, 16).astype(np.float16).view(np.uint16)
+        assert np.array_equal(got[0], want)
+
+
+def _parse_scale(tok: str, n: int) -> float:
+    if tok == "2^-n":
+        return 2.0 ** -n
+    if tok.startswith("2^"):
+        return 2.0 ** float(tok[2:])
+    return float(tok)
+
+
+def read_hand_gemvs():
+    cases = []
+    with open(os.path.join(GOLDEN, "hand_gemv_1x8x128.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            p = line.split()
+            name, K = p[0], int(p[1])
+            words = [int(t, 16) for t in p[2:4] if t != "-"]
+            scale_tok, x_tok = p[4], p[5]
+            expected = [float(t) for t in p[6:]]
+            cases.append((name, K, words, scale_tok, x_tok, expected))
+    return cases
+
+
+def build_hand_case(K, words, scale_tok, x_tok):
+    N, G = 8, 128
+    qw = np.zeros((N, K // 8), np.uint32)
+    for g, w in enumerate(words):
+        qw[:, g * 16:(g + 1) * 16] = w
+    sc = np.zeros((N, K // G), np.uint16)
+    for n in range(N):
+        toks = scale_tok.split(",")
+        for g in range(K // G):
+            sc[n, g] = np.float16(_parse_scale(toks[g], n)).view(np.uint16)
+    if x_tok == "ones":
+        x = np.full((1, K), 0x3C00, np.uint16)
+    else:
+        k = int(x_tok.split("_")[1])
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3C00
+    return qw, sc, x
+
+
+def pin_hand_gemvs(L):
+    for name, K, words, scale_tok, x_tok, expected in read_hand_gemvs():
+        qw, sc, x = build_hand_case(K, words, scale_tok, x_tok)
+        y = oracle.gemv(qw, sc, x, 128, L)
+        assert y[0].tolist() == expected, (name, x_tok, y[0].tolist(), expected)
+        # the row-sampled entry point gives the same numbers
+        yr = oracle.gemv_rows(qw, sc, x, np.array([7, 0, 3]), 128, L)
+        assert yr[0].tolist() == [expected[7], expected[0], expected[3]]
+
+
+# --------------------------------------------------------------------------- quantiser
+
+def pin_quantizer_properties(L, N=64, K=1024, seed=0):
+    """On Normal(0, 0.02) weights: s = fp16_RN(fp32(max|w| / 7)) (checked with
+    numpy's fp32 division and float16 rounding), q in [-8, 7], every group has
+    a |q| = 7, and |w - q s| <= s / 2 for every element."""
+    w = synth.weights(N, K, seed).numpy()
+    qw, sc = oracle.quantize(w, 128, L)
+    G = 128
+    wg = w.reshape(N, K // G, G)
+    amax = np.abs(wg).max(axis=2).astype(np.float32)
+    s_want = (amax / np.float32(7.0)).astype(np.float32).astype(np.float16).view(np.uint16)
+    assert np.array_equal(sc, s_want)
+    q = oracle.unpack(qw, L).astype(np.int64).reshape(N, K // G, G)
+    assert q.min() >= -8 and q.max() <= 7
+    assert np.all(np.abs(q).max(axis=2) == 7)
+    s = sc.view(np.float16).astype(np.float64)[:, :, None]
+    err = np.abs(wg.astype(np.float64) - q * s)
+    assert np.all(err <= s / 2.0)
+
+
+def pin_quantizer_exact_recovery(L, seed=3):
+    """W built as q * s (each group holding a +-7) quantises back to exactly
+    (q, s): pins the scale formula, the rounding and the packing round trip."""
+    rng = np.random.default_rng(seed)
+    N, K, G = 16, 512, 128
+    q = rng.integers(-7, 8, (N, K))
+    q = q.reshape(N, K // G, G)
+    q[:, :, 5] = np.where(rng.random((N, K // G)) < 0.5, 7, -7)
+    q = q.reshape(N, K)
+    s = np.exp2(rng.integers(-12, 0, (N, K // G))) * rng.integers(1024, 2048, (N, K // G)) / 1024.0
+    s = s.astype(np.float16).astype(np.float64)
+    w = (q * np.repeat(s, G, axis=1)).astype(np.float32)
+    assert np.array_equal(w.astype(np.float64), q * np.repeat(s, G, axis=1))  # exact in fp32
+    qw, sc = oracle.quantize(w, G, L)
+    assert np.array_equal(sc.view(np.float16).astype(np.float64), s)
+    assert np.array_equal(oracle.unpack(qw, L).astype(np.int64), q)
+
+
+def pin_quantizer_rounding_ties(L):
+    """w / s exactly at a half-integer rounds away from zero."""
+    G = 128
+    w = np.zeros((1, G), np.float32)
+    w[0, 0] = 7.0            # max -> s = 1
+    w[0, 1] = 2.5            # -> 3
+    w[0, 2] = -2.5           # -> -3
+    w[0, 3] = 0.5            # -> 1
+    w[0, 4] = -0.5           # -> -1
+    w[0, 5] = 2.4999998      # -> 2
+    w[0, 6] = -6.5           # -> -7
+    qw, sc = oracle.quantize(w, G, L)
+    assert int(sc[0, 0]) == 0x3C00
+    q = oracle.unpack(qw, L)[0, :7].tolist()
+    assert q == [7, 3, -3, 1, -1, 2, -7], q
+
+
+def pin_quantizer_zero_group(L):
+    w = np.zeros((2, 256), np.float32)
+    w[1, 200] = -0.25
+    qw, sc = oracle.quantize(w, 128, L)
+    assert sc.tolist() == [[0, 0], [0, int(np.float16(0.25 / 7).view(np.uint16))]]
+    q = oracle.unpack(qw, L)
+    assert np.count_nonzero(q) == 1 and q[1, 200] == -7
+
+
+def pin_quantizer_errors(L):
+    w = np.zeros((1, 128), np.float32)
+    w[0, 3] = np.inf
+    try:
+        oracle.quantize(w, 128, L)
+        raise AssertionError("non-finite input accepted")
+    except oracle.OracleError as e:
+        assert "status 2" in str(e)
+    w[0, 3] = 7.0 * 65520.0
+    try:
+        oracle.quantize(w, 128, L)
+        raise AssertionError("scale overflow accepted")
+    except oracle.OracleError as e:
+        assert "status 3" in str(e)
+    w[0, 3] = 7.0 * 65504.0  # largest finite scale
+    qw, sc = oracle.quantize(w, 128, L)
+    assert int(sc[0, 0]) == 0x7BFF
+
+
+# --------------------------------------------------------------------------- GEMV
+
+def pin_gemv_vs_numpy_matmul(L):
+    """Brute force on small shapes: the oracle GEMV equals numpy's float64
+    matmul of x and the dense w_hat built from (q, s), to double rounding."""
+    for seed, (M, N, K) in enumerate([(1, 1, 128), (3, 3, 256), (16, 8, 128), (5, 13, 384),
+                                      (16, 17, 1024)]):
+        rng = np.random.default_rng(100 + seed)
+        G = 128
+        q = np.clip(rng.integers(-8, 8, (N, K)), -7, 7)
+        q.reshape(N, K // G, G)[:, :, 7] = 7
+        s = (rng.integers(1024, 2048, (N, K // G)) / 1024.0) * np.exp2(rng.integers(-10, -3, (N, K // G)))
+        s = s.astype(np.float16).astype(np.float64)
+        w_hat = q * np.repeat(s, G, axis=1)
+        qw, sc = oracle.quantize(w_hat.astype(np.float32), G, L)
+        x = rng.standard_normal((M, K)).astype(np.float16)
+        y = oracle.gemv(qw, sc, x.view(np.uint16), G, L)
+        y_np = x.astype(np.float64) @ w_hat.T
+        scale = np.abs(x.astype(np.float64)) @ np.abs(w_hat).T
+        assert np.all(np.abs(y - y_np) <= 4 * K * 2.0 ** -53 * scale + 1e-300), (M, N, K)
+        # dequant agrees with the dense matrix, rounded to fp16
+        dq = oracle.dequant(qw, sc, G, L)
+        assert np.array_equal(dq, w_hat.astype(np.float16).view(np.uint16))
+
+
+def pin_gemv_m_consistency(L):
+    """A GEMV over M activation rows is M GEMVs over one row each (bitwise)."""
+    w = synth.weights(24, 256, 7).numpy()
+    qw, sc = oracle.quantize(w, 128, L)
+    x = synth.activations(6, 256, 7).numpy().view(np.uint16)
+    y = oracle.gemv(qw, sc, x, 128, L)
+    for m in range(6):
+        assert np.array_equal(y[m], oracle.gemv(qw, sc, x[m], 128, L)[0])
+
+
+def pin_gemv_fused_equals_separate(L):
+    """[gate; up] stacked along N gives [y_gate, y_up] (the fused gate+up GEMV)."""
+    wg = synth.weights(16, 256, 11).numpy()
+    wu = synth.weights(16, 256, 12).numpy()
+    qg, sg = oracle.quantize(wg, 128, L)
+    qu, su = oracle.quantize(wu, 128, L)
+    x = synth.activations(2, 256, 11).numpy().view(np.uint16)
+    y = oracle.gemv(np.vstack([qg, qu]), np.vstack([sg, su]), x, 128, L)
+    assert np.array_equal(y, np.hstack([oracle.gemv(qg, sg, x, 128, L), oracle.gemv(qu, su, x, 128, L)]))
+
+
+ALL_PINS = [
+    pin_half_to_double_exhaustive, pin_half_roundtrip, pin_half_midpoints_ties_to_even,
+    pin_half_overflow_and_specials, pin_half_vs_numpy_random, pin_hand_words,
+    pin_dequant_half_scale, pin_hand_gemvs, pin_quantizer_properties,
+    pin_quantizer_exact_recovery, pin_quantizer_rounding_ties, pin_quantizer_zero_group,
+    pin_quantizer_errors, pin_gemv_vs_numpy_matmul, pin_gemv_m_consistency,
+    pin_gemv_fused_equals_separate,
+]
+
+
+def failing_pins(L) -> list[str]:
+    """Names of the pins that fail (or crash) against oracle library L."""
+    bad = []
+    for pin in ALL_PINS:
+        try:
+            pin(L)
+        except Exception as e:  # noqa: BLE001 -- a crash is a failure too
+            bad.append(f"{pin.__name__}: {type(e).__name__}")
+    return bad
