@@ -1,0 +1,490 @@
+"""Benchmark of the W4A16 decode GEMV library on GB300.
+
+One step = one replay of the CUDA graph that streams a whole Qwen-7B-shaped
+decode step's INT4 projection weights: 28 layers x {q, k, v, o, gate+up,
+down}, M = 1 (168 GEMV launches, 3.37 GB of packed weights and scales).
+The metric is achieved GB/s of algorithmic bytes (packed weights + fp16
+scales + fp16 activations + fp16 outputs); the weights (3.37 GB) are far
+larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  Besides the contract keys it reports
+  roofline      the dominant kernel against the measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+  e2e           the same metric through w4a16_layer_seq_run_host: host x in,
+                every output back, copies inside the timed region
+  configs       per-workload-shape us/GEMV and GB/s (28 rotated instances
+                per CUDA graph, cold L2), including the M = 1..16 down sweep
+  clocks        SM clock and throttle reasons sampled during the timed region
+
+--impl reference times the CPU oracle (the only reference implementation
+there is) on the same config, metric and unit.  --gpus N under torchrun runs
+N independent replicas (the GEMV has no data-path exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT4 GEMV achieved HBM GB/s and % of GB300 roofline (µs/GEMV, M=1..16)"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-shape table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- workload
+
+def workload_gemvs(M=1):
+    """The GEMVs of one decode step: (name, N, K, M) per launch, in order."""
+    import synth
+    H, KV, F = synth.HIDDEN, synth.KV_DIM, synth.FFN
+    one = [("q", H, H), ("k", KV, H), ("v", KV, H), ("o", H, H), ("gate_up", 2 * F, H), ("down", H, F)]
+    return [(n, N, K, M) for _ in range(synth.N_LAYERS) for (n, N, K) in one]
+
+
+def gemv_bytes(N, K, M, group=128):
+    """Algorithmic bytes of one GEMV: packed weights, fp16 scales, x, y."""
+    return N * K // 2 + 2 * N * (K // group) + 2 * M * K + 2 * M * N
+
+
+def config_block():
+    import synth
+    g = workload_gemvs()
+    return {
+        "workload": "Qwen-7B-shaped decode weight stream: 28 layers x {q,k,v,o,gate+up,down} "
+                    "INT4 g128 GEMVs at M=1, one CUDA-graph replay per step",
+        "layers": synth.N_LAYERS, "hidden": synth.HIDDEN, "kv_dim": synth.KV_DIM, "ffn": synth.FFN,
+        "M": 1, "group": 128, "gemvs_per_step": len(g),
+        "bytes_per_step": sum(gemv_bytes(N, K, M) for _, N, K, M in g),
+        "l2_policy": "inputs larger than L2 (3.37 GB of weights vs 129 MB L2); no flush",
+        "inputs": "seeded synthetic: W ~ N(0, 0.02) quantised to INT4 g128, x ~ N(0, 1) fp16",
+    }
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "int4_weight_only_gemv_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per step from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        if d.get("kernel_source_hash") == kernel_source_hash():
+            return d.get("dram_bytes_per_step")
+    except Exception:  # noqa: BLE001
+        pass
+    return None
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of x over all ranks (the slowest replica's time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbps(bytes_per_step: int, ms_per_step: float, world: int) -> float:
+    """Whole-job GB/s: every replica streams bytes_per_step per step."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"w4a16_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [t.strip() for t in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample_plan(budget_s, steps):
+    """Rows of layer 0's projections the oracle computes per step, sized so
+    `steps` steps take about budget_s seconds; returns (plan, bytes)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    rate = _oracle_mac_rate()
+    macs = rate * budget_s / max(steps, 1)
+    shapes = [(name, *synth.proj_shape(name)) for name in synth.PROJ_NAMES]
+    total_macs = sum(N * K for _, N, K in shapes)
+    frac = min(1.0, macs / total_macs)
+    plan, nbytes = [], 0
+    for pj, (name, N, K) in enumerate(shapes):
+        nrows = max(1, int(N * frac))
+        w = synth.weights(N, K, synth.layer_seed(0, pj))
+        qw, sc = oracle.quantize(w.numpy())
+        x = synth.activations(1, K, synth.layer_seed(0, 7)).numpy().view(np.uint16)
+        rows = np.linspace(0, N - 1, nrows).astype(np.int64)
+        plan.append((qw, sc, x, rows))
+        nbytes += nrows * (K // 2 + 2 * (K // 128) + 2) + 2 * K
+    return plan, nbytes, frac
+
+
+def _oracle_mac_rate():
+    import numpy as np
+
+    import oracle
+    import synth
+    w = synth.weights(64, 3584, 1).numpy()
+    qw, sc = oracle.quantize(w)
+    x = synth.activations(1, 3584, 1).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.gemv(qw, sc, x)
+    dt = time.perf_counter() - t0
+    return 64 * 3584 / dt
+
+
+def run_oracle_steps(plan, steps):
+    import oracle
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        for qw, sc, x, rows in plan:
+            oracle.gemv_rows(qw, sc, x, rows)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_baseline(budget_s=15.0):
+    plan, nbytes, frac = oracle_sample_plan(budget_s, 1)
+    t = run_oracle_steps(plan, 1)[0]
+    return {"value": nbytes / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"single-threaded C oracle (FP64) on {frac:.4f} of the rows of each of "
+                      f"layer 0's 7 projections ({nbytes} algorithmic bytes), {t:.1f} s"}
+
+
+def bench_reference(args, rank, world):
+    """The reference arm: the CPU oracle, timed on the host, rank 0 only."""
+    if rank != 0:
+        return None
+    budget = 100.0
+    plan, nbytes, frac = oracle_sample_plan(budget, args.steps + args.warmup)
+    run_oracle_steps(plan, args.warmup)
+    times = run_oracle_steps(plan, args.steps)
+    total = sum(times)
+    value = nbytes * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: {frac:.5f} of the rows of each of layer 0's "
+                                   f"7 projections ({nbytes} algorithmic bytes)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def build_weights(dev):
+    """28 layers of packed weights, drawn on the GPU and quantised there."""
+    import torch
+
+    import int4_weight_only_gemv_gb300 as w4
+    import synth
+    H, F = synth.HIDDEN, synth.FFN
+    layers = []
+    for l in range(synth.N_LAYERS):
+        lw = {}
+        for pj, name in enumerate(synth.PROJ_NAMES):
+            if name == "up":
+                continue
+            if name == "gate":
+                wg = synth.weights(F, H, synth.layer_seed(l, 4), dev)
+                wu = synth.weights(F, H, synth.layer_seed(l, 5), dev)
+                qw, sc = w4.w4a16_quantize(torch.cat([wg, wu]))
+                del wg, wu
+                lw["gate"], lw["up"] = (qw[:F], sc[:F]), (qw[F:], sc[F:])
+                lw["gate_up"] = (qw, sc)
+                continue
+            N, K = synth.proj_shape(name)
+            lw[name] = w4.w4a16_quantize(synth.weights(N, K, synth.layer_seed(l, pj), dev))
+        layers.append(lw)
+    torch.cuda.synchronize()
+    if w4.w4a16_device_status(clear=True):
+        raise RuntimeError("quantisation flagged bad input")
+    return layers
+
+
+def make_io(dev, M=1):
+    import torch
+
+    import synth
+    L, H, KV, F = synth.N_LAYERS, synth.HIDDEN, synth.KV_DIM, synth.FFN
+    x = torch.cat([synth.activations(M, H, synth.layer_seed(l, 7), dev) for l in range(L)])
+    io = {"x": x.view(L, M, H)}
+    for name, width in (("y_q", H), ("y_k", KV), ("y_v", KV), ("y_o", H), ("y_gu", 2 * F),
+                        ("y_down", H)):
+        io[name] = torch.empty((L, M, width), dtype=torch.float16, device=dev)
+    return io
+
+
+def time_graph_replays(seq, stream, steps, dist_barrier):
+    import torch
+    torch.cuda.synchronize()
+    dist_barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        seq.run(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier()
+    return start.elapsed_time(end)
+
+
+def per_config_table(layers, dev, reps=20):
+    """us/GEMV and GB/s per workload shape: a CUDA graph of 28 GEMVs over the
+    28 layers' distinct weights (cold L2), replayed `reps` times."""
+    import torch
+
+    import int4_weight_only_gemv_gb300 as w4
+    import synth
+    H, F = synth.HIDDEN, synth.FFN
+    out = {}
+    shapes = [("q_proj", "q", H, 1), ("kv_proj", "k", H, 1), ("gate_up", "gate_up", H, 1)]
+    shapes += [(f"down_m{m}", "down", F, m) for m in (1, 2, 4, 8, 16)]
+    stream = torch.cuda.Stream()
+    for label, key, K, M in shapes:
+        xs = [synth.activations(M, K, 77 + l, dev) for l in range(len(layers))]
+        N = layers[0][key][0].shape[0]
+        ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in layers]
+        with torch.cuda.stream(stream):
+            for l, lw in enumerate(layers):  # warm-up, also outside capture
+                w4.w4a16_gemv(*lw[key], xs[l], ys[l])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l, lw in enumerate(layers):
+                w4.w4a16_gemv(*lw[key], xs[l], ys[l])
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream()
+        s.record(cur)
+        for _ in range(reps):
+            g.replay()
+        e.record(cur)
+        torch.cuda.synchronize()
+        us = 1e3 * s.elapsed_time(e) / (reps * len(layers))
+        b = gemv_bytes(N, K, M)
+        out[label] = {"M": M, "N": N, "K": K, "us_per_gemv": round(us, 3),
+                      "GBps": round(b / us / 1e3, 1), "bytes": b}
+    # the tiny workload fits in L2: latency-bound, measured warm
+    cfg = synth.TINY
+    wq, sc = w4.w4a16_quantize(synth.weights(cfg.N, cfg.K, cfg.seed, dev))
+    x = synth.activations(1, cfg.K, cfg.seed, dev)
+    y = torch.empty((1, cfg.N), dtype=torch.float16, device=dev)
+    w4.w4a16_gemv(wq, sc, x, y)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(28):
+            w4.w4a16_gemv(wq, sc, x, y)
+    g.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    us = 1e3 * s.elapsed_time(e) / (reps * 28)
+    b = gemv_bytes(cfg.N, cfg.K, 1)
+    out["tiny"] = {"M": 1, "N": cfg.N, "K": cfg.K, "us_per_gemv": round(us, 3),
+                   "GBps": round(b / us / 1e3, 1), "bytes": b, "note": "L2-resident, latency-bound"}
+    return out
+
+
+def bench_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    import int4_weight_only_gemv_gb300 as w4
+    import synth
+    from int4_weight_only_gemv_gb300 import build as wbuild
+
+    wbuild.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    layers = build_weights(dev)
+    io = make_io(dev)
+    seq = w4.LayerSeq([{k: v for k, v in lw.items() if k != "gate_up"} for lw in layers], io, 1,
+                      synth.HIDDEN, synth.KV_DIM, synth.FFN)
+    stream = torch.cuda.current_stream()
+    cfg = config_block()
+    bytes_step = cfg["bytes_per_step"]
+
+    for _ in range(args.warmup):
+        seq.run(stream)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = time_graph_replays(seq, stream, args.steps, barrier)
+    clocks = clk.summary()
+    ms = max_over_ranks(ms, world, dev)
+    ms_step = ms / args.steps
+    value = aggregate_gbps(bytes_step, ms_step, world)
+
+    # end to end: host x in, every output back, through the C ABI
+    host = {"x": io["x"].cpu().pin_memory()}
+    for k in ("y_q", "y_k", "y_v", "y_o", "y_gu", "y_down"):
+        host[k] = torch.empty(io[k].shape, dtype=torch.float16).pin_memory()
+    h2d = host["x"].numel() * 2
+    d2h = sum(host[k].numel() * 2 for k in host if k != "x")
+    for _ in range(min(args.warmup, 5)):
+        seq.run_host(host, stream)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        seq.run_host(host, stream)
+    seq.sync()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world, dev)
+    barrier()
+    e2e_value = aggregate_gbps(bytes_step, 1e3 * e2e_s, world)
+    if w4.w4a16_device_status(clear=True):
+        raise RuntimeError("a kernel flagged a failure during the bench")
+
+    configs = None if args.no_configs or rank != 0 else per_config_table(layers, dev)
+    peak, peak_kind = measured_peak()
+    achieved = bytes_step / (ms_step * 1e-3) / 1e9
+    traffic = recorded_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "w4a16", "data": "synthetic",
+        "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "kernel": "gemv_m1_kernel (all 168 launches of the step)"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * seq.num_launches,
+        "clocks": clocks,
+        "configs": configs,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline()
+    seq.close()
+    return line if rank == 0 else None
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        line = bench_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            dist.init_process_group("nccl")
+        line = bench_ours(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

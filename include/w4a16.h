@@ -1,0 +1,211 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) INT4 weight-only GEMV library.
+ *
+ * The operation.  y[m][n] = sum_k x[m][k] * w_hat[n][k] with
+ * w_hat[n][k] = q[n][k] * s[n][k / 128]: INT4 weights, symmetric and
+ * group-wise with group 128 along K and one FP16 scale per group, times FP16
+ * activations, unpacked inside the kernel and accumulated in FP32.  This is
+ * the weight format of the page "Costruire un runtime di inference LLM da
+ * zero" (datastack.it), section "Tre bug che insegnano": last paragraph (INT4
+ * symmetric group-wise, group 128, on the seven per-layer projections) and
+ * third bug (the gate/up/down GEMVs unpack INT4 in-kernel and multiply FP16
+ * activations).  The page gives no layout; this library's layout is:
+ *
+ *   qweight  uint32[N][K/8]   nibble i (bits 4i..4i+3) of word j of row n is
+ *                             q[n][8j + i], 4-bit two's complement in [-8, 7]
+ *   scales   fp16[N][K/128]   row-major, s[n][g] for k in [128g, 128g + 128)
+ *   x        fp16[M][K]       row-major activations
+ *   y        fp16[M][N]       row-major output, fp16 round-to-nearest of the
+ *                             FP32 accumulator
+ *
+ * fp16 values travel as uint16_t bit patterns.  W is stored like an
+ * nn.Linear weight (out x in).
+ *
+ * Conventions for every entry point
+ *   - All data pointers are DEVICE pointers unless the name says host.  The
+ *     caller owns every buffer; no entry point frees or keeps a caller buffer
+ *     beyond the call, except layer_seq (which records the pointers it is
+ *     given in a CUDA graph: they must stay valid until it is destroyed).
+ *   - Every data pointer must be 16-byte aligned (W4A16_ERR_ALIGN otherwise).
+ *   - group must be 128 (W4A16_ERR_GROUP); K must be a positive multiple of
+ *     128 and at most W4A16_MAX_K (W4A16_ERR_SHAPE); 0 <= N <= W4A16_MAX_N.
+ *   - Arguments are checked on the host before anything is enqueued; a bad
+ *     argument returns its status and enqueues nothing.
+ *   - Work is enqueued on `stream` (a cudaStream_t; 0 = legacy default
+ *     stream) and the call returns without waiting.  W4A16_ERR_CUDA means a
+ *     launch or runtime call failed (cudaGetLastError is cleared).
+ *   - No entry point traps or asserts on the device.  Kernels whose internal
+ *     waits are bounded record a run-time failure in a per-device status word
+ *     instead; read it with w4a16_device_status.
+ *   - The current CUDA device is the one the pointers belong to.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4A16_ABI_VERSION 1
+#define W4A16_GROUP 128
+#define W4A16_MAX_M 16
+#define W4A16_MAX_K 32768
+#define W4A16_MAX_N (1 << 24)
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_NULL = 1,       /* a required pointer is NULL */
+  W4A16_ERR_SHAPE = 2,      /* N, K out of range, or K not a multiple of 128 */
+  W4A16_ERR_ALIGN = 3,      /* a data pointer is not 16-byte aligned */
+  W4A16_ERR_GROUP = 4,      /* group != 128 */
+  W4A16_ERR_M_RANGE = 5,    /* M outside 0..16 */
+  W4A16_ERR_ALIAS = 6,      /* an output buffer overlaps an input buffer */
+  W4A16_ERR_CUDA = 7,       /* a CUDA runtime call or kernel launch failed */
+  W4A16_ERR_TIMEOUT = 8,    /* a bounded host wait ran out */
+  W4A16_ERR_STATE = 9,      /* NULL or unusable object handle */
+  W4A16_ERR_DEVICE = 10     /* a kernel recorded a failure (see w4a16_device_status) */
+} w4a16_status;
+
+/* Bits of the per-device status word written by kernels. */
+#define W4A16_DEV_NONFINITE 0x1u     /* w4a16_quantize met a non-finite weight   */
+#define W4A16_DEV_SCALE_OVERFLOW 0x2u /* w4a16_quantize: max|w|/7 overflows fp16 */
+#define W4A16_DEV_PIPE_TIMEOUT 0x4u  /* a GEMV pipeline wait ran past its bound  */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* w4a16_status_str(w4a16_status s);
+
+/* Returns W4A16_ABI_VERSION of the loaded library. */
+int w4a16_abi_version(void);
+
+/*
+ * w4a16_gemv -- y = x . w_hat^T for 1 <= M <= 16 activation rows (the decode
+ * GEMV of the third bug of "Tre bug che insegnano"; M > 1 is small-batch
+ * decode).  M == 0 or N == 0 is an empty product: OK, nothing is launched.
+ *   qweight, scales  the packed weight of N output rows and K inputs
+ *   x                fp16 [M][K]
+ *   y                fp16 [M][N]; must not overlap x, qweight or scales
+ * Dispatch: M in 1..7 runs the CUDA-core kernel (nibble unpack in registers,
+ * FP32 accumulation), M in 8..16 the tensor-core kernel (mma.sync over each
+ * group of 128, FP32 accumulators).  The result is deterministic: the same
+ * inputs give the same bits on every call.  Never allocates, never
+ * synchronises; safe to call during CUDA stream capture.
+ */
+w4a16_status w4a16_gemv(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
+                        uint16_t* y, int M, int N, int K, int group, void* stream);
+
+/*
+ * w4a16_dequant -- debugging aid: w_out fp16[N][K] = fp16_RN(q * s) (exact
+ * product, one rounding).  w_out must not overlap qweight or scales.
+ */
+w4a16_status w4a16_dequant(const uint32_t* qweight, const uint16_t* scales, uint16_t* w_out,
+                           int N, int K, int group, void* stream);
+
+/*
+ * w4a16_quantize -- the load-time encoder: fp32 W[N][K] -> (qweight, scales).
+ * Per row n and group g:  s = fp16_RN(fp32(max|w| / 7));
+ *                         q = clamp(round_half_away(w / s), -8, 7)  (s = 0: q = 0)
+ * The rounding decision is the one of the exact quotient w / s.  A
+ * non-finite weight sets W4A16_DEV_NONFINITE and a group whose scale would
+ * overflow fp16 sets W4A16_DEV_SCALE_OVERFLOW in the device status word (that
+ * group is written as zeros); call w4a16_device_status after the stream
+ * completes to learn of it.  Outputs must not overlap w.
+ */
+w4a16_status w4a16_quantize(const float* w, uint32_t* qweight, uint16_t* scales, int N, int K,
+                            int group, void* stream);
+
+/*
+ * w4a16_device_status -- read (and if clear != 0, reset) the status word of
+ * the current device.  Synchronises the device first (it is a debugging and
+ * test call, not for the hot path).  *flags gets the W4A16_DEV_* bits seen
+ * since the last reset.  Returns W4A16_ERR_DEVICE if any bit is set, OK
+ * otherwise, W4A16_ERR_CUDA if the device could not be read.
+ */
+w4a16_status w4a16_device_status(uint32_t* flags, int clear);
+
+/* ------------------------------------------------------------------------
+ * layer_seq -- the seven projections of a Qwen-7B-shaped decoder layer,
+ * repeated for n_layers, captured once as one CUDA graph and replayed.  The
+ * second bug of "Tre bug che insegnano" is that eager decode pays a launch
+ * overhead per kernel (about 119 -> 17 ms/token once captured); this is the
+ * GEMV part of such a captured decode step.
+ *
+ * Per layer l (M activation rows):
+ *   y_q    = gemv(W_q,  x_l)        N = hidden, K = hidden
+ *   y_k    = gemv(W_k,  x_l)        N = kv_dim, K = hidden
+ *   y_v    = gemv(W_v,  x_l)        N = kv_dim, K = hidden
+ *   y_o    = gemv(W_o,  y_q)        N = hidden, K = hidden
+ *   y_gu   = gemv([W_gate; W_up], x_l)   N = 2 ffn, K = hidden (one launch
+ *            when the up weight directly follows the gate weight in memory,
+ *            two launches otherwise)
+ *   y_down = gemv(W_down, gate half of y_gu)   N = hidden, K = ffn
+ * Layers are independent (each takes its own x_l), so magnitudes stay in the
+ * fp16 range for any depth.
+ * ---------------------------------------------------------------------- */
+typedef struct w4a16_layer_seq w4a16_layer_seq;
+
+enum { W4A16_Q = 0, W4A16_K = 1, W4A16_V = 2, W4A16_O = 3, W4A16_GATE = 4, W4A16_UP = 5,
+       W4A16_DOWN = 6, W4A16_NPROJ = 7 };
+
+typedef struct {
+  const uint32_t* qweight[W4A16_NPROJ]; /* indexed by W4A16_Q .. W4A16_DOWN */
+  const uint16_t* scales[W4A16_NPROJ];
+} w4a16_layer_weights;
+
+/* Activation / output buffers of all layers, each [n_layers][M][width]. */
+typedef struct {
+  const uint16_t* x; /* width hidden */
+  uint16_t* y_q;     /* width hidden */
+  uint16_t* y_k;     /* width kv_dim */
+  uint16_t* y_v;     /* width kv_dim */
+  uint16_t* y_o;     /* width hidden */
+  uint16_t* y_gu;    /* width 2 * ffn: gate then up */
+  uint16_t* y_down;  /* width hidden */
+} w4a16_seq_io;
+
+/*
+ * Validate every weight and io pointer (as w4a16_gemv would), capture the
+ * n_layers x 6-or-7 GEMV launches into a CUDA graph on a private stream and
+ * instantiate it.  layers[l] holds the weights of layer l.  The library
+ * allocates the graph and an event; nothing else.  The pointers are recorded
+ * in the graph and must outlive the object.  Blocks until instantiation is
+ * done (a set-up call, not a hot-path call).  *out is NULL on failure.
+ */
+w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_layers, int M,
+                                    int hidden, int kv_dim, int ffn, int group,
+                                    const w4a16_seq_io* io, w4a16_layer_seq** out);
+
+/* Number of kernel launches one replay performs. */
+int w4a16_layer_seq_num_launches(const w4a16_layer_seq* seq);
+
+/* Enqueue one replay of the graph on `stream`; returns after enqueue. */
+w4a16_status w4a16_layer_seq_run(w4a16_layer_seq* seq, void* stream);
+
+/*
+ * End-to-end replay with HOST buffers: on `stream`, copy host->x (if
+ * host->x is not NULL) into the device x buffer, replay the graph, copy each
+ * non-NULL host output pointer of `host` back from the matching device output.
+ * Each host buffer has the size of its device counterpart.  Host buffers
+ * should be page-locked for the copies to be asynchronous.  Returns after
+ * enqueue; wait with w4a16_layer_seq_sync before reading the host outputs.
+ */
+w4a16_status w4a16_layer_seq_run_host(w4a16_layer_seq* seq, const w4a16_seq_io* host,
+                                      void* stream);
+
+/*
+ * Wait for the most recent run / run_host of `seq`: timeout_ms < 0 waits
+ * without bound, timeout_ms >= 0 polls and returns W4A16_ERR_TIMEOUT if the
+ * replay has not finished in that time (the replay keeps running; call again
+ * to keep waiting).
+ */
+w4a16_status w4a16_layer_seq_sync(w4a16_layer_seq* seq, int timeout_ms);
+
+/* Free the graph and the event.  NULL is a no-op.  Waits for pending replays. */
+void w4a16_layer_seq_destroy(w4a16_layer_seq* seq);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4A16_H */

@@ -1,0 +1,225 @@
+"""Python binding of the W4A16 GEMV library (include/w4a16.h).
+
+Argument marshalling only: every function passes device pointers, sizes and
+the current CUDA stream of torch to the C ABI of libw4a16.so, and raises
+W4A16Error on a non-OK status.  No step of the computation runs in Python or
+in torch; if the compiled library is missing, importing the functions raises
+instead of falling back to anything.
+
+Tensors: qweight int32 [N][K/8] (the uint32 bit patterns), scales float16
+[N][K/128], x float16 [M][K], y float16 [M][N], all CUDA, contiguous and
+16-byte aligned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "W4A16Error", "lib", "w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
+    "LayerSeq", "GROUP", "MAX_M", "MAX_K", "DEV_NONFINITE", "DEV_SCALE_OVERFLOW",
+    "DEV_PIPE_TIMEOUT", "STATUS", "EXPORTED_SYMBOLS",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libw4a16.so")
+
+GROUP = 128
+MAX_M = 16
+MAX_K = 32768
+DEV_NONFINITE = 0x1
+DEV_SCALE_OVERFLOW = 0x2
+DEV_PIPE_TIMEOUT = 0x4
+NPROJ = 7
+
+STATUS = {
+    0: "W4A16_OK", 1: "W4A16_ERR_NULL", 2: "W4A16_ERR_SHAPE", 3: "W4A16_ERR_ALIGN",
+    4: "W4A16_ERR_GROUP", 5: "W4A16_ERR_M_RANGE", 6: "W4A16_ERR_ALIAS", 7: "W4A16_ERR_CUDA",
+    8: "W4A16_ERR_TIMEOUT", 9: "W4A16_ERR_STATE", 10: "W4A16_ERR_DEVICE",
+}
+
+# Every function include/w4a16.h declares.
+EXPORTED_SYMBOLS = (
+    "w4a16_status_str", "w4a16_abi_version", "w4a16_gemv", "w4a16_dequant", "w4a16_quantize",
+    "w4a16_device_status", "w4a16_layer_seq_create", "w4a16_layer_seq_num_launches",
+    "w4a16_layer_seq_run", "w4a16_layer_seq_run_host", "w4a16_layer_seq_sync",
+    "w4a16_layer_seq_destroy",
+)
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__(f"{what}: {self.name}")
+
+
+class _LayerWeights(ctypes.Structure):
+    _fields_ = [("qweight", ctypes.c_void_p * NPROJ), ("scales", ctypes.c_void_p * NPROJ)]
+
+
+class _SeqIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("x", "y_q", "y_k", "y_v", "y_o", "y_gu", "y_down")]
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libw4a16.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m int4_weight_only_gemv_gb300.build` "
+                "(or __graft_entry__.build()); there is no fallback implementation")
+        L = ctypes.CDLL(LIB_PATH)
+        p, i = ctypes.c_void_p, ctypes.c_int
+        L.w4a16_status_str.argtypes = [i]
+        L.w4a16_status_str.restype = ctypes.c_char_p
+        L.w4a16_abi_version.argtypes = []
+        L.w4a16_abi_version.restype = i
+        L.w4a16_gemv.argtypes = [p, p, p, p, i, i, i, i, p]
+        L.w4a16_dequant.argtypes = [p, p, p, i, i, i, p]
+        L.w4a16_quantize.argtypes = [p, p, p, i, i, i, p]
+        L.w4a16_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
+        L.w4a16_layer_seq_create.argtypes = [ctypes.POINTER(_LayerWeights), i, i, i, i, i, i,
+                                             ctypes.POINTER(_SeqIO), ctypes.POINTER(p)]
+        L.w4a16_layer_seq_num_launches.argtypes = [p]
+        L.w4a16_layer_seq_num_launches.restype = i
+        L.w4a16_layer_seq_run.argtypes = [p, p]
+        L.w4a16_layer_seq_run_host.argtypes = [p, ctypes.POINTER(_SeqIO), p]
+        L.w4a16_layer_seq_sync.argtypes = [p, i]
+        L.w4a16_layer_seq_destroy.argtypes = [p]
+        L.w4a16_layer_seq_destroy.restype = None
+        for f in ("w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
+                  "w4a16_layer_seq_create", "w4a16_layer_seq_run", "w4a16_layer_seq_run_host",
+                  "w4a16_layer_seq_sync"):
+            getattr(L, f).restype = i
+        _LIB = L
+    return _LIB
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise W4A16Error(rc, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def w4a16_gemv(qweight, scales, x, y=None, stream=None):
+    """y[M][N] = x[M][K] . w_hat^T.  Allocates y (float16) if not given."""
+    import torch
+    M, K = x.shape
+    N = qweight.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check(lib().w4a16_gemv(_ptr(qweight), _ptr(scales), _ptr(x), _ptr(y), M, N, K, GROUP,
+                            _stream(stream)), "w4a16_gemv")
+    return y
+
+
+def w4a16_gemv_raw(qw_ptr, sc_ptr, x_ptr, y_ptr, M, N, K, group=GROUP, stream=None) -> int:
+    """Unchecked status passthrough (tests of the argument checks use it)."""
+    return lib().w4a16_gemv(qw_ptr, sc_ptr, x_ptr, y_ptr, M, N, K, group, stream)
+
+
+def w4a16_dequant(qweight, scales, w_out=None, stream=None):
+    import torch
+    N = qweight.shape[0]
+    K = qweight.shape[1] * 8
+    if w_out is None:
+        w_out = torch.empty((N, K), dtype=torch.float16, device=qweight.device)
+    _check(lib().w4a16_dequant(_ptr(qweight), _ptr(scales), _ptr(w_out), N, K, GROUP,
+                               _stream(stream)), "w4a16_dequant")
+    return w_out
+
+
+def w4a16_quantize(w, qweight=None, scales=None, stream=None):
+    """fp32 W[N][K] -> (qweight int32 [N][K/8], scales float16 [N][K/128])."""
+    import torch
+    N, K = w.shape
+    if qweight is None:
+        qweight = torch.empty((N, K // 8), dtype=torch.int32, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, K // GROUP), dtype=torch.float16, device=w.device)
+    _check(lib().w4a16_quantize(_ptr(w), _ptr(qweight), _ptr(scales), N, K, GROUP,
+                                _stream(stream)), "w4a16_quantize")
+    return qweight, scales
+
+
+def w4a16_device_status(clear: bool = True) -> int:
+    """The W4A16_DEV_* bits recorded by kernels on the current device."""
+    flags = ctypes.c_uint32(0)
+    rc = lib().w4a16_device_status(ctypes.byref(flags), int(clear))
+    if rc not in (0, 10):
+        raise W4A16Error(rc, "w4a16_device_status")
+    return int(flags.value)
+
+
+class LayerSeq:
+    """n_layers x {q, k, v, o, gate+up, down} GEMVs captured as one CUDA graph.
+
+    layers: list of dicts name -> (qweight, scales) with names q, k, v, o,
+    gate, up, down; io: dict of device tensors x, y_q, y_k, y_v, y_o, y_gu,
+    y_down, each [n_layers][M][width].  The tensors must outlive the object.
+    """
+
+    NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+    IO = ("x", "y_q", "y_k", "y_v", "y_o", "y_gu", "y_down")
+
+    def __init__(self, layers, io, M, hidden, kv_dim, ffn):
+        arr = (_LayerWeights * len(layers))()
+        for li, lw in enumerate(layers):
+            for pj, name in enumerate(self.NAMES):
+                qw, sc = lw[name]
+                arr[li].qweight[pj] = qw.data_ptr()
+                arr[li].scales[pj] = sc.data_ptr()
+        sio = _SeqIO(*[io[n].data_ptr() for n in self.IO])
+        handle = ctypes.c_void_p(None)
+        self._keep = (layers, io)
+        _check(lib().w4a16_layer_seq_create(arr, len(layers), M, hidden, kv_dim, ffn, GROUP,
+                                            ctypes.byref(sio), ctypes.byref(handle)),
+               "w4a16_layer_seq_create")
+        self.handle = handle
+        self.io = io
+
+    @property
+    def num_launches(self) -> int:
+        return lib().w4a16_layer_seq_num_launches(self.handle)
+
+    def run(self, stream=None) -> None:
+        _check(lib().w4a16_layer_seq_run(self.handle, _stream(stream)), "w4a16_layer_seq_run")
+
+    def run_host(self, host: dict, stream=None) -> None:
+        """host: dict of pinned CPU tensors (any subset of IO names)."""
+        hio = _SeqIO(*[_ptr(host.get(n)) for n in self.IO])
+        _check(lib().w4a16_layer_seq_run_host(self.handle, ctypes.byref(hio), _stream(stream)),
+               "w4a16_layer_seq_run_host")
+
+    def sync(self, timeout_ms: int = -1) -> int:
+        """0 when done; W4A16_ERR_TIMEOUT (8) if the bound ran out; raises otherwise."""
+        rc = lib().w4a16_layer_seq_sync(self.handle, timeout_ms)
+        if rc not in (0, 8):
+            raise W4A16Error(rc, "w4a16_layer_seq_sync")
+        return rc
+
+    def close(self) -> None:
+        if self.handle is not None and self.handle.value:
+            lib().w4a16_layer_seq_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 -- interpreter shutdown
+            pass

@@ -1,0 +1,469 @@
+// api.cu -- the C ABI of include/w4a16.h: argument checks, kernel dispatch,
+// the per-device status word and the graph-captured layer sequence.
+//
+// Every argument is checked on the host before anything is enqueued.  The
+// library allocates device memory nowhere; layer_seq owns only its CUDA graph,
+// stream and event.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <thread>
+#include <chrono>
+#include <vector>
+
+#include "kernels.h"
+#include "w4a16.h"
+
+namespace w4a16 {
+namespace {
+
+// Per-device word into which kernels OR the W4A16_DEV_* bits.
+__device__ uint32_t g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  DeviceInfo info{};
+  uint32_t* status = nullptr;  // device address of g_device_status on this device
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Query and cache the facts and attributes of the current device.  Runs
+// cudaFuncSetAttribute, so the first call per device must not be made during
+// stream capture; every entry point calls it before launching anything.
+w4a16_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    int sms = 0, smem = 0;
+    void* addr = nullptr;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) {
+      cudaGetLastError();
+      return W4A16_ERR_CUDA;
+    }
+    d.info.sms = sms;
+    d.info.max_smem_optin = smem;
+    d.status = static_cast<uint32_t*>(addr);
+    if (prepare_gemv_m1(d.info) != cudaSuccess || prepare_gemv_mma(d.info) != cudaSuccess) {
+      cudaGetLastError();
+      return W4A16_ERR_CUDA;
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return W4A16_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+  if (abytes == 0 || bbytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+// Shape / group checks shared by every weight-taking entry point.
+w4a16_status check_weight_shape(int N, int K, int group) {
+  if (group != W4A16_GROUP) return W4A16_ERR_GROUP;
+  if (N < 0 || N > W4A16_MAX_N) return W4A16_ERR_SHAPE;
+  if (K <= 0 || K % W4A16_GROUP != 0 || K > W4A16_MAX_K) return W4A16_ERR_SHAPE;
+  return W4A16_OK;
+}
+
+// Full validation of one GEMV; x has row stride ldx (== K for the public call).
+w4a16_status check_gemv(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
+                        const uint16_t* y, int M, int N, int K, int group, int64_t ldx) {
+  w4a16_status s = check_weight_shape(N, K, group);
+  if (s != W4A16_OK) return s;
+  if (M < 0 || M > W4A16_MAX_M) return W4A16_ERR_M_RANGE;
+  if (M == 0 || N == 0) return W4A16_OK;  // empty product
+  if (!qweight || !scales || !x || !y) return W4A16_ERR_NULL;
+  if (!aligned16(qweight) || !aligned16(scales) || !aligned16(x) || !aligned16(y))
+    return W4A16_ERR_ALIGN;
+  if (ldx < K || ldx % 8 != 0) return W4A16_ERR_SHAPE;
+  const size_t wbytes = static_cast<size_t>(N) * (K / 2);
+  const size_t sbytes = static_cast<size_t>(N) * (K / W4A16_GROUP) * 2;
+  const size_t xbytes = (static_cast<size_t>(M - 1) * ldx + K) * 2;
+  const size_t ybytes = static_cast<size_t>(M) * N * 2;
+  if (overlaps(y, ybytes, x, xbytes) || overlaps(y, ybytes, qweight, wbytes) ||
+      overlaps(y, ybytes, scales, sbytes))
+    return W4A16_ERR_ALIAS;
+  return W4A16_OK;
+}
+
+// Enqueue one checked GEMV (M, N > 0).
+w4a16_status enqueue_gemv(const DeviceState& d, const uint32_t* qweight, const uint16_t* scales,
+                          const uint16_t* x, uint16_t* y, int M, int N, int K, int64_t ldx,
+                          cudaStream_t st) {
+  GemvArgs a;
+  a.qweight = qweight;
+  a.scales = scales;
+  a.x = x;
+  a.y = y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.ldx = ldx;
+  a.status = d.status;
+  cudaError_t e;
+  if (M == 1 && gemv_m1_supported(K))
+    e = launch_gemv_m1(a, d.info, st);
+  else if (M <= 7)
+    e = launch_gemv_rows(a, d.info, st);
+  else
+    e = launch_gemv_mma(a, d.info, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+const char* w4a16_status_str(w4a16_status s) {
+  switch (s) {
+    case W4A16_OK: return "ok";
+    case W4A16_ERR_NULL: return "null pointer";
+    case W4A16_ERR_SHAPE: return "bad shape (N, K or stride out of range, or K not a multiple of 128)";
+    case W4A16_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case W4A16_ERR_GROUP: return "group size is not 128";
+    case W4A16_ERR_M_RANGE: return "M outside 0..16";
+    case W4A16_ERR_ALIAS: return "output overlaps an input";
+    case W4A16_ERR_CUDA: return "CUDA runtime error";
+    case W4A16_ERR_TIMEOUT: return "wait timed out";
+    case W4A16_ERR_STATE: return "invalid object handle";
+    case W4A16_ERR_DEVICE: return "a kernel reported an error in the device status word";
+  }
+  return "unknown status";
+}
+
+int w4a16_abi_version(void) { return W4A16_ABI_VERSION; }
+
+w4a16_status w4a16_gemv(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
+                        uint16_t* y, int M, int N, int K, int group, void* stream) {
+  w4a16_status s = check_gemv(qweight, scales, x, y, M, N, K, group, K);
+  if (s != W4A16_OK) return s;
+  if (M == 0 || N == 0) return W4A16_OK;
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != W4A16_OK) return s;
+  return enqueue_gemv(*d, qweight, scales, x, y, M, N, K, K, static_cast<cudaStream_t>(stream));
+}
+
+w4a16_status w4a16_dequant(const uint32_t* qweight, const uint16_t* scales, uint16_t* w_out,
+                           int N, int K, int group, void* stream) {
+  w4a16_status s = check_weight_shape(N, K, group);
+  if (s != W4A16_OK) return s;
+  if (N == 0) return W4A16_OK;
+  if (!qweight || !scales || !w_out) return W4A16_ERR_NULL;
+  if (!aligned16(qweight) || !aligned16(scales) || !aligned16(w_out)) return W4A16_ERR_ALIGN;
+  const size_t obytes = static_cast<size_t>(N) * K * 2;
+  if (overlaps(w_out, obytes, qweight, static_cast<size_t>(N) * (K / 2)) ||
+      overlaps(w_out, obytes, scales, static_cast<size_t>(N) * (K / W4A16_GROUP) * 2))
+    return W4A16_ERR_ALIAS;
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != W4A16_OK) return s;
+  if (launch_dequant(qweight, scales, w_out, N, K, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_quantize(const float* w, uint32_t* qweight, uint16_t* scales, int N, int K,
+                            int group, void* stream) {
+  w4a16_status s = check_weight_shape(N, K, group);
+  if (s != W4A16_OK) return s;
+  if (N == 0) return W4A16_OK;
+  if (!w || !qweight || !scales) return W4A16_ERR_NULL;
+  if (!aligned16(w) || !aligned16(qweight) || !aligned16(scales)) return W4A16_ERR_ALIGN;
+  const size_t wbytes = static_cast<size_t>(N) * K * 4;
+  const size_t qbytes = static_cast<size_t>(N) * (K / 2);
+  const size_t sbytes = static_cast<size_t>(N) * (K / W4A16_GROUP) * 2;
+  if (overlaps(qweight, qbytes, w, wbytes) || overlaps(scales, sbytes, w, wbytes) ||
+      overlaps(qweight, qbytes, scales, sbytes))
+    return W4A16_ERR_ALIAS;
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != W4A16_OK) return s;
+  if (launch_quantize(w, qweight, scales, N, K, d->status, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_device_status(uint32_t* flags, int clear) {
+  if (!flags) return W4A16_ERR_NULL;
+  DeviceState* d = nullptr;
+  w4a16_status s = device_state(&d);
+  if (s != W4A16_OK) return s;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  if (clear && v != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return W4A16_ERR_CUDA;
+    }
+  }
+  *flags = v;
+  return v ? W4A16_ERR_DEVICE : W4A16_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- layer_seq
+
+struct w4a16_layer_seq {
+  int device = 0;
+  int n_layers = 0, M = 0, hidden = 0, kv_dim = 0, ffn = 0;
+  int launches = 0;
+  w4a16_seq_io io{};
+  cudaStream_t capture_stream = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaEvent_t done = nullptr;
+};
+
+namespace {
+
+void seq_free(w4a16_layer_seq* s) {
+  if (!s) return;
+  if (s->exec) cudaGraphExecDestroy(s->exec);
+  if (s->graph) cudaGraphDestroy(s->graph);
+  if (s->done) cudaEventDestroy(s->done);
+  if (s->capture_stream) cudaStreamDestroy(s->capture_stream);
+  delete s;
+}
+
+struct ProjSpec {
+  int idx;        // W4A16_Q..W4A16_DOWN
+  int N, K;
+};
+
+}  // namespace
+
+extern "C" {
+
+w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_layers, int M,
+                                    int hidden, int kv_dim, int ffn, int group,
+                                    const w4a16_seq_io* io, w4a16_layer_seq** out) {
+  if (!out) return W4A16_ERR_NULL;
+  *out = nullptr;
+  if (!layers || !io) return W4A16_ERR_NULL;
+  if (group != W4A16_GROUP) return W4A16_ERR_GROUP;
+  if (n_layers <= 0) return W4A16_ERR_SHAPE;
+  if (M <= 0 || M > W4A16_MAX_M) return W4A16_ERR_M_RANGE;
+  if (hidden <= 0 || kv_dim <= 0 || ffn <= 0) return W4A16_ERR_SHAPE;
+  if (!io->x || !io->y_q || !io->y_k || !io->y_v || !io->y_o || !io->y_gu || !io->y_down)
+    return W4A16_ERR_NULL;
+
+  const ProjSpec specs[W4A16_NPROJ] = {
+      {W4A16_Q, hidden, hidden},   {W4A16_K, kv_dim, hidden}, {W4A16_V, kv_dim, hidden},
+      {W4A16_O, hidden, hidden},   {W4A16_GATE, ffn, hidden}, {W4A16_UP, ffn, hidden},
+      {W4A16_DOWN, hidden, ffn}};
+  const int64_t Mh = static_cast<int64_t>(M) * hidden, Mkv = static_cast<int64_t>(M) * kv_dim,
+                Mgu = static_cast<int64_t>(M) * 2 * ffn;
+
+  // every GEMV of every layer is checked exactly as w4a16_gemv would check it
+  for (int l = 0; l < n_layers; ++l) {
+    const w4a16_layer_weights& w = layers[l];
+    const uint16_t* xl = io->x + l * Mh;
+    const uint16_t* yq = io->y_q + l * Mh;
+    const uint16_t* ygu = io->y_gu + l * Mgu;
+    const uint16_t* yout[W4A16_NPROJ] = {yq, io->y_k + l * Mkv, io->y_v + l * Mkv,
+                                         io->y_o + l * Mh, ygu, ygu + ffn, io->y_down + l * Mh};
+    const uint16_t* xin[W4A16_NPROJ] = {xl, xl, xl, yq, xl, xl, ygu};
+    const int64_t ldx[W4A16_NPROJ] = {hidden, hidden, hidden, hidden, hidden, hidden, 2 * ffn};
+    for (int pj = 0; pj < W4A16_NPROJ; ++pj) {
+      const ProjSpec& ps = specs[pj];
+      // the up projection writes the second half of each y_gu row: check it
+      // as a GEMV with output row stride 2 ffn by treating rows as M = 1 views
+      for (int m = 0; m < (pj == W4A16_GATE || pj == W4A16_UP ? M : 1); ++m) {
+        const int mm = (pj == W4A16_GATE || pj == W4A16_UP) ? 1 : M;
+        const uint16_t* yy = (pj == W4A16_GATE || pj == W4A16_UP) ? yout[pj] + m * 2 * ffn : yout[pj];
+        const uint16_t* xx = xin[pj] + ((pj == W4A16_GATE || pj == W4A16_UP) ? m * ldx[pj] : 0);
+        w4a16_status s = check_gemv(w.qweight[pj], w.scales[pj], xx, yy, mm, ps.N, ps.K, group,
+                                    ldx[pj]);
+        if (s != W4A16_OK) return s;
+      }
+    }
+  }
+
+  DeviceState* d = nullptr;
+  w4a16_status st = device_state(&d);
+  if (st != W4A16_OK) return st;
+
+  w4a16_layer_seq* s = new (std::nothrow) w4a16_layer_seq();
+  if (!s) return W4A16_ERR_CUDA;
+  cudaGetDevice(&s->device);
+  s->n_layers = n_layers;
+  s->M = M;
+  s->hidden = hidden;
+  s->kv_dim = kv_dim;
+  s->ffn = ffn;
+  s->io = *io;
+  if (cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&s->done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    seq_free(s);
+    return W4A16_ERR_CUDA;
+  }
+  if (cudaStreamBeginCapture(s->capture_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    seq_free(s);
+    return W4A16_ERR_CUDA;
+  }
+  w4a16_status cap = W4A16_OK;
+  int launches = 0;
+  for (int l = 0; l < n_layers && cap == W4A16_OK; ++l) {
+    const w4a16_layer_weights& w = layers[l];
+    const uint16_t* xl = io->x + l * Mh;
+    uint16_t* yq = io->y_q + l * Mh;
+    uint16_t* ygu = io->y_gu + l * Mgu;
+    auto run = [&](int pj, const uint16_t* x, uint16_t* y, int N, int K, int64_t ldx) {
+      if (cap != W4A16_OK) return;
+      cap = enqueue_gemv(*d, w.qweight[pj], w.scales[pj], x, y, M, N, K, ldx, s->capture_stream);
+      ++launches;
+    };
+    run(W4A16_Q, xl, yq, hidden, hidden, hidden);
+    run(W4A16_K, xl, io->y_k + l * Mkv, kv_dim, hidden, hidden);
+    run(W4A16_V, xl, io->y_v + l * Mkv, kv_dim, hidden, hidden);
+    run(W4A16_O, yq, io->y_o + l * Mh, hidden, hidden, hidden);
+    // [gate; up] as one N = 2 ffn GEMV writes exactly the y_gu rows [gate | up]
+    const bool fused = w.qweight[W4A16_UP] == w.qweight[W4A16_GATE] + static_cast<size_t>(ffn) * (hidden / 8) &&
+                       w.scales[W4A16_UP] == w.scales[W4A16_GATE] + static_cast<size_t>(ffn) * (hidden / W4A16_GROUP);
+    if (fused) {
+      run(W4A16_GATE, xl, ygu, 2 * ffn, hidden, hidden);
+    } else {
+      // separate weights: each half of a y_gu row is strided by 2 ffn, so
+      // each activation row gets its own pair of M = 1 launches
+      for (int m = 0; m < M && cap == W4A16_OK; ++m) {
+        const uint16_t* xm = xl + static_cast<int64_t>(m) * hidden;
+        uint16_t* ym = ygu + static_cast<int64_t>(m) * 2 * ffn;
+        cap = enqueue_gemv(*d, w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xm, ym, 1, ffn, hidden,
+                           hidden, s->capture_stream);
+        ++launches;
+        if (cap != W4A16_OK) break;
+        cap = enqueue_gemv(*d, w.qweight[W4A16_UP], w.scales[W4A16_UP], xm, ym + ffn, 1, ffn, hidden,
+                           hidden, s->capture_stream);
+        ++launches;
+      }
+    }
+    run(W4A16_DOWN, ygu, io->y_down + l * Mh, hidden, ffn, 2 * static_cast<int64_t>(ffn));
+  }
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(s->capture_stream, &graph);
+  if (cap != W4A16_OK || ec != cudaSuccess) {
+    cudaGetLastError();
+    if (graph) cudaGraphDestroy(graph);
+    seq_free(s);
+    return cap != W4A16_OK ? cap : W4A16_ERR_CUDA;
+  }
+  s->graph = graph;
+  if (cudaGraphInstantiate(&s->exec, graph, 0) != cudaSuccess) {
+    cudaGetLastError();
+    seq_free(s);
+    return W4A16_ERR_CUDA;
+  }
+  s->launches = launches;
+  *out = s;
+  return W4A16_OK;
+}
+
+int w4a16_layer_seq_num_launches(const w4a16_layer_seq* seq) { return seq ? seq->launches : 0; }
+
+w4a16_status w4a16_layer_seq_run(w4a16_layer_seq* seq, void* stream) {
+  if (!seq || !seq->exec) return W4A16_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaGraphLaunch(seq->exec, st) != cudaSuccess || cudaEventRecord(seq->done, st) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_layer_seq_run_host(w4a16_layer_seq* seq, const w4a16_seq_io* host, void* stream) {
+  if (!seq || !seq->exec) return W4A16_ERR_STATE;
+  if (!host) return W4A16_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t L = static_cast<size_t>(seq->n_layers) * seq->M * 2;  // bytes per element x rows x layers
+  const size_t bh = L * seq->hidden, bkv = L * seq->kv_dim, bgu = L * 2 * seq->ffn;
+  bool ok = true;
+  if (host->x)
+    ok = ok && cudaMemcpyAsync(const_cast<uint16_t*>(seq->io.x), host->x, bh, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok = ok && cudaGraphLaunch(seq->exec, st) == cudaSuccess;
+  struct {
+    uint16_t* h;
+    const uint16_t* d;
+    size_t bytes;
+  } outs[6] = {{host->y_q, seq->io.y_q, bh},   {host->y_k, seq->io.y_k, bkv},
+               {host->y_v, seq->io.y_v, bkv},  {host->y_o, seq->io.y_o, bh},
+               {host->y_gu, seq->io.y_gu, bgu}, {host->y_down, seq->io.y_down, bh}};
+  for (auto& o : outs)
+    if (o.h) ok = ok && cudaMemcpyAsync(o.h, o.d, o.bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  ok = ok && cudaEventRecord(seq->done, st) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_layer_seq_sync(w4a16_layer_seq* seq, int timeout_ms) {
+  if (!seq || !seq->done) return W4A16_ERR_STATE;
+  if (timeout_ms < 0) {
+    if (cudaEventSynchronize(seq->done) != cudaSuccess) {
+      cudaGetLastError();
+      return W4A16_ERR_CUDA;
+    }
+    return W4A16_OK;
+  }
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t e = cudaEventQuery(seq->done);
+    if (e == cudaSuccess) return W4A16_OK;
+    if (e != cudaErrorNotReady) {
+      cudaGetLastError();
+      return W4A16_ERR_CUDA;
+    }
+    const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                        std::chrono::steady_clock::now() - t0).count();
+    if (ms >= timeout_ms) return W4A16_ERR_TIMEOUT;
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+void w4a16_layer_seq_destroy(w4a16_layer_seq* seq) {
+  if (!seq) return;
+  if (seq->done) cudaEventSynchronize(seq->done);
+  seq_free(seq);
+}
+
+}  // extern "C"

@@ -1,0 +1,279 @@
+// gemv_m1.cu -- the M = 1 decode GEMV: a persistent, TMA-fed, warp-specialised
+// CUDA-core kernel.
+//
+// The operation is the INT4 x FP16 GEMV of "Costruire un runtime di inference
+// LLM da zero" (datastack.it), section "Tre bug che insegnano", third bug
+// (gate/up/down GEMVs unpack INT4 in-kernel against FP16 activations), with
+// the group-128 symmetric format of the same section's last paragraph.
+//
+// Design (one CTA per SM, one pass over the weight stream):
+//   warp 0      producer + reducer.  Streams tiles of RB consecutive rows into
+//               an S-stage shared-memory ring with 1-D bulk copies (one copy
+//               per row into a padded row slot, one copy for the tile's
+//               scale window), completing on a per-stage mbarrier.  After the
+//               consumers release a stage it sums their per-unit partials of
+//               that tile in a fixed order, writes y, and refills the stage.
+//   warps 1..   consumers.  Consumer thread c owns unit u = c / RL (64
+//               consecutive k, half a group) of row c % RL of every tile, so
+//               its 64 activations stay in registers for the whole kernel and
+//               no activation traffic touches shared memory.  Per packed word
+//               it does one shift, four LOP3s (nibble -> biased fp16, see
+//               ptx.cuh) and eight f16 x f16 -> f32 FMAs; the biases 1032 and
+//               72 are removed once per unit with the precomputed sum
+//               C = 1032 sum x_even + 72 sum x_odd.
+// Rows are split over the CTAs in balanced contiguous ranges (at most one row
+// of imbalance).  Every wait is bounded; a timeout sets W4A16_DEV_PIPE_TIMEOUT.
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "w4a16.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kM1MaxThreads = 640;  // 20 warps -> the compiler may use up to 102 registers
+constexpr int kM1MaxStages = 16;
+constexpr int kM1SmemBudget = 200 * 1024;
+
+struct M1Plan {
+  int U;            // units (64 k) per row
+  int RL;           // rows per tile (rows across lanes)
+  int T;            // consumer threads = U * RL
+  int CW;           // consumer warps
+  int pitch;        // shared-memory row pitch, bytes
+  int sc_cap;       // bytes of the per-stage scale window
+  int stage_bytes;  // RL * pitch + sc_cap
+  int red_stride;   // floats per row in the partial buffer (U + 1: odd stride)
+  int S;            // pipeline stages
+  int smem;         // dynamic shared memory, bytes
+};
+
+__host__ __device__ inline int m1_rows_per_tile(int U) {
+  // Rows across lanes, chosen so that a warp covers (32 / RL) whole units of
+  // RL rows and every shared-memory read of a stage is bank-conflict free
+  // with a row pitch of K/2 + 16 bytes (pitch / 16 odd).
+  return U > 64 ? 2 : (U > 16 ? 8 : (U > 4 ? 16 : 32));
+}
+
+M1Plan make_m1_plan(int K, int smem_limit) {
+  M1Plan p{};
+  p.U = K / 64;
+  p.RL = m1_rows_per_tile(p.U);
+  p.T = p.U * p.RL;
+  p.CW = (p.T + 31) / 32;
+  p.pitch = K / 2 + 16;
+  p.sc_cap = ((p.RL * (K / 64) + 32) + 15) & ~15;
+  p.stage_bytes = p.RL * p.pitch + p.sc_cap;
+  p.red_stride = p.U + 1;
+  const int per_stage = p.stage_bytes + p.RL * p.red_stride * 4;
+  const int budget = (smem_limit < kM1SmemBudget ? smem_limit : kM1SmemBudget) - 512;
+  p.S = budget / per_stage;
+  if (p.S > kM1MaxStages) p.S = kM1MaxStages;
+  p.smem = 512 + p.S * per_stage;
+  return p;
+}
+
+struct M1Params {
+  const uint32_t* qweight;
+  const uint8_t* scales;  // bytes
+  const uint16_t* x;
+  uint16_t* y;
+  uint32_t* status;
+  int N, K;
+  int U, RL, T, pitch, stage_bytes, red_stride, S;
+};
+
+__global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int S = p.S;
+  const int RL = p.RL;
+  // layout: [full S][cons S] barriers | partials S*RL*red_stride f32 | stages
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* cons = full + S;
+  float* red = reinterpret_cast<float*>(smem + 512);
+  uint8_t* stages = smem + 512 + S * RL * p.red_stride * 4;
+  stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(stages) + 127) & ~uintptr_t(127));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int CW = (p.T + 31) >> 5;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&cons[s]), CW);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int64_t N = p.N;
+  const int K = p.K;
+  const int64_t G = gridDim.x;
+  const int64_t row_begin = (N * blockIdx.x) / G;
+  const int64_t row_end = (N * (blockIdx.x + 1)) / G;
+  const int ntiles = static_cast<int>((row_end - row_begin + RL - 1) / RL);
+  const int64_t row_bytes = K / 2;          // packed bytes per row
+  const int64_t sc_row_bytes = K / 64;      // scale bytes per row
+  const int64_t sc_total = N * sc_row_bytes;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int t) {
+      const int s = t % S;
+      const int64_t r0 = row_begin + static_cast<int64_t>(t) * RL;
+      const int nr = static_cast<int>(row_end - r0 < RL ? row_end - r0 : RL);
+      const int64_t sb0 = r0 * sc_row_bytes;
+      const int64_t sb1 = (r0 + nr) * sc_row_bytes;
+      const int64_t a = sb0 & ~int64_t(15);
+      int64_t e = (sb1 + 15) & ~int64_t(15);
+      if (e > sc_total) e = sc_total & ~int64_t(15);  // never read past the buffer
+      const int64_t ecopy = e > a ? e : a;
+      uint8_t* base = stages + static_cast<size_t>(s) * p.stage_bytes;
+      uint8_t* scw = base + RL * p.pitch;
+      const uint32_t bar = smem_addr(&full[s]);
+      if (lane == 0) {
+        // the last few scale bytes of the matrix, if the aligned copy stops short
+        for (int64_t b = ecopy; b < sb1; b += 2)
+          *reinterpret_cast<uint16_t*>(scw + (b - a)) = ld_nc_u16(p.scales + b);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * row_bytes + (ecopy - a)));
+      }
+      __syncwarp();
+      if (lane < nr)
+        bulk_g2s(smem_addr(base + lane * p.pitch), p.qweight + (r0 + lane) * (K / 8),
+                 static_cast<uint32_t>(row_bytes), bar, pol);
+      if (lane == 31 && ecopy > a)
+        bulk_g2s(smem_addr(scw), p.scales + a, static_cast<uint32_t>(ecopy - a), bar, pol);
+    };
+
+    const int prolog = ntiles < S ? ntiles : S;
+    for (int t = 0; t < prolog; ++t) issue(t);
+
+    const int lpr = 32 / RL;  // reducer lanes per row
+    const int my_row = lane / lpr;
+    const int part = lane % lpr;
+    bool ok = true;
+    int t = 0;
+    for (; t < ntiles; ++t) {
+      const int s = t % S;
+      if (!mbar_wait_bounded(smem_addr(&cons[s]), (t / S) & 1, kWaitLimitNs)) {
+        ok = false;
+        break;
+      }
+      const int64_t r0 = row_begin + static_cast<int64_t>(t) * RL;
+      const int nr = static_cast<int>(row_end - r0 < RL ? row_end - r0 : RL);
+      const float* rp = red + (static_cast<size_t>(s) * RL + my_row) * p.red_stride;
+      float sum = 0.f;
+      for (int u = part; u < p.U; u += lpr) sum += rp[u];
+      for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (part == 0 && my_row < nr) p.y[r0 + my_row] = __half_as_ushort(__float2half_rn(sum));
+      __syncwarp();
+      if (t + S < ntiles) issue(t + S);
+    }
+    if (!ok) {
+      if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+      // let the copies already in flight land before the CTA exits
+      for (int u = t; u < ntiles && u < t + S; ++u)
+        mbar_wait_bounded(smem_addr(&full[u % S]), (u / S) & 1, kWaitLimitNs);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int c = tid - 32;
+  const bool active = c < p.T;
+  const int rl = c % RL;
+  const int u = active ? c / RL : 0;
+
+  // activations of this thread's 64 k, paired to match the unpacked lanes
+  XPairs X[8];
+  float C = 0.f;
+  {
+    const uint16_t* xp = p.x + u * 64;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xp + 8 * j);
+      X[j] = pair_activations(v);
+      const float even = (half_lo(X[j].p0) + half_hi(X[j].p0)) + (half_lo(X[j].p2) + half_hi(X[j].p2));
+      const float odd = (half_lo(X[j].p1) + half_hi(X[j].p1)) + (half_lo(X[j].p3) + half_hi(X[j].p3));
+      C = fmaf(1032.f, even, fmaf(72.f, odd, C));
+    }
+  }
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % S;
+    if (!mbar_wait_bounded(smem_addr(&full[s]), (t / S) & 1, kWaitLimitNs)) {
+      if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+      return;
+    }
+    const int64_t r0 = row_begin + static_cast<int64_t>(t) * RL;
+    const int nr = static_cast<int>(row_end - r0 < RL ? row_end - r0 : RL);
+    if (active && rl < nr) {
+      const uint8_t* base = stages + static_cast<size_t>(s) * p.stage_bytes;
+      const uint4* wp = reinterpret_cast<const uint4*>(base + rl * p.pitch + u * 32);
+      const uint4 w0 = wp[0];
+      const uint4 w1 = wp[1];
+      const int64_t a = (r0 * (K / 64)) & ~int64_t(15);
+      const uint8_t* scw = base + RL * p.pitch;
+      const int64_t sb = (r0 + rl) * (K / 64) + (u >> 1) * 2 - a;
+      const float sc = __half2float(*reinterpret_cast<const __half*>(scw + sb));
+      float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;
+      const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const Unpacked h = unpack_biased(words[j]);
+        fma_f32_f16x2(e0, e1, h.h0, X[j].p0);
+        fma_f32_f16x2(o0, o1, h.h1, X[j].p1);
+        fma_f32_f16x2(e0, e1, h.h2, X[j].p2);
+        fma_f32_f16x2(o0, o1, h.h3, X[j].p3);
+      }
+      const float dot = fmaf(0.0625f, o0 + o1, e0 + e1) - C;
+      red[(static_cast<size_t>(s) * RL + rl) * p.red_stride + u] = dot * sc;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&cons[s]));
+  }
+}
+
+}  // namespace
+
+bool gemv_m1_supported(int K) {
+  if (K <= 0 || K % 128 != 0) return false;
+  const int U = K / 64;
+  const int T = U * m1_rows_per_tile(U);
+  return T + 32 <= kM1MaxThreads;
+}
+
+cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
+  const M1Plan plan = make_m1_plan(a.K, d.max_smem_optin);
+  if (plan.S < 2) return cudaErrorInvalidConfiguration;
+  M1Params p;
+  p.qweight = a.qweight;
+  p.scales = reinterpret_cast<const uint8_t*>(a.scales);
+  p.x = a.x;
+  p.y = a.y;
+  p.status = a.status;
+  p.N = a.N;
+  p.K = a.K;
+  p.U = plan.U;
+  p.RL = plan.RL;
+  p.T = plan.T;
+  p.pitch = plan.pitch;
+  p.stage_bytes = plan.stage_bytes;
+  p.red_stride = plan.red_stride;
+  p.S = plan.S;
+  const int grid = a.N < d.sms ? a.N : d.sms;
+  const int threads = 32 + plan.CW * 32;
+  gemv_m1_kernel<<<grid, threads, plan.smem + 128, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_gemv_m1(const DeviceInfo& d) {
+  const int limit = d.max_smem_optin < kM1SmemBudget + 1024 ? d.max_smem_optin : kM1SmemBudget + 1024;
+  return cudaFuncSetAttribute(gemv_m1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+}
+
+}  // namespace w4a16

@@ -1,0 +1,129 @@
+"""The C-ABI library on a host without a GPU: it loads, exports every function
+include/w4a16.h declares, and rejects bad arguments with the documented
+status before touching CUDA (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int4_weight_only_gemv_gb300 as w4
+from int4_weight_only_gemv_gb300 import build as wbuild
+
+HEADER = os.path.join(wbuild.ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    wbuild.build()
+    return w4.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding_list():
+    assert declared_functions() == sorted(w4.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_library_is_built_for_sm_103a_only():
+    # the architecture flags of the build: one -gencode, sm_103a
+    assert wbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_abi_version_and_status_strings(L):
+    assert L.w4a16_abi_version() == 1
+    for code, name in w4.STATUS.items():
+        s = L.w4a16_status_str(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert L.w4a16_status_str(999) == b"unknown status"
+
+
+# fake, never-dereferenced device addresses: argument checks only look at values
+A = 0x10000
+B = 0x20000
+C = 0x40000
+D = 0x80000
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, B, C, D, 1, 8, 128, 128), 1),          # null qweight
+    ((A, 0, C, D, 1, 8, 128, 128), 1),          # null scales
+    ((A, B, 0, D, 1, 8, 128, 128), 1),          # null x
+    ((A, B, C, 0, 1, 8, 128, 128), 1),          # null y
+    ((A, B, C, D, 1, 8, 128, 64), 4),           # group != 128
+    ((A, B, C, D, 1, 8, 100, 128), 2),          # K not a multiple of 128
+    ((A, B, C, D, 1, 8, 0, 128), 2),            # K = 0
+    ((A, B, C, D, 1, 8, 32768 + 128, 128), 2),  # K above the maximum
+    ((A, B, C, D, 1, -1, 128, 128), 2),         # negative N
+    ((A, B, C, D, 17, 8, 128, 128), 5),         # M above 16
+    ((A, B, C, D, -1, 8, 128, 128), 5),         # negative M
+    ((A + 4, B, C, D, 1, 8, 128, 128), 3),      # misaligned qweight
+    ((A, B + 2, C, D, 1, 8, 128, 128), 3),      # misaligned scales
+    ((A, B, C + 8, D, 1, 8, 128, 128), 3),      # misaligned x
+    ((A, B, C, D + 2, 1, 8, 128, 128), 3),      # misaligned y
+    ((A, B, C, C, 1, 8, 128, 128), 6),          # y overlaps x
+    ((A, B, C, A + 16, 1, 8, 128, 128), 6),     # y overlaps qweight
+    ((A, B, C, B, 1, 8, 128, 128), 6),          # y overlaps scales
+    ((0, 0, 0, 0, 0, 8, 128, 128), 0),          # M = 0: empty product, nothing launched
+    ((0, 0, 0, 0, 4, 0, 128, 128), 0),          # N = 0: empty product
+])
+def test_gemv_argument_checks(L, args, expect):
+    qw, sc, x, y, M, N, K, g = args
+    assert L.w4a16_gemv(qw, sc, x, y, M, N, K, g, None) == expect
+
+
+def test_dequant_and_quantize_argument_checks(L):
+    assert L.w4a16_dequant(0, B, C, 8, 128, 128, None) == 1
+    assert L.w4a16_dequant(A, B, C, 8, 128, 96, None) == 4
+    assert L.w4a16_dequant(A, B, C, 8, 200, 128, None) == 2
+    assert L.w4a16_dequant(A, B, C + 2, 8, 128, 128, None) == 3
+    assert L.w4a16_dequant(A, B, A, 8, 128, 128, None) == 6
+    assert L.w4a16_dequant(0, 0, 0, 0, 128, 128, None) == 0
+    assert L.w4a16_quantize(0, B, C, 8, 128, 128, None) == 1
+    assert L.w4a16_quantize(A, B, C, 8, 129, 128, None) == 2
+    assert L.w4a16_quantize(A, B + 2, C, 8, 128, 128, None) == 3
+    assert L.w4a16_quantize(A, A + 64, C, 8, 128, 128, None) == 6   # qweight inside w
+    assert L.w4a16_quantize(0, 0, 0, 0, 128, 128, None) == 0
+
+
+def test_layer_seq_argument_checks(L):
+    out = ctypes.c_void_p(None)
+    lw = (w4._LayerWeights * 1)()
+    io = w4._SeqIO()
+    assert L.w4a16_layer_seq_create(lw, 1, 1, 3584, 512, 18944, 128, ctypes.byref(io), None) == 1
+    assert L.w4a16_layer_seq_create(None, 1, 1, 3584, 512, 18944, 128, ctypes.byref(io), ctypes.byref(out)) == 1
+    assert L.w4a16_layer_seq_create(lw, 0, 1, 3584, 512, 18944, 128, ctypes.byref(io), ctypes.byref(out)) == 2
+    assert L.w4a16_layer_seq_create(lw, 1, 0, 3584, 512, 18944, 128, ctypes.byref(io), ctypes.byref(out)) == 5
+    assert L.w4a16_layer_seq_create(lw, 1, 1, 3584, 512, 18944, 64, ctypes.byref(io), ctypes.byref(out)) == 4
+    # io pointers NULL
+    assert L.w4a16_layer_seq_create(lw, 1, 1, 3584, 512, 18944, 128, ctypes.byref(io), ctypes.byref(out)) == 1
+    assert out.value is None
+    # weights NULL with valid-looking io
+    io2 = w4._SeqIO(*[0x100000 * (i + 1) for i in range(7)])
+    assert L.w4a16_layer_seq_create(lw, 1, 1, 256, 128, 512, 128, ctypes.byref(io2), ctypes.byref(out)) == 1
+    # NULL handles
+    assert L.w4a16_layer_seq_run(None, None) == 9
+    assert L.w4a16_layer_seq_run_host(None, ctypes.byref(io), None) == 9
+    assert L.w4a16_layer_seq_sync(None, 0) == 9
+    assert L.w4a16_layer_seq_num_launches(None) == 0
+    L.w4a16_layer_seq_destroy(None)  # no-op
+
+
+def test_device_status_null(L):
+    assert L.w4a16_device_status(None, 0) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(w4, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(w4, "_LIB", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        w4.lib()

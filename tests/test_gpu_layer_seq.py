@@ -1,0 +1,189 @@
+"""GPU tests of layer_seq: the seven projections of a Qwen-7B-shaped layer,
+28 layers, captured as one CUDA graph.
+
+Layers 0 and 27 are drawn on the CPU and checked against the oracle on
+sampled rows (each GEMV alone: o and down take the GPU's own fp16
+intermediate as their input); every layer is checked bit for bit against
+separate w4a16_gemv calls; run_host, the fused/unfused gate+up paths, M > 1
+and the bounded sync are covered too.
+"""
+import numpy as np
+import pytest
+import torch
+
+import int4_weight_only_gemv_gb300 as w4
+import oracle
+import synth
+from gpu_helpers import sample_rows, to_np_u16, to_np_u32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+H, KV, F, L = synth.HIDDEN, synth.KV_DIM, synth.FFN, synth.N_LAYERS
+CHECKED_LAYERS = (0, L - 1)
+
+
+def _layer_weights(layer, fused=True, cpu=False):
+    """One layer's packed weights; gate and up share one allocation when fused."""
+    out, w_cpu = {}, {}
+    dev_gen = "cpu" if cpu else DEV
+    for pj, name in enumerate(synth.PROJ_NAMES):
+        if fused and name == "up":
+            continue
+        if fused and name == "gate":
+            wg = synth.weights(F, H, synth.layer_seed(layer, 4), dev_gen)
+            wu = synth.weights(F, H, synth.layer_seed(layer, 5), dev_gen)
+            qw, sc = w4.w4a16_quantize(torch.cat([wg, wu]).to(DEV))
+            out["gate"] = (qw[:F], sc[:F])
+            out["up"] = (qw[F:], sc[F:])
+            w_cpu["gate"], w_cpu["up"] = wg.cpu(), wu.cpu()
+            continue
+        N, K = synth.proj_shape(name)
+        w = synth.weights(N, K, synth.layer_seed(layer, pj), dev_gen)
+        out[name] = w4.w4a16_quantize(w.to(DEV))
+        w_cpu[name] = w.cpu()
+    return out, (w_cpu if cpu else None)
+
+
+def _io(M, n_layers):
+    x = torch.cat([synth.activations(M, H, synth.layer_seed(l, 7)) for l in range(n_layers)])
+    io = {"x": x.view(n_layers, M, H).to(DEV)}
+    for name, width in (("y_q", H), ("y_k", KV), ("y_v", KV), ("y_o", H), ("y_gu", 2 * F),
+                        ("y_down", H)):
+        io[name] = torch.full((n_layers, M, width), float("nan"), dtype=torch.float16, device=DEV)
+    return io
+
+
+@pytest.fixture(scope="module")
+def seq28():
+    from int4_weight_only_gemv_gb300 import build as wbuild
+    wbuild.build()
+    layers, cpu_w = [], {}
+    for l in range(L):
+        lw, wc = _layer_weights(l, fused=True, cpu=l in CHECKED_LAYERS)
+        layers.append(lw)
+        if wc is not None:
+            cpu_w[l] = wc
+    io = _io(1, L)
+    seq = w4.LayerSeq(layers, io, 1, H, KV, F)
+    seq.run()
+    assert seq.sync() == 0
+    torch.cuda.synchronize()
+    yield seq, layers, io, cpu_w
+    seq.close()
+
+
+def test_layer_seq_launch_count(seq28):
+    seq = seq28[0]
+    assert seq.num_launches == 6 * L  # gate and up fused
+
+
+def test_layer_seq_outputs_written(seq28):
+    _, _, io, _ = seq28
+    for name in ("y_q", "y_k", "y_v", "y_o", "y_gu", "y_down"):
+        assert not torch.isnan(io[name]).any(), name
+
+
+def test_layer_seq_equals_separate_calls(seq28):
+    """Every projection of every layer equals a separate w4a16_gemv (bitwise:
+    same kernels, same inputs)."""
+    _, layers, io, _ = seq28
+    for l in range(L):
+        lw = layers[l]
+        x = io["x"][l]
+        pairs = [("q", x, io["y_q"][l]), ("k", x, io["y_k"][l]), ("v", x, io["y_v"][l]),
+                 ("o", io["y_q"][l], io["y_o"][l]),
+                 ("down", io["y_gu"][l][:, :F].contiguous(), io["y_down"][l])]
+        for name, xin, yout in pairs:
+            y = w4.w4a16_gemv(*lw[name], xin)
+            assert torch.equal(y.view(torch.int16), yout.view(torch.int16)), (l, name)
+        for name, half in (("gate", slice(0, F)), ("up", slice(F, 2 * F))):
+            y = w4.w4a16_gemv(*lw[name], x)
+            assert torch.equal(y.view(torch.int16), io["y_gu"][l][:, half].view(torch.int16)), (l, name)
+
+
+@pytest.mark.parametrize("layer", CHECKED_LAYERS)
+def test_layer_seq_against_oracle(seq28, layer):
+    """Packed weights bit-exact, and every GEMV of the layer within tolerance
+    of the oracle on sampled rows (the full-size graph, as timed)."""
+    _, layers, io, cpu_w = seq28
+    lw, wc = layers[layer], cpu_w[layer]
+    x_l = io["x"][layer].cpu()
+    inputs = {"q": x_l, "k": x_l, "v": x_l, "gate": x_l, "up": x_l,
+              "o": io["y_q"][layer].cpu(), "down": io["y_gu"][layer][:, :F].cpu()}
+    outputs = {"q": io["y_q"][layer], "k": io["y_k"][layer], "v": io["y_v"][layer],
+               "o": io["y_o"][layer], "gate": io["y_gu"][layer][:, :F],
+               "up": io["y_gu"][layer][:, F:], "down": io["y_down"][layer]}
+    for name in synth.PROJ_NAMES:
+        qw_ref, sc_ref = oracle.quantize(wc[name].numpy())
+        qw, sc = lw[name]
+        assert np.array_equal(to_np_u32(qw), qw_ref) and np.array_equal(to_np_u16(sc), sc_ref), name
+        xin = inputs[name].contiguous()
+        x_u16 = xin.view(torch.int16).numpy().view(np.uint16)
+        rows = sample_rows(qw_ref.shape[0], 96, layer)
+        y_ref = oracle.gemv_rows(qw_ref, sc_ref, x_u16, rows)
+        y = outputs[name].to(torch.float64).cpu().numpy()[:, rows]
+        norms = oracle.row_norms(qw_ref, sc_ref)
+        rep = oracle.check_gemv(y, y_ref, xin.to(torch.float64).numpy(), float(norms.max()))
+        assert rep["ok"], (name, rep)
+
+
+def test_layer_seq_replay_is_deterministic(seq28):
+    seq, _, io, _ = seq28
+    before = {k: v.clone() for k, v in io.items() if k != "x"}
+    seq.run()
+    seq.sync()
+    for k, v in before.items():
+        assert torch.equal(v.view(torch.int16), io[k].view(torch.int16)), k
+
+
+def test_layer_seq_run_host(seq28):
+    """End-to-end replay with host buffers: x in, every output back."""
+    seq, _, io, _ = seq28
+    host = {"x": io["x"].cpu().pin_memory()}
+    for k in ("y_q", "y_k", "y_v", "y_o", "y_gu", "y_down"):
+        host[k] = torch.empty(io[k].shape, dtype=torch.float16).pin_memory()
+    seq.run_host(host)
+    assert seq.sync() == 0
+    for k in ("y_q", "y_k", "y_v", "y_o", "y_gu", "y_down"):
+        assert torch.equal(host[k].view(torch.int16), io[k].cpu().view(torch.int16)), k
+
+
+def test_layer_seq_sync_timeout(seq28):
+    """A zero-millisecond bound on a replay that cannot have finished returns
+    W4A16_ERR_TIMEOUT; waiting without bound then completes."""
+    seq = seq28[0]
+    for _ in range(20):  # ~20 x 0.5 ms of queued work
+        seq.run()
+    assert seq.sync(0) == 8
+    assert seq.sync(-1) == 0
+
+
+@pytest.mark.parametrize("M,fused", [(1, False), (3, True), (3, False), (16, True)])
+def test_layer_seq_small(M, fused):
+    """Two layers, unfused gate/up and batched activations, vs separate calls."""
+    n = 2
+    layers = [_layer_weights(l, fused=fused)[0] for l in range(n)]
+    io = _io(M, n)
+    seq = w4.LayerSeq(layers, io, M, H, KV, F)
+    expect_launches = n * (6 if fused else 5 + 2 * M)
+    assert seq.num_launches == expect_launches
+    seq.run()
+    assert seq.sync() == 0
+    for l in range(n):
+        lw = layers[l]
+        x = io["x"][l]
+        y = w4.w4a16_gemv(*lw["q"], x)
+        assert torch.equal(y.view(torch.int16), io["y_q"][l].view(torch.int16))
+        y = w4.w4a16_gemv(*lw["down"], io["y_gu"][l][:, :F].contiguous())
+        assert torch.equal(y.view(torch.int16), io["y_down"][l].view(torch.int16))
+        for name, half in (("gate", slice(0, F)), ("up", slice(F, 2 * F))):
+            for m in range(M):
+                y = w4.w4a16_gemv(*lw[name], x[m:m + 1])
+                ref = io["y_gu"][l][m:m + 1, half]
+                if fused and M > 1:
+                    # the batched kernel differs from the M = 1 one: tolerance
+                    d = (y.double() - ref.double()).abs().max().item()
+                    assert d < 0.05, (l, name, m, d)
+                else:
+                    assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), (l, name, m)
+    seq.close()
