@@ -1,8 +1,8 @@
 """Benchmark of the W4A16 decode GEMV library on GB300.
 
 One step = one replay of the CUDA graph that streams a whole Qwen-7B-shaped
-decode step's INT4 projection weights: 28 layers x {q, k, v, o, gate+up,
-down}, M = 1 (168 GEMV launches, 3.37 GB of packed weights and scales).
+decode step's INT4 projection weights: 28 layers x {[q;k;v], o, [gate;up],
+down}, M = 1 (112 GEMV launches, 3.37 GB of packed weights and scales).
 The metric is achieved GB/s of algorithmic bytes (packed weights + fp16
 scales + fp16 activations + fp16 outputs); the weights (3.37 GB) are far
 larger than the 129 MB L2, so no flush is needed between steps.
@@ -48,16 +48,21 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-shape table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--case", default=None,
+                    help="profiling mode: run one workload GEMV (tiny, q_proj, kv_proj, gate_up, "
+                         "down_m1 .. down_m16) --launches times and exit")
+    ap.add_argument("--launches", type=int, default=4)
     return ap.parse_args()
 
 
 # ---------------------------------------------------------------- workload
 
 def workload_gemvs(M=1):
-    """The GEMVs of one decode step: (name, N, K, M) per launch, in order."""
+    """The GEMVs of one decode step: (name, N, K, M) per launch, in order
+    ([q; k; v] and [gate; up] are one launch each)."""
     import synth
     H, KV, F = synth.HIDDEN, synth.KV_DIM, synth.FFN
-    one = [("q", H, H), ("k", KV, H), ("v", KV, H), ("o", H, H), ("gate_up", 2 * F, H), ("down", H, F)]
+    one = [("qkv", H + 2 * KV, H), ("o", H, H), ("gate_up", 2 * F, H), ("down", H, F)]
     return [(n, N, K, M) for _ in range(synth.N_LAYERS) for (n, N, K) in one]
 
 
@@ -70,8 +75,9 @@ def config_block():
     import synth
     g = workload_gemvs()
     return {
-        "workload": "Qwen-7B-shaped decode weight stream: 28 layers x {q,k,v,o,gate+up,down} "
-                    "INT4 g128 GEMVs at M=1, one CUDA-graph replay per step",
+        "workload": "Qwen-7B-shaped decode weight stream: 28 layers x {q,k,v,o,gate,up,down} "
+                    "INT4 g128 GEMVs at M=1 ([q;k;v] and [gate;up] one launch each), one "
+                    "CUDA-graph replay per step",
         "layers": synth.N_LAYERS, "hidden": synth.HIDDEN, "kv_dim": synth.KV_DIM, "ffn": synth.FFN,
         "M": 1, "group": 128, "gemvs_per_step": len(g),
         "bytes_per_step": sum(gemv_bytes(N, K, M) for _, N, K, M in g),
@@ -267,28 +273,29 @@ def bench_reference(args, rank, world):
 # ---------------------------------------------------------------- GPU arm
 
 def build_weights(dev):
-    """28 layers of packed weights, drawn on the GPU and quantised there."""
+    """28 layers of packed weights, drawn on the GPU and quantised there; the
+    q, k, v weights of a layer are stacked in one allocation, and so are gate
+    and up, so that each stack is one launch."""
     import torch
 
     import int4_weight_only_gemv_gb300 as w4
     import synth
-    H, F = synth.HIDDEN, synth.FFN
     layers = []
     for l in range(synth.N_LAYERS):
         lw = {}
-        for pj, name in enumerate(synth.PROJ_NAMES):
-            if name == "up":
-                continue
-            if name == "gate":
-                wg = synth.weights(F, H, synth.layer_seed(l, 4), dev)
-                wu = synth.weights(F, H, synth.layer_seed(l, 5), dev)
-                qw, sc = w4.w4a16_quantize(torch.cat([wg, wu]))
-                del wg, wu
-                lw["gate"], lw["up"] = (qw[:F], sc[:F]), (qw[F:], sc[F:])
-                lw["gate_up"] = (qw, sc)
-                continue
-            N, K = synth.proj_shape(name)
-            lw[name] = w4.w4a16_quantize(synth.weights(N, K, synth.layer_seed(l, pj), dev))
+        for names, idx, key in ((("q", "k", "v"), (0, 1, 2), "qkv"), (("gate", "up"), (4, 5), "gate_up"),
+                                (("o",), (3,), None), (("down",), (6,), None)):
+            ws = [synth.weights(*synth.proj_shape(synth.PROJ_NAMES[i]), synth.layer_seed(l, i), dev)
+                  for i in idx]
+            qw, sc = w4.w4a16_quantize(torch.cat(ws) if len(ws) > 1 else ws[0])
+            del ws
+            r = 0
+            for name, i in zip(names, idx):
+                n = synth.proj_shape(synth.PROJ_NAMES[i])[0]
+                lw[name] = (qw[r:r + n], sc[r:r + n])
+                r += n
+            if key:
+                lw[key] = (qw, sc)
         layers.append(lw)
     torch.cuda.synchronize()
     if w4.w4a16_device_status(clear=True):
@@ -332,7 +339,8 @@ def per_config_table(layers, dev, reps=20):
     import synth
     H, F = synth.HIDDEN, synth.FFN
     out = {}
-    shapes = [("q_proj", "q", H, 1), ("kv_proj", "k", H, 1), ("gate_up", "gate_up", H, 1)]
+    shapes = [("q_proj", "q", H, 1), ("kv_proj", "k", H, 1), ("qkv", "qkv", H, 1),
+              ("gate_up", "gate_up", H, 1)]
     shapes += [(f"down_m{m}", "down", F, m) for m in (1, 2, 4, 8, 16)]
     stream = torch.cuda.Stream()
     for label, key, K, M in shapes:
@@ -405,7 +413,7 @@ def bench_ours(args, rank, world):
 
     layers = build_weights(dev)
     io = make_io(dev)
-    seq = w4.LayerSeq([{k: v for k, v in lw.items() if k != "gate_up"} for lw in layers], io, 1,
+    seq = w4.LayerSeq([{k: lw[k] for k in synth.PROJ_NAMES} for lw in layers], io, 1,
                       synth.HIDDEN, synth.KV_DIM, synth.FFN)
     stream = torch.cuda.current_stream()
     cfg = config_block()
@@ -453,7 +461,7 @@ def bench_ours(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic,
-                     "kernel": "gemv_m1_kernel (all 168 launches of the step)"},
+                     "kernel": "gemv_m1_kernel (every launch of the step)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * seq.num_launches,
@@ -466,8 +474,39 @@ def bench_ours(args, rank, world):
     return line if rank == 0 else None
 
 
+def run_case(args):
+    """One workload GEMV, launched --launches times on the default stream (a
+    small, self-contained command for ncu captures)."""
+    import torch
+
+    import int4_weight_only_gemv_gb300 as w4
+    import synth
+    from int4_weight_only_gemv_gb300 import build as wbuild
+    wbuild.build()
+    cfg = {c.name: c for c in synth.ALL_GEMVS}[args.case]
+    dev = torch.device("cuda", 0)
+    qw, sc = w4.w4a16_quantize(synth.weights(cfg.N, cfg.K, cfg.seed, dev))
+    x = synth.activations(cfg.M, cfg.K, cfg.seed, dev)
+    y = torch.empty((cfg.M, cfg.N), dtype=torch.float16, device=dev)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.launches):
+        w4.w4a16_gemv(qw, sc, x, y)
+    e.record()
+    torch.cuda.synchronize()
+    if w4.w4a16_device_status(clear=True):
+        raise RuntimeError("a kernel flagged a failure")
+    us = 1e3 * s.elapsed_time(e) / args.launches
+    print(json.dumps({"case": cfg.name, "M": cfg.M, "N": cfg.N, "K": cfg.K, "launches": args.launches,
+                      "us_per_gemv_warm_l2": us, "bytes": gemv_bytes(cfg.N, cfg.K, cfg.M)}))
+
+
 def main():
     args = parse_args()
+    if args.case:
+        run_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -91,7 +91,9 @@ int w4a16_abi_version(void);
  * FP32 accumulation), M in 8..16 the tensor-core kernel (mma.sync over each
  * group of 128, FP32 accumulators).  The result is deterministic: the same
  * inputs give the same bits on every call.  Never allocates, never
- * synchronises; safe to call during CUDA stream capture.
+ * synchronises.  The first call of any entry point on a device does a
+ * one-time set-up (device queries, kernel attributes); make it outside
+ * CUDA stream capture.  After that, w4a16_gemv may be captured.
  */
 w4a16_status w4a16_gemv(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
                         uint16_t* y, int M, int N, int K, int group, void* stream);
@@ -124,6 +126,15 @@ w4a16_status w4a16_quantize(const float* w, uint32_t* qweight, uint16_t* scales,
  * otherwise, W4A16_ERR_CUDA if the device could not be read.
  */
 w4a16_status w4a16_device_status(uint32_t* flags, int clear);
+
+/*
+ * w4a16_selftest_wait_timeout -- exercise the failure path of the bounded
+ * in-kernel waits without any fault: one GPU thread waits on a barrier that
+ * nothing arrives on, gives up after limit_us microseconds (0..10,000,000),
+ * sets W4A16_DEV_PIPE_TIMEOUT in the device status word and returns.  The
+ * context stays usable.  Returns after enqueue.
+ */
+w4a16_status w4a16_selftest_wait_timeout(int limit_us, void* stream);
 
 /* ------------------------------------------------------------------------
  * layer_seq -- the seven projections of a Qwen-7B-shaped decoder layer,

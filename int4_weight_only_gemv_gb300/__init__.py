@@ -17,6 +17,7 @@ import os
 
 __all__ = [
     "W4A16Error", "lib", "w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
+    "w4a16_selftest_wait_timeout",
     "LayerSeq", "GROUP", "MAX_M", "MAX_K", "DEV_NONFINITE", "DEV_SCALE_OVERFLOW",
     "DEV_PIPE_TIMEOUT", "STATUS", "EXPORTED_SYMBOLS",
 ]
@@ -41,7 +42,7 @@ STATUS = {
 # Every function include/w4a16.h declares.
 EXPORTED_SYMBOLS = (
     "w4a16_status_str", "w4a16_abi_version", "w4a16_gemv", "w4a16_dequant", "w4a16_quantize",
-    "w4a16_device_status", "w4a16_layer_seq_create", "w4a16_layer_seq_num_launches",
+    "w4a16_device_status", "w4a16_selftest_wait_timeout", "w4a16_layer_seq_create", "w4a16_layer_seq_num_launches",
     "w4a16_layer_seq_run", "w4a16_layer_seq_run_host", "w4a16_layer_seq_sync",
     "w4a16_layer_seq_destroy",
 )
@@ -83,6 +84,7 @@ def lib() -> ctypes.CDLL:
         L.w4a16_dequant.argtypes = [p, p, p, i, i, i, p]
         L.w4a16_quantize.argtypes = [p, p, p, i, i, i, p]
         L.w4a16_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
+        L.w4a16_selftest_wait_timeout.argtypes = [i, p]
         L.w4a16_layer_seq_create.argtypes = [ctypes.POINTER(_LayerWeights), i, i, i, i, i, i,
                                              ctypes.POINTER(_SeqIO), ctypes.POINTER(p)]
         L.w4a16_layer_seq_num_launches.argtypes = [p]
@@ -93,6 +95,7 @@ def lib() -> ctypes.CDLL:
         L.w4a16_layer_seq_destroy.argtypes = [p]
         L.w4a16_layer_seq_destroy.restype = None
         for f in ("w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
+                  "w4a16_selftest_wait_timeout",
                   "w4a16_layer_seq_create", "w4a16_layer_seq_run", "w4a16_layer_seq_run_host",
                   "w4a16_layer_seq_sync"):
             getattr(L, f).restype = i
@@ -164,6 +167,12 @@ def w4a16_device_status(clear: bool = True) -> int:
     if rc not in (0, 10):
         raise W4A16Error(rc, "w4a16_device_status")
     return int(flags.value)
+
+
+def w4a16_selftest_wait_timeout(limit_us: int = 20000, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (sets DEV_PIPE_TIMEOUT)."""
+    _check(lib().w4a16_selftest_wait_timeout(limit_us, _stream(stream)),
+           "w4a16_selftest_wait_timeout")
 
 
 class LayerSeq:

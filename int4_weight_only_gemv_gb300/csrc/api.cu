@@ -104,24 +104,14 @@ w4a16_status check_gemv(const uint32_t* qweight, const uint16_t* scales, const u
   return W4A16_OK;
 }
 
-// Enqueue one checked GEMV (M, N > 0).
-w4a16_status enqueue_gemv(const DeviceState& d, const uint32_t* qweight, const uint16_t* scales,
-                          const uint16_t* x, uint16_t* y, int M, int N, int K, int64_t ldx,
-                          cudaStream_t st) {
-  GemvArgs a;
-  a.qweight = qweight;
-  a.scales = scales;
-  a.x = x;
-  a.y = y;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.ldx = ldx;
+// Enqueue one checked GEMV (M, N > 0) whose output rows go to the segments
+// of `a` (pointers, sizes, strides and segments already filled in).
+w4a16_status enqueue(const DeviceState& d, GemvArgs a, cudaStream_t st) {
   a.status = d.status;
   cudaError_t e;
-  if (M == 1 && gemv_m1_supported(K))
+  if (a.M == 1 && gemv_m1_supported(a.K))
     e = launch_gemv_m1(a, d.info, st);
-  else if (M <= 7)
+  else if (a.M <= 7)
     e = launch_gemv_rows(a, d.info, st);
   else
     e = launch_gemv_mma(a, d.info, st);
@@ -130,6 +120,22 @@ w4a16_status enqueue_gemv(const DeviceState& d, const uint32_t* qweight, const u
     return W4A16_ERR_CUDA;
   }
   return W4A16_OK;
+}
+
+GemvArgs plain_args(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
+                    uint16_t* y, int M, int N, int K, int64_t ldx, int64_t ldy) {
+  GemvArgs a{};
+  a.qweight = qweight;
+  a.scales = scales;
+  a.x = x;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.ldx = ldx;
+  a.nseg = 1;
+  a.seg[0] = OutSeg{y, ldy, N};
+  a.pdl = false;
+  return a;
 }
 
 }  // namespace
@@ -165,7 +171,8 @@ w4a16_status w4a16_gemv(const uint32_t* qweight, const uint16_t* scales, const u
   if (M == 0 || N == 0) return W4A16_OK;
   DeviceState* d = nullptr;
   if ((s = device_state(&d)) != W4A16_OK) return s;
-  return enqueue_gemv(*d, qweight, scales, x, y, M, N, K, K, static_cast<cudaStream_t>(stream));
+  return enqueue(*d, plain_args(qweight, scales, x, y, M, N, K, K, N),
+                 static_cast<cudaStream_t>(stream));
 }
 
 w4a16_status w4a16_dequant(const uint32_t* qweight, const uint16_t* scales, uint16_t* w_out,
@@ -205,6 +212,19 @@ w4a16_status w4a16_quantize(const float* w, uint32_t* qweight, uint16_t* scales,
   if ((s = device_state(&d)) != W4A16_OK) return s;
   if (launch_quantize(w, qweight, scales, N, K, d->status, static_cast<cudaStream_t>(stream)) !=
       cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 0 || limit_us > 10000000) return W4A16_ERR_SHAPE;
+  DeviceState* d = nullptr;
+  w4a16_status s = device_state(&d);
+  if (s != W4A16_OK) return s;
+  if (launch_wait_timeout_selftest(static_cast<uint64_t>(limit_us) * 1000u, d->status,
+                                   static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return W4A16_ERR_CUDA;
   }
@@ -340,43 +360,59 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
     seq_free(s);
     return W4A16_ERR_CUDA;
   }
+  // Per layer: [q; k; v] as one launch when the three weights are stacked in
+  // one allocation (outputs still go to y_q, y_k, y_v), o, [gate; up] as one
+  // launch when stacked, down.  Every launch but the first of the graph is a
+  // programmatic dependent of its predecessor: it streams its (constant)
+  // weights while the previous GEMV finishes and waits for it before reading
+  // activations or writing outputs.
   w4a16_status cap = W4A16_OK;
   int launches = 0;
+  const size_t hw = static_cast<size_t>(hidden) / 8, hg = static_cast<size_t>(hidden) / W4A16_GROUP;
+  auto stacked = [&](const w4a16_layer_weights& w, int first, int second, int rows_first) {
+    return w.qweight[second] == w.qweight[first] + static_cast<size_t>(rows_first) * hw &&
+           w.scales[second] == w.scales[first] + static_cast<size_t>(rows_first) * hg;
+  };
+  auto launch = [&](GemvArgs a) {
+    if (cap != W4A16_OK) return;
+    a.pdl = launches > 0;
+    cap = enqueue(*d, a, s->capture_stream);
+    ++launches;
+  };
   for (int l = 0; l < n_layers && cap == W4A16_OK; ++l) {
     const w4a16_layer_weights& w = layers[l];
     const uint16_t* xl = io->x + l * Mh;
     uint16_t* yq = io->y_q + l * Mh;
+    uint16_t* yk = io->y_k + l * Mkv;
+    uint16_t* yv = io->y_v + l * Mkv;
     uint16_t* ygu = io->y_gu + l * Mgu;
-    auto run = [&](int pj, const uint16_t* x, uint16_t* y, int N, int K, int64_t ldx) {
-      if (cap != W4A16_OK) return;
-      cap = enqueue_gemv(*d, w.qweight[pj], w.scales[pj], x, y, M, N, K, ldx, s->capture_stream);
-      ++launches;
-    };
-    run(W4A16_Q, xl, yq, hidden, hidden, hidden);
-    run(W4A16_K, xl, io->y_k + l * Mkv, kv_dim, hidden, hidden);
-    run(W4A16_V, xl, io->y_v + l * Mkv, kv_dim, hidden, hidden);
-    run(W4A16_O, yq, io->y_o + l * Mh, hidden, hidden, hidden);
-    // [gate; up] as one N = 2 ffn GEMV writes exactly the y_gu rows [gate | up]
-    const bool fused = w.qweight[W4A16_UP] == w.qweight[W4A16_GATE] + static_cast<size_t>(ffn) * (hidden / 8) &&
-                       w.scales[W4A16_UP] == w.scales[W4A16_GATE] + static_cast<size_t>(ffn) * (hidden / W4A16_GROUP);
-    if (fused) {
-      run(W4A16_GATE, xl, ygu, 2 * ffn, hidden, hidden);
+    if (stacked(w, W4A16_Q, W4A16_K, hidden) && stacked(w, W4A16_K, W4A16_V, kv_dim)) {
+      GemvArgs a = plain_args(w.qweight[W4A16_Q], w.scales[W4A16_Q], xl, yq, M,
+                              hidden + 2 * kv_dim, hidden, hidden, hidden);
+      a.nseg = 3;
+      a.seg[0] = OutSeg{yq, hidden, hidden};
+      a.seg[1] = OutSeg{yk, kv_dim, static_cast<int64_t>(hidden) + kv_dim};
+      a.seg[2] = OutSeg{yv, kv_dim, static_cast<int64_t>(hidden) + 2 * kv_dim};
+      launch(a);
     } else {
-      // separate weights: each half of a y_gu row is strided by 2 ffn, so
-      // each activation row gets its own pair of M = 1 launches
-      for (int m = 0; m < M && cap == W4A16_OK; ++m) {
-        const uint16_t* xm = xl + static_cast<int64_t>(m) * hidden;
-        uint16_t* ym = ygu + static_cast<int64_t>(m) * 2 * ffn;
-        cap = enqueue_gemv(*d, w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xm, ym, 1, ffn, hidden,
-                           hidden, s->capture_stream);
-        ++launches;
-        if (cap != W4A16_OK) break;
-        cap = enqueue_gemv(*d, w.qweight[W4A16_UP], w.scales[W4A16_UP], xm, ym + ffn, 1, ffn, hidden,
-                           hidden, s->capture_stream);
-        ++launches;
-      }
+      launch(plain_args(w.qweight[W4A16_Q], w.scales[W4A16_Q], xl, yq, M, hidden, hidden, hidden, hidden));
+      launch(plain_args(w.qweight[W4A16_K], w.scales[W4A16_K], xl, yk, M, kv_dim, hidden, hidden, kv_dim));
+      launch(plain_args(w.qweight[W4A16_V], w.scales[W4A16_V], xl, yv, M, kv_dim, hidden, hidden, kv_dim));
     }
-    run(W4A16_DOWN, ygu, io->y_down + l * Mh, hidden, ffn, 2 * static_cast<int64_t>(ffn));
+    launch(plain_args(w.qweight[W4A16_O], w.scales[W4A16_O], yq, io->y_o + l * Mh, M, hidden,
+                      hidden, hidden, hidden));
+    // y_gu rows are [gate | up]: row stride 2 ffn
+    if (stacked(w, W4A16_GATE, W4A16_UP, ffn)) {
+      launch(plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, 2 * ffn, hidden,
+                        hidden, 2 * static_cast<int64_t>(ffn)));
+    } else {
+      launch(plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, ffn, hidden,
+                        hidden, 2 * static_cast<int64_t>(ffn)));
+      launch(plain_args(w.qweight[W4A16_UP], w.scales[W4A16_UP], xl, ygu + ffn, M, ffn, hidden,
+                        hidden, 2 * static_cast<int64_t>(ffn)));
+    }
+    launch(plain_args(w.qweight[W4A16_DOWN], w.scales[W4A16_DOWN], ygu, io->y_down + l * Mh, M,
+                      hidden, ffn, 2 * static_cast<int64_t>(ffn), hidden));
   }
   cudaGraph_t graph = nullptr;
   const cudaError_t ec = cudaStreamEndCapture(s->capture_stream, &graph);

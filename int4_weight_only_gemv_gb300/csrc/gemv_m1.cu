@@ -75,12 +75,8 @@ M1Plan make_m1_plan(int K, int smem_limit) {
 }
 
 struct M1Params {
-  const uint32_t* qweight;
-  const uint8_t* scales;  // bytes
-  const uint16_t* x;
-  uint16_t* y;
-  uint32_t* status;
-  int N, K;
+  GemvArgs a;             // pointers, sizes and output segments
+  const uint8_t* scales;  // a.scales as bytes
   int U, RL, T, pitch, stage_bytes, red_stride, S;
 };
 
@@ -108,9 +104,10 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_launch_dependents();
 
-  const int64_t N = p.N;
-  const int K = p.K;
+  const int64_t N = p.a.N;
+  const int K = p.a.K;
   const int64_t G = gridDim.x;
   const int64_t row_begin = (N * blockIdx.x) / G;
   const int64_t row_end = (N * (blockIdx.x + 1)) / G;
@@ -143,14 +140,17 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
       }
       __syncwarp();
       if (lane < nr)
-        bulk_g2s(smem_addr(base + lane * p.pitch), p.qweight + (r0 + lane) * (K / 8),
+        bulk_g2s(smem_addr(base + lane * p.pitch), p.a.qweight + (r0 + lane) * (K / 8),
                  static_cast<uint32_t>(row_bytes), bar, pol);
       if (lane == 31 && ecopy > a)
         bulk_g2s(smem_addr(scw), p.scales + a, static_cast<uint32_t>(ecopy - a), bar, pol);
     };
 
+    // the weights and scales are constant: stream them before the previous
+    // kernel has finished, wait for it only before the first write of y
     const int prolog = ntiles < S ? ntiles : S;
     for (int t = 0; t < prolog; ++t) issue(t);
+    pdl_wait();
 
     const int lpr = 32 / RL;  // reducer lanes per row
     const int my_row = lane / lpr;
@@ -166,15 +166,25 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
       const int64_t r0 = row_begin + static_cast<int64_t>(t) * RL;
       const int nr = static_cast<int>(row_end - r0 < RL ? row_end - r0 : RL);
       const float* rp = red + (static_cast<size_t>(s) * RL + my_row) * p.red_stride;
-      float sum = 0.f;
-      for (int u = part; u < p.U; u += lpr) sum += rp[u];
+      // four independent running sums so the shared loads overlap; the order
+      // of additions is fixed, so the result is the same on every run
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      int u = part;
+      for (; u + 3 * lpr < p.U; u += 4 * lpr) {
+        s0 += rp[u];
+        s1 += rp[u + lpr];
+        s2 += rp[u + 2 * lpr];
+        s3 += rp[u + 3 * lpr];
+      }
+      for (; u < p.U; u += lpr) s0 += rp[u];
+      float sum = (s0 + s1) + (s2 + s3);
       for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (part == 0 && my_row < nr) p.y[r0 + my_row] = __half_as_ushort(__float2half_rn(sum));
+      if (part == 0 && my_row < nr) *out_ptr(p.a, 0, r0 + my_row) = __half_as_ushort(__float2half_rn(sum));
       __syncwarp();
       if (t + S < ntiles) issue(t + S);
     }
     if (!ok) {
-      if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+      if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
       // let the copies already in flight land before the CTA exits
       for (int u = t; u < ntiles && u < t + S; ++u)
         mbar_wait_bounded(smem_addr(&full[u % S]), (u / S) & 1, kWaitLimitNs);
@@ -189,10 +199,12 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
   const int u = active ? c / RL : 0;
 
   // activations of this thread's 64 k, paired to match the unpacked lanes
+  // (x may be the previous kernel's output: wait for it first)
+  pdl_wait();
   XPairs X[8];
   float C = 0.f;
   {
-    const uint16_t* xp = p.x + u * 64;
+    const uint16_t* xp = p.a.x + u * 64;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint4 v = *reinterpret_cast<const uint4*>(xp + 8 * j);
@@ -206,7 +218,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % S;
     if (!mbar_wait_bounded(smem_addr(&full[s]), (t / S) & 1, kWaitLimitNs)) {
-      if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+      if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
       return;
     }
     const int64_t r0 = row_begin + static_cast<int64_t>(t) * RL;
@@ -251,13 +263,8 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   const M1Plan plan = make_m1_plan(a.K, d.max_smem_optin);
   if (plan.S < 2) return cudaErrorInvalidConfiguration;
   M1Params p;
-  p.qweight = a.qweight;
+  p.a = a;
   p.scales = reinterpret_cast<const uint8_t*>(a.scales);
-  p.x = a.x;
-  p.y = a.y;
-  p.status = a.status;
-  p.N = a.N;
-  p.K = a.K;
   p.U = plan.U;
   p.RL = plan.RL;
   p.T = plan.T;
@@ -265,9 +272,18 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   p.stage_bytes = plan.stage_bytes;
   p.red_stride = plan.red_stride;
   p.S = plan.S;
-  const int grid = a.N < d.sms ? a.N : d.sms;
-  const int threads = 32 + plan.CW * 32;
-  gemv_m1_kernel<<<grid, threads, plan.smem + 128, st>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.N < d.sms ? a.N : d.sms);
+  cfg.blockDim = dim3(32 + plan.CW * 32);
+  cfg.dynamicSmemBytes = plan.smem + 128;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_m1_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

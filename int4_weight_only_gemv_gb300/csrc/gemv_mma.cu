@@ -26,6 +26,10 @@
 // (deterministic, no atomics, no global workspace) and written as fp16.
 #include <cuda_fp16.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "w4a16.h"
@@ -88,6 +92,9 @@ __global__ void __launch_bounds__(kMmaMaxWarps * 32) gemv_mma_kernel(const MmaPa
   // one partial tile per warp [warps][16 rows][8 NT] f32
   uint4* xf = reinterpret_cast<uint4*>(smem);
   float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(p.max_groups) * NT * 4 * 32 * 16);
+
+  pdl_launch_dependents();
+  pdl_wait();  // x may be the previous kernel's output
 
   // ---- stage the activations of this K slice in fragment order
   {
@@ -194,12 +201,12 @@ __global__ void __launch_bounds__(kMmaMaxWarps * 32) gemv_mma_kernel(const MmaPa
       for (int nt = 0; nt < NT; ++nt) {
         const int m0 = nt * 8 + 2 * t4;
         if (ra < N) {
-          if (m0 < a.M) a.y[m0 * N + ra] = __half_as_ushort(__float2half_rn(acc[nt][0]));
-          if (m0 + 1 < a.M) a.y[(m0 + 1) * N + ra] = __half_as_ushort(__float2half_rn(acc[nt][1]));
+          if (m0 < a.M) *out_ptr(a, m0, ra) = __half_as_ushort(__float2half_rn(acc[nt][0]));
+          if (m0 + 1 < a.M) *out_ptr(a, m0 + 1, ra) = __half_as_ushort(__float2half_rn(acc[nt][1]));
         }
         if (rb < N) {
-          if (m0 < a.M) a.y[m0 * N + rb] = __half_as_ushort(__float2half_rn(acc[nt][2]));
-          if (m0 + 1 < a.M) a.y[(m0 + 1) * N + rb] = __half_as_ushort(__float2half_rn(acc[nt][3]));
+          if (m0 < a.M) *out_ptr(a, m0, rb) = __half_as_ushort(__float2half_rn(acc[nt][2]));
+          if (m0 + 1 < a.M) *out_ptr(a, m0 + 1, rb) = __half_as_ushort(__float2half_rn(acc[nt][3]));
         }
       }
     } else {
@@ -230,46 +237,86 @@ __global__ void __launch_bounds__(kMmaMaxWarps * 32) gemv_mma_kernel(const MmaPa
       const uint32_t addr = smem_addr(part + e);
       float v = 0.f;
       for (int q = 0; q < KS; ++q) v += ld_cluster_f32(map_to_rank(addr, q));
-      a.y[m * N + n] = __half_as_ushort(__float2half_rn(v));
+      *out_ptr(a, m, n) = __half_as_ushort(__float2half_rn(v));
     }
     cluster_sync();  // partials may be overwritten (next round) or freed (exit) only now
   }
   }  // rounds
 }
 
-MmaPlan make_mma_plan(const GemvArgs& a, const DeviceInfo& d, int NT) {
-  // Smallest power-of-two K split (cluster size) that gives each CTA at least
-  // 8 tiles (8 warps streaming) and fits one K slice of activations in shared
-  // memory; 8 if none does.
-  MmaPlan pl{};
+// How many clusters of `ks` CTAs (16 warps, `smem` bytes each) the GPU can
+// hold at once: clusters must fit inside one GPC, so large clusters can leave
+// SMs idle.  Cached, the query is not free.
+template <int NT>
+int max_active_clusters(int ks, int smem) {
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, int> cache;  // (device * 16 + ks, smem) -> clusters
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const std::pair<int, int> key(dev * 16 + ks, smem);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ks * 64);
+  cfg.blockDim = dim3(kMmaMaxWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemv_mma_kernel<NT>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = n;
+  return n;
+}
+
+// Choose the K split (cluster size) that keeps the most warps streaming: the
+// SMs the co-resident clusters cover, times the warps (tiles) per CTA, capped
+// at 12 warps (enough bytes in flight per SM).
+template <int NT>
+MmaPlan make_mma_plan(const GemvArgs& a, const DeviceInfo& d) {
+  MmaPlan best{};
+  int64_t best_score = -1;
   const int64_t T16 = (static_cast<int64_t>(a.N) + 15) / 16;
   const int NG = a.K / 128;
   const int smem_cap = d.max_smem_optin - 1024;
-  for (int ks = 1; ks <= 8; ks *= 2) {
-    const int clusters_fit = d.sms / ks;
-    const int64_t clusters = T16 < clusters_fit ? T16 : clusters_fit;
+  for (int ks = 1; ks <= 8 && ks <= NG; ks *= 2) {
+    const int max_groups = (NG + ks - 1) / ks;
+    const int smem = max_groups * NT * 4 * 32 * 16 + (ks > 1 ? kMmaMaxWarps * 16 * 8 * NT * 4 : 0);
+    if (smem > smem_cap) continue;
+    const int active = max_active_clusters<NT>(ks, smem);
+    if (active <= 0) continue;
+    const int64_t clusters = T16 < active ? T16 : active;
     const int64_t max_tiles = (T16 + clusters - 1) / clusters;
     const int warps = static_cast<int>(max_tiles < kMmaMaxWarps ? max_tiles : kMmaMaxWarps);
-    const int max_groups = (NG + ks - 1) / ks;
-    const int smem = max_groups * NT * 4 * 32 * 16 + (ks > 1 ? warps * 16 * 8 * NT * 4 : 0);
-    const bool fits = smem <= smem_cap;
-    const bool last = ks == 8 || ks * 2 > NG;
-    if (fits || last) {
-      pl.KS = ks;
-      pl.clusters = static_cast<int>(clusters);
-      pl.max_tiles = static_cast<int>(max_tiles);
-      pl.max_groups = max_groups;
-      pl.smem = smem;
-      pl.warps = warps;
+    const int64_t score = clusters * ks * (warps < 12 ? warps : 12);
+    if (score > best_score) {
+      best_score = score;
+      best.KS = ks;
+      best.clusters = static_cast<int>(clusters);
+      best.max_tiles = static_cast<int>(max_tiles);
+      best.max_groups = max_groups;
+      best.smem = smem;
+      best.warps = warps;
     }
-    if ((fits && warps >= 8) || last) break;
   }
-  return pl;
+  return best;
 }
 
 template <int NT>
 cudaError_t launch_mma_nt(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
-  const MmaPlan pl = make_mma_plan(a, d, NT);
+  const MmaPlan pl = make_mma_plan<NT>(a, d);
+  if (pl.KS == 0) return cudaErrorInvalidConfiguration;
   MmaParams p;
   p.a = a;
   p.KS = pl.KS;
@@ -280,13 +327,15 @@ cudaError_t launch_mma_nt(const GemvArgs& a, const DeviceInfo& d, cudaStream_t s
   cfg.blockDim = dim3(pl.warps * 32);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = pl.KS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<NT>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -33,6 +33,8 @@ struct RowsCfg {
 template <int M>
 __global__ void __launch_bounds__(kRowsThreads) gemv_rows_kernel(const GemvArgs a) {
   constexpr int R = RowsCfg<M>::R;
+  pdl_launch_dependents();
+  pdl_wait();  // x may be the previous kernel's output
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * kRowsThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kRowsThreads) >> 5;
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(kRowsThreads) gemv_rows_kernel(const GemvArgs 
         if (r0 + r < N)
 #pragma unroll
           for (int m = 0; m < M; ++m)
-            a.y[m * N + r0 + r] = __half_as_ushort(__float2half_rn(acc[r][m]));
+            *out_ptr(a, m, r0 + r) = __half_as_ushort(__float2half_rn(acc[r][m]));
     }
   }
 }
@@ -135,7 +137,17 @@ cudaError_t launch_rows_m(const GemvArgs& a, const DeviceInfo& d, cudaStream_t s
   int64_t grid = (nblocks + warps_per_cta - 1) / warps_per_cta;
   const int64_t cap = static_cast<int64_t>(d.sms) * 8;
   if (grid > cap) grid = cap;
-  gemv_rows_kernel<M><<<static_cast<int>(grid), kRowsThreads, 0, st>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kRowsThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows_kernel<M>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

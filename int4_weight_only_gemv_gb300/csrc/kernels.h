@@ -7,16 +7,48 @@
 
 namespace w4a16 {
 
+// Where output row n of activation row m goes.  A GEMV over a weight made of
+// up to three stacked matrices (e.g. [W_q; W_k; W_v]) can write each part to
+// its own buffer: rows [n_begin(s), n_end(s)) go to seg[s].y with row stride
+// seg[s].ldy (elements), n_begin(0) = 0, n_begin(s) = seg[s-1].n_end.
+struct OutSeg {
+  uint16_t* y;
+  int64_t ldy;
+  int64_t n_end;
+};
+constexpr int kMaxSegs = 3;
+
 // One GEMV: y[m][n] = sum_k x[m*ldx + k] * q[n][k] * s[n][k/128].
 struct GemvArgs {
   const uint32_t* qweight;  // [N][K/8]
   const uint16_t* scales;   // [N][K/128] fp16 bits
   const uint16_t* x;        // [M][ldx] fp16 bits (first K used per row)
-  uint16_t* y;              // [M][N] fp16 bits
   int M, N, K;
   int64_t ldx;              // row stride of x in elements (K for a dense x)
+  int nseg;                 // 1..kMaxSegs
+  OutSeg seg[kMaxSegs];
   uint32_t* status;         // device status word (W4A16_DEV_* bits)
+  // Programmatic dependent launch: the kernel may start while the previous
+  // kernel on the stream is still running; it reads only the (constant)
+  // weights and scales before waiting for that kernel to finish.
+  bool pdl;
 };
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint16_t* out_ptr(const GemvArgs& a, int m, int64_t n) {
+  int s = 0;
+  int64_t n0 = 0;
+  if (a.nseg > 1 && n >= a.seg[0].n_end) {
+    n0 = a.seg[0].n_end;
+    s = 1;
+    if (a.nseg > 2 && n >= a.seg[1].n_end) {
+      n0 = a.seg[1].n_end;
+      s = 2;
+    }
+  }
+  return a.seg[s].y + m * a.seg[s].ldy + (n - n0);
+}
+#endif
 
 // Device facts the launchers size their grids with.
 struct DeviceInfo {
@@ -37,6 +69,9 @@ cudaError_t launch_dequant(const uint32_t* qweight, const uint16_t* scales, uint
                            int N, int K, cudaStream_t st);
 cudaError_t launch_quantize(const float* w, uint32_t* qweight, uint16_t* scales, int N, int K,
                             uint32_t* status, cudaStream_t st);
+
+// One thread waits (bounded by limit_ns) on an mbarrier nothing arrives on.
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, uint32_t* status, cudaStream_t st);
 
 // Set per-device function attributes (dynamic shared memory opt-in); each
 // must run once per device before the first launch and outside stream capture.

@@ -84,6 +84,16 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Let the next kernel on the stream launch (it still waits for this one to
+// finish before touching anything this one writes).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the previous kernel on the stream has completed and its writes
+// are visible.  A no-op when the kernel was not launched as a dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -15,6 +15,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 #include "w4a16.h"
 
 namespace w4a16 {
@@ -137,6 +138,29 @@ cudaError_t launch_dequant(const uint32_t* qweight, const uint16_t* scales, uint
   const int64_t blocks = (words + kQuantThreads - 1) / kQuantThreads;
   dequant_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, st>>>(qweight, scales, w_out,
                                                                           words, K);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16
+
+namespace w4a16 {
+namespace {
+
+// Self-test of the bounded wait used by the pipelined kernels: one thread
+// waits on an mbarrier that nothing ever arrives on.  The wait gives up after
+// limit_ns, records W4A16_DEV_PIPE_TIMEOUT and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  mbar_init(b, 1);
+  fence_barrier_init();
+  if (!mbar_wait_bounded(b, 0, limit_ns)) atomicOr(status, W4A16_DEV_PIPE_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, uint32_t* status, cudaStream_t st) {
+  wait_timeout_selftest_kernel<<<1, 1, 0, st>>>(limit_ns, status);
   return cudaGetLastError();
 }
 

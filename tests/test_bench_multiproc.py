@@ -37,8 +37,8 @@ def test_max_over_ranks_gloo_world2():
 
 def test_aggregate_is_whole_job():
     b = bench.config_block()["bytes_per_step"]
-    # 7 projections x 28 layers with gate and up fused into one launch (x read once)
-    assert b == 3369447424
+    # 7 projections x 28 layers, [q; k; v] and [gate; up] one launch each (x read once)
+    assert b == 3369046016
     one = bench.aggregate_gbps(b, 0.5, 1)
     assert bench.aggregate_gbps(b, 0.5, 2) == pytest.approx(2 * one)
     assert one == pytest.approx(b / 0.5e-3 / 1e9)
@@ -47,9 +47,9 @@ def test_aggregate_is_whole_job():
 
 def test_workload_matches_the_decode_step():
     g = bench.workload_gemvs()
-    assert len(g) == 28 * 6
-    names = [n for n, *_ in g[:6]]
-    assert names == ["q", "k", "v", "o", "gate_up", "down"]
+    assert len(g) == 28 * 4
+    names = [n for n, *_ in g[:4]]
+    assert names == ["qkv", "o", "gate_up", "down"]
     # per-GEMV byte counts of the shapes
     assert bench.gemv_bytes(512, 1024, 1) == 273408
     assert bench.gemv_bytes(3584, 3584, 1) == 6637568

@@ -223,3 +223,14 @@ def test_gemv_rejects_bad_args_on_gpu():
         w4.w4a16_gemv(c.qw, c.sc, c.x_dev, torch.empty(64 * 2 + 1, dtype=torch.float16, device=DEV)[1:].view(1, 128)[:, :64])
     with pytest.raises(w4.W4A16Error, match="ALIAS"):
         w4.w4a16_gemv(c.qw, c.sc, c.x_dev, c.x_dev.view(1, 256)[:, :64])
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait on a barrier nothing arrives on gives up after its bound, sets
+    DEV_PIPE_TIMEOUT, and the device keeps working."""
+    assert w4.w4a16_device_status(clear=True) == 0
+    w4.w4a16_selftest_wait_timeout(20000)
+    assert w4.w4a16_device_status(clear=True) == w4.DEV_PIPE_TIMEOUT
+    c = Case(256, 1024, 1, seed=2)
+    assert c.check(c.gemv())["ok"]
+    assert w4.w4a16_device_status(clear=True) == 0
