@@ -35,38 +35,41 @@ namespace {
 constexpr int kM1MaxThreads = 640;  // 20 warps -> the compiler may use up to 102 registers
 constexpr int kM1MaxStages = 16;
 constexpr int kM1SmemBudget = 200 * 1024;
+constexpr int kRR = 2;  // rows per consumer thread per tile (independent chains)
 
 struct M1Plan {
   int U;            // units (64 k) per row
-  int RL;           // rows per tile (rows across lanes)
+  int RL;           // rows across lanes
+  int RB;           // rows per tile = RL * kRR
   int T;            // consumer threads = U * RL
   int CW;           // consumer warps
   int pitch;        // shared-memory row pitch, bytes
   int sc_cap;       // bytes of the per-stage scale window
-  int stage_bytes;  // RL * pitch + sc_cap
+  int stage_bytes;  // RB * pitch + sc_cap
   int red_stride;   // floats per row in the partial buffer (U + 1: odd stride)
   int S;            // pipeline stages
   int smem;         // dynamic shared memory, bytes
 };
 
-__host__ __device__ inline int m1_rows_per_tile(int U) {
-  // Rows across lanes, chosen so that a warp covers (32 / RL) whole units of
-  // RL rows and every shared-memory read of a stage is bank-conflict free
-  // with a row pitch of K/2 + 16 bytes (pitch / 16 odd).
+__host__ __device__ inline int m1_rows_across_lanes(int U) {
+  // A warp covers (32 / RL) whole units of RL rows; with a row pitch of
+  // K/2 + 16 bytes (pitch / 16 odd) every 16-byte shared read of a stage is
+  // bank-conflict free for these RL.
   return U > 64 ? 2 : (U > 16 ? 8 : (U > 4 ? 16 : 32));
 }
 
 M1Plan make_m1_plan(int K, int smem_limit) {
   M1Plan p{};
   p.U = K / 64;
-  p.RL = m1_rows_per_tile(p.U);
+  p.RL = m1_rows_across_lanes(p.U);
+  p.RB = p.RL * kRR;
   p.T = p.U * p.RL;
   p.CW = (p.T + 31) / 32;
   p.pitch = K / 2 + 16;
-  p.sc_cap = ((p.RL * (K / 64) + 32) + 15) & ~15;
-  p.stage_bytes = p.RL * p.pitch + p.sc_cap;
+  p.sc_cap = ((p.RB * (K / 64) + 32) + 15) & ~15;
+  p.stage_bytes = p.RB * p.pitch + p.sc_cap;
   p.red_stride = p.U + 1;
-  const int per_stage = p.stage_bytes + p.RL * p.red_stride * 4;
+  const int per_stage = p.stage_bytes + p.RB * p.red_stride * 4;
   const int budget = (smem_limit < kM1SmemBudget ? smem_limit : kM1SmemBudget) - 512;
   p.S = budget / per_stage;
   if (p.S > kM1MaxStages) p.S = kM1MaxStages;
@@ -77,18 +80,19 @@ M1Plan make_m1_plan(int K, int smem_limit) {
 struct M1Params {
   GemvArgs a;             // pointers, sizes and output segments
   const uint8_t* scales;  // a.scales as bytes
-  int U, RL, T, pitch, stage_bytes, red_stride, S;
+  int U, RL, RB, T, pitch, stage_bytes, red_stride, S;
 };
 
 __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = p.S;
   const int RL = p.RL;
-  // layout: [full S][cons S] barriers | partials S*RL*red_stride f32 | stages
+  const int RB = p.RB;
+  // layout: [full S][cons S] barriers | partials S*RB*red_stride f32 | stages
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* cons = full + S;
   float* red = reinterpret_cast<float*>(smem + 512);
-  uint8_t* stages = smem + 512 + S * RL * p.red_stride * 4;
+  uint8_t* stages = smem + 512 + S * RB * p.red_stride * 4;
   stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(stages) + 127) & ~uintptr_t(127));
 
   const int tid = threadIdx.x;
@@ -110,27 +114,32 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
   const int K = p.a.K;
   const int64_t G = gridDim.x;
   const int64_t row_begin = (N * blockIdx.x) / G;
-  const int64_t row_end = (N * (blockIdx.x + 1)) / G;
-  const int ntiles = static_cast<int>((row_end - row_begin + RL - 1) / RL);
-  const int64_t row_bytes = K / 2;          // packed bytes per row
-  const int64_t sc_row_bytes = K / 64;      // scale bytes per row
-  const int64_t sc_total = N * sc_row_bytes;
+  const int rows = static_cast<int>((N * (blockIdx.x + 1)) / G - row_begin);  // rows of this CTA
+  const int ntiles = (rows + RB - 1) / RB;
+  const int row_bytes = K / 2;      // packed bytes per row
+  const int sc_row_bytes = K / 64;  // scale bytes per row
+  // scale bytes are addressed relative to the first row of this CTA; only the
+  // alignment of the absolute offset matters, and that is its low 4 bits
+  const int64_t sc_cta = row_begin * sc_row_bytes;
+  const int sc_cta_lo = static_cast<int>(sc_cta & 15);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int t) {
-      const int s = t % S;
-      const int64_t r0 = row_begin + static_cast<int64_t>(t) * RL;
-      const int nr = static_cast<int>(row_end - r0 < RL ? row_end - r0 : RL);
-      const int64_t sb0 = r0 * sc_row_bytes;
-      const int64_t sb1 = (r0 + nr) * sc_row_bytes;
+    const int64_t sc_total = N * sc_row_bytes;
+    const uint32_t* qrows = p.a.qweight + row_begin * (K / 8);
+    // issue tile t into stage s
+    auto issue = [&](int t, int s) {
+      const int lr0 = t * RB;
+      const int nr = rows - lr0 < RB ? rows - lr0 : RB;
+      const int64_t sb0 = sc_cta + static_cast<int64_t>(lr0) * sc_row_bytes;
+      const int64_t sb1 = sb0 + static_cast<int64_t>(nr) * sc_row_bytes;
       const int64_t a = sb0 & ~int64_t(15);
       int64_t e = (sb1 + 15) & ~int64_t(15);
       if (e > sc_total) e = sc_total & ~int64_t(15);  // never read past the buffer
       const int64_t ecopy = e > a ? e : a;
-      uint8_t* base = stages + static_cast<size_t>(s) * p.stage_bytes;
-      uint8_t* scw = base + RL * p.pitch;
+      uint8_t* base = stages + s * p.stage_bytes;
+      uint8_t* scw = base + RB * p.pitch;
       const uint32_t bar = smem_addr(&full[s]);
       if (lane == 0) {
         // the last few scale bytes of the matrix, if the aligned copy stops short
@@ -139,8 +148,8 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * row_bytes + (ecopy - a)));
       }
       __syncwarp();
-      if (lane < nr)
-        bulk_g2s(smem_addr(base + lane * p.pitch), p.a.qweight + (r0 + lane) * (K / 8),
+      for (int r = lane; r < nr; r += 32)
+        bulk_g2s(smem_addr(base + r * p.pitch), qrows + static_cast<int64_t>(lr0 + r) * (K / 8),
                  static_cast<uint32_t>(row_bytes), bar, pol);
       if (lane == 31 && ecopy > a)
         bulk_g2s(smem_addr(scw), p.scales + a, static_cast<uint32_t>(ecopy - a), bar, pol);
@@ -149,45 +158,53 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
     // the weights and scales are constant: stream them before the previous
     // kernel has finished, wait for it only before the first write of y
     const int prolog = ntiles < S ? ntiles : S;
-    for (int t = 0; t < prolog; ++t) issue(t);
+    for (int t = 0; t < prolog; ++t) issue(t, t);
     pdl_wait();
 
-    const int lpr = 32 / RL;  // reducer lanes per row
-    const int my_row = lane / lpr;
+    const int lpr = RB >= 32 ? 1 : 32 / RB;  // reducer lanes per row
+    const int rows_per_pass = 32 / lpr;
     const int part = lane % lpr;
     bool ok = true;
-    int t = 0;
+    int t = 0, s = 0;
+    uint32_t phase = 0;
     for (; t < ntiles; ++t) {
-      const int s = t % S;
-      if (!mbar_wait_bounded(smem_addr(&cons[s]), (t / S) & 1, kWaitLimitNs)) {
+      if (!mbar_wait_bounded(smem_addr(&cons[s]), phase, kWaitLimitNs)) {
         ok = false;
         break;
       }
-      const int64_t r0 = row_begin + static_cast<int64_t>(t) * RL;
-      const int nr = static_cast<int>(row_end - r0 < RL ? row_end - r0 : RL);
-      const float* rp = red + (static_cast<size_t>(s) * RL + my_row) * p.red_stride;
-      // four independent running sums so the shared loads overlap; the order
-      // of additions is fixed, so the result is the same on every run
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      int u = part;
-      for (; u + 3 * lpr < p.U; u += 4 * lpr) {
-        s0 += rp[u];
-        s1 += rp[u + lpr];
-        s2 += rp[u + 2 * lpr];
-        s3 += rp[u + 3 * lpr];
+      const int lr0 = t * RB;
+      const int nr = rows - lr0 < RB ? rows - lr0 : RB;
+      const float* rs = red + s * RB * p.red_stride;
+      for (int row = lane / lpr; row < RB; row += rows_per_pass) {
+        const float* rp = rs + row * p.red_stride;
+        // four independent running sums so the shared loads overlap; the
+        // order of additions is fixed, so every run gives the same bits
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int u = part;
+        for (; u + 3 * lpr < p.U; u += 4 * lpr) {
+          s0 += rp[u];
+          s1 += rp[u + lpr];
+          s2 += rp[u + 2 * lpr];
+          s3 += rp[u + 3 * lpr];
+        }
+        for (; u < p.U; u += lpr) s0 += rp[u];
+        float sum = (s0 + s1) + (s2 + s3);
+        for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (part == 0 && row < nr)
+          *out_ptr(p.a, 0, row_begin + lr0 + row) = __half_as_ushort(__float2half_rn(sum));
       }
-      for (; u < p.U; u += lpr) s0 += rp[u];
-      float sum = (s0 + s1) + (s2 + s3);
-      for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (part == 0 && my_row < nr) *out_ptr(p.a, 0, r0 + my_row) = __half_as_ushort(__float2half_rn(sum));
       __syncwarp();
-      if (t + S < ntiles) issue(t + S);
+      if (t + S < ntiles) issue(t + S, s);
+      if (++s == S) {
+        s = 0;
+        phase ^= 1u;
+      }
     }
     if (!ok) {
       if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
       // let the copies already in flight land before the CTA exits
-      for (int u = t; u < ntiles && u < t + S; ++u)
-        mbar_wait_bounded(smem_addr(&full[u % S]), (u / S) & 1, kWaitLimitNs);
+      for (int v = t; v < ntiles && v < t + S; ++v)
+        mbar_wait_bounded(smem_addr(&full[v % S]), (v / S) & 1, kWaitLimitNs);
     }
     return;
   }
@@ -215,38 +232,66 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
     }
   }
 
+  // per-thread offsets inside a stage (32-bit, fixed for the whole kernel)
+  const int w_off0 = rl * p.pitch + u * 32;             // row rl
+  const int w_off1 = (rl + RL) * p.pitch + u * 32;      // row rl + RL
+  const int sc_off0 = RB * p.pitch + rl * sc_row_bytes + (u >> 1) * 2;
+  const int sc_off1 = sc_off0 + RL * sc_row_bytes;
+  const int red_off0 = rl * p.red_stride + u;
+  const int red_off1 = (rl + RL) * p.red_stride + u;
+  const int sc_tile_step = RB * sc_row_bytes;
+  int sc_lo = sc_cta_lo;  // low 4 bits of the absolute scale offset of the tile
+
+  int s = 0;
+  uint32_t phase = 0;
   for (int t = 0; t < ntiles; ++t) {
-    const int s = t % S;
-    if (!mbar_wait_bounded(smem_addr(&full[s]), (t / S) & 1, kWaitLimitNs)) {
+    if (!mbar_wait_bounded(smem_addr(&full[s]), phase, kWaitLimitNs)) {
       if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
       return;
     }
-    const int64_t r0 = row_begin + static_cast<int64_t>(t) * RL;
-    const int nr = static_cast<int>(row_end - r0 < RL ? row_end - r0 : RL);
-    if (active && rl < nr) {
-      const uint8_t* base = stages + static_cast<size_t>(s) * p.stage_bytes;
-      const uint4* wp = reinterpret_cast<const uint4*>(base + rl * p.pitch + u * 32);
-      const uint4 w0 = wp[0];
-      const uint4 w1 = wp[1];
-      const int64_t a = (r0 * (K / 64)) & ~int64_t(15);
-      const uint8_t* scw = base + RL * p.pitch;
-      const int64_t sb = (r0 + rl) * (K / 64) + (u >> 1) * 2 - a;
-      const float sc = __half2float(*reinterpret_cast<const __half*>(scw + sb));
-      float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;
-      const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const int nr = rows - t * RB;  // rows of this tile (may exceed RB)
+    const uint8_t* base = stages + s * p.stage_bytes;
+    float* rs = red + s * RB * p.red_stride;
+    if (active) {
+      const bool v1 = rl + RL < nr;
+      if (rl < nr) {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(base + w_off0);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(base + w_off0 + 16);
+        uint4 b0 = make_uint4(0u, 0u, 0u, 0u), b1 = b0;
+        if (v1) {
+          b0 = *reinterpret_cast<const uint4*>(base + w_off1);
+          b1 = *reinterpret_cast<const uint4*>(base + w_off1 + 16);
+        }
+        const float sa = __half2float(*reinterpret_cast<const __half*>(base + sc_off0 + sc_lo));
+        const float sb = v1 ? __half2float(*reinterpret_cast<const __half*>(base + sc_off1 + sc_lo)) : 0.f;
+        float ea0 = 0.f, ea1 = 0.f, oa0 = 0.f, oa1 = 0.f;
+        float eb0 = 0.f, eb1 = 0.f, ob0 = 0.f, ob1 = 0.f;
+        const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const Unpacked h = unpack_biased(words[j]);
-        fma_f32_f16x2(e0, e1, h.h0, X[j].p0);
-        fma_f32_f16x2(o0, o1, h.h1, X[j].p1);
-        fma_f32_f16x2(e0, e1, h.h2, X[j].p2);
-        fma_f32_f16x2(o0, o1, h.h3, X[j].p3);
+        for (int j = 0; j < 8; ++j) {
+          const Unpacked ha = unpack_biased(wa[j]);
+          const Unpacked hb = unpack_biased(wb[j]);
+          fma_f32_f16x2(ea0, ea1, ha.h0, X[j].p0);
+          fma_f32_f16x2(eb0, eb1, hb.h0, X[j].p0);
+          fma_f32_f16x2(oa0, oa1, ha.h1, X[j].p1);
+          fma_f32_f16x2(ob0, ob1, hb.h1, X[j].p1);
+          fma_f32_f16x2(ea0, ea1, ha.h2, X[j].p2);
+          fma_f32_f16x2(eb0, eb1, hb.h2, X[j].p2);
+          fma_f32_f16x2(oa0, oa1, ha.h3, X[j].p3);
+          fma_f32_f16x2(ob0, ob1, hb.h3, X[j].p3);
+        }
+        rs[red_off0] = (fmaf(0.0625f, oa0 + oa1, ea0 + ea1) - C) * sa;
+        if (v1) rs[red_off1] = (fmaf(0.0625f, ob0 + ob1, eb0 + eb1) - C) * sb;
       }
-      const float dot = fmaf(0.0625f, o0 + o1, e0 + e1) - C;
-      red[(static_cast<size_t>(s) * RL + rl) * p.red_stride + u] = dot * sc;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&cons[s]));
+    sc_lo = (sc_lo + sc_tile_step) & 15;
+    if (++s == S) {
+      s = 0;
+      phase ^= 1u;
+    }
   }
 }
 
@@ -255,7 +300,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
 bool gemv_m1_supported(int K) {
   if (K <= 0 || K % 128 != 0) return false;
   const int U = K / 64;
-  const int T = U * m1_rows_per_tile(U);
+  const int T = U * m1_rows_across_lanes(U);
   return T + 32 <= kM1MaxThreads;
 }
 
@@ -267,6 +312,7 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   p.scales = reinterpret_cast<const uint8_t*>(a.scales);
   p.U = plan.U;
   p.RL = plan.RL;
+  p.RB = plan.RB;
   p.T = plan.T;
   p.pitch = plan.pitch;
   p.stage_bytes = plan.stage_bytes;

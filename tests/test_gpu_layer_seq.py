@@ -55,6 +55,13 @@ def _layer_weights(layer, fused=True, cpu=False, qkv=False):
     return out, (w_cpu if cpu else None)
 
 
+def _adjacent(first, second):
+    """True when `second`'s packed weight and scales directly follow `first`'s."""
+    (qa, sa), (qb, sb) = first, second
+    return (qb.data_ptr() == qa.data_ptr() + qa.numel() * 4
+            and sb.data_ptr() == sa.data_ptr() + sa.numel() * 2)
+
+
 def _io(M, n_layers):
     x = torch.cat([synth.activations(M, H, synth.layer_seed(l, 7)) for l in range(n_layers)])
     io = {"x": x.view(n_layers, M, H).to(DEV)}
@@ -178,7 +185,15 @@ def test_layer_seq_small(M, fused, qkv):
     layers = [_layer_weights(l, fused=fused, qkv=qkv)[0] for l in range(n)]
     io = _io(M, n)
     seq = w4.LayerSeq(layers, io, M, H, KV, F)
-    expect_launches = n * ((1 if qkv else 3) + 1 + (1 if fused else 2) + 1)
+    # separately allocated weights may still land back to back in memory, in
+    # which case the library launches them as one stack: count what is adjacent
+    expect_launches = 0
+    for lw in layers:
+        q_k = _adjacent(lw["q"], lw["k"]) and _adjacent(lw["k"], lw["v"])
+        g_u = _adjacent(lw["gate"], lw["up"])
+        expect_launches += (1 if q_k else 3) + 1 + (1 if g_u else 2) + 1
+        assert q_k or not qkv
+        assert g_u or not fused
     assert seq.num_launches == expect_launches
     seq.run()
     assert seq.sync() == 0
