@@ -7,16 +7,19 @@
 // the group-128 symmetric format of the same section's last paragraph.
 //
 // Design (one CTA per SM, one pass over the weight stream):
-//   warp 0      producer + reducer.  Streams tiles of RB consecutive rows into
-//               an S-stage shared-memory ring with 1-D bulk copies (one copy
-//               per row into a padded row slot, one copy for the tile's
-//               scale window), completing on a per-stage mbarrier.  After the
-//               consumers release a stage it sums their per-unit partials of
-//               that tile in a fixed order, writes y, and refills the stage.
-//   warps 1..   consumers.  Consumer thread c owns unit u = c / RL (64
-//               consecutive k, half a group) of row c % RL of every tile, so
-//               its 64 activations stay in registers for the whole kernel and
-//               no activation traffic touches shared memory.  Per packed word
+//   warp 0      producer.  Streams tiles of RB consecutive rows into an
+//               S-stage shared-memory ring with 1-D bulk copies (the tile's
+//               rows are contiguous in memory: one copy, plus one for the
+//               tile's scale window), completing on a per-stage mbarrier, and
+//               refills a stage as soon as the consumers hold its tile in
+//               registers.
+//   warp 1      reducer.  Sums the consumers' per-unit partials of each tile
+//               in a fixed order and writes y.
+//   warps 1..   consumers.  Consumer thread c owns unit u = c mod U (64
+//               consecutive k, half a group) of rows c / U + r RL (r < kRR)
+//               of every tile, so its 64 activations stay in registers for
+//               the whole kernel and no activation traffic touches shared
+//               memory.  Per packed word
 //               it does one shift, four LOP3s (nibble -> biased fp16, see
 //               ptx.cuh) and eight f16 x f16 -> f32 FMAs; the biases 1032 and
 //               72 are removed once per unit with the precomputed sum
@@ -32,7 +35,7 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kM1MaxThreads = 640;  // 20 warps -> the compiler may use up to 102 registers
+constexpr int kM1MaxThreads = 672;  // 21 warps -> the compiler may use up to 96 registers
 constexpr int kM1MaxStages = 16;
 constexpr int kM1SmemBudget = 200 * 1024;
 constexpr int kRR = 2;  // rows per consumer thread per tile (independent chains)
@@ -52,9 +55,7 @@ struct M1Plan {
 };
 
 __host__ __device__ inline int m1_rows_across_lanes(int U) {
-  // A warp covers (32 / RL) whole units of RL rows; with a row pitch of
-  // K/2 + 16 bytes (pitch / 16 odd) every 16-byte shared read of a stage is
-  // bank-conflict free for these RL.
+  // consumer threads = U * RL: about 450-600 threads for every K
   return U > 64 ? 2 : (U > 16 ? 8 : (U > 4 ? 16 : 32));
 }
 
@@ -65,7 +66,7 @@ M1Plan make_m1_plan(int K, int smem_limit) {
   p.RB = p.RL * kRR;
   p.T = p.U * p.RL;
   p.CW = (p.T + 31) / 32;
-  p.pitch = K / 2 + 16;
+  p.pitch = K / 2;  // rows stored densely: a tile is one contiguous bulk copy
   p.sc_cap = ((p.RB * (K / 64) + 32) + 15) & ~15;
   p.stage_bytes = p.RB * p.pitch + p.sc_cap;
   p.red_stride = p.U + 1;
@@ -88,12 +89,20 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
   const int S = p.S;
   const int RL = p.RL;
   const int RB = p.RB;
-  // layout: [full S][cons S] barriers | partials S*RB*red_stride f32 | stages
+  // layout: barriers [full S][empty S][redfull S][redempty S] | partials
+  // S*RB*red_stride f32 | stages.  All hot accesses use 32-bit shared
+  // addresses (explicit ld/st.shared).
+  //   full[s]      producer -> consumers: the tile's bytes landed (tx count)
+  //   empty[s]     consumers -> producer: the tile is in registers, refill
+  //   redfull[s]   consumers -> reducer: the tile's partial sums are written
+  //   redempty[s]  reducer -> consumers: partial slot s may be rewritten
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* cons = full + S;
-  float* red = reinterpret_cast<float*>(smem + 512);
-  uint8_t* stages = smem + 512 + S * RB * p.red_stride * 4;
-  stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(stages) + 127) & ~uintptr_t(127));
+  uint64_t* empty = full + S;
+  uint64_t* redfull = empty + S;
+  uint64_t* redempty = redfull + S;
+  const uint32_t smem0 = smem_addr(smem);
+  const uint32_t red0 = smem0 + 512;
+  const uint32_t stage0 = (red0 + S * RB * p.red_stride * 4 + 127) & ~127u;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -103,7 +112,9 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
-      mbar_init(smem_addr(&cons[s]), CW);
+      mbar_init(smem_addr(&empty[s]), CW);
+      mbar_init(smem_addr(&redfull[s]), CW);
+      mbar_init(smem_addr(&redempty[s]), 1);
     }
     fence_barrier_init();
   }
@@ -138,63 +149,39 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
       int64_t e = (sb1 + 15) & ~int64_t(15);
       if (e > sc_total) e = sc_total & ~int64_t(15);  // never read past the buffer
       const int64_t ecopy = e > a ? e : a;
-      uint8_t* base = stages + s * p.stage_bytes;
-      uint8_t* scw = base + RB * p.pitch;
+      const uint32_t base = stage0 + s * p.stage_bytes;
+      const uint32_t scw = base + RB * p.pitch;
       const uint32_t bar = smem_addr(&full[s]);
       if (lane == 0) {
         // the last few scale bytes of the matrix, if the aligned copy stops short
         for (int64_t b = ecopy; b < sb1; b += 2)
-          *reinterpret_cast<uint16_t*>(scw + (b - a)) = ld_nc_u16(p.scales + b);
+          sts_u16(scw + static_cast<uint32_t>(b - a), ld_nc_u16(p.scales + b));
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * row_bytes + (ecopy - a)));
       }
       __syncwarp();
-      for (int r = lane; r < nr; r += 32)
-        bulk_g2s(smem_addr(base + r * p.pitch), qrows + static_cast<int64_t>(lr0 + r) * (K / 8),
-                 static_cast<uint32_t>(row_bytes), bar, pol);
-      if (lane == 31 && ecopy > a)
-        bulk_g2s(smem_addr(scw), p.scales + a, static_cast<uint32_t>(ecopy - a), bar, pol);
+      // consecutive rows are contiguous in memory: one copy for the whole tile
+      if (lane == 0)
+        bulk_g2s(base, qrows + static_cast<int64_t>(lr0) * (K / 8),
+                 static_cast<uint32_t>(nr * row_bytes), bar, pol);
+      if (lane == 1 && ecopy > a)
+        bulk_g2s(scw, p.scales + a, static_cast<uint32_t>(ecopy - a), bar, pol);
     };
 
-    // the weights and scales are constant: stream them before the previous
-    // kernel has finished, wait for it only before the first write of y
+    // the weights and scales are constant: stream them without waiting for
+    // the previous kernel on the stream
     const int prolog = ntiles < S ? ntiles : S;
     for (int t = 0; t < prolog; ++t) issue(t, t);
-    pdl_wait();
-
-    const int lpr = RB >= 32 ? 1 : 32 / RB;  // reducer lanes per row
-    const int rows_per_pass = 32 / lpr;
-    const int part = lane % lpr;
-    bool ok = true;
-    int t = 0, s = 0;
+    // then refill each stage as soon as the consumers hold its tile in registers
+    int s = 0;
     uint32_t phase = 0;
+    int t = S;
+    bool ok = true;
     for (; t < ntiles; ++t) {
-      if (!mbar_wait_bounded(smem_addr(&cons[s]), phase, kWaitLimitNs)) {
+      if (!mbar_wait_bounded(smem_addr(&empty[s]), phase, kWaitLimitNs)) {
         ok = false;
         break;
       }
-      const int lr0 = t * RB;
-      const int nr = rows - lr0 < RB ? rows - lr0 : RB;
-      const float* rs = red + s * RB * p.red_stride;
-      for (int row = lane / lpr; row < RB; row += rows_per_pass) {
-        const float* rp = rs + row * p.red_stride;
-        // four independent running sums so the shared loads overlap; the
-        // order of additions is fixed, so every run gives the same bits
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        int u = part;
-        for (; u + 3 * lpr < p.U; u += 4 * lpr) {
-          s0 += rp[u];
-          s1 += rp[u + lpr];
-          s2 += rp[u + 2 * lpr];
-          s3 += rp[u + 3 * lpr];
-        }
-        for (; u < p.U; u += lpr) s0 += rp[u];
-        float sum = (s0 + s1) + (s2 + s3);
-        for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (part == 0 && row < nr)
-          *out_ptr(p.a, 0, row_begin + lr0 + row) = __half_as_ushort(__float2half_rn(sum));
-      }
-      __syncwarp();
-      if (t + S < ntiles) issue(t + S, s);
+      issue(t, s);
       if (++s == S) {
         s = 0;
         phase ^= 1u;
@@ -203,17 +190,66 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
     if (!ok) {
       if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
       // let the copies already in flight land before the CTA exits
-      for (int v = t; v < ntiles && v < t + S; ++v)
-        mbar_wait_bounded(smem_addr(&full[v % S]), (v / S) & 1, kWaitLimitNs);
+      for (int v = t - S; v < t; ++v)
+        if (v >= 0) mbar_wait_bounded(smem_addr(&full[v % S]), (v / S) & 1, kWaitLimitNs);
+    }
+    return;
+  }
+
+  if (warp == 1) {
+    // ------------------------------------------------------------ reducer
+    pdl_wait();  // y may still be read by the previous kernel on the stream
+    const int lpr = RB >= 32 ? 1 : 32 / RB;  // reducer lanes per row
+    const int rows_per_pass = 32 / lpr;
+    const int part = lane % lpr;
+    int s = 0;
+    uint32_t phase = 0;
+    for (int t = 0; t < ntiles; ++t) {
+      if (!mbar_wait_bounded(smem_addr(&redfull[s]), phase, kWaitLimitNs)) {
+        if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
+        return;
+      }
+      const int lr0 = t * RB;
+      const int nr = rows - lr0 < RB ? rows - lr0 : RB;
+      const uint32_t rs = red0 + s * RB * p.red_stride * 4;
+      for (int row = lane / lpr; row < RB; row += rows_per_pass) {
+        const uint32_t rp = rs + row * p.red_stride * 4;
+        // four independent running sums so the shared loads overlap; the
+        // order of additions is fixed, so every run gives the same bits
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int u = part;
+        for (; u + 3 * lpr < p.U; u += 4 * lpr) {
+          s0 += lds_f32(rp + 4 * u);
+          s1 += lds_f32(rp + 4 * (u + lpr));
+          s2 += lds_f32(rp + 4 * (u + 2 * lpr));
+          s3 += lds_f32(rp + 4 * (u + 3 * lpr));
+        }
+        for (; u < p.U; u += lpr) s0 += lds_f32(rp + 4 * u);
+        float sum = (s0 + s1) + (s2 + s3);
+        for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (part == 0 && row < nr)
+          *out_ptr(p.a, 0, row_begin + lr0 + row) = __half_as_ushort(__float2half_rn(sum));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&redempty[s]));
+      if (++s == S) {
+        s = 0;
+        phase ^= 1u;
+      }
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  const int c = tid - 32;
+  // consecutive threads take consecutive 64-k units of one row, so a warp
+  // reads 32 x 32 contiguous bytes; threads whose unit index has bit 2 set
+  // read their two 16-byte chunks in the opposite order, which makes every
+  // quarter-warp phase of the 16-byte shared loads hit 8 distinct bank groups
+  const int c = tid - 64;
   const bool active = c < p.T;
-  const int rl = c % RL;
-  const int u = active ? c / RL : 0;
+  const int u = c % p.U;
+  const int rl = active ? c / p.U : 0;
+  const int rot = ((u >> 2) & 1) * 16;
 
   // activations of this thread's 64 k, paired to match the unpacked lanes
   // (x may be the previous kernel's output: wait for it first)
@@ -224,7 +260,10 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
     const uint16_t* xp = p.a.x + u * 64;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint4 v = *reinterpret_cast<const uint4*>(xp + 8 * j);
+      // X[j] pairs with the j-th word as this thread loads them: with the
+      // chunk order rotated, words 4..7 come first
+      const int jj = rot ? (j ^ 4) : j;
+      const uint4 v = *reinterpret_cast<const uint4*>(xp + 8 * jj);
       X[j] = pair_activations(v);
       const float even = (half_lo(X[j].p0) + half_hi(X[j].p0)) + (half_lo(X[j].p2) + half_hi(X[j].p2));
       const float odd = (half_lo(X[j].p1) + half_hi(X[j].p1)) + (half_lo(X[j].p3) + half_hi(X[j].p3));
@@ -232,13 +271,14 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
     }
   }
 
-  // per-thread offsets inside a stage (32-bit, fixed for the whole kernel)
-  const int w_off0 = rl * p.pitch + u * 32;             // row rl
-  const int w_off1 = (rl + RL) * p.pitch + u * 32;      // row rl + RL
-  const int sc_off0 = RB * p.pitch + rl * sc_row_bytes + (u >> 1) * 2;
-  const int sc_off1 = sc_off0 + RL * sc_row_bytes;
-  const int red_off0 = rl * p.red_stride + u;
-  const int red_off1 = (rl + RL) * p.red_stride + u;
+  // per-thread offsets inside a stage (32-bit, fixed for the whole kernel):
+  // this thread handles rows rl + r RL, r < kRR, of every tile
+  const int w_off = rl * p.pitch + u * 32;
+  const int w_row_step = RL * p.pitch;
+  const int sc_off = RB * p.pitch + rl * sc_row_bytes + (u >> 1) * 2;
+  const int sc_row_step = RL * sc_row_bytes;
+  const int red_off = 4 * (rl * p.red_stride + u);
+  const int red_row_step = 4 * RL * p.red_stride;
   const int sc_tile_step = RB * sc_row_bytes;
   int sc_lo = sc_cta_lo;  // low 4 bits of the absolute scale offset of the tile
 
@@ -250,43 +290,61 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
       return;
     }
     const int nr = rows - t * RB;  // rows of this tile (may exceed RB)
-    const uint8_t* base = stages + s * p.stage_bytes;
-    float* rs = red + s * RB * p.red_stride;
-    if (active) {
-      const bool v1 = rl + RL < nr;
-      if (rl < nr) {
-        const uint4 a0 = *reinterpret_cast<const uint4*>(base + w_off0);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(base + w_off0 + 16);
-        uint4 b0 = make_uint4(0u, 0u, 0u, 0u), b1 = b0;
-        if (v1) {
-          b0 = *reinterpret_cast<const uint4*>(base + w_off1);
-          b1 = *reinterpret_cast<const uint4*>(base + w_off1 + 16);
-        }
-        const float sa = __half2float(*reinterpret_cast<const __half*>(base + sc_off0 + sc_lo));
-        const float sb = v1 ? __half2float(*reinterpret_cast<const __half*>(base + sc_off1 + sc_lo)) : 0.f;
-        float ea0 = 0.f, ea1 = 0.f, oa0 = 0.f, oa1 = 0.f;
-        float eb0 = 0.f, eb1 = 0.f, ob0 = 0.f, ob1 = 0.f;
-        const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const uint32_t base = stage0 + s * p.stage_bytes;
+    const uint32_t rs = red0 + s * RB * p.red_stride * 4;
+    // the tile's bytes go to registers; the stage is then free for a refill
+    uint32_t w[kRR][8];
+    float sc[kRR];
+    const bool work = active && rl < nr;
+    if (work) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const Unpacked ha = unpack_biased(wa[j]);
-          const Unpacked hb = unpack_biased(wb[j]);
-          fma_f32_f16x2(ea0, ea1, ha.h0, X[j].p0);
-          fma_f32_f16x2(eb0, eb1, hb.h0, X[j].p0);
-          fma_f32_f16x2(oa0, oa1, ha.h1, X[j].p1);
-          fma_f32_f16x2(ob0, ob1, hb.h1, X[j].p1);
-          fma_f32_f16x2(ea0, ea1, ha.h2, X[j].p2);
-          fma_f32_f16x2(eb0, eb1, hb.h2, X[j].p2);
-          fma_f32_f16x2(oa0, oa1, ha.h3, X[j].p3);
-          fma_f32_f16x2(ob0, ob1, hb.h3, X[j].p3);
+      for (int r = 0; r < kRR; ++r) {
+        if (r == 0 || rl + r * RL < nr) {
+          const uint4 lo = lds_u4(base + w_off + r * w_row_step + rot);
+          const uint4 hi = lds_u4(base + w_off + r * w_row_step + (16 - rot));
+          w[r][0] = lo.x; w[r][1] = lo.y; w[r][2] = lo.z; w[r][3] = lo.w;
+          w[r][4] = hi.x; w[r][5] = hi.y; w[r][6] = hi.z; w[r][7] = hi.w;
+          sc[r] = __half2float(__ushort_as_half(lds_u16(base + sc_off + r * sc_row_step + sc_lo)));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w[r][j] = 0u;
+          sc[r] = 0.f;
         }
-        rs[red_off0] = (fmaf(0.0625f, oa0 + oa1, ea0 + ea1) - C) * sa;
-        if (v1) rs[red_off1] = (fmaf(0.0625f, ob0 + ob1, eb0 + eb1) - C) * sb;
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&cons[s]));
+    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+    float res[kRR];
+    if (work) {
+      float e0[kRR], e1[kRR], o0[kRR], o1[kRR];
+#pragma unroll
+      for (int r = 0; r < kRR; ++r) e0[r] = e1[r] = o0[r] = o1[r] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int r = 0; r < kRR; ++r) {
+          const Unpacked h = unpack_biased(w[r][j]);
+          fma_f32_f16x2(e0[r], e1[r], h.h0, X[j].p0);
+          fma_f32_f16x2(o0[r], o1[r], h.h1, X[j].p1);
+          fma_f32_f16x2(e0[r], e1[r], h.h2, X[j].p2);
+          fma_f32_f16x2(o0[r], o1[r], h.h3, X[j].p3);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kRR; ++r) res[r] = (fmaf(0.0625f, o0[r] + o1[r], e0[r] + e1[r]) - C) * sc[r];
+    }
+    // partial slot s still holds tile t - S until the reducer has read it
+    if (t >= S && !mbar_wait_bounded(smem_addr(&redempty[s]), phase ^ 1u, kWaitLimitNs)) {
+      if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
+      return;
+    }
+    if (work) {
+#pragma unroll
+      for (int r = 0; r < kRR; ++r)
+        if (r == 0 || rl + r * RL < nr) sts_f32(rs + red_off + r * red_row_step, res[r]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&redfull[s]));
     sc_lo = (sc_lo + sc_tile_step) & 15;
     if (++s == S) {
       s = 0;
@@ -301,7 +359,7 @@ bool gemv_m1_supported(int K) {
   if (K <= 0 || K % 128 != 0) return false;
   const int U = K / 64;
   const int T = U * m1_rows_across_lanes(U);
-  return T + 32 <= kM1MaxThreads;
+  return T + 64 <= kM1MaxThreads;
 }
 
 cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
@@ -320,7 +378,7 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   p.S = plan.S;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.N < d.sms ? a.N : d.sms);
-  cfg.blockDim = dim3(32 + plan.CW * 32);
+  cfg.blockDim = dim3(64 + plan.CW * 32);
   cfg.dynamicSmemBytes = plan.smem + 128;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
