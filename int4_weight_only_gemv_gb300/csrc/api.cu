@@ -2,8 +2,8 @@
 // the per-device status word and the graph-captured layer sequence.
 //
 // Every argument is checked on the host before anything is enqueued.  The
-// library allocates device memory nowhere; layer_seq owns only its CUDA graph,
-// stream and event.
+// only device memory the library allocates is a layer_seq's completion
+// counters (one int per GEMV, M = 1), next to its CUDA graph, stream and event.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -269,6 +269,7 @@ struct w4a16_layer_seq {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
   cudaEvent_t done = nullptr;
+  int* task_done = nullptr;  // per-GEMV completion counters of the task lists (M = 1)
 };
 
 namespace {
@@ -279,6 +280,7 @@ void seq_free(w4a16_layer_seq* s) {
   if (s->graph) cudaGraphDestroy(s->graph);
   if (s->done) cudaEventDestroy(s->done);
   if (s->capture_stream) cudaStreamDestroy(s->capture_stream);
+  if (s->task_done) cudaFree(s->task_done);
   delete s;
 }
 
@@ -287,15 +289,10 @@ struct ProjSpec {
   int N, K;
 };
 
-}  // namespace
-
-extern "C" {
-
-w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_layers, int M,
-                                    int hidden, int kv_dim, int ffn, int group,
-                                    const w4a16_seq_io* io, w4a16_layer_seq** out) {
-  if (!out) return W4A16_ERR_NULL;
-  *out = nullptr;
+// Argument checks of a layer sequence: every GEMV of every layer is checked
+// exactly as w4a16_gemv would check it.
+w4a16_status check_seq_args(const w4a16_layer_weights* layers, int n_layers, int M, int hidden,
+                            int kv_dim, int ffn, int group, const w4a16_seq_io* io) {
   if (!layers || !io) return W4A16_ERR_NULL;
   if (group != W4A16_GROUP) return W4A16_ERR_GROUP;
   if (n_layers <= 0) return W4A16_ERR_SHAPE;
@@ -310,8 +307,6 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
       {W4A16_DOWN, hidden, ffn}};
   const int64_t Mh = static_cast<int64_t>(M) * hidden, Mkv = static_cast<int64_t>(M) * kv_dim,
                 Mgu = static_cast<int64_t>(M) * 2 * ffn;
-
-  // every GEMV of every layer is checked exactly as w4a16_gemv would check it
   for (int l = 0; l < n_layers; ++l) {
     const w4a16_layer_weights& w = layers[l];
     const uint16_t* xl = io->x + l * Mh;
@@ -335,10 +330,153 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
       }
     }
   }
+  return W4A16_OK;
+}
+
+// The GEMVs of a checked layer sequence, in order.  Per layer: [q; k; v] as
+// one GEMV when the three weights are stacked in one allocation (outputs
+// still go to y_q, y_k, y_v), o, [gate; up] as one GEMV when stacked, down.
+// dep[i] is the GEMV whose output GEMV i reads (o reads y_q, down the gate
+// half of y_gu), or -1; layer_first[l] is the index of layer l's first GEMV
+// (layer_first[n_layers] = number of GEMVs).
+void build_seq_gemvs(const w4a16_layer_weights* layers, int n_layers, int M, int hidden, int kv_dim,
+                     int ffn, const w4a16_seq_io* io, std::vector<GemvArgs>* gemvs,
+                     std::vector<int>* dep, std::vector<int>* layer_first) {
+  gemvs->clear();
+  dep->clear();
+  layer_first->clear();
+  const int64_t Mh = static_cast<int64_t>(M) * hidden, Mkv = static_cast<int64_t>(M) * kv_dim,
+                Mgu = static_cast<int64_t>(M) * 2 * ffn;
+  const size_t hw = static_cast<size_t>(hidden) / 8, hg = static_cast<size_t>(hidden) / W4A16_GROUP;
+  auto stacked = [&](const w4a16_layer_weights& w, int first, int second, int rows_first) {
+    return w.qweight[second] == w.qweight[first] + static_cast<size_t>(rows_first) * hw &&
+           w.scales[second] == w.scales[first] + static_cast<size_t>(rows_first) * hg;
+  };
+  auto add = [&](const GemvArgs& a, int d) {
+    gemvs->push_back(a);
+    dep->push_back(d);
+    return static_cast<int>(gemvs->size()) - 1;
+  };
+  for (int l = 0; l < n_layers; ++l) {
+    layer_first->push_back(static_cast<int>(gemvs->size()));
+    const w4a16_layer_weights& w = layers[l];
+    const uint16_t* xl = io->x + l * Mh;
+    uint16_t* yq = io->y_q + l * Mh;
+    uint16_t* yk = io->y_k + l * Mkv;
+    uint16_t* yv = io->y_v + l * Mkv;
+    uint16_t* ygu = io->y_gu + l * Mgu;
+    int iq;
+    if (stacked(w, W4A16_Q, W4A16_K, hidden) && stacked(w, W4A16_K, W4A16_V, kv_dim)) {
+      GemvArgs a = plain_args(w.qweight[W4A16_Q], w.scales[W4A16_Q], xl, yq, M,
+                              hidden + 2 * kv_dim, hidden, hidden, hidden);
+      a.nseg = 3;
+      a.seg[0] = OutSeg{yq, hidden, hidden};
+      a.seg[1] = OutSeg{yk, kv_dim, static_cast<int64_t>(hidden) + kv_dim};
+      a.seg[2] = OutSeg{yv, kv_dim, static_cast<int64_t>(hidden) + 2 * kv_dim};
+      iq = add(a, -1);
+    } else {
+      iq = add(plain_args(w.qweight[W4A16_Q], w.scales[W4A16_Q], xl, yq, M, hidden, hidden, hidden,
+                          hidden), -1);
+      add(plain_args(w.qweight[W4A16_K], w.scales[W4A16_K], xl, yk, M, kv_dim, hidden, hidden,
+                     kv_dim), -1);
+      add(plain_args(w.qweight[W4A16_V], w.scales[W4A16_V], xl, yv, M, kv_dim, hidden, hidden,
+                     kv_dim), -1);
+    }
+    add(plain_args(w.qweight[W4A16_O], w.scales[W4A16_O], yq, io->y_o + l * Mh, M, hidden, hidden,
+                   hidden, hidden), iq);
+    // y_gu rows are [gate | up]: row stride 2 ffn
+    int ig;
+    if (stacked(w, W4A16_GATE, W4A16_UP, ffn)) {
+      ig = add(plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, 2 * ffn, hidden,
+                          hidden, 2 * static_cast<int64_t>(ffn)), -1);
+    } else {
+      ig = add(plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, ffn, hidden,
+                          hidden, 2 * static_cast<int64_t>(ffn)), -1);
+      add(plain_args(w.qweight[W4A16_UP], w.scales[W4A16_UP], xl, ygu + ffn, M, ffn, hidden, hidden,
+                     2 * static_cast<int64_t>(ffn)), -1);
+    }
+    add(plain_args(w.qweight[W4A16_DOWN], w.scales[W4A16_DOWN], ygu, io->y_down + l * Mh, M, hidden,
+                   ffn, 2 * static_cast<int64_t>(ffn), hidden), ig);
+  }
+  layer_first->push_back(static_cast<int>(gemvs->size()));
+}
+
+// GEMVs [t0, t1) of a sequence as a task table; dependencies become indices
+// relative to t0 (a dependency before t0 is met by the launch order).
+void seq_tasks(const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep, int t0, int t1,
+               std::vector<M1Task>* tasks) {
+  tasks->clear();
+  for (int i = t0; i < t1; ++i) {
+    const GemvArgs& a = gemvs[i];
+    M1Task tk{};
+    tk.qweight = a.qweight;
+    tk.scales = a.scales;
+    tk.x = a.x;
+    tk.N = a.N;
+    tk.K = a.K;
+    tk.nseg = a.nseg;
+    tk.dep = dep[i] < t0 ? -1 : dep[i] - t0;
+    for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = a.seg[g];
+    tasks->push_back(tk);
+  }
+}
+
+// Whether a checked sequence runs as task lists of the M = 1 kernel.
+bool seq_uses_tasks(int M, const std::vector<GemvArgs>& gemvs) {
+  if (M != 1) return false;
+  for (const GemvArgs& a : gemvs)
+    if (!gemv_m1_supported(a.K)) return false;
+  return true;
+}
+
+// Enqueue a sequence's task lists: as many whole layers per launch as fit in
+// one task table, each launch after the first a programmatic dependent of the
+// previous one.  done: one zeroed counter per GEMV.  Returns the launch count
+// through *launches.
+w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs,
+                               const std::vector<int>& dep, const std::vector<int>& layer_first,
+                               int* done, cudaStream_t st, int* launches) {
+  const int n_layers = static_cast<int>(layer_first.size()) - 1;
+  std::vector<M1Task> tasks;
+  int l0 = 0;
+  *launches = 0;
+  while (l0 < n_layers) {
+    int l1 = l0 + 1;
+    while (l1 < n_layers && layer_first[l1 + 1] - layer_first[l0] <= kM1MaxTasks) ++l1;
+    const int t0 = layer_first[l0], t1 = layer_first[l1];
+    if (t1 - t0 > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
+    seq_tasks(gemvs, dep, t0, t1, &tasks);
+    const cudaError_t e =
+        launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d.status, *launches > 0, d.info, st);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return W4A16_ERR_CUDA;
+    }
+    ++*launches;
+    l0 = l1;
+  }
+  return W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_layers, int M,
+                                    int hidden, int kv_dim, int ffn, int group,
+                                    const w4a16_seq_io* io, w4a16_layer_seq** out) {
+  if (!out) return W4A16_ERR_NULL;
+  *out = nullptr;
+  w4a16_status st = check_seq_args(layers, n_layers, M, hidden, kv_dim, ffn, group, io);
+  if (st != W4A16_OK) return st;
 
   DeviceState* d = nullptr;
-  w4a16_status st = device_state(&d);
-  if (st != W4A16_OK) return st;
+  if ((st = device_state(&d)) != W4A16_OK) return st;
+
+  std::vector<GemvArgs> gemvs;
+  std::vector<int> dep, layer_first;
+  build_seq_gemvs(layers, n_layers, M, hidden, kv_dim, ffn, io, &gemvs, &dep, &layer_first);
+  const bool tasks = seq_uses_tasks(M, gemvs);
 
   w4a16_layer_seq* s = new (std::nothrow) w4a16_layer_seq();
   if (!s) return W4A16_ERR_CUDA;
@@ -350,7 +488,8 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
   s->ffn = ffn;
   s->io = *io;
   if (cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&s->done, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventCreateWithFlags(&s->done, cudaEventDisableTiming) != cudaSuccess ||
+      (tasks && cudaMalloc(&s->task_done, sizeof(int) * gemvs.size()) != cudaSuccess)) {
     cudaGetLastError();
     seq_free(s);
     return W4A16_ERR_CUDA;
@@ -360,59 +499,26 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
     seq_free(s);
     return W4A16_ERR_CUDA;
   }
-  // Per layer: [q; k; v] as one launch when the three weights are stacked in
-  // one allocation (outputs still go to y_q, y_k, y_v), o, [gate; up] as one
-  // launch when stacked, down.  Every launch but the first of the graph is a
-  // programmatic dependent of its predecessor: it streams its (constant)
+  // M = 1: the whole sequence runs as task lists of the persistent M = 1
+  // kernel; its per-GEMV completion counters are zeroed by a memset node
+  // before every replay.  M > 1: one launch per GEMV, each after the first a
+  // programmatic dependent of its predecessor (it streams its constant
   // weights while the previous GEMV finishes and waits for it before reading
-  // activations or writing outputs.
+  // activations or writing outputs).
   w4a16_status cap = W4A16_OK;
   int launches = 0;
-  const size_t hw = static_cast<size_t>(hidden) / 8, hg = static_cast<size_t>(hidden) / W4A16_GROUP;
-  auto stacked = [&](const w4a16_layer_weights& w, int first, int second, int rows_first) {
-    return w.qweight[second] == w.qweight[first] + static_cast<size_t>(rows_first) * hw &&
-           w.scales[second] == w.scales[first] + static_cast<size_t>(rows_first) * hg;
-  };
-  auto launch = [&](GemvArgs a) {
-    if (cap != W4A16_OK) return;
-    a.pdl = launches > 0;
-    cap = enqueue(*d, a, s->capture_stream);
-    ++launches;
-  };
-  for (int l = 0; l < n_layers && cap == W4A16_OK; ++l) {
-    const w4a16_layer_weights& w = layers[l];
-    const uint16_t* xl = io->x + l * Mh;
-    uint16_t* yq = io->y_q + l * Mh;
-    uint16_t* yk = io->y_k + l * Mkv;
-    uint16_t* yv = io->y_v + l * Mkv;
-    uint16_t* ygu = io->y_gu + l * Mgu;
-    if (stacked(w, W4A16_Q, W4A16_K, hidden) && stacked(w, W4A16_K, W4A16_V, kv_dim)) {
-      GemvArgs a = plain_args(w.qweight[W4A16_Q], w.scales[W4A16_Q], xl, yq, M,
-                              hidden + 2 * kv_dim, hidden, hidden, hidden);
-      a.nseg = 3;
-      a.seg[0] = OutSeg{yq, hidden, hidden};
-      a.seg[1] = OutSeg{yk, kv_dim, static_cast<int64_t>(hidden) + kv_dim};
-      a.seg[2] = OutSeg{yv, kv_dim, static_cast<int64_t>(hidden) + 2 * kv_dim};
-      launch(a);
-    } else {
-      launch(plain_args(w.qweight[W4A16_Q], w.scales[W4A16_Q], xl, yq, M, hidden, hidden, hidden, hidden));
-      launch(plain_args(w.qweight[W4A16_K], w.scales[W4A16_K], xl, yk, M, kv_dim, hidden, hidden, kv_dim));
-      launch(plain_args(w.qweight[W4A16_V], w.scales[W4A16_V], xl, yv, M, kv_dim, hidden, hidden, kv_dim));
+  if (tasks) {
+    if (cudaMemsetAsync(s->task_done, 0, sizeof(int) * gemvs.size(), s->capture_stream) != cudaSuccess)
+      cap = W4A16_ERR_CUDA;
+    else
+      cap = enqueue_seq_tasks(*d, gemvs, dep, layer_first, s->task_done, s->capture_stream, &launches);
+  } else {
+    for (size_t i = 0; i < gemvs.size() && cap == W4A16_OK; ++i) {
+      GemvArgs a = gemvs[i];
+      a.pdl = launches > 0;
+      cap = enqueue(*d, a, s->capture_stream);
+      ++launches;
     }
-    launch(plain_args(w.qweight[W4A16_O], w.scales[W4A16_O], yq, io->y_o + l * Mh, M, hidden,
-                      hidden, hidden, hidden));
-    // y_gu rows are [gate | up]: row stride 2 ffn
-    if (stacked(w, W4A16_GATE, W4A16_UP, ffn)) {
-      launch(plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, 2 * ffn, hidden,
-                        hidden, 2 * static_cast<int64_t>(ffn)));
-    } else {
-      launch(plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, ffn, hidden,
-                        hidden, 2 * static_cast<int64_t>(ffn)));
-      launch(plain_args(w.qweight[W4A16_UP], w.scales[W4A16_UP], xl, ygu + ffn, M, ffn, hidden,
-                        hidden, 2 * static_cast<int64_t>(ffn)));
-    }
-    launch(plain_args(w.qweight[W4A16_DOWN], w.scales[W4A16_DOWN], ygu, io->y_down + l * Mh, M,
-                      hidden, ffn, 2 * static_cast<int64_t>(ffn), hidden));
   }
   cudaGraph_t graph = nullptr;
   const cudaError_t ec = cudaStreamEndCapture(s->capture_stream, &graph);

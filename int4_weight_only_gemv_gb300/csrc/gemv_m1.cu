@@ -1,31 +1,38 @@
 // gemv_m1.cu -- the M = 1 decode GEMV: a persistent, TMA-fed, warp-specialised
-// CUDA-core kernel.
+// CUDA-core kernel that runs a list of GEMVs in one launch.
 //
 // The operation is the INT4 x FP16 GEMV of "Costruire un runtime di inference
 // LLM da zero" (datastack.it), section "Tre bug che insegnano", third bug
 // (gate/up/down GEMVs unpack INT4 in-kernel against FP16 activations), with
-// the group-128 symmetric format of the same section's last paragraph.
+// the group-128 symmetric format of the same section's last paragraph.  The
+// second bug of that section is the cost of launching every kernel of a
+// decode step on its own; here a list of GEMVs (a decode step's projections)
+// runs as one persistent launch whose weight stream does not stop between
+// GEMVs.  A single GEMV is a list of one.
 //
-// Design (one CTA per SM, one pass over the weight stream):
+// Design (one CTA per SM; every CTA takes a balanced contiguous range of the
+// rows of every task, at most one row of imbalance):
 //   warp 0      producer.  Streams tiles of RB consecutive rows into an
-//               S-stage shared-memory ring with 1-D bulk copies (the tile's
-//               rows are contiguous in memory: one copy, plus one for the
-//               tile's scale window), completing on a per-stage mbarrier, and
-//               refills a stage as soon as the consumers hold its tile in
-//               registers.
+//               S-stage shared-memory ring: one 1-D bulk copy for the tile's
+//               rows (contiguous in memory) and one for its scale window,
+//               completing on the stage's mbarrier.  It runs ahead across
+//               task boundaries and never waits for a dependency: weights
+//               and scales are constant.
 //   warp 1      reducer.  Sums the consumers' per-unit partials of each tile
-//               in a fixed order and writes y.
-//   warps 1..   consumers.  Consumer thread c owns unit u = c mod U (64
-//               consecutive k, half a group) of rows c / U + r RL (r < kRR)
-//               of every tile, so its 64 activations stay in registers for
-//               the whole kernel and no activation traffic touches shared
-//               memory.  Per packed word
-//               it does one shift, four LOP3s (nibble -> biased fp16, see
-//               ptx.cuh) and eight f16 x f16 -> f32 FMAs; the biases 1032 and
-//               72 are removed once per unit with the precomputed sum
-//               C = 1032 sum x_even + 72 sum x_odd.
-// Rows are split over the CTAs in balanced contiguous ranges (at most one row
-// of imbalance).  Every wait is bounded; a timeout sets W4A16_DEV_PIPE_TIMEOUT.
+//               in a fixed order and writes y; after a task's last tile it
+//               publishes the CTA's completion of the task (fence + atomic
+//               on the task's counter).  Before a task that reads another
+//               task's output it waits until every CTA has published that
+//               task, then releases the consumers through an mbarrier.
+//   warps 2..   consumers.  Consumer thread c owns unit u = c mod U (64
+//               consecutive k, half a group) of rows c / U + r RL (r < 4) of
+//               every tile, so its 64 activations stay in registers for the
+//               whole task.  Per packed word: one shift, four LOP3s (nibble
+//               -> biased fp16, see ptx.cuh) and eight f16 x f16 -> f32 FMAs;
+//               the biases 1032 and 72 are removed once per unit and row with
+//               the precomputed C = 1032 sum x_even + 72 sum x_odd.
+// Every wait is bounded; on a timeout the kernel sets W4A16_DEV_PIPE_TIMEOUT
+// and the CTA returns once its copies in flight have landed.
 #include <cuda_fp16.h>
 
 #include "kernels.h"
@@ -35,163 +42,238 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kM1MaxThreads = 672;  // 21 warps -> the compiler may use up to 96 registers
-constexpr int kM1MaxStages = 16;
+// 16 warps: producer, reducer and up to 14 consumer warps.  Registers are
+// handed out to warps in groups of four, so 16 warps leave up to 128
+// registers per thread.
+constexpr int kM1MaxThreads = 512;
+constexpr int kM1MaxConsumers = kM1MaxThreads - 64;
+constexpr int kRR = 4;  // rows per consumer thread per tile
+constexpr int kM1MaxStages = 8;
 constexpr int kM1SmemBudget = 200 * 1024;
-constexpr int kRR = 2;  // rows per consumer thread per tile (independent chains)
 
-struct M1Plan {
-  int U;            // units (64 k) per row
-  int RL;           // rows across lanes
-  int RB;           // rows per tile = RL * kRR
-  int T;            // consumer threads = U * RL
-  int CW;           // consumer warps
-  int pitch;        // shared-memory row pitch, bytes
-  int sc_cap;       // bytes of the per-stage scale window
-  int stage_bytes;  // RB * pitch + sc_cap
-  int red_stride;   // floats per row in the partial buffer (U + 1: odd stride)
-  int S;            // pipeline stages
-  int smem;         // dynamic shared memory, bytes
+// Per-task tiling, a pure function of K (U <= kM1MaxConsumers).
+struct TaskPlan {
+  int U;             // units (64 k) per row
+  int RL;            // rows across consumer threads
+  int RB;            // rows per tile = RL * kRR
+  int T;             // consumer threads = U * RL (<= kM1MaxConsumers)
+  int row_bytes;     // K / 2: packed bytes per row, also the row pitch in a stage
+  int sc_row_bytes;  // K / 64: scale bytes per row
+  int red_stride;    // floats per row in a partial slot (U + 1)
 };
 
-__host__ __device__ inline int m1_rows_across_lanes(int U) {
-  // consumer threads = U * RL: about 450-600 threads for every K
-  return U > 64 ? 2 : (U > 16 ? 8 : (U > 4 ? 16 : 32));
-}
-
-M1Plan make_m1_plan(int K, int smem_limit) {
-  M1Plan p{};
-  p.U = K / 64;
-  p.RL = m1_rows_across_lanes(p.U);
+__host__ __device__ inline TaskPlan task_plan(int K) {
+  TaskPlan p;
+  p.U = K >> 6;
+  p.RL = p.U >= kM1MaxConsumers ? 1 : kM1MaxConsumers / p.U;
   p.RB = p.RL * kRR;
   p.T = p.U * p.RL;
-  p.CW = (p.T + 31) / 32;
-  p.pitch = K / 2;  // rows stored densely: a tile is one contiguous bulk copy
-  p.sc_cap = ((p.RB * (K / 64) + 32) + 15) & ~15;
-  p.stage_bytes = p.RB * p.pitch + p.sc_cap;
+  p.row_bytes = K >> 1;
+  p.sc_row_bytes = K >> 6;
   p.red_stride = p.U + 1;
-  const int per_stage = p.stage_bytes + p.RB * p.red_stride * 4;
-  const int budget = (smem_limit < kM1SmemBudget ? smem_limit : kM1SmemBudget) - 512;
-  p.S = budget / per_stage;
-  if (p.S > kM1MaxStages) p.S = kM1MaxStages;
-  p.smem = 512 + p.S * per_stage;
   return p;
 }
 
-struct M1Params {
-  GemvArgs a;             // pointers, sizes and output segments
-  const uint8_t* scales;  // a.scales as bytes
-  int U, RL, RB, T, pitch, stage_bytes, red_stride, S;
+// Bytes of a stage's scale window: RB rows plus up to 15 bytes of alignment
+// slack on each side, rounded to 16.
+__host__ __device__ inline int sc_window_cap(const TaskPlan& tp) {
+  return (tp.RB * tp.sc_row_bytes + 32 + 15) & ~15;
+}
+
+// Sizes shared by every task of a launch.
+struct RingPlan {
+  int stage_bytes;  // max over tasks of RB * row_bytes + scale window, 128-aligned
+  int red_bytes;    // max over tasks of RB * red_stride * 4, 16-aligned
+  int CW;           // consumer warps = max over tasks of ceil(T / 32)
+  int S;            // stages
+  int smem;         // dynamic shared memory, bytes
 };
 
-__global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Params p) {
+constexpr int kBarrierBytes = 512;  // [full S][empty S][redfull S][redempty S][xready]
+
+RingPlan make_ring_plan(const int* Ks, int n, int smem_limit) {
+  RingPlan r{};
+  for (int i = 0; i < n; ++i) {
+    const TaskPlan tp = task_plan(Ks[i]);
+    const int st = tp.RB * tp.row_bytes + sc_window_cap(tp);
+    const int rb = tp.RB * tp.red_stride * 4;
+    const int cw = (tp.T + 31) / 32;
+    if (st > r.stage_bytes) r.stage_bytes = st;
+    if (rb > r.red_bytes) r.red_bytes = rb;
+    if (cw > r.CW) r.CW = cw;
+  }
+  r.stage_bytes = (r.stage_bytes + 127) & ~127;
+  r.red_bytes = (r.red_bytes + 15) & ~15;
+  const int per_stage = r.stage_bytes + r.red_bytes;
+  // 128 bytes of slack: the stages start at the next 128-byte boundary
+  const int budget = (smem_limit < kM1SmemBudget ? smem_limit : kM1SmemBudget) - kBarrierBytes - 128;
+  r.S = budget / per_stage;
+  if (r.S > kM1MaxStages) r.S = kM1MaxStages;
+  r.smem = kBarrierBytes + r.S * per_stage + 128;
+  return r;
+}
+
+template <int MAXT>
+struct M1Params {
+  int ntasks;
+  int S, stage_bytes, red_bytes, CW;
+  int* done;         // per-task completion counters (null: no task has a dependency)
+  uint32_t* status;  // device status word
+  M1Task task[MAXT];
+};
+
+// This CTA's rows of an N-row task: [row_begin, row_begin + return value).
+__device__ __forceinline__ int cta_rows(int N, int64_t* row_begin) {
+  const int64_t G = gridDim.x;
+  const int64_t b = blockIdx.x;
+  *row_begin = (static_cast<int64_t>(N) * b) / G;
+  return static_cast<int>((static_cast<int64_t>(N) * (b + 1)) / G - *row_begin);
+}
+
+// Bounded wait until *counter >= target (acquire).  False if the bound ran out.
+__device__ __forceinline__ bool wait_count(const int* counter, int target, uint64_t limit_ns) {
+  if (ld_acquire_gpu(counter) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    __nanosleep(256);
+    if (ld_acquire_gpu(counter) >= target) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Dot products of two rows (8 packed words each, registers wa, wb) with this
+// thread's 64 activations.  Returns sum_k (1032 + q or 1152 + 16 q) x, the
+// second kind scaled back by 1/16, i.e. sum_k q x + C.
+__device__ __forceinline__ void dot_pair(const uint32_t (&wa)[8], const uint32_t (&wb)[8],
+                                         const XPairs (&X)[8], float& ra, float& rb) {
+  float ea0 = 0.f, ea1 = 0.f, oa0 = 0.f, oa1 = 0.f;
+  float eb0 = 0.f, eb1 = 0.f, ob0 = 0.f, ob1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const Unpacked a = unpack_biased(wa[j]);
+    const Unpacked b = unpack_biased(wb[j]);
+    fma_f32_f16x2(ea0, ea1, a.h0, X[j].p0);
+    fma_f32_f16x2(eb0, eb1, b.h0, X[j].p0);
+    fma_f32_f16x2(oa0, oa1, a.h1, X[j].p1);
+    fma_f32_f16x2(ob0, ob1, b.h1, X[j].p1);
+    fma_f32_f16x2(ea0, ea1, a.h2, X[j].p2);
+    fma_f32_f16x2(eb0, eb1, b.h2, X[j].p2);
+    fma_f32_f16x2(oa0, oa1, a.h3, X[j].p3);
+    fma_f32_f16x2(ob0, ob1, b.h3, X[j].p3);
+  }
+  ra = fmaf(0.0625f, oa0 + oa1, ea0 + ea1);
+  rb = fmaf(0.0625f, ob0 + ob1, eb0 + eb1);
+}
+
+// The 8 packed words of one row at a stage address: two 16-byte shared loads,
+// the second chunk first when rot = 16.
+__device__ __forceinline__ void load_row(uint32_t addr, int rot, uint32_t (&w)[8]) {
+  const uint4 lo = lds_u4(addr + rot);
+  const uint4 hi = lds_u4(addr + (16 - rot));
+  w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+  w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+}
+
+template <int MAXT>
+__global__ void __launch_bounds__(kM1MaxThreads, 1)
+    gemv_m1_kernel(const __grid_constant__ M1Params<MAXT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = p.S;
-  const int RL = p.RL;
-  const int RB = p.RB;
-  // layout: barriers [full S][empty S][redfull S][redempty S] | partials
-  // S*RB*red_stride f32 | stages.  All hot accesses use 32-bit shared
-  // addresses (explicit ld/st.shared).
+  // shared layout: barriers | S partial slots of red_bytes | S stages of
+  // stage_bytes (128-aligned).  All hot accesses use 32-bit shared addresses.
   //   full[s]      producer -> consumers: the tile's bytes landed (tx count)
-  //   empty[s]     consumers -> producer: the tile is in registers, refill
+  //   empty[s]     consumers -> producer: the stage may be refilled
   //   redfull[s]   consumers -> reducer: the tile's partial sums are written
   //   redempty[s]  reducer -> consumers: partial slot s may be rewritten
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + S;
-  uint64_t* redfull = empty + S;
-  uint64_t* redempty = redfull + S;
-  const uint32_t smem0 = smem_addr(smem);
-  const uint32_t red0 = smem0 + 512;
-  const uint32_t stage0 = (red0 + S * RB * p.red_stride * 4 + 127) & ~127u;
+  //   xready       reducer -> consumers: a dependency is satisfied
+  const uint32_t full0 = smem_addr(smem);
+  const uint32_t empty0 = full0 + 8 * S;
+  const uint32_t redfull0 = full0 + 16 * S;
+  const uint32_t redempty0 = full0 + 24 * S;
+  const uint32_t xready = full0 + 32 * S;
+  const uint32_t red0 = full0 + kBarrierBytes;
+  const uint32_t stage0 = (red0 + S * p.red_bytes + 127) & ~127u;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int CW = (p.T + 31) >> 5;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_addr(&full[s]), 1);
-      mbar_init(smem_addr(&empty[s]), CW);
-      mbar_init(smem_addr(&redfull[s]), CW);
-      mbar_init(smem_addr(&redempty[s]), 1);
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, p.CW);
+      mbar_init(redfull0 + 8 * s, p.CW);
+      mbar_init(redempty0 + 8 * s, 1);
     }
+    mbar_init(xready, 1);
     fence_barrier_init();
   }
   __syncthreads();
   pdl_launch_dependents();
 
-  const int64_t N = p.a.N;
-  const int K = p.a.K;
-  const int64_t G = gridDim.x;
-  const int64_t row_begin = (N * blockIdx.x) / G;
-  const int rows = static_cast<int>((N * (blockIdx.x + 1)) / G - row_begin);  // rows of this CTA
-  const int ntiles = (rows + RB - 1) / RB;
-  const int row_bytes = K / 2;      // packed bytes per row
-  const int sc_row_bytes = K / 64;  // scale bytes per row
-  // scale bytes are addressed relative to the first row of this CTA; only the
-  // alignment of the absolute offset matters, and that is its low 4 bits
-  const int64_t sc_cta = row_begin * sc_row_bytes;
-  const int sc_cta_lo = static_cast<int>(sc_cta & 15);
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
-    const int64_t sc_total = N * sc_row_bytes;
-    const uint32_t* qrows = p.a.qweight + row_begin * (K / 8);
-    // issue tile t into stage s
-    auto issue = [&](int t, int s) {
-      const int lr0 = t * RB;
-      const int nr = rows - lr0 < RB ? rows - lr0 : RB;
-      const int64_t sb0 = sc_cta + static_cast<int64_t>(lr0) * sc_row_bytes;
-      const int64_t sb1 = sb0 + static_cast<int64_t>(nr) * sc_row_bytes;
-      const int64_t a = sb0 & ~int64_t(15);
-      int64_t e = (sb1 + 15) & ~int64_t(15);
-      if (e > sc_total) e = sc_total & ~int64_t(15);  // never read past the buffer
-      const int64_t ecopy = e > a ? e : a;
-      const uint32_t base = stage0 + s * p.stage_bytes;
-      const uint32_t scw = base + RB * p.pitch;
-      const uint32_t bar = smem_addr(&full[s]);
-      if (lane == 0) {
-        // the last few scale bytes of the matrix, if the aligned copy stops short
-        for (int64_t b = ecopy; b < sb1; b += 2)
-          sts_u16(scw + static_cast<uint32_t>(b - a), ld_nc_u16(p.scales + b));
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * row_bytes + (ecopy - a)));
-      }
-      __syncwarp();
-      // consecutive rows are contiguous in memory: one copy for the whole tile
-      if (lane == 0)
-        bulk_g2s(base, qrows + static_cast<int64_t>(lr0) * (K / 8),
-                 static_cast<uint32_t>(nr * row_bytes), bar, pol);
-      if (lane == 1 && ecopy > a)
-        bulk_g2s(scw, p.scales + a, static_cast<uint32_t>(ecopy - a), bar, pol);
-    };
-
-    // the weights and scales are constant: stream them without waiting for
-    // the previous kernel on the stream
-    const int prolog = ntiles < S ? ntiles : S;
-    for (int t = 0; t < prolog; ++t) issue(t, t);
-    // then refill each stage as soon as the consumers hold its tile in registers
-    int s = 0;
+    int s = 0, g = 0;  // stage, tiles issued so far (all tasks)
     uint32_t phase = 0;
-    int t = S;
+    uint32_t base = stage0;
     bool ok = true;
-    for (; t < ntiles; ++t) {
-      if (!mbar_wait_bounded(smem_addr(&empty[s]), phase, kWaitLimitNs)) {
-        ok = false;
-        break;
-      }
-      issue(t, s);
-      if (++s == S) {
-        s = 0;
-        phase ^= 1u;
+    for (int i = 0; i < p.ntasks && ok; ++i) {
+      const M1Task& tk = p.task[i];
+      const TaskPlan tp = task_plan(tk.K);
+      int64_t row_begin;
+      const int rows = cta_rows(tk.N, &row_begin);
+      const int ntiles = (rows + tp.RB - 1) / tp.RB;
+      const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(tk.qweight) + row_begin * tp.row_bytes;
+      const uint8_t* scb = reinterpret_cast<const uint8_t*>(tk.scales);
+      const int64_t sc_total = static_cast<int64_t>(tk.N) * tp.sc_row_bytes;
+      int64_t sb0 = row_begin * tp.sc_row_bytes;  // first scale byte of the tile
+      for (int t = 0; t < ntiles; ++t) {
+        // stage s still holds tile g - S until every consumer warp is done with it
+        if (g >= S && !mbar_wait_bounded(empty0 + 8 * s, phase ^ 1u, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const int lr0 = t * tp.RB;
+        const int nr = rows - lr0 < tp.RB ? rows - lr0 : tp.RB;
+        const int64_t sb1 = sb0 + static_cast<int64_t>(nr) * tp.sc_row_bytes;
+        const int64_t a = sb0 & ~int64_t(15);
+        int64_t e = (sb1 + 15) & ~int64_t(15);
+        if (e > sc_total) e = sc_total & ~int64_t(15);  // never read past the buffer
+        const int64_t ecopy = e > a ? e : a;
+        const uint32_t scw = base + tp.RB * tp.row_bytes;
+        const uint32_t bar = full0 + 8 * s;
+        if (lane == 0) {
+          // the last few scale bytes of the matrix, where the aligned copy stops short
+          for (int64_t b = ecopy; b < sb1; b += 2)
+            sts_u16(scw + static_cast<uint32_t>(b - a), ld_nc_u16(scb + b));
+          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * tp.row_bytes + (ecopy - a)));
+        }
+        __syncwarp();
+        // consecutive rows are contiguous in memory: one copy for the whole tile
+        if (lane == 0)
+          bulk_g2s(base, wsrc + static_cast<int64_t>(lr0) * tp.row_bytes,
+                   static_cast<uint32_t>(nr * tp.row_bytes), bar, pol);
+        if (lane == 1 && ecopy > a)
+          bulk_g2s(scw, scb + a, static_cast<uint32_t>(ecopy - a), bar, pol);
+        sb0 = sb1;
+        ++g;
+        base += p.stage_bytes;
+        if (++s == S) {
+          s = 0;
+          phase ^= 1u;
+          base = stage0;
+        }
       }
     }
     if (!ok) {
-      if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
-      // let the copies already in flight land before the CTA exits
-      for (int v = t - S; v < t; ++v)
-        if (v >= 0) mbar_wait_bounded(smem_addr(&full[v % S]), (v / S) & 1, kWaitLimitNs);
+      if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+      // let the copies in flight land before the CTA exits: the last S tiles
+      // issued sit in stages s, s + 1, ... (mod S)
+      for (int v = 0; v < S; ++v) {
+        const int gg = g - S + v;  // index of the tile in stage (s + v) mod S
+        if (gg >= 0) mbar_wait_bounded(full0 + 8 * ((s + v) % S), (gg / S) & 1, kWaitLimitNs);
+      }
     }
     return;
   }
@@ -199,201 +281,280 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1) gemv_m1_kernel(const M1Param
   if (warp == 1) {
     // ------------------------------------------------------------ reducer
     pdl_wait();  // y may still be read by the previous kernel on the stream
-    const int lpr = RB >= 32 ? 1 : 32 / RB;  // reducer lanes per row
-    const int rows_per_pass = 32 / lpr;
-    const int part = lane % lpr;
     int s = 0;
     uint32_t phase = 0;
-    for (int t = 0; t < ntiles; ++t) {
-      if (!mbar_wait_bounded(smem_addr(&redfull[s]), phase, kWaitLimitNs)) {
-        if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
-        return;
-      }
-      const int lr0 = t * RB;
-      const int nr = rows - lr0 < RB ? rows - lr0 : RB;
-      const uint32_t rs = red0 + s * RB * p.red_stride * 4;
-      for (int row = lane / lpr; row < RB; row += rows_per_pass) {
-        const uint32_t rp = rs + row * p.red_stride * 4;
-        // four independent running sums so the shared loads overlap; the
-        // order of additions is fixed, so every run gives the same bits
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        int u = part;
-        for (; u + 3 * lpr < p.U; u += 4 * lpr) {
-          s0 += lds_f32(rp + 4 * u);
-          s1 += lds_f32(rp + 4 * (u + lpr));
-          s2 += lds_f32(rp + 4 * (u + 2 * lpr));
-          s3 += lds_f32(rp + 4 * (u + 3 * lpr));
+    uint32_t rs = red0;
+    for (int i = 0; i < p.ntasks; ++i) {
+      const M1Task& tk = p.task[i];
+      const TaskPlan tp = task_plan(tk.K);
+      int64_t row_begin;
+      const int rows = cta_rows(tk.N, &row_begin);
+      const int ntiles = (rows + tp.RB - 1) / tp.RB;
+      if (ntiles > 0 && tk.dep >= 0 && p.done != nullptr) {
+        // x of task i is task dep's output: once every CTA has published it,
+        // let this CTA's consumers read it (acquire, then release to the CTA)
+        int ok = 1;
+        if (lane == 0) {
+          ok = wait_count(p.done + tk.dep, static_cast<int>(gridDim.x), kWaitLimitNs) ? 1 : 0;
+          if (ok)
+            mbar_arrive(xready);
+          else
+            atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
         }
-        for (; u < p.U; u += lpr) s0 += lds_f32(rp + 4 * u);
-        float sum = (s0 + s1) + (s2 + s3);
-        for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (part == 0 && row < nr)
-          *out_ptr(p.a, 0, row_begin + lr0 + row) = __half_as_ushort(__float2half_rn(sum));
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&redempty[s]));
-      if (++s == S) {
-        s = 0;
-        phase ^= 1u;
+      // lanes per row: a power of two (for the butterfly) with lpr * RB <= 32
+      int lpr = 1;
+      while (2 * lpr * tp.RB <= 32) lpr *= 2;
+      const int rows_per_pass = 32 / lpr;
+      const int part = lane & (lpr - 1);
+      for (int t = 0; t < ntiles; ++t) {
+        if (!mbar_wait_bounded(redfull0 + 8 * s, phase, kWaitLimitNs)) {
+          if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+          return;
+        }
+        const int lr0 = t * tp.RB;
+        const int nr = rows - lr0 < tp.RB ? rows - lr0 : tp.RB;
+        // every lane runs every pass: the shuffles take the whole warp
+        for (int row0 = 0; row0 < tp.RB; row0 += rows_per_pass) {
+          const int row = row0 + lane / lpr;
+          const uint32_t rp = rs + row * tp.red_stride * 4;
+          // four running sums so the shared loads overlap; the order of the
+          // additions is fixed, so every run gives the same bits
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+          if (row < tp.RB) {
+            int u = part;
+            for (; u + 3 * lpr < tp.U; u += 4 * lpr) {
+              s0 += lds_f32(rp + 4 * u);
+              s1 += lds_f32(rp + 4 * (u + lpr));
+              s2 += lds_f32(rp + 4 * (u + 2 * lpr));
+              s3 += lds_f32(rp + 4 * (u + 3 * lpr));
+            }
+            for (; u < tp.U; u += lpr) s0 += lds_f32(rp + 4 * u);
+          }
+          float sum = (s0 + s1) + (s2 + s3);
+          for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          if (part == 0 && row < nr)
+            *out_ptr(tk, row_begin + lr0 + row) = __half_as_ushort(__float2half_rn(sum));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(redempty0 + 8 * s);
+        rs += p.red_bytes;
+        if (++s == S) {
+          s = 0;
+          phase ^= 1u;
+          rs = red0;
+        }
+      }
+      if (p.done != nullptr) {
+        // this CTA's rows of task i are written: publish them to the grid
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.done + i, 1);
       }
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  // consecutive threads take consecutive 64-k units of one row, so a warp
-  // reads 32 x 32 contiguous bytes; threads whose unit index has bit 2 set
-  // read their two 16-byte chunks in the opposite order, which makes every
-  // quarter-warp phase of the 16-byte shared loads hit 8 distinct bank groups
   const int c = tid - 64;
-  const bool active = c < p.T;
-  const int u = c % p.U;
-  const int rl = active ? c / p.U : 0;
-  const int rot = ((u >> 2) & 1) * 16;
-
-  // activations of this thread's 64 k, paired to match the unpacked lanes
-  // (x may be the previous kernel's output: wait for it first)
-  pdl_wait();
-  XPairs X[8];
-  float C = 0.f;
-  {
-    const uint16_t* xp = p.a.x + u * 64;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      // X[j] pairs with the j-th word as this thread loads them: with the
-      // chunk order rotated, words 4..7 come first
-      const int jj = rot ? (j ^ 4) : j;
-      const uint4 v = *reinterpret_cast<const uint4*>(xp + 8 * jj);
-      X[j] = pair_activations(v);
-      const float even = (half_lo(X[j].p0) + half_hi(X[j].p0)) + (half_lo(X[j].p2) + half_hi(X[j].p2));
-      const float odd = (half_lo(X[j].p1) + half_hi(X[j].p1)) + (half_lo(X[j].p3) + half_hi(X[j].p3));
-      C = fmaf(1032.f, even, fmaf(72.f, odd, C));
-    }
-  }
-
-  // per-thread offsets inside a stage (32-bit, fixed for the whole kernel):
-  // this thread handles rows rl + r RL, r < kRR, of every tile
-  const int w_off = rl * p.pitch + u * 32;
-  const int w_row_step = RL * p.pitch;
-  const int sc_off = RB * p.pitch + rl * sc_row_bytes + (u >> 1) * 2;
-  const int sc_row_step = RL * sc_row_bytes;
-  const int red_off = 4 * (rl * p.red_stride + u);
-  const int red_row_step = 4 * RL * p.red_stride;
-  const int sc_tile_step = RB * sc_row_bytes;
-  int sc_lo = sc_cta_lo;  // low 4 bits of the absolute scale offset of the tile
-
-  int s = 0;
-  uint32_t phase = 0;
-  for (int t = 0; t < ntiles; ++t) {
-    if (!mbar_wait_bounded(smem_addr(&full[s]), phase, kWaitLimitNs)) {
-      if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
-      return;
-    }
-    const int nr = rows - t * RB;  // rows of this tile (may exceed RB)
-    const uint32_t base = stage0 + s * p.stage_bytes;
-    const uint32_t rs = red0 + s * RB * p.red_stride * 4;
-    // the tile's bytes go to registers; the stage is then free for a refill
-    uint32_t w[kRR][8];
-    float sc[kRR];
-    const bool work = active && rl < nr;
-    if (work) {
-#pragma unroll
-      for (int r = 0; r < kRR; ++r) {
-        if (r == 0 || rl + r * RL < nr) {
-          const uint4 lo = lds_u4(base + w_off + r * w_row_step + rot);
-          const uint4 hi = lds_u4(base + w_off + r * w_row_step + (16 - rot));
-          w[r][0] = lo.x; w[r][1] = lo.y; w[r][2] = lo.z; w[r][3] = lo.w;
-          w[r][4] = hi.x; w[r][5] = hi.y; w[r][6] = hi.z; w[r][7] = hi.w;
-          sc[r] = __half2float(__ushort_as_half(lds_u16(base + sc_off + r * sc_row_step + sc_lo)));
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) w[r][j] = 0u;
-          sc[r] = 0.f;
-        }
+  const int cw = warp - 2;
+  pdl_wait();  // x may be the previous kernel's output
+  int s = 0, g = 0;  // stage, tiles consumed so far (all tasks)
+  uint32_t phase = 0, xphase = 0;
+  uint32_t base = stage0, rs = red0;
+  for (int i = 0; i < p.ntasks; ++i) {
+    const M1Task& tk = p.task[i];
+    const TaskPlan tp = task_plan(tk.K);
+    int64_t row_begin;
+    const int rows = cta_rows(tk.N, &row_begin);
+    const int ntiles = (rows + tp.RB - 1) / tp.RB;
+    if (ntiles == 0) continue;
+    const bool dependent = tk.dep >= 0 && p.done != nullptr;
+    if (dependent) {
+      if (!mbar_wait_bounded(xready, xphase, kWaitLimitNs)) {
+        if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+        return;
       }
+      xphase ^= 1u;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
-    float res[kRR];
-    if (work) {
-      float e0[kRR], e1[kRR], o0[kRR], o1[kRR];
-#pragma unroll
-      for (int r = 0; r < kRR; ++r) e0[r] = e1[r] = o0[r] = o1[r] = 0.f;
+
+    // Consecutive threads take consecutive 64-k units of one row, so a warp
+    // reads 32 x 32 contiguous bytes of a stage; threads whose unit index has
+    // bit 2 set read their two 16-byte chunks in the opposite order, which
+    // puts every quarter-warp phase of the 16-byte shared loads on 8
+    // distinct bank groups.  Threads past T (in a partly used warp) compute
+    // on unit 0 of row 0 and store nothing; wholly unused warps only keep
+    // the barrier counts.
+    const bool wact = cw * 32 < tp.T;
+    const bool active = c < tp.T;
+    const int u = active ? c % tp.U : 0;
+    const int rl = active ? c / tp.U : 0;
+    const int rot = ((u >> 2) & 1) * 16;
+
+    // this thread's 64 activations, paired to match the unpacked lanes
+    XPairs X[8];
+    float C = 0.f;
+    if (wact) {
+      const uint16_t* xp = tk.x + u * 64;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
+        // X[j] pairs with the j-th word as this thread loads them: with the
+        // chunk order rotated, words 4..7 come first
+        const int jj = rot ? (j ^ 4) : j;
+        // x written by an earlier task of this launch is read after the
+        // reducer's acquire (plain loads); otherwise the read-only path
+        const uint4 v = dependent ? ld_u4(xp + 8 * jj) : ld_nc_u4(xp + 8 * jj);
+        X[j] = pair_activations(v);
+        const float even = (half_lo(X[j].p0) + half_hi(X[j].p0)) + (half_lo(X[j].p2) + half_hi(X[j].p2));
+        const float odd = (half_lo(X[j].p1) + half_hi(X[j].p1)) + (half_lo(X[j].p3) + half_hi(X[j].p3));
+        C = fmaf(1032.f, even, fmaf(72.f, odd, C));
+      }
+    }
+
+    // per-thread offsets inside a stage and a partial slot: rows rl + r RL
+    const int w_off = rl * tp.row_bytes + u * 32;
+    const int w_row_step = tp.RL * tp.row_bytes;
+    const int sc_off = tp.RB * tp.row_bytes + rl * tp.sc_row_bytes + (u >> 1) * 2;
+    const int sc_row_step = tp.RL * tp.sc_row_bytes;
+    const int red_off = 4 * (rl * tp.red_stride + u);
+    const int red_row_step = 4 * tp.RL * tp.red_stride;
+    const int sc_tile_step = tp.RB * tp.sc_row_bytes;
+    int sc_lo = static_cast<int>((row_begin * tp.sc_row_bytes) & 15);  // window offset of the tile
+
+    for (int t = 0; t < ntiles; ++t) {
+      if (!mbar_wait_bounded(full0 + 8 * s, phase, kWaitLimitNs)) {
+        if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+        return;
+      }
+      const int nr = rows - t * tp.RB;  // rows of this tile (may exceed RB)
+      float res[kRR];
+      if (wact) {
+        const uint32_t sa = base + sc_off + sc_lo;
+        float sc[kRR];
 #pragma unroll
-        for (int r = 0; r < kRR; ++r) {
-          const Unpacked h = unpack_biased(w[r][j]);
-          fma_f32_f16x2(e0[r], e1[r], h.h0, X[j].p0);
-          fma_f32_f16x2(o0[r], o1[r], h.h1, X[j].p1);
-          fma_f32_f16x2(e0[r], e1[r], h.h2, X[j].p2);
-          fma_f32_f16x2(o0[r], o1[r], h.h3, X[j].p3);
+        for (int r = 0; r < kRR; ++r) sc[r] = __half2float(__ushort_as_half(lds_u16(sa + r * sc_row_step)));
+        const uint32_t wa = base + w_off;
+#pragma unroll
+        for (int h = 0; h < kRR / 2; ++h) {
+          uint32_t w0[8], w1[8];
+          load_row(wa + (2 * h) * w_row_step, rot, w0);
+          load_row(wa + (2 * h + 1) * w_row_step, rot, w1);
+          float d0, d1;
+          dot_pair(w0, w1, X, d0, d1);
+          res[2 * h] = (d0 - C) * sc[2 * h];
+          res[2 * h + 1] = (d1 - C) * sc[2 * h + 1];
         }
       }
+      // every value read from the stage has been used: release it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      // partial slot s still holds tile g - S until the reducer has read it
+      if (g >= S && !mbar_wait_bounded(redempty0 + 8 * s, phase ^ 1u, kWaitLimitNs)) {
+        if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+        return;
+      }
+      if (active) {
 #pragma unroll
-      for (int r = 0; r < kRR; ++r) res[r] = (fmaf(0.0625f, o0[r] + o1[r], e0[r] + e1[r]) - C) * sc[r];
-    }
-    // partial slot s still holds tile t - S until the reducer has read it
-    if (t >= S && !mbar_wait_bounded(smem_addr(&redempty[s]), phase ^ 1u, kWaitLimitNs)) {
-      if (lane == 0) atomicOr(p.a.status, W4A16_DEV_PIPE_TIMEOUT);
-      return;
-    }
-    if (work) {
-#pragma unroll
-      for (int r = 0; r < kRR; ++r)
-        if (r == 0 || rl + r * RL < nr) sts_f32(rs + red_off + r * red_row_step, res[r]);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&redfull[s]));
-    sc_lo = (sc_lo + sc_tile_step) & 15;
-    if (++s == S) {
-      s = 0;
-      phase ^= 1u;
+        for (int r = 0; r < kRR; ++r)
+          if (rl + r * tp.RL < nr) sts_f32(rs + red_off + r * red_row_step, res[r]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(redfull0 + 8 * s);
+      sc_lo = (sc_lo + sc_tile_step) & 15;
+      ++g;
+      base += p.stage_bytes;
+      rs += p.red_bytes;
+      if (++s == S) {
+        s = 0;
+        phase ^= 1u;
+        base = stage0;
+        rs = red0;
+      }
     }
   }
 }
 
-}  // namespace
-
-bool gemv_m1_supported(int K) {
-  if (K <= 0 || K % 128 != 0) return false;
-  const int U = K / 64;
-  const int T = U * m1_rows_across_lanes(U);
-  return T + 64 <= kM1MaxThreads;
-}
-
-cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
-  const M1Plan plan = make_m1_plan(a.K, d.max_smem_optin);
-  if (plan.S < 2) return cudaErrorInvalidConfiguration;
-  M1Params p;
-  p.a = a;
-  p.scales = reinterpret_cast<const uint8_t*>(a.scales);
-  p.U = plan.U;
-  p.RL = plan.RL;
-  p.RB = plan.RB;
-  p.T = plan.T;
-  p.pitch = plan.pitch;
-  p.stage_bytes = plan.stage_bytes;
-  p.red_stride = plan.red_stride;
-  p.S = plan.S;
+template <int MAXT>
+cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, bool pdl,
+                         cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.N < d.sms ? a.N : d.sms);
-  cfg.blockDim = dim3(64 + plan.CW * 32);
-  cfg.dynamicSmemBytes = plan.smem + 128;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(64 + rp.CW * 32);
+  cfg.dynamicSmemBytes = rp.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = a.pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_m1_kernel, p);
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
+}  // namespace
+
+bool gemv_m1_supported(int K) {
+  return K > 0 && K % 128 == 0 && K / 64 <= kM1MaxConsumers;
+}
+
+cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
+  if (!gemv_m1_supported(a.K) || a.M != 1) return cudaErrorInvalidValue;
+  M1Params<1> p{};
+  p.ntasks = 1;
+  p.done = nullptr;
+  p.status = a.status;
+  M1Task& tk = p.task[0];
+  tk.qweight = a.qweight;
+  tk.scales = a.scales;
+  tk.x = a.x;
+  tk.N = a.N;
+  tk.K = a.K;
+  tk.nseg = a.nseg;
+  tk.dep = -1;
+  for (int s = 0; s < kMaxSegs; ++s) tk.seg[s] = a.seg[s];
+  const RingPlan rp = make_ring_plan(&a.K, 1, d.max_smem_optin);
+  if (rp.S < 2) return cudaErrorInvalidConfiguration;
+  p.S = rp.S;
+  p.stage_bytes = rp.stage_bytes;
+  p.red_bytes = rp.red_bytes;
+  p.CW = rp.CW;
+  // no dependency counting: CTAs beyond N would have no rows
+  const int grid = a.N < d.sms ? a.N : d.sms;
+  return launch_tasks(p, rp, grid, a.pdl, st);
+}
+
+cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uint32_t* status,
+                                 bool pdl, const DeviceInfo& d, cudaStream_t st) {
+  if (tasks == nullptr || ntasks <= 0 || ntasks > kM1MaxTasks) return cudaErrorInvalidValue;
+  static thread_local M1Params<kM1MaxTasks> p;  // ~25 KB: kept off the stack
+  int Ks[kM1MaxTasks];
+  for (int i = 0; i < ntasks; ++i) {
+    if (!gemv_m1_supported(tasks[i].K) || tasks[i].N <= 0) return cudaErrorInvalidValue;
+    if (tasks[i].dep >= i || (tasks[i].dep >= 0 && done == nullptr)) return cudaErrorInvalidValue;
+    p.task[i] = tasks[i];
+    Ks[i] = tasks[i].K;
+  }
+  p.ntasks = ntasks;
+  p.done = done;
+  p.status = status;
+  const RingPlan rp = make_ring_plan(Ks, ntasks, d.max_smem_optin);
+  if (rp.S < 2) return cudaErrorInvalidConfiguration;
+  p.S = rp.S;
+  p.stage_bytes = rp.stage_bytes;
+  p.red_bytes = rp.red_bytes;
+  p.CW = rp.CW;
+  // one CTA per SM: every CTA must be resident for the dependency counts
+  return launch_tasks(p, rp, d.sms, pdl, st);
+}
+
 cudaError_t prepare_gemv_m1(const DeviceInfo& d) {
   const int limit = d.max_smem_optin < kM1SmemBudget + 1024 ? d.max_smem_optin : kM1SmemBudget + 1024;
-  return cudaFuncSetAttribute(gemv_m1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+  cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemv_m1_kernel<kM1MaxTasks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              limit);
 }
 
 }  // namespace w4a16

@@ -50,6 +50,33 @@ __device__ __forceinline__ uint16_t* out_ptr(const GemvArgs& a, int m, int64_t n
 }
 #endif
 
+// One GEMV (M = 1) of a task list that a single launch of the M = 1 kernel
+// runs in order.  Task i may read the output of an earlier task `dep` of the
+// same list as its activations: its consumer warps then start once every CTA
+// of the launch has written that output.  Weights and scales of every task
+// must stay constant for the whole launch (they are streamed ahead of any
+// dependency wait).
+struct M1Task {
+  const uint32_t* qweight;  // [N][K/8]
+  const uint16_t* scales;   // [N][K/128] fp16 bits
+  const uint16_t* x;        // [K] fp16 bits
+  int N, K;
+  int nseg;                 // 1..kMaxSegs
+  int dep;                  // index of the task whose output x is, or -1
+  OutSeg seg[kMaxSegs];     // ldy unused (one activation row)
+};
+constexpr int kM1MaxTasks = 224;  // the task table travels in the kernel parameters
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint16_t* out_ptr(const M1Task& a, int64_t n) {
+  // selects, not an indexed segment: keeps the task table in parameter space
+  const int64_t e0 = a.seg[0].n_end, e1 = a.seg[1].n_end;
+  if (a.nseg < 2 || n < e0) return a.seg[0].y + n;
+  if (a.nseg < 3 || n < e1) return a.seg[1].y + (n - e0);
+  return a.seg[2].y + (n - e1);
+}
+#endif
+
 // Device facts the launchers size their grids with.
 struct DeviceInfo {
   int sms;
@@ -60,6 +87,12 @@ struct DeviceInfo {
 // M = 1, K within the pipelined kernel's limit (see gemv_m1_supported).
 bool gemv_m1_supported(int K);
 cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
+// A task list (1 <= ntasks <= kM1MaxTasks, every K supported, M = 1) in one
+// launch of one CTA per SM.  done: ntasks ints, zero before the launch
+// (per-task completion counters); required when a task has a dependency,
+// may be null otherwise.  pdl: as GemvArgs::pdl.
+cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uint32_t* status,
+                                 bool pdl, const DeviceInfo& d, cudaStream_t st);
 // M = 1..7 (any K): warp-per-row-block CUDA-core kernel.
 cudaError_t launch_gemv_rows(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 // M = 8..16: mma.sync tensor-core kernel with cluster split-K.

@@ -92,7 +92,8 @@ def seq28():
 
 def test_layer_seq_launch_count(seq28):
     seq = seq28[0]
-    assert seq.num_launches == 4 * L  # [q; k; v] and [gate; up] each one launch
+    # M = 1: the 4 x 28 GEMVs ([q; k; v] and [gate; up] stacked) are one task list
+    assert seq.num_launches == 1
 
 
 def test_layer_seq_outputs_written(seq28):
@@ -194,7 +195,8 @@ def test_layer_seq_small(M, fused, qkv):
         expect_launches += (1 if q_k else 3) + 1 + (1 if g_u else 2) + 1
         assert q_k or not qkv
         assert g_u or not fused
-    assert seq.num_launches == expect_launches
+    # M = 1 runs the whole sequence as one task list
+    assert seq.num_launches == (1 if M == 1 else expect_launches)
     seq.run()
     assert seq.sync() == 0
     for l in range(n):
@@ -221,4 +223,51 @@ def test_layer_seq_small(M, fused, qkv):
                 assert d < 0.05, (l, name, d)
             else:
                 assert torch.equal(y.view(torch.int16), ref.contiguous().view(torch.int16)), (l, name)
+    seq.close()
+
+
+def test_layer_seq_task_lists_split_between_layers():
+    """M = 1 with more GEMVs than one task table holds: the sequence is split
+    between layers into several launches (each a programmatic dependent of the
+    previous one); every GEMV equals a separate call bit for bit, outputs
+    prefilled with NaN are all written, and two replays agree."""
+    h, kv, ffn, n = 256, 128, 512, 60
+    layers = []
+    for l in range(n):
+        lw = {}
+        ws = [synth.weights(N, h, 50000 + 8 * l + i) for i, N in enumerate((h, kv, kv))]
+        qw, sc = w4.w4a16_quantize(torch.cat(ws).to(DEV))
+        lw["q"], lw["k"], lw["v"] = (qw[:h], sc[:h]), (qw[h:h + kv], sc[h:h + kv]), (qw[h + kv:], sc[h + kv:])
+        ws = [synth.weights(ffn, h, 50000 + 8 * l + 4 + i) for i in range(2)]
+        qw, sc = w4.w4a16_quantize(torch.cat(ws).to(DEV))
+        lw["gate"], lw["up"] = (qw[:ffn], sc[:ffn]), (qw[ffn:], sc[ffn:])
+        lw["o"] = w4.w4a16_quantize(synth.weights(h, h, 50000 + 8 * l + 3).to(DEV))
+        lw["down"] = w4.w4a16_quantize(synth.weights(h, ffn, 50000 + 8 * l + 6).to(DEV))
+        layers.append(lw)
+    x = torch.cat([synth.activations(1, h, 60000 + l) for l in range(n)]).view(n, 1, h).to(DEV)
+    io = {"x": x}
+    for name, width in (("y_q", h), ("y_k", kv), ("y_v", kv), ("y_o", h), ("y_gu", 2 * ffn),
+                        ("y_down", h)):
+        io[name] = torch.full((n, 1, width), float("nan"), dtype=torch.float16, device=DEV)
+    seq = w4.LayerSeq(layers, io, 1, h, kv, ffn)
+    assert seq.num_launches == 2  # 4 GEMVs per layer, 224 per task table
+    seq.run()
+    assert seq.sync() == 0
+    for name in ("y_q", "y_k", "y_v", "y_o", "y_gu", "y_down"):
+        assert not torch.isnan(io[name]).any(), name
+    first = {k: v.clone() for k, v in io.items() if k != "x"}
+    for l in range(n):
+        lw = layers[l]
+        pairs = [("q", io["x"][l], io["y_q"][l]), ("k", io["x"][l], io["y_k"][l]),
+                 ("v", io["x"][l], io["y_v"][l]), ("o", io["y_q"][l], io["y_o"][l]),
+                 ("gate", io["x"][l], io["y_gu"][l][:, :ffn]), ("up", io["x"][l], io["y_gu"][l][:, ffn:]),
+                 ("down", io["y_gu"][l][:, :ffn].contiguous(), io["y_down"][l])]
+        for name, xin, yout in pairs:
+            y = w4.w4a16_gemv(*lw[name], xin)
+            assert torch.equal(y.view(torch.int16), yout.contiguous().view(torch.int16)), (l, name)
+    seq.run()
+    assert seq.sync() == 0
+    for k, v in first.items():
+        assert torch.equal(v.view(torch.int16), io[k].view(torch.int16)), k
+    assert w4.w4a16_device_status(clear=True) == 0
     seq.close()
