@@ -148,9 +148,9 @@ w4a16_status w4a16_selftest_wait_timeout(int limit_us, void* stream);
  *   y_k    = gemv(W_k,  x_l)        N = kv_dim, K = hidden
  *   y_v    = gemv(W_v,  x_l)        N = kv_dim, K = hidden
  *   y_o    = gemv(W_o,  y_q)        N = hidden, K = hidden
- *   y_gu   = gemv([W_gate; W_up], x_l)   N = 2 ffn, K = hidden (one launch
+ *   y_gu   = gemv([W_gate; W_up], x_l)   N = 2 ffn, K = hidden (one GEMV
  *            when the up weight directly follows the gate weight in memory,
- *            two launches otherwise)
+ *            two otherwise)
  *   y_down = gemv(W_down, gate half of y_gu)   N = hidden, K = ffn
  * Layers are independent (each takes its own x_l), so magnitudes stay in the
  * fp16 range for any depth.
@@ -178,11 +178,22 @@ typedef struct {
 
 /*
  * Validate every weight and io pointer (as w4a16_gemv would), capture the
- * n_layers x 6-or-7 GEMV launches into a CUDA graph on a private stream and
- * instantiate it.  layers[l] holds the weights of layer l.  The library
- * allocates the graph and an event; nothing else.  The pointers are recorded
- * in the graph and must outlive the object.  Blocks until instantiation is
- * done (a set-up call, not a hot-path call).  *out is NULL on failure.
+ * sequence into a CUDA graph on a private stream and instantiate it.
+ * layers[l] holds the weights of layer l.  [q; k; v] run as one GEMV when
+ * the three weights are stacked in one allocation, [gate; up] likewise.
+ *   M = 1:  the GEMVs run as task lists of the persistent M = 1 kernel, whole
+ *           layers per launch and up to 224 GEMVs per launch (28 Qwen-7B-
+ *           shaped layers with stacked weights: one launch), after a memset
+ *           node that zeroes one completion counter per GEMV.  A GEMV that
+ *           reads another's output (o, down) starts once every CTA has
+ *           written that output.
+ *   M > 1:  one launch per GEMV, each a programmatic dependent of the
+ *           previous one.
+ * The library allocates the graph, a stream, an event and, for M = 1, one
+ * int of device memory per GEMV (the counters); nothing else.  The pointers
+ * are recorded in the graph and must outlive the object.  Blocks until
+ * instantiation is done (a set-up call, not a hot-path call).  *out is NULL
+ * on failure.
  */
 w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_layers, int M,
                                     int hidden, int kv_dim, int ffn, int group,
@@ -213,7 +224,8 @@ w4a16_status w4a16_layer_seq_run_host(w4a16_layer_seq* seq, const w4a16_seq_io* 
  */
 w4a16_status w4a16_layer_seq_sync(w4a16_layer_seq* seq, int timeout_ms);
 
-/* Free the graph and the event.  NULL is a no-op.  Waits for pending replays. */
+/* Free the graph, stream, event and counters.  NULL is a no-op.  Waits for
+ * pending replays. */
 void w4a16_layer_seq_destroy(w4a16_layer_seq* seq);
 
 #ifdef __cplusplus
