@@ -66,7 +66,8 @@ typedef enum {
   W4A16_ERR_CUDA = 7,       /* a CUDA runtime call or kernel launch failed */
   W4A16_ERR_TIMEOUT = 8,    /* a bounded host wait ran out */
   W4A16_ERR_STATE = 9,      /* NULL or unusable object handle */
-  W4A16_ERR_DEVICE = 10     /* a kernel recorded a failure (see w4a16_device_status) */
+  W4A16_ERR_DEVICE = 10,    /* a kernel recorded a failure (see w4a16_device_status) */
+  W4A16_ERR_LIMIT = 11      /* beyond the fixed limits of w4a16_layer_seq_run_static */
 } w4a16_status;
 
 /* Bits of the per-device status word written by kernels. */
@@ -227,6 +228,45 @@ w4a16_status w4a16_layer_seq_sync(w4a16_layer_seq* seq, int timeout_ms);
 /* Free the graph, stream, event and counters.  NULL is a no-op.  Waits for
  * pending replays. */
 void w4a16_layer_seq_destroy(w4a16_layer_seq* seq);
+
+/* GEMVs one call of w4a16_layer_seq_run_static may run (its fixed scratch). */
+#define W4A16_STATIC_MAX_GEMVS 512
+
+/*
+ * w4a16_layer_seq_run_static -- run the layer sequence once, M = 1, without
+ * allocating anything.  The page has no counterpart of this entry point: it
+ * exists for callers that cannot allocate device memory, such as a serving
+ * process that hands all free device memory to its own pool (a KV cache)
+ * up front, so that any cudaMalloc outside the pool fails or breaks its
+ * budget, or code that must not call cudaFree (it waits for the whole device).
+ * w4a16_layer_seq_create allocates its completion counters and a CUDA graph;
+ * this call uses neither.
+ *
+ * Arguments and checks are those of w4a16_layer_seq_create with M = 1; the
+ * work is the same task-list launches (one per up to 224 GEMVs), enqueued on
+ * `stream` directly, so the outputs are the same bits.  Limits: at most
+ * W4A16_STATIC_MAX_GEMVS GEMVs per call (4 per layer with stacked [q; k; v]
+ * and [gate; up], up to 7 otherwise) and every K at most 28672 (the M = 1
+ * kernel's range); beyond either the call returns W4A16_ERR_LIMIT and
+ * enqueues nothing.
+ *
+ * Scratch: the per-GEMV completion counters are one fixed device array of
+ * W4A16_STATIC_MAX_GEMVS ints (2 KB) inside the library, held on every device
+ * that loads the library until the process exits.  Each call zeroes the
+ * counters it uses with a memset on `stream` before its launches.  All calls
+ * on a device share that array: calls whose work overlaps on the GPU (on
+ * different streams, or from different host threads) race on it and give
+ * wrong results; order them (one stream, or events).
+ *
+ * The first call on a device does a one-time set-up (device queries, kernel
+ * attributes, the device address of the counter array); make that first call
+ * before any CUDA stream capture.  Host-side tables are thread-local and keep
+ * their capacity, so later calls allocate no host memory either.  Returns
+ * after enqueue.
+ */
+w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* layers, int n_layers,
+                                        int hidden, int kv_dim, int ffn, int group,
+                                        const w4a16_seq_io* io, void* stream);
 
 #ifdef __cplusplus
 }

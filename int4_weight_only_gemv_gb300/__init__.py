@@ -17,7 +17,7 @@ import os
 
 __all__ = [
     "W4A16Error", "lib", "w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
-    "w4a16_selftest_wait_timeout",
+    "w4a16_selftest_wait_timeout", "w4a16_layer_seq_run_static", "STATIC_MAX_GEMVS",
     "LayerSeq", "GROUP", "MAX_M", "MAX_K", "DEV_NONFINITE", "DEV_SCALE_OVERFLOW",
     "DEV_PIPE_TIMEOUT", "STATUS", "EXPORTED_SYMBOLS",
 ]
@@ -32,11 +32,12 @@ DEV_NONFINITE = 0x1
 DEV_SCALE_OVERFLOW = 0x2
 DEV_PIPE_TIMEOUT = 0x4
 NPROJ = 7
+STATIC_MAX_GEMVS = 512
 
 STATUS = {
     0: "W4A16_OK", 1: "W4A16_ERR_NULL", 2: "W4A16_ERR_SHAPE", 3: "W4A16_ERR_ALIGN",
     4: "W4A16_ERR_GROUP", 5: "W4A16_ERR_M_RANGE", 6: "W4A16_ERR_ALIAS", 7: "W4A16_ERR_CUDA",
-    8: "W4A16_ERR_TIMEOUT", 9: "W4A16_ERR_STATE", 10: "W4A16_ERR_DEVICE",
+    8: "W4A16_ERR_TIMEOUT", 9: "W4A16_ERR_STATE", 10: "W4A16_ERR_DEVICE", 11: "W4A16_ERR_LIMIT",
 }
 
 # Every function include/w4a16.h declares.
@@ -44,7 +45,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_status_str", "w4a16_abi_version", "w4a16_gemv", "w4a16_dequant", "w4a16_quantize",
     "w4a16_device_status", "w4a16_selftest_wait_timeout", "w4a16_layer_seq_create", "w4a16_layer_seq_num_launches",
     "w4a16_layer_seq_run", "w4a16_layer_seq_run_host", "w4a16_layer_seq_sync",
-    "w4a16_layer_seq_destroy",
+    "w4a16_layer_seq_destroy", "w4a16_layer_seq_run_static",
 )
 
 
@@ -94,10 +95,12 @@ def lib() -> ctypes.CDLL:
         L.w4a16_layer_seq_sync.argtypes = [p, i]
         L.w4a16_layer_seq_destroy.argtypes = [p]
         L.w4a16_layer_seq_destroy.restype = None
+        L.w4a16_layer_seq_run_static.argtypes = [ctypes.POINTER(_LayerWeights), i, i, i, i, i,
+                                                 ctypes.POINTER(_SeqIO), p]
         for f in ("w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
                   "w4a16_selftest_wait_timeout",
                   "w4a16_layer_seq_create", "w4a16_layer_seq_run", "w4a16_layer_seq_run_host",
-                  "w4a16_layer_seq_sync"):
+                  "w4a16_layer_seq_sync", "w4a16_layer_seq_run_static"):
             getattr(L, f).restype = i
         _LIB = L
     return _LIB
@@ -173,6 +176,28 @@ def w4a16_selftest_wait_timeout(limit_us: int = 20000, stream=None) -> None:
     """Run the bounded-wait self-test kernel (sets DEV_PIPE_TIMEOUT)."""
     _check(lib().w4a16_selftest_wait_timeout(limit_us, _stream(stream)),
            "w4a16_selftest_wait_timeout")
+
+
+def _layer_tables(layers, io):
+    arr = (_LayerWeights * len(layers))()
+    for li, lw in enumerate(layers):
+        for pj, name in enumerate(LayerSeq.NAMES):
+            qw, sc = lw[name]
+            arr[li].qweight[pj] = qw.data_ptr()
+            arr[li].scales[pj] = sc.data_ptr()
+    return arr, _SeqIO(*[io[n].data_ptr() for n in LayerSeq.IO])
+
+
+def w4a16_layer_seq_run_static(layers, io, hidden, kv_dim, ffn, stream=None) -> None:
+    """Run the M = 1 layer sequence once on `stream` through the entry point
+    that allocates nothing (for callers that cannot allocate device memory:
+    its scratch is a fixed array inside the library, W4A16_ERR_LIMIT beyond
+    STATIC_MAX_GEMVS GEMVs).  Same layers / io conventions as LayerSeq, M = 1.
+    Calls that overlap on the GPU share that scratch and race."""
+    arr, sio = _layer_tables(layers, io)
+    _check(lib().w4a16_layer_seq_run_static(arr, len(layers), hidden, kv_dim, ffn, GROUP,
+                                            ctypes.byref(sio), _stream(stream)),
+           "w4a16_layer_seq_run_static")
 
 
 class LayerSeq:

@@ -158,6 +158,8 @@ const char* w4a16_status_str(w4a16_status s) {
     case W4A16_ERR_TIMEOUT: return "wait timed out";
     case W4A16_ERR_STATE: return "invalid object handle";
     case W4A16_ERR_DEVICE: return "a kernel reported an error in the device status word";
+    case W4A16_ERR_LIMIT:
+      return "beyond the fixed limits of w4a16_layer_seq_run_static (GEMV count or K)";
   }
   return "unknown status";
 }
@@ -538,6 +540,98 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
   *out = s;
   return W4A16_OK;
 }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free run
+//
+// For callers that cannot allocate device memory (a serving process whose
+// device memory all belongs to its own pool, or code that must not call
+// cudaFree, which waits for the whole device): the counters of the task
+// lists live in a fixed array of this library's device image instead of a
+// cudaMalloc'd buffer, and no CUDA graph is built.
+
+namespace w4a16 {
+namespace {
+
+// In host code this name is only a stand-in for the device symbol, not an
+// address a kernel may be given: the device address comes from
+// cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) int g_static_task_done[W4A16_STATIC_MAX_GEMVS];
+
+int* g_static_task_done_addr[kMaxDevices];  // device address per device, under g_mu
+
+// Device address of g_static_task_done on the current device (looked up once
+// per device, with that device current).
+w4a16_status static_task_done(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_static_task_done_addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_task_done);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return W4A16_ERR_CUDA;
+    }
+    g_static_task_done_addr[dev] = static_cast<int*>(p);
+  }
+  *out = g_static_task_done_addr[dev];
+  return W4A16_OK;
+}
+
+}  // namespace
+}  // namespace w4a16
+
+extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* layers, int n_layers,
+                                                   int hidden, int kv_dim, int ffn, int group,
+                                                   const w4a16_seq_io* io, void* stream) {
+  w4a16_status st = check_seq_args(layers, n_layers, 1, hidden, kv_dim, ffn, group, io);
+  if (st != W4A16_OK) return st;
+  if (n_layers > W4A16_STATIC_MAX_GEMVS / 4) return W4A16_ERR_LIMIT;  // >= 4 GEMVs per layer
+
+  // host tables: thread-local, their capacity kept from call to call
+  static thread_local std::vector<GemvArgs> gemvs;
+  static thread_local std::vector<int> dep, layer_first;
+  static thread_local std::vector<M1Task> tasks;
+  build_seq_gemvs(layers, n_layers, 1, hidden, kv_dim, ffn, io, &gemvs, &dep, &layer_first);
+  const int n = static_cast<int>(gemvs.size());
+  if (n > W4A16_STATIC_MAX_GEMVS || !seq_uses_tasks(1, gemvs)) return W4A16_ERR_LIMIT;
+
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != W4A16_OK) return st;
+  int* done = nullptr;
+  if ((st = static_task_done(&done)) != W4A16_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the counters keep the previous call's values: zero the ones this call uses
+  if (cudaMemsetAsync(done, 0, sizeof(int) * n, s) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  // whole layers per launch, up to one task table each; every launch after
+  // the first is a programmatic dependent of the previous one
+  int launches = 0;
+  for (int l0 = 0; l0 < n_layers;) {
+    int l1 = l0 + 1;
+    while (l1 < n_layers && layer_first[l1 + 1] - layer_first[l0] <= kM1MaxTasks) ++l1;
+    const int t0 = layer_first[l0], t1 = layer_first[l1];
+    seq_tasks(gemvs, dep, t0, t1, &tasks);
+    if (launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d->status, launches > 0, d->info, s) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return W4A16_ERR_CUDA;
+    }
+    ++launches;
+    l0 = l1;
+  }
+  return W4A16_OK;
+}
+
+extern "C" {
 
 int w4a16_layer_seq_num_launches(const w4a16_layer_seq* seq) { return seq ? seq->launches : 0; }
 

@@ -118,6 +118,34 @@ def test_layer_seq_argument_checks(L):
     L.w4a16_layer_seq_destroy(None)  # no-op
 
 
+def test_layer_seq_run_static_argument_checks(L):
+    """The allocation-free entry point checks everything on the host, limits
+    included, before touching the device."""
+    io = w4._SeqIO(*[0x20_0000_0000 + 0x1000_0000 * i for i in range(7)])
+
+    def layers(n, hidden, kv, ffn):
+        arr = (w4._LayerWeights * n)()
+        for l in range(n):
+            for pj in range(7):
+                arr[l].qweight[pj] = 0x10_0000_0000 + (7 * l + pj) * 0x100_0000
+                arr[l].scales[pj] = 0x10_0000_0000 + (7 * l + pj) * 0x100_0000 + 0x80_0000
+        return arr
+
+    lw = layers(1, 256, 128, 512)
+    assert L.w4a16_layer_seq_run_static(None, 1, 256, 128, 512, 128, ctypes.byref(io), None) == 1
+    assert L.w4a16_layer_seq_run_static(lw, 1, 256, 128, 512, 128, None, None) == 1
+    assert L.w4a16_layer_seq_run_static(lw, 0, 256, 128, 512, 128, ctypes.byref(io), None) == 2
+    assert L.w4a16_layer_seq_run_static(lw, 1, 256, 128, 512, 64, ctypes.byref(io), None) == 4
+    # more GEMVs than the fixed scratch holds (at least 4 per layer)
+    n = w4.STATIC_MAX_GEMVS // 4 + 1
+    assert L.w4a16_layer_seq_run_static(layers(n, 128, 128, 256), n, 128, 128, 256, 128,
+                                        ctypes.byref(io), None) == 11
+    # a K beyond the M = 1 kernel (down: K = ffn = 28800 > 28672)
+    assert L.w4a16_layer_seq_run_static(layers(1, 128, 128, 28800), 1, 128, 128, 28800, 128,
+                                        ctypes.byref(io), None) == 11
+    assert L.w4a16_status_str(11) and b"limit" in L.w4a16_status_str(11)
+
+
 def test_device_status_null(L):
     assert L.w4a16_device_status(None, 0) == 1
 
