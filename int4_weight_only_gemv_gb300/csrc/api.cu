@@ -403,23 +403,41 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, int n_layers, int M, int
   layer_first->push_back(static_cast<int>(gemvs->size()));
 }
 
-// GEMVs [t0, t1) of a sequence as a task table; dependencies become indices
-// relative to t0 (a dependency before t0 is met by the launch order).
-void seq_tasks(const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep, int t0, int t1,
-               std::vector<M1Task>* tasks) {
+// The GEMVs of layers [l0, l1) as one task table, in launch order.  Layers
+// are independent of each other, so the table interleaves them: stage A of
+// a layer (the GEMVs that read the layer's x) runs one layer ahead of its
+// stage B (o and down, which read stage A's outputs):
+//   A(l0) A(l0+1) B(l0) A(l0+2) B(l0+1) ... B(l1-1)
+// A dependent GEMV then finds its producer finished one stage earlier by the
+// whole grid, instead of waiting for the grid to finish it.  Dependencies
+// become task indices within the table (the done counters are per table
+// slot); a producer before l0 is met by the launch order.
+void seq_tasks(const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep,
+               const std::vector<int>& layer_first, int l0, int l1, std::vector<M1Task>* tasks) {
   tasks->clear();
-  for (int i = t0; i < t1; ++i) {
-    const GemvArgs& a = gemvs[i];
-    M1Task tk{};
-    tk.qweight = a.qweight;
-    tk.scales = a.scales;
-    tk.x = a.x;
-    tk.N = a.N;
-    tk.K = a.K;
-    tk.nseg = a.nseg;
-    tk.dep = dep[i] < t0 ? -1 : dep[i] - t0;
-    for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = a.seg[g];
-    tasks->push_back(tk);
+  static thread_local std::vector<int> slot;  // table slot of each emitted GEMV (capacity kept)
+  slot.assign(gemvs.size(), -1);
+  auto emit = [&](int l, bool stage_b) {
+    for (int i = layer_first[l]; i < layer_first[l + 1]; ++i) {
+      if ((dep[i] >= 0) != stage_b) continue;
+      const GemvArgs& a = gemvs[i];
+      M1Task tk{};
+      tk.qweight = a.qweight;
+      tk.scales = a.scales;
+      tk.x = a.x;
+      tk.N = a.N;
+      tk.K = a.K;
+      tk.nseg = a.nseg;
+      tk.dep = dep[i] < 0 ? -1 : slot[dep[i]];
+      for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = a.seg[g];
+      slot[i] = static_cast<int>(tasks->size());
+      tasks->push_back(tk);
+    }
+  };
+  emit(l0, false);
+  for (int l = l0; l < l1; ++l) {
+    if (l + 1 < l1) emit(l + 1, false);
+    emit(l, true);
   }
 }
 
@@ -447,7 +465,7 @@ w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>
     while (l1 < n_layers && layer_first[l1 + 1] - layer_first[l0] <= kM1MaxTasks) ++l1;
     const int t0 = layer_first[l0], t1 = layer_first[l1];
     if (t1 - t0 > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
-    seq_tasks(gemvs, dep, t0, t1, &tasks);
+    seq_tasks(gemvs, dep, layer_first, l0, l1, &tasks);
     const cudaError_t e =
         launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d.status, *launches > 0, d.info, st);
     if (e != cudaSuccess) {
@@ -619,7 +637,7 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
     int l1 = l0 + 1;
     while (l1 < n_layers && layer_first[l1 + 1] - layer_first[l0] <= kM1MaxTasks) ++l1;
     const int t0 = layer_first[l0], t1 = layer_first[l1];
-    seq_tasks(gemvs, dep, t0, t1, &tasks);
+    seq_tasks(gemvs, dep, layer_first, l0, l1, &tasks);
     if (launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d->status, launches > 0, d->info, s) !=
         cudaSuccess) {
       cudaGetLastError();

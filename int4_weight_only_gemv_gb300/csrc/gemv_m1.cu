@@ -435,20 +435,25 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
 #pragma unroll
         for (int r = 0; r < kRR; ++r) sc[r] = __half2float(__ushort_as_half(lds_u16(sa + r * sc_row_step)));
         const uint32_t wa = base + w_off;
-#pragma unroll
-        for (int h = 0; h < kRR / 2; ++h) {
-          uint32_t w0[8], w1[8];
-          load_row(wa + (2 * h) * w_row_step, rot, w0);
-          load_row(wa + (2 * h + 1) * w_row_step, rot, w1);
-          float d0, d1;
-          dot_pair(w0, w1, X, d0, d1);
-          res[2 * h] = (d0 - C) * sc[2 * h];
-          res[2 * h + 1] = (d1 - C) * sc[2 * h + 1];
-        }
+        uint32_t w0[8], w1[8];
+        float d0, d1;
+        load_row(wa, rot, w0);
+        load_row(wa + w_row_step, rot, w1);
+        dot_pair(w0, w1, X, d0, d1);
+        res[0] = (d0 - C) * sc[0];
+        res[1] = (d1 - C) * sc[1];
+        load_row(wa + 2 * w_row_step, rot, w0);
+        load_row(wa + 3 * w_row_step, rot, w1);
+        // the last reads of the stage are issued: release it (release order)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        dot_pair(w0, w1, X, d0, d1);
+        res[2] = (d0 - C) * sc[2];
+        res[3] = (d1 - C) * sc[3];
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
       }
-      // every value read from the stage has been used: release it
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
       // partial slot s still holds tile g - S until the reducer has read it
       if (g >= S && !mbar_wait_bounded(redempty0 + 8 * s, phase ^ 1u, kWaitLimitNs)) {
         if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
