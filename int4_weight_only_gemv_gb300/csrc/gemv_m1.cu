@@ -89,7 +89,7 @@ struct RingPlan {
   int smem;         // dynamic shared memory, bytes
 };
 
-constexpr int kBarrierBytes = 512;  // [full S][empty S][redfull S][redempty S][xready]
+constexpr int kBarrierBytes = 512;  // [full S][empty S][redfull S][redempty S][xready 2]
 
 RingPlan make_ring_plan(const int* Ks, int n, int smem_limit) {
   RingPlan r{};
@@ -122,12 +122,16 @@ struct M1Params {
   M1Task task[MAXT];
 };
 
-// This CTA's rows of an N-row task: [row_begin, row_begin + return value).
-__device__ __forceinline__ int cta_rows(int N, int64_t* row_begin) {
-  const int64_t G = gridDim.x;
-  const int64_t b = blockIdx.x;
-  *row_begin = (static_cast<int64_t>(N) * b) / G;
-  return static_cast<int>((static_cast<int64_t>(N) * (b + 1)) / G - *row_begin);
+// This CTA's rows of a task: [row_begin, row_begin + return value).  The
+// launcher split the N rows as rq per CTA plus one for the first rr CTAs.
+__device__ __forceinline__ int cta_rows(const M1Task& tk, int64_t* row_begin) {
+  const int b = blockIdx.x;
+  *row_begin = static_cast<int64_t>(b) * tk.rq + (b < tk.rr ? b : tk.rr);
+  return tk.rq + (b < tk.rr ? 1 : 0);
+}
+
+__device__ __forceinline__ bool cta_has_rows(const M1Task& tk) {
+  return tk.rq > 0 || static_cast<int>(blockIdx.x) < tk.rr;
 }
 
 // Bounded wait until *counter >= target (acquire).  False if the bound ran out.
@@ -185,12 +189,14 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
   //   empty[s]     consumers -> producer: the stage may be refilled
   //   redfull[s]   consumers -> reducer: the tile's partial sums are written
   //   redempty[s]  reducer -> consumers: partial slot s may be rewritten
-  //   xready       reducer -> consumers: a dependency is satisfied
+  //   xready[2]    reducer -> consumers: the next dependent task's input is
+  //                complete (two barriers, alternating, so the reducer may
+  //                signal one dependent task ahead)
   const uint32_t full0 = smem_addr(smem);
   const uint32_t empty0 = full0 + 8 * S;
   const uint32_t redfull0 = full0 + 16 * S;
   const uint32_t redempty0 = full0 + 24 * S;
-  const uint32_t xready = full0 + 32 * S;
+  const uint32_t xready0 = full0 + 32 * S;
   const uint32_t red0 = full0 + kBarrierBytes;
   const uint32_t stage0 = (red0 + S * p.red_bytes + 127) & ~127u;
 
@@ -205,7 +211,8 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       mbar_init(redfull0 + 8 * s, p.CW);
       mbar_init(redempty0 + 8 * s, 1);
     }
-    mbar_init(xready, 1);
+    mbar_init(xready0, 1);
+    mbar_init(xready0 + 8, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -222,7 +229,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       const M1Task& tk = p.task[i];
       const TaskPlan tp = task_plan(tk.K);
       int64_t row_begin;
-      const int rows = cta_rows(tk.N, &row_begin);
+      const int rows = cta_rows(tk, &row_begin);
       const int ntiles = (rows + tp.RB - 1) / tp.RB;
       const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(tk.qweight) + row_begin * tp.row_bytes;
       const uint8_t* scb = reinterpret_cast<const uint8_t*>(tk.scales);
@@ -284,25 +291,36 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     int s = 0;
     uint32_t phase = 0;
     uint32_t rs = red0;
+    // Consumers start a task that reads task dep's output once every CTA has
+    // published dep.  The reducer checks (acquire) and tells them (release,
+    // xready[n & 1] for the n-th such task with rows here), in task order:
+    // task j is signalled at the start of task j - 1 when dep < j - 1 (the
+    // usual case in an interleaved layer sequence, so the check is off the
+    // consumers' path), else at the start of task j itself.
+    int nsig = 0;
+    auto needs_signal = [&](int j) {
+      return p.done != nullptr && p.task[j].dep >= 0 && cta_has_rows(p.task[j]);
+    };
+    auto signal = [&](int j) -> bool {
+      int ok = 1;
+      if (lane == 0) {
+        ok = wait_count(p.done + p.task[j].dep, static_cast<int>(gridDim.x), kWaitLimitNs) ? 1 : 0;
+        if (ok)
+          mbar_arrive(xready0 + 8 * (nsig & 1));
+        else
+          atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+      }
+      ++nsig;
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
     for (int i = 0; i < p.ntasks; ++i) {
       const M1Task& tk = p.task[i];
       const TaskPlan tp = task_plan(tk.K);
       int64_t row_begin;
-      const int rows = cta_rows(tk.N, &row_begin);
+      const int rows = cta_rows(tk, &row_begin);
       const int ntiles = (rows + tp.RB - 1) / tp.RB;
-      if (ntiles > 0 && tk.dep >= 0 && p.done != nullptr) {
-        // x of task i is task dep's output: once every CTA has published it,
-        // let this CTA's consumers read it (acquire, then release to the CTA)
-        int ok = 1;
-        if (lane == 0) {
-          ok = wait_count(p.done + tk.dep, static_cast<int>(gridDim.x), kWaitLimitNs) ? 1 : 0;
-          if (ok)
-            mbar_arrive(xready);
-          else
-            atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-      }
+      if (needs_signal(i) && tk.dep == i - 1 && !signal(i)) return;
+      if (i + 1 < p.ntasks && needs_signal(i + 1) && p.task[i + 1].dep < i && !signal(i + 1)) return;
       // lanes per row: a power of two (for the butterfly) with lpr * RB <= 32
       int lpr = 1;
       while (2 * lpr * tp.RB <= 32) lpr *= 2;
@@ -361,22 +379,22 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
   const int cw = warp - 2;
   pdl_wait();  // x may be the previous kernel's output
   int s = 0, g = 0;  // stage, tiles consumed so far (all tasks)
-  uint32_t phase = 0, xphase = 0;
+  uint32_t phase = 0;
+  int nwait = 0;  // dependent tasks with rows here waited on so far
   uint32_t base = stage0, rs = red0;
   for (int i = 0; i < p.ntasks; ++i) {
     const M1Task& tk = p.task[i];
     const TaskPlan tp = task_plan(tk.K);
     int64_t row_begin;
-    const int rows = cta_rows(tk.N, &row_begin);
+    const int rows = cta_rows(tk, &row_begin);
     const int ntiles = (rows + tp.RB - 1) / tp.RB;
     if (ntiles == 0) continue;
-    const bool dependent = tk.dep >= 0 && p.done != nullptr;
-    if (dependent) {
-      if (!mbar_wait_bounded(xready, xphase, kWaitLimitNs)) {
+    if (tk.dep >= 0 && p.done != nullptr) {
+      if (!mbar_wait_bounded(xready0 + 8 * (nwait & 1), (nwait >> 1) & 1, kWaitLimitNs)) {
         if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
         return;
       }
-      xphase ^= 1u;
+      ++nwait;
     }
 
     // Consecutive threads take consecutive 64-k units of one row, so a warp
@@ -402,9 +420,9 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         // X[j] pairs with the j-th word as this thread loads them: with the
         // chunk order rotated, words 4..7 come first
         const int jj = rot ? (j ^ 4) : j;
-        // x written by an earlier task of this launch is read after the
-        // reducer's acquire (plain loads); otherwise the read-only path
-        const uint4 v = dependent ? ld_u4(xp + 8 * jj) : ld_nc_u4(xp + 8 * jj);
+        // plain loads through L1: x of a dependent task is read after the
+        // reducer's acquire, and the line may have been prefetched (below)
+        const uint4 v = ld_u4(xp + 8 * jj);
         X[j] = pair_activations(v);
         const float even = (half_lo(X[j].p0) + half_hi(X[j].p0)) + (half_lo(X[j].p2) + half_hi(X[j].p2));
         const float odd = (half_lo(X[j].p1) + half_hi(X[j].p1)) + (half_lo(X[j].p3) + half_hi(X[j].p3));
@@ -422,12 +440,31 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     const int sc_tile_step = tp.RB * tp.sc_row_bytes;
     int sc_lo = static_cast<int>((row_begin * tp.sc_row_bytes) & 15);  // window offset of the tile
 
+    // The next task with rows here: its activations go to L1 ahead of time,
+    // one 128-byte line per thread (K / 64 lines), right away when it reads
+    // nothing written in this launch, else once its signal has arrived.
+    int inext = i + 1;
+    while (inext < p.ntasks && !cta_has_rows(p.task[inext])) ++inext;
+    const uint16_t* xnext = nullptr;
+    bool pending = false;
+    if (inext < p.ntasks && c < (p.task[inext].K >> 6)) {
+      xnext = p.task[inext].x + c * 64;
+      if (p.task[inext].dep < 0 || p.done == nullptr)
+        prefetch_l1(xnext);
+      else
+        pending = true;
+    }
+
     for (int t = 0; t < ntiles; ++t) {
       if (!mbar_wait_bounded(full0 + 8 * s, phase, kWaitLimitNs)) {
         if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
         return;
       }
       const int nr = rows - t * tp.RB;  // rows of this tile (may exceed RB)
+      if (pending && mbar_try_wait(xready0 + 8 * (nwait & 1), (nwait >> 1) & 1)) {
+        prefetch_l1(xnext);
+        pending = false;
+      }
       float res[kRR];
       if (wact) {
         const uint32_t sa = base + sc_off + sc_lo;
@@ -519,14 +556,16 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   tk.nseg = a.nseg;
   tk.dep = -1;
   for (int s = 0; s < kMaxSegs; ++s) tk.seg[s] = a.seg[s];
+  // no dependency counting: CTAs beyond N would have no rows
+  const int grid = a.N < d.sms ? a.N : d.sms;
+  tk.rq = a.N / grid;
+  tk.rr = a.N % grid;
   const RingPlan rp = make_ring_plan(&a.K, 1, d.max_smem_optin);
   if (rp.S < 2) return cudaErrorInvalidConfiguration;
   p.S = rp.S;
   p.stage_bytes = rp.stage_bytes;
   p.red_bytes = rp.red_bytes;
   p.CW = rp.CW;
-  // no dependency counting: CTAs beyond N would have no rows
-  const int grid = a.N < d.sms ? a.N : d.sms;
   return launch_tasks(p, rp, grid, a.pdl, st);
 }
 
@@ -539,6 +578,8 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
     if (!gemv_m1_supported(tasks[i].K) || tasks[i].N <= 0) return cudaErrorInvalidValue;
     if (tasks[i].dep >= i || (tasks[i].dep >= 0 && done == nullptr)) return cudaErrorInvalidValue;
     p.task[i] = tasks[i];
+    p.task[i].rq = tasks[i].N / d.sms;
+    p.task[i].rr = tasks[i].N % d.sms;
     Ks[i] = tasks[i].K;
   }
   p.ntasks = ntasks;

@@ -195,6 +195,11 @@ __device__ __forceinline__ uint4 ld_nc_u4(const void* p) {
   return v;
 }
 
+// Bring the 128-byte line holding p into this SM's L1 (no register result).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Acquire load at GPU scope: later loads of this thread see every write that
 // was released (fence + atomic) before the value it returns was written.
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
