@@ -89,7 +89,9 @@ struct RingPlan {
   int smem;         // dynamic shared memory, bytes
 };
 
-constexpr int kBarrierBytes = 512;  // [full S][empty S][redfull S][redempty S][xready 2]
+constexpr int kXReady = 4;          // dependency-signal barriers
+constexpr int kBarrierBytes = 512;  // [full S][empty S][redfull S][redempty S][xready kXReady]
+static_assert(32 * kM1MaxStages + 8 * kXReady <= kBarrierBytes, "barriers overflow their area");
 
 RingPlan make_ring_plan(const int* Ks, int n, int smem_limit) {
   RingPlan r{};
@@ -189,9 +191,9 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
   //   empty[s]     consumers -> producer: the stage may be refilled
   //   redfull[s]   consumers -> reducer: the tile's partial sums are written
   //   redempty[s]  reducer -> consumers: partial slot s may be rewritten
-  //   xready[2]    reducer -> consumers: the next dependent task's input is
-  //                complete (two barriers, alternating, so the reducer may
-  //                signal one dependent task ahead)
+  //   xready[4]    reducer -> consumers: a dependent task's input is
+  //                complete (a ring of kXReady barriers, so the reducer may
+  //                signal up to kXReady - 1 dependent tasks ahead)
   const uint32_t full0 = smem_addr(smem);
   const uint32_t empty0 = full0 + 8 * S;
   const uint32_t redfull0 = full0 + 16 * S;
@@ -211,8 +213,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       mbar_init(redfull0 + 8 * s, p.CW);
       mbar_init(redempty0 + 8 * s, 1);
     }
-    mbar_init(xready0, 1);
-    mbar_init(xready0 + 8, 1);
+    for (int b = 0; b < kXReady; ++b) mbar_init(xready0 + 8 * b, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -292,26 +293,19 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     uint32_t phase = 0;
     uint32_t rs = red0;
     // Consumers start a task that reads task dep's output once every CTA has
-    // published dep.  The reducer checks (acquire) and tells them (release,
-    // xready[n & 1] for the n-th such task with rows here), in task order:
-    // task j is signalled at the start of task j - 1 when dep < j - 1 (the
-    // usual case in an interleaved layer sequence, so the check is off the
-    // consumers' path), else at the start of task j itself.
-    int nsig = 0;
+    // published dep.  The reducer checks (acquire) and tells them (release),
+    // the n-th such task with rows here on xready[n % kXReady], in task
+    // order.  At the start of task i it signals, ahead of time, every next
+    // such task whose producer is older than i (so this CTA has published
+    // it), up to kXReady - 1 signals beyond what the consumers have used;
+    // the polls of one batch run in parallel lanes.  In an interleaved layer
+    // sequence a dependent task is signalled a few tasks early, off the
+    // consumers' path.
+    int nsig = 0;    // signals sent
+    int nused = 0;   // dependent tasks with rows here before task i (consumed)
+    int jnext = 0;   // next task that may need a signal
     auto needs_signal = [&](int j) {
       return p.done != nullptr && p.task[j].dep >= 0 && cta_has_rows(p.task[j]);
-    };
-    auto signal = [&](int j) -> bool {
-      int ok = 1;
-      if (lane == 0) {
-        ok = wait_count(p.done + p.task[j].dep, static_cast<int>(gridDim.x), kWaitLimitNs) ? 1 : 0;
-        if (ok)
-          mbar_arrive(xready0 + 8 * (nsig & 1));
-        else
-          atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
-      }
-      ++nsig;
-      return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
     for (int i = 0; i < p.ntasks; ++i) {
       const M1Task& tk = p.task[i];
@@ -319,8 +313,28 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       int64_t row_begin;
       const int rows = cta_rows(tk, &row_begin);
       const int ntiles = (rows + tp.RB - 1) / tp.RB;
-      if (needs_signal(i) && tk.dep == i - 1 && !signal(i)) return;
-      if (i + 1 < p.ntasks && needs_signal(i + 1) && p.task[i + 1].dep < i && !signal(i + 1)) return;
+      {
+        int nc = 0, my_dep = -1;
+        while (nc < kXReady) {
+          while (jnext < p.ntasks && !needs_signal(jnext)) ++jnext;
+          if (jnext >= p.ntasks || p.task[jnext].dep >= i || nsig + nc >= nused + kXReady) break;
+          if (lane == nc) my_dep = p.task[jnext].dep;
+          ++nc;
+          ++jnext;
+        }
+        if (nc > 0) {
+          const int ok = my_dep < 0 ||
+                         wait_count(p.done + my_dep, static_cast<int>(gridDim.x), kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+            return;
+          }
+          if (lane == 0)
+            for (int c = 0; c < nc; ++c) mbar_arrive(xready0 + 8 * ((nsig + c) % kXReady));
+          nsig += nc;
+        }
+      }
+      if (needs_signal(i)) ++nused;
       // lanes per row: a power of two (for the butterfly) with lpr * RB <= 32
       int lpr = 1;
       while (2 * lpr * tp.RB <= 32) lpr *= 2;
@@ -364,7 +378,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
           rs = red0;
         }
       }
-      if (p.done != nullptr) {
+      if (p.done != nullptr && tk.publish) {
         // this CTA's rows of task i are written: publish them to the grid
         __threadfence();
         __syncwarp();
@@ -390,7 +404,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     const int ntiles = (rows + tp.RB - 1) / tp.RB;
     if (ntiles == 0) continue;
     if (tk.dep >= 0 && p.done != nullptr) {
-      if (!mbar_wait_bounded(xready0 + 8 * (nwait & 1), (nwait >> 1) & 1, kWaitLimitNs)) {
+      if (!mbar_wait_bounded(xready0 + 8 * (nwait % kXReady), (nwait / kXReady) & 1, kWaitLimitNs)) {
         if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
         return;
       }
@@ -461,7 +475,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         return;
       }
       const int nr = rows - t * tp.RB;  // rows of this tile (may exceed RB)
-      if (pending && mbar_try_wait(xready0 + 8 * (nwait & 1), (nwait >> 1) & 1)) {
+      if (pending && mbar_try_wait(xready0 + 8 * (nwait % kXReady), (nwait / kXReady) & 1)) {
         prefetch_l1(xnext);
         pending = false;
       }
@@ -555,6 +569,7 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   tk.K = a.K;
   tk.nseg = a.nseg;
   tk.dep = -1;
+  tk.publish = 0;
   for (int s = 0; s < kMaxSegs; ++s) tk.seg[s] = a.seg[s];
   // no dependency counting: CTAs beyond N would have no rows
   const int grid = a.N < d.sms ? a.N : d.sms;
@@ -580,8 +595,11 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
     p.task[i] = tasks[i];
     p.task[i].rq = tasks[i].N / d.sms;
     p.task[i].rr = tasks[i].N % d.sms;
+    p.task[i].publish = 0;
     Ks[i] = tasks[i].K;
   }
+  for (int i = 0; i < ntasks; ++i)
+    if (tasks[i].dep >= 0) p.task[tasks[i].dep].publish = 1;
   p.ntasks = ntasks;
   p.done = done;
   p.status = status;

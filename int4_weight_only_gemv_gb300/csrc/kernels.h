@@ -64,6 +64,7 @@ struct M1Task {
   int nseg;                 // 1..kMaxSegs
   int dep;                  // index of the task whose output x is, or -1
   int rq, rr;               // rows per CTA (set by the launcher): rq, one more for CTAs < rr
+  int publish;              // a later task reads this one's output (set by the launcher)
   OutSeg seg[kMaxSegs];     // ldy unused (one activation row)
 };
 constexpr int kM1MaxTasks = 224;  // the task table travels in the kernel parameters
