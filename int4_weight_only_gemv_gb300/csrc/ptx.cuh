@@ -92,6 +92,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// 2-D tiled bulk (TMA) copy global -> this CTA's shared memory through a
+// tensor map (a __grid_constant__ kernel parameter), completing on `bar` with
+// the box's bytes of transaction count.  x: innermost coordinate in elements
+// (x * element size a multiple of 16 bytes), y: row.  Rows or columns past
+// the tensor's extent are filled with zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // L2 policy for data read exactly once (streamed weights).
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
