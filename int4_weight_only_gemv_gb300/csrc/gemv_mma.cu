@@ -448,8 +448,9 @@ struct MmaPlan {
 };
 
 // Choose the K split (cluster size): every rank's x slice must fit next to a
-// ring of at least 3 stages; among those, keep the most consumer warps busy
-// (clusters x ranks x min(16, blocks per cluster)), then the smaller split.
+// ring of at least 3 stages; among those, keep the most SMs streaming with
+// enough warps (clusters x ranks x min(8, blocks per cluster)), then the
+// smaller split.
 template <int NT>
 MmaPlan make_mma_plan(const GemvArgs& a, const DeviceInfo& d) {
   MmaPlan best{};
@@ -457,7 +458,9 @@ MmaPlan make_mma_plan(const GemvArgs& a, const DeviceInfo& d) {
   const int T16 = (a.N + 15) / 16;
   const int G = a.K / 128;
   const int smem_cap = d.max_smem_optin;
-  for (int ks = 1; ks <= 8 && ks <= G; ks *= 2) {
+  // any cluster size up to the portable 8: a GPC holds a whole number of
+  // clusters, so sizes that are not powers of two can cover more SMs
+  for (int ks = 1; ks <= 8 && ks <= G; ++ks) {
     const int x_bytes = ((G + ks - 1) / ks) * NT * 4 * 32 * 16;
     const int active = max_active_clusters<NT>(ks, smem_cap);
     if (active <= 0) continue;
@@ -470,17 +473,20 @@ MmaPlan make_mma_plan(const GemvArgs& a, const DeviceInfo& d) {
     int avail = smem_cap - kMmaBarrierBytes - 1024 - x_bytes;
     if (ks > 1) {
       const int per_block = 16 * 8 * NT * 4;
-      const int max_pb = (avail - 3 * stage) / per_block;
+      const int max_pb = (avail - 3 * stage - ks * 4) / per_block;
       if (max_pb < W) continue;
       if (pass_blocks > max_pb) pass_blocks = max_pb / W * W;
     }
-    const int part_bytes = pass_blocks * 16 * 8 * NT * 4;
+    // owner slots: ceil(entries / ks) x ks floats
+    const int part_bytes = ((pass_blocks * 16 * 8 * NT + ks - 1) / ks) * ks * 4;
     const int sc_bytes = (W * 16 * ((G + ks - 1) / ks) * 2 + 15) & ~15;
     avail -= part_bytes + sc_bytes;
     int S = avail / stage;
     if (S > kMmaMaxStages) S = kMmaMaxStages;
     if (S < 3) continue;
-    const int64_t score = static_cast<int64_t>(clusters) * ks * W;
+    // SMs streaming, each with up to 8 busy warps (enough to keep its share
+    // of the bandwidth); ties go to the smaller split
+    const int64_t score = static_cast<int64_t>(clusters) * ks * (W < 8 ? W : 8);
     if (score > best_score) {
       best_score = score;
       best.KS = ks;
