@@ -200,6 +200,41 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
                                     int hidden, int kv_dim, int ffn, int group,
                                     const w4a16_seq_io* io, w4a16_layer_seq** out);
 
+/* ------------------------------------------------------------------------
+ * Fused layer epilogues (w4a16_layer_seq_create2): the steps either side of
+ * the GEMVs in a Qwen2 decoder layer, as the page on hipfire describes its
+ * Qwen2 decoder ("Overview of hipfire-arch-qwen2", "Key Technical
+ * Specifications": a SwiGLU feed-forward and attention_bias on the Q, K and
+ * V projections).
+ * ---------------------------------------------------------------------- */
+
+/* Flag: down reads h = silu(gate) * up instead of the gate half of y_gu:
+ * h[m][j] = fp16_RN(silu(g) u), g = y_gu[m][j], u = y_gu[m][ffn + j] (fp16),
+ * silu(g) = g / (1 + e^-g), evaluated in FP32.  y_gu is still written. */
+#define W4A16_SEQ_SWIGLU 0x1u
+
+/* Optional per-layer output biases, fp16 bits, one per output row of a
+ * projection (NULL: none), indexed by W4A16_Q .. W4A16_DOWN.  A bias is
+ * added to the FP32 sum before the fp16 rounding: y = fp16_RN(sum + b[n]).
+ * 16-byte aligned; must not overlap any output of the sequence. */
+typedef struct {
+  const uint16_t* bias[W4A16_NPROJ];
+} w4a16_layer_bias;
+
+/*
+ * w4a16_layer_seq_create with epilogues: biases (n_layers entries, or NULL
+ * for none) and flags (0 or W4A16_SEQ_SWIGLU; other bits return
+ * W4A16_ERR_SHAPE).  At M = 1 (every K within the M = 1 kernel's range) the
+ * SwiGLU is computed inside the down tasks as they load their activations, so
+ * h is never written to memory; otherwise a separate kernel writes h to a
+ * device buffer of n_layers x M x ffn fp16 values that the object allocates
+ * and frees.  Everything else as w4a16_layer_seq_create (which is this call
+ * with no biases and no flags).
+ */
+w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4a16_layer_bias* biases,
+                                     unsigned flags, int n_layers, int M, int hidden, int kv_dim, int ffn,
+                                     int group, const w4a16_seq_io* io, w4a16_layer_seq** out);
+
 /* Number of kernel launches one replay performs. */
 int w4a16_layer_seq_num_launches(const w4a16_layer_seq* seq);
 

@@ -31,6 +31,7 @@ MAX_K = 32768
 DEV_NONFINITE = 0x1
 DEV_SCALE_OVERFLOW = 0x2
 DEV_PIPE_TIMEOUT = 0x4
+SEQ_SWIGLU = 0x1
 NPROJ = 7
 STATIC_MAX_GEMVS = 512
 
@@ -45,7 +46,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_status_str", "w4a16_abi_version", "w4a16_gemv", "w4a16_dequant", "w4a16_quantize",
     "w4a16_device_status", "w4a16_selftest_wait_timeout", "w4a16_layer_seq_create", "w4a16_layer_seq_num_launches",
     "w4a16_layer_seq_run", "w4a16_layer_seq_run_host", "w4a16_layer_seq_sync",
-    "w4a16_layer_seq_destroy", "w4a16_layer_seq_run_static",
+    "w4a16_layer_seq_destroy", "w4a16_layer_seq_run_static", "w4a16_layer_seq_create2",
 )
 
 
@@ -58,6 +59,10 @@ class W4A16Error(RuntimeError):
 
 class _LayerWeights(ctypes.Structure):
     _fields_ = [("qweight", ctypes.c_void_p * NPROJ), ("scales", ctypes.c_void_p * NPROJ)]
+
+
+class _LayerBias(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p * NPROJ)]
 
 
 class _SeqIO(ctypes.Structure):
@@ -88,6 +93,9 @@ def lib() -> ctypes.CDLL:
         L.w4a16_selftest_wait_timeout.argtypes = [i, p]
         L.w4a16_layer_seq_create.argtypes = [ctypes.POINTER(_LayerWeights), i, i, i, i, i, i,
                                              ctypes.POINTER(_SeqIO), ctypes.POINTER(p)]
+        L.w4a16_layer_seq_create2.argtypes = [ctypes.POINTER(_LayerWeights), ctypes.POINTER(_LayerBias),
+                                              ctypes.c_uint, i, i, i, i, i, i, ctypes.POINTER(_SeqIO),
+                                              ctypes.POINTER(p)]
         L.w4a16_layer_seq_num_launches.argtypes = [p]
         L.w4a16_layer_seq_num_launches.restype = i
         L.w4a16_layer_seq_run.argtypes = [p, p]
@@ -100,7 +108,7 @@ def lib() -> ctypes.CDLL:
         for f in ("w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
                   "w4a16_selftest_wait_timeout",
                   "w4a16_layer_seq_create", "w4a16_layer_seq_run", "w4a16_layer_seq_run_host",
-                  "w4a16_layer_seq_sync", "w4a16_layer_seq_run_static"):
+                  "w4a16_layer_seq_sync", "w4a16_layer_seq_run_static", "w4a16_layer_seq_create2"):
             getattr(L, f).restype = i
         _LIB = L
     return _LIB
@@ -205,13 +213,16 @@ class LayerSeq:
 
     layers: list of dicts name -> (qweight, scales) with names q, k, v, o,
     gate, up, down; io: dict of device tensors x, y_q, y_k, y_v, y_o, y_gu,
-    y_down, each [n_layers][M][width].  The tensors must outlive the object.
+    y_down, each [n_layers][M][width].  Optional epilogues
+    (w4a16_layer_seq_create2): biases, a list of dicts name -> fp16 tensor of
+    the projection's output width (missing names: no bias); swiglu=True makes
+    down read silu(gate) * up.  The tensors must outlive the object.
     """
 
     NAMES = ("q", "k", "v", "o", "gate", "up", "down")
     IO = ("x", "y_q", "y_k", "y_v", "y_o", "y_gu", "y_down")
 
-    def __init__(self, layers, io, M, hidden, kv_dim, ffn):
+    def __init__(self, layers, io, M, hidden, kv_dim, ffn, biases=None, swiglu=False):
         arr = (_LayerWeights * len(layers))()
         for li, lw in enumerate(layers):
             for pj, name in enumerate(self.NAMES):
@@ -220,10 +231,22 @@ class LayerSeq:
                 arr[li].scales[pj] = sc.data_ptr()
         sio = _SeqIO(*[io[n].data_ptr() for n in self.IO])
         handle = ctypes.c_void_p(None)
-        self._keep = (layers, io)
-        _check(lib().w4a16_layer_seq_create(arr, len(layers), M, hidden, kv_dim, ffn, GROUP,
-                                            ctypes.byref(sio), ctypes.byref(handle)),
-               "w4a16_layer_seq_create")
+        self._keep = (layers, io, biases)
+        if biases is None and not swiglu:
+            _check(lib().w4a16_layer_seq_create(arr, len(layers), M, hidden, kv_dim, ffn, GROUP,
+                                                ctypes.byref(sio), ctypes.byref(handle)),
+                   "w4a16_layer_seq_create")
+        else:
+            barr = None
+            if biases is not None:
+                barr = (_LayerBias * len(layers))()
+                for li, lb in enumerate(biases):
+                    for pj, name in enumerate(self.NAMES):
+                        barr[li].bias[pj] = _ptr(lb.get(name))
+            _check(lib().w4a16_layer_seq_create2(arr, barr, SEQ_SWIGLU if swiglu else 0, len(layers), M,
+                                                 hidden, kv_dim, ffn, GROUP, ctypes.byref(sio),
+                                                 ctypes.byref(handle)),
+                   "w4a16_layer_seq_create2")
         self.handle = handle
         self.io = io
 

@@ -133,7 +133,7 @@ GemvArgs plain_args(const uint32_t* qweight, const uint16_t* scales, const uint1
   a.K = K;
   a.ldx = ldx;
   a.nseg = 1;
-  a.seg[0] = OutSeg{y, ldy, N};
+  a.seg[0] = OutSeg{y, ldy, N, nullptr};
   a.pdl = false;
   return a;
 }
@@ -272,6 +272,7 @@ struct w4a16_layer_seq {
   cudaGraphExec_t exec = nullptr;
   cudaEvent_t done = nullptr;
   int* task_done = nullptr;  // per-GEMV completion counters of the task lists (M = 1)
+  uint16_t* hbuf = nullptr;  // SwiGLU activations of the unfused path
 };
 
 namespace {
@@ -283,6 +284,7 @@ void seq_free(w4a16_layer_seq* s) {
   if (s->done) cudaEventDestroy(s->done);
   if (s->capture_stream) cudaStreamDestroy(s->capture_stream);
   if (s->task_done) cudaFree(s->task_done);
+  if (s->hbuf) cudaFree(s->hbuf);
   delete s;
 }
 
@@ -341,15 +343,71 @@ w4a16_status check_seq_args(const w4a16_layer_weights* layers, int n_layers, int
 // dep[i] is the GEMV whose output GEMV i reads (o reads y_q, down the gate
 // half of y_gu), or -1; layer_first[l] is the index of layer l's first GEMV
 // (layer_first[n_layers] = number of GEMVs).
-void build_seq_gemvs(const w4a16_layer_weights* layers, int n_layers, int M, int hidden, int kv_dim,
-                     int ffn, const w4a16_seq_io* io, std::vector<GemvArgs>* gemvs,
-                     std::vector<int>* dep, std::vector<int>* layer_first) {
+// Checks of the optional biases: 16-byte aligned, and no output of the
+// sequence overlapping any bias.
+w4a16_status check_seq_biases(const w4a16_layer_bias* biases, int n_layers, int M, int hidden,
+                              int kv_dim, int ffn, const w4a16_seq_io* io) {
+  if (biases == nullptr) return W4A16_OK;
+  const int width[W4A16_NPROJ] = {hidden, kv_dim, kv_dim, hidden, ffn, ffn, hidden};
+  const size_t L = static_cast<size_t>(n_layers) * M * 2;  // bytes per element x rows x layers
+  const struct {
+    const void* p;
+    size_t bytes;
+  } outs[6] = {{io->y_q, L * hidden},  {io->y_k, L * kv_dim},  {io->y_v, L * kv_dim},
+               {io->y_o, L * hidden},  {io->y_gu, L * 2 * ffn}, {io->y_down, L * hidden}};
+  for (int l = 0; l < n_layers; ++l)
+    for (int pj = 0; pj < W4A16_NPROJ; ++pj) {
+      const uint16_t* b = biases[l].bias[pj];
+      if (b == nullptr) continue;
+      if (!aligned16(b)) return W4A16_ERR_ALIGN;
+      for (const auto& o : outs)
+        if (overlaps(o.p, o.bytes, b, static_cast<size_t>(width[pj]) * 2)) return W4A16_ERR_ALIAS;
+    }
+  return W4A16_OK;
+}
+
+// Epilogue options of a layer sequence (w4a16_layer_seq_create2).
+struct SeqOptions {
+  const w4a16_layer_bias* biases = nullptr;  // n_layers entries or null
+  unsigned flags = 0;                        // W4A16_SEQ_*
+  uint16_t* hbuf = nullptr;  // SwiGLU activations [n_layers][M][ffn] (unfused path), or null
+};
+
+// The SwiGLU step before a down GEMV when it is not fused into the M = 1
+// task: h[m][j] = fp16_RN(silu(g[m][j]) u[m][j]) for j < n (rows of g, u have
+// stride ld, rows of h stride n).
+struct ActOp {
+  const uint16_t* g = nullptr;
+  const uint16_t* u = nullptr;
+  int64_t ld = 0;
+  uint16_t* h = nullptr;  // null: no step
+  int M = 0, n = 0;
+};
+
+// The GEMVs of a checked layer sequence, in order.  Per layer: [q; k; v] as
+// one GEMV when the three weights are stacked in one allocation (outputs
+// still go to y_q, y_k, y_v), o, [gate; up] as one GEMV when stacked, down.
+// dep[i] is the GEMV whose output GEMV i reads (o reads y_q, down the gate
+// half of y_gu, or with SwiGLU both halves: the later of gate and up), or -1;
+// x2[i] is the SwiGLU partner of GEMV i's x (the up half) when the sequence
+// fuses SwiGLU into the M = 1 task, else null; act[i] the separate SwiGLU
+// step before GEMV i (unfused path); layer_first[l] is the index of layer l's
+// first GEMV (layer_first[n_layers] = number of GEMVs).  Biases go to the
+// output segments.
+void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, int n_layers, int M,
+                     int hidden, int kv_dim, int ffn, const w4a16_seq_io* io, bool fuse_swiglu,
+                     std::vector<GemvArgs>* gemvs, std::vector<int>* dep,
+                     std::vector<const uint16_t*>* x2, std::vector<ActOp>* act,
+                     std::vector<int>* layer_first) {
   gemvs->clear();
   dep->clear();
+  x2->clear();
+  act->clear();
   layer_first->clear();
   const int64_t Mh = static_cast<int64_t>(M) * hidden, Mkv = static_cast<int64_t>(M) * kv_dim,
                 Mgu = static_cast<int64_t>(M) * 2 * ffn;
   const size_t hw = static_cast<size_t>(hidden) / 8, hg = static_cast<size_t>(hidden) / W4A16_GROUP;
+  const bool swiglu = (opt.flags & W4A16_SEQ_SWIGLU) != 0;
   auto stacked = [&](const w4a16_layer_weights& w, int first, int second, int rows_first) {
     return w.qweight[second] == w.qweight[first] + static_cast<size_t>(rows_first) * hw &&
            w.scales[second] == w.scales[first] + static_cast<size_t>(rows_first) * hg;
@@ -357,11 +415,15 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, int n_layers, int M, int
   auto add = [&](const GemvArgs& a, int d) {
     gemvs->push_back(a);
     dep->push_back(d);
+    x2->push_back(nullptr);
+    act->push_back(ActOp{});
     return static_cast<int>(gemvs->size()) - 1;
   };
   for (int l = 0; l < n_layers; ++l) {
     layer_first->push_back(static_cast<int>(gemvs->size()));
     const w4a16_layer_weights& w = layers[l];
+    const uint16_t* const* bias = opt.biases != nullptr ? opt.biases[l].bias : nullptr;
+    auto b = [&](int pj) { return bias != nullptr ? bias[pj] : nullptr; };
     const uint16_t* xl = io->x + l * Mh;
     uint16_t* yq = io->y_q + l * Mh;
     uint16_t* yk = io->y_k + l * Mkv;
@@ -372,33 +434,62 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, int n_layers, int M, int
       GemvArgs a = plain_args(w.qweight[W4A16_Q], w.scales[W4A16_Q], xl, yq, M,
                               hidden + 2 * kv_dim, hidden, hidden, hidden);
       a.nseg = 3;
-      a.seg[0] = OutSeg{yq, hidden, hidden};
-      a.seg[1] = OutSeg{yk, kv_dim, static_cast<int64_t>(hidden) + kv_dim};
-      a.seg[2] = OutSeg{yv, kv_dim, static_cast<int64_t>(hidden) + 2 * kv_dim};
+      a.seg[0] = OutSeg{yq, hidden, hidden, b(W4A16_Q)};
+      a.seg[1] = OutSeg{yk, kv_dim, static_cast<int64_t>(hidden) + kv_dim, b(W4A16_K)};
+      a.seg[2] = OutSeg{yv, kv_dim, static_cast<int64_t>(hidden) + 2 * kv_dim, b(W4A16_V)};
       iq = add(a, -1);
     } else {
-      iq = add(plain_args(w.qweight[W4A16_Q], w.scales[W4A16_Q], xl, yq, M, hidden, hidden, hidden,
-                          hidden), -1);
-      add(plain_args(w.qweight[W4A16_K], w.scales[W4A16_K], xl, yk, M, kv_dim, hidden, hidden,
-                     kv_dim), -1);
-      add(plain_args(w.qweight[W4A16_V], w.scales[W4A16_V], xl, yv, M, kv_dim, hidden, hidden,
-                     kv_dim), -1);
+      GemvArgs a = plain_args(w.qweight[W4A16_Q], w.scales[W4A16_Q], xl, yq, M, hidden, hidden, hidden,
+                              hidden);
+      a.seg[0].bias = b(W4A16_Q);
+      iq = add(a, -1);
+      a = plain_args(w.qweight[W4A16_K], w.scales[W4A16_K], xl, yk, M, kv_dim, hidden, hidden, kv_dim);
+      a.seg[0].bias = b(W4A16_K);
+      add(a, -1);
+      a = plain_args(w.qweight[W4A16_V], w.scales[W4A16_V], xl, yv, M, kv_dim, hidden, hidden, kv_dim);
+      a.seg[0].bias = b(W4A16_V);
+      add(a, -1);
     }
-    add(plain_args(w.qweight[W4A16_O], w.scales[W4A16_O], yq, io->y_o + l * Mh, M, hidden, hidden,
-                   hidden, hidden), iq);
+    {
+      GemvArgs a = plain_args(w.qweight[W4A16_O], w.scales[W4A16_O], yq, io->y_o + l * Mh, M, hidden,
+                              hidden, hidden, hidden);
+      a.seg[0].bias = b(W4A16_O);
+      add(a, iq);
+    }
     // y_gu rows are [gate | up]: row stride 2 ffn
-    int ig;
+    int ilast;  // the GEMV down waits for
+    const int64_t ldgu = 2 * static_cast<int64_t>(ffn);
     if (stacked(w, W4A16_GATE, W4A16_UP, ffn)) {
-      ig = add(plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, 2 * ffn, hidden,
-                          hidden, 2 * static_cast<int64_t>(ffn)), -1);
+      GemvArgs a = plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, 2 * ffn, hidden,
+                              hidden, ldgu);
+      a.nseg = 2;
+      a.seg[0] = OutSeg{ygu, ldgu, ffn, b(W4A16_GATE)};
+      a.seg[1] = OutSeg{ygu + ffn, ldgu, 2 * static_cast<int64_t>(ffn), b(W4A16_UP)};
+      ilast = add(a, -1);
     } else {
-      ig = add(plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, ffn, hidden,
-                          hidden, 2 * static_cast<int64_t>(ffn)), -1);
-      add(plain_args(w.qweight[W4A16_UP], w.scales[W4A16_UP], xl, ygu + ffn, M, ffn, hidden, hidden,
-                     2 * static_cast<int64_t>(ffn)), -1);
+      GemvArgs a = plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, ffn, hidden, hidden,
+                              ldgu);
+      a.seg[0].bias = b(W4A16_GATE);
+      ilast = add(a, -1);
+      a = plain_args(w.qweight[W4A16_UP], w.scales[W4A16_UP], xl, ygu + ffn, M, ffn, hidden, hidden, ldgu);
+      a.seg[0].bias = b(W4A16_UP);
+      const int iu = add(a, -1);
+      if (swiglu) ilast = iu;  // down reads both halves; publication is in task order
     }
-    add(plain_args(w.qweight[W4A16_DOWN], w.scales[W4A16_DOWN], ygu, io->y_down + l * Mh, M, hidden,
-                   ffn, 2 * static_cast<int64_t>(ffn), hidden), ig);
+    {
+      GemvArgs a = plain_args(w.qweight[W4A16_DOWN], w.scales[W4A16_DOWN], ygu, io->y_down + l * Mh, M,
+                              hidden, ffn, ldgu, hidden);
+      a.seg[0].bias = b(W4A16_DOWN);
+      ActOp op;
+      if (swiglu && !fuse_swiglu) {
+        op = ActOp{ygu, ygu + ffn, ldgu, opt.hbuf + static_cast<int64_t>(l) * M * ffn, M, ffn};
+        a.x = op.h;
+        a.ldx = ffn;
+      }
+      const int id = add(a, ilast);
+      if (swiglu && fuse_swiglu) (*x2)[id] = ygu + ffn;
+      (*act)[id] = op;
+    }
   }
   layer_first->push_back(static_cast<int>(gemvs->size()));
 }
@@ -413,7 +504,8 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, int n_layers, int M, int
 // become task indices within the table (the done counters are per table
 // slot); a producer before l0 is met by the launch order.
 void seq_tasks(const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep,
-               const std::vector<int>& layer_first, int l0, int l1, std::vector<M1Task>* tasks) {
+               const std::vector<const uint16_t*>& x2, const std::vector<int>& layer_first, int l0, int l1,
+               std::vector<M1Task>* tasks) {
   tasks->clear();
   static thread_local std::vector<int> slot;  // table slot of each emitted GEMV (capacity kept)
   slot.assign(gemvs.size(), -1);
@@ -425,11 +517,12 @@ void seq_tasks(const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep,
       tk.qweight = a.qweight;
       tk.scales = a.scales;
       tk.x = a.x;
+      tk.x2 = x2[i];
       tk.N = a.N;
       tk.K = a.K;
       tk.nseg = a.nseg;
       tk.dep = dep[i] < 0 ? -1 : slot[dep[i]];
-      for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = a.seg[g];
+      for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = M1Seg{a.seg[g].y, a.seg[g].bias, a.seg[g].n_end};
       slot[i] = static_cast<int>(tasks->size());
       tasks->push_back(tk);
     }
@@ -454,8 +547,9 @@ bool seq_uses_tasks(int M, const std::vector<GemvArgs>& gemvs) {
 // previous one.  done: one zeroed counter per GEMV.  Returns the launch count
 // through *launches.
 w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs,
-                               const std::vector<int>& dep, const std::vector<int>& layer_first,
-                               int* done, cudaStream_t st, int* launches) {
+                               const std::vector<int>& dep, const std::vector<const uint16_t*>& x2,
+                               const std::vector<int>& layer_first, int* done, cudaStream_t st,
+                               int* launches) {
   const int n_layers = static_cast<int>(layer_first.size()) - 1;
   std::vector<M1Task> tasks;
   int l0 = 0;
@@ -465,7 +559,7 @@ w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>
     while (l1 < n_layers && layer_first[l1 + 1] - layer_first[l0] <= kM1MaxTasks) ++l1;
     const int t0 = layer_first[l0], t1 = layer_first[l1];
     if (t1 - t0 > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
-    seq_tasks(gemvs, dep, layer_first, l0, l1, &tasks);
+    seq_tasks(gemvs, dep, x2, layer_first, l0, l1, &tasks);
     const cudaError_t e =
         launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d.status, *launches > 0, d.info, st);
     if (e != cudaSuccess) {
@@ -485,18 +579,30 @@ extern "C" {
 w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_layers, int M,
                                     int hidden, int kv_dim, int ffn, int group,
                                     const w4a16_seq_io* io, w4a16_layer_seq** out) {
+  return w4a16_layer_seq_create2(layers, nullptr, 0u, n_layers, M, hidden, kv_dim, ffn, group, io, out);
+}
+
+w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4a16_layer_bias* biases,
+                                     unsigned flags, int n_layers, int M, int hidden, int kv_dim, int ffn,
+                                     int group, const w4a16_seq_io* io, w4a16_layer_seq** out) {
   if (!out) return W4A16_ERR_NULL;
   *out = nullptr;
+  if ((flags & ~static_cast<unsigned>(W4A16_SEQ_SWIGLU)) != 0) return W4A16_ERR_SHAPE;
   w4a16_status st = check_seq_args(layers, n_layers, M, hidden, kv_dim, ffn, group, io);
   if (st != W4A16_OK) return st;
+  if ((st = check_seq_biases(biases, n_layers, M, hidden, kv_dim, ffn, io)) != W4A16_OK) return st;
 
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != W4A16_OK) return st;
 
-  std::vector<GemvArgs> gemvs;
-  std::vector<int> dep, layer_first;
-  build_seq_gemvs(layers, n_layers, M, hidden, kv_dim, ffn, io, &gemvs, &dep, &layer_first);
-  const bool tasks = seq_uses_tasks(M, gemvs);
+  // M = 1 with every K in the M = 1 kernel's range: task lists, SwiGLU fused
+  // into the down tasks; otherwise one launch per GEMV and, with SwiGLU, a
+  // separate activation step into a buffer this object owns
+  const bool tasks = M == 1 && gemv_m1_supported(hidden) && gemv_m1_supported(ffn);
+  const bool swiglu = (flags & W4A16_SEQ_SWIGLU) != 0;
+  SeqOptions opt;
+  opt.biases = biases;
+  opt.flags = flags;
 
   w4a16_layer_seq* s = new (std::nothrow) w4a16_layer_seq();
   if (!s) return W4A16_ERR_CUDA;
@@ -509,7 +615,20 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
   s->io = *io;
   if (cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&s->done, cudaEventDisableTiming) != cudaSuccess ||
-      (tasks && cudaMalloc(&s->task_done, sizeof(int) * gemvs.size()) != cudaSuccess)) {
+      (swiglu && !tasks &&
+       cudaMalloc(&s->hbuf, sizeof(uint16_t) * static_cast<size_t>(n_layers) * M * ffn) != cudaSuccess)) {
+    cudaGetLastError();
+    seq_free(s);
+    return W4A16_ERR_CUDA;
+  }
+  opt.hbuf = s->hbuf;
+  std::vector<GemvArgs> gemvs;
+  std::vector<int> dep, layer_first;
+  std::vector<const uint16_t*> x2;
+  std::vector<ActOp> act;
+  build_seq_gemvs(layers, opt, n_layers, M, hidden, kv_dim, ffn, io, tasks, &gemvs, &dep, &x2, &act,
+                  &layer_first);
+  if (tasks && cudaMalloc(&s->task_done, sizeof(int) * gemvs.size()) != cudaSuccess) {
     cudaGetLastError();
     seq_free(s);
     return W4A16_ERR_CUDA;
@@ -531,9 +650,19 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
     if (cudaMemsetAsync(s->task_done, 0, sizeof(int) * gemvs.size(), s->capture_stream) != cudaSuccess)
       cap = W4A16_ERR_CUDA;
     else
-      cap = enqueue_seq_tasks(*d, gemvs, dep, layer_first, s->task_done, s->capture_stream, &launches);
+      cap = enqueue_seq_tasks(*d, gemvs, dep, x2, layer_first, s->task_done, s->capture_stream, &launches);
   } else {
     for (size_t i = 0; i < gemvs.size() && cap == W4A16_OK; ++i) {
+      if (act[i].h != nullptr) {
+        const ActOp& op = act[i];
+        if (launch_swiglu(op.g, op.u, op.ld, op.h, op.M, op.n, launches > 0, s->capture_stream) !=
+            cudaSuccess) {
+          cudaGetLastError();
+          cap = W4A16_ERR_CUDA;
+          break;
+        }
+        ++launches;
+      }
       GemvArgs a = gemvs[i];
       a.pdl = launches > 0;
       cap = enqueue(*d, a, s->capture_stream);
@@ -614,8 +743,11 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
   // host tables: thread-local, their capacity kept from call to call
   static thread_local std::vector<GemvArgs> gemvs;
   static thread_local std::vector<int> dep, layer_first;
+  static thread_local std::vector<const uint16_t*> x2;
+  static thread_local std::vector<ActOp> act;
   static thread_local std::vector<M1Task> tasks;
-  build_seq_gemvs(layers, n_layers, 1, hidden, kv_dim, ffn, io, &gemvs, &dep, &layer_first);
+  build_seq_gemvs(layers, SeqOptions{}, n_layers, 1, hidden, kv_dim, ffn, io, true, &gemvs, &dep, &x2, &act,
+                  &layer_first);
   const int n = static_cast<int>(gemvs.size());
   if (n > W4A16_STATIC_MAX_GEMVS || !seq_uses_tasks(1, gemvs)) return W4A16_ERR_LIMIT;
 
@@ -637,7 +769,7 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
     int l1 = l0 + 1;
     while (l1 < n_layers && layer_first[l1 + 1] - layer_first[l0] <= kM1MaxTasks) ++l1;
     const int t0 = layer_first[l0], t1 = layer_first[l1];
-    seq_tasks(gemvs, dep, layer_first, l0, l1, &tasks);
+    seq_tasks(gemvs, dep, x2, layer_first, l0, l1, &tasks);
     if (launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d->status, launches > 0, d->info, s) !=
         cudaSuccess) {
       cudaGetLastError();

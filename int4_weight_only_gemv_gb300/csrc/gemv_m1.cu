@@ -147,6 +147,21 @@ __device__ __forceinline__ bool wait_count(const int* counter, int target, uint6
   }
 }
 
+// SwiGLU of 8 packed fp16 values: fp16_RN(silu(g) u), silu(g) = g / (1 + e^-g),
+// computed in FP32 from the fp16 inputs.
+__device__ __forceinline__ uint4 swiglu8(uint4 g, uint4 u) {
+  uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w}, hw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float g0 = half_lo(gw[i]), g1 = half_hi(gw[i]);
+    const float h0 = g0 / (1.f + expf(-g0)) * half_lo(uw[i]);
+    const float h1 = g1 / (1.f + expf(-g1)) * half_hi(uw[i]);
+    hw[i] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(h0))) |
+            (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(h1))) << 16);
+  }
+  return make_uint4(hw[0], hw[1], hw[2], hw[3]);
+}
+
 // Dot products of two rows (8 packed words each, registers wa, wb) with this
 // thread's 64 activations.  Returns sum_k (1032 + q or 1152 + 16 q) x, the
 // second kind scaled back by 1/16, i.e. sum_k q x + C.
@@ -180,7 +195,10 @@ __device__ __forceinline__ void load_row(uint32_t addr, int rot, uint32_t (&w)[8
   w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
 }
 
-template <int MAXT>
+// kAct: some task of the list takes SwiGLU activations (x2 set).  The
+// instantiation without it carries no trace of that path, so the plain task
+// lists compile exactly as they would without the feature.
+template <int MAXT, bool kAct>
 __global__ void __launch_bounds__(kM1MaxThreads, 1)
     gemv_m1_kernel(const __grid_constant__ M1Params<MAXT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -335,6 +353,16 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         }
       }
       if (needs_signal(i)) ++nused;
+      // the task's output segments, in registers for the whole task
+      const int64_t e0 = tk.nseg < 2 ? INT64_MAX : tk.seg[0].n_end;
+      const int64_t e1 = tk.nseg < 3 ? INT64_MAX : tk.seg[1].n_end;
+      uint16_t* const y0 = tk.seg[0].y;
+      uint16_t* const y1 = tk.seg[1].y;
+      uint16_t* const y2 = tk.seg[2].y;
+      const uint16_t* const b0 = tk.seg[0].bias;
+      const uint16_t* const b1 = tk.seg[1].bias;
+      const uint16_t* const b2 = tk.seg[2].bias;
+      const bool has_bias = b0 != nullptr || b1 != nullptr || b2 != nullptr;
       // lanes per row: a power of two (for the butterfly) with lpr * RB <= 32
       int lpr = 1;
       while (2 * lpr * tp.RB <= 32) lpr *= 2;
@@ -367,7 +395,18 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
           float sum = (s0 + s1) + (s2 + s3);
           for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
           if (part == 0 && row < nr)
-            *out_ptr(tk, row_begin + lr0 + row) = __half_as_ushort(__float2half_rn(sum));
+          {
+            // y[n] = fp16_RN(sum + bias), routed to n's segment
+            const int64_t n = row_begin + lr0 + row;
+            const int seg = n < e0 ? 0 : (n < e1 ? 1 : 2);
+            const int64_t j = seg == 0 ? n : (seg == 1 ? n - e0 : n - e1);
+            if (has_bias) {
+              const uint16_t* b = seg == 0 ? b0 : (seg == 1 ? b1 : b2);
+              if (b != nullptr) sum += __half2float(__ushort_as_half(__ldg(b + j)));
+            }
+            uint16_t* y = seg == 0 ? y0 : (seg == 1 ? y1 : y2);
+            y[j] = __half_as_ushort(__float2half_rn(sum));
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(redempty0 + 8 * s);
@@ -436,7 +475,8 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         const int jj = rot ? (j ^ 4) : j;
         // plain loads through L1: x of a dependent task is read after the
         // reducer's acquire, and the line may have been prefetched (below)
-        const uint4 v = ld_u4(xp + 8 * jj);
+        uint4 v = ld_u4(xp + 8 * jj);
+        if (kAct && tk.x2 != nullptr) v = swiglu8(v, ld_u4(tk.x2 + u * 64 + 8 * jj));
         X[j] = pair_activations(v);
         const float even = (half_lo(X[j].p0) + half_hi(X[j].p0)) + (half_lo(X[j].p2) + half_hi(X[j].p2));
         const float odd = (half_lo(X[j].p1) + half_hi(X[j].p1)) + (half_lo(X[j].p3) + half_hi(X[j].p3));
@@ -461,12 +501,16 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     while (inext < p.ntasks && !cta_has_rows(p.task[inext])) ++inext;
     const uint16_t* xnext = nullptr;
     bool pending = false;
+    const uint16_t* x2next = nullptr;
     if (inext < p.ntasks && c < (p.task[inext].K >> 6)) {
       xnext = p.task[inext].x + c * 64;
-      if (p.task[inext].dep < 0 || p.done == nullptr)
+      if (kAct && p.task[inext].x2 != nullptr) x2next = p.task[inext].x2 + c * 64;
+      if (p.task[inext].dep < 0 || p.done == nullptr) {
         prefetch_l1(xnext);
-      else
+        if (kAct && x2next != nullptr) prefetch_l1(x2next);
+      } else {
         pending = true;
+      }
     }
 
     for (int t = 0; t < ntiles; ++t) {
@@ -477,6 +521,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       const int nr = rows - t * tp.RB;  // rows of this tile (may exceed RB)
       if (pending && mbar_try_wait(xready0 + 8 * (nwait % kXReady), (nwait / kXReady) & 1)) {
         prefetch_l1(xnext);
+        if (kAct && x2next != nullptr) prefetch_l1(x2next);
         pending = false;
       }
       float res[kRR];
@@ -532,7 +577,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
 }
 
 template <int MAXT>
-cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, bool pdl,
+cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, bool pdl, bool act,
                          cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -544,7 +589,8 @@ cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT>, p);
+  cudaError_t e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true>, p)
+                      : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -567,10 +613,11 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   tk.x = a.x;
   tk.N = a.N;
   tk.K = a.K;
+  tk.x2 = nullptr;
   tk.nseg = a.nseg;
   tk.dep = -1;
   tk.publish = 0;
-  for (int s = 0; s < kMaxSegs; ++s) tk.seg[s] = a.seg[s];
+  for (int s = 0; s < kMaxSegs; ++s) tk.seg[s] = M1Seg{a.seg[s].y, a.seg[s].bias, a.seg[s].n_end};
   // no dependency counting: CTAs beyond N would have no rows
   const int grid = a.N < d.sms ? a.N : d.sms;
   tk.rq = a.N / grid;
@@ -581,7 +628,7 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   p.stage_bytes = rp.stage_bytes;
   p.red_bytes = rp.red_bytes;
   p.CW = rp.CW;
-  return launch_tasks(p, rp, grid, a.pdl, st);
+  return launch_tasks(p, rp, grid, a.pdl, false, st);
 }
 
 cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uint32_t* status,
@@ -598,8 +645,11 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
     p.task[i].publish = 0;
     Ks[i] = tasks[i].K;
   }
-  for (int i = 0; i < ntasks; ++i)
+  bool act = false;
+  for (int i = 0; i < ntasks; ++i) {
     if (tasks[i].dep >= 0) p.task[tasks[i].dep].publish = 1;
+    act = act || tasks[i].x2 != nullptr;
+  }
   p.ntasks = ntasks;
   p.done = done;
   p.status = status;
@@ -610,14 +660,18 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
   p.red_bytes = rp.red_bytes;
   p.CW = rp.CW;
   // one CTA per SM: every CTA must be resident for the dependency counts
-  return launch_tasks(p, rp, d.sms, pdl, st);
+  return launch_tasks(p, rp, d.sms, pdl, act, st);
 }
 
 cudaError_t prepare_gemv_m1(const DeviceInfo& d) {
   const int limit = d.max_smem_optin < kM1SmemBudget + 1024 ? d.max_smem_optin : kM1SmemBudget + 1024;
-  cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+  cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       limit);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemv_m1_kernel<kM1MaxTasks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(gemv_m1_kernel<kM1MaxTasks, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           limit);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemv_m1_kernel<kM1MaxTasks, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               limit);
 }
 

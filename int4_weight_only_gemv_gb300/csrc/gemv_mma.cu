@@ -325,12 +325,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           for (int nt = 0; nt < NT; ++nt) {
             const int m0 = nt * 8 + 2 * t4;
             if (ra < N) {
-              if (m0 < a.M) *out_ptr(a, m0, ra) = __half_as_ushort(__float2half_rn(acc[nt][0]));
-              if (m0 + 1 < a.M) *out_ptr(a, m0 + 1, ra) = __half_as_ushort(__float2half_rn(acc[nt][1]));
+              if (m0 < a.M) store_out(a, m0, ra, acc[nt][0]);
+              if (m0 + 1 < a.M) store_out(a, m0 + 1, ra, acc[nt][1]);
             }
             if (rb < N) {
-              if (m0 < a.M) *out_ptr(a, m0, rb) = __half_as_ushort(__float2half_rn(acc[nt][2]));
-              if (m0 + 1 < a.M) *out_ptr(a, m0 + 1, rb) = __half_as_ushort(__float2half_rn(acc[nt][3]));
+              if (m0 < a.M) store_out(a, m0, rb, acc[nt][2]);
+              if (m0 + 1 < a.M) store_out(a, m0 + 1, rb, acc[nt][3]);
             }
           }
         } else {
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const uint32_t addr = part0 + 4 * static_cast<uint32_t>(i * KS);
         float v = 0.f;
         for (int q = 0; q < KS; ++q) v += lds_f32(addr + 4 * q);
-        *out_ptr(a, m, n) = __half_as_ushort(__float2half_rn(v));
+        store_out(a, m, n, v);
       }
       if (pe < blk_end) cluster_sync();  // the buffers may be rewritten by the next pass
     }

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2) gemv_rows_kernel(const GemvAr
     float v = 0.f;
 #pragma unroll
     for (int w = 0; w < kRowsWarps; ++w) v += red[w][threadIdx.x];
-    if (r0 + r < N) *out_ptr(a, m, r0 + r) = __half_as_ushort(__float2half_rn(v));
+    if (r0 + r < N) store_out(a, m, r0 + r, v);
   }
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace w4a16 {
@@ -10,11 +11,14 @@ namespace w4a16 {
 // Where output row n of activation row m goes.  A GEMV over a weight made of
 // up to three stacked matrices (e.g. [W_q; W_k; W_v]) can write each part to
 // its own buffer: rows [n_begin(s), n_end(s)) go to seg[s].y with row stride
-// seg[s].ldy (elements), n_begin(0) = 0, n_begin(s) = seg[s-1].n_end.
+// seg[s].ldy (elements), n_begin(0) = 0, n_begin(s) = seg[s-1].n_end.  With
+// a bias, y = fp16_RN(sum + bias[n - n_begin(s)]) (the fp16 bias added to the
+// FP32 sum before the one rounding).
 struct OutSeg {
   uint16_t* y;
   int64_t ldy;
   int64_t n_end;
+  const uint16_t* bias;  // fp16 bits, one per row of the segment, or null
 };
 constexpr int kMaxSegs = 3;
 
@@ -35,7 +39,8 @@ struct GemvArgs {
 };
 
 #ifdef __CUDACC__
-__device__ __forceinline__ uint16_t* out_ptr(const GemvArgs& a, int m, int64_t n) {
+// Epilogue: y[m][n] = fp16_RN(v + bias), routed to n's segment.
+__device__ __forceinline__ void store_out(const GemvArgs& a, int m, int64_t n, float v) {
   int s = 0;
   int64_t n0 = 0;
   if (a.nseg > 1 && n >= a.seg[0].n_end) {
@@ -46,7 +51,9 @@ __device__ __forceinline__ uint16_t* out_ptr(const GemvArgs& a, int m, int64_t n
       s = 2;
     }
   }
-  return a.seg[s].y + m * a.seg[s].ldy + (n - n0);
+  const OutSeg& sg = a.seg[s];
+  if (sg.bias != nullptr) v += __half2float(__ushort_as_half(__ldg(sg.bias + (n - n0))));
+  sg.y[m * sg.ldy + (n - n0)] = __half_as_ushort(__float2half_rn(v));
 }
 #endif
 
@@ -56,26 +63,43 @@ __device__ __forceinline__ uint16_t* out_ptr(const GemvArgs& a, int m, int64_t n
 // of the launch has written that output.  Weights and scales of every task
 // must stay constant for the whole launch (they are streamed ahead of any
 // dependency wait).
+// An output segment of an M = 1 task (one activation row: no row stride).
+struct M1Seg {
+  uint16_t* y;
+  const uint16_t* bias;  // fp16 bits or null (as OutSeg::bias)
+  int64_t n_end;
+};
+
 struct M1Task {
   const uint32_t* qweight;  // [N][K/8]
   const uint16_t* scales;   // [N][K/128] fp16 bits
   const uint16_t* x;        // [K] fp16 bits
+  // With x2, the activations are h[k] = fp16_RN(silu(x[k]) x2[k]) computed
+  // in FP32 from the fp16 inputs (SwiGLU: x the gate, x2 the up output);
+  // null: x itself.
+  const uint16_t* x2;
   int N, K;
-  int nseg;                 // 1..kMaxSegs
   int dep;                  // index of the task whose output x is, or -1
   int rq, rr;               // rows per CTA (set by the launcher): rq, one more for CTAs < rr
-  int publish;              // a later task reads this one's output (set by the launcher)
-  OutSeg seg[kMaxSegs];     // ldy unused (one activation row)
+  uint8_t nseg;             // 1..kMaxSegs
+  uint8_t publish;          // a later task reads this one's output (set by the launcher)
+  M1Seg seg[kMaxSegs];
 };
+static_assert(sizeof(M1Task) == 128, "a task record is 128 bytes (the table is kernel parameters)");
 constexpr int kM1MaxTasks = 224;  // the task table travels in the kernel parameters
 
 #ifdef __CUDACC__
-__device__ __forceinline__ uint16_t* out_ptr(const M1Task& a, int64_t n) {
-  // selects, not an indexed segment: keeps the task table in parameter space
+// Epilogue of an M = 1 task: y[n] = fp16_RN(v + bias), routed to n's segment
+// (selects, not an indexed segment: keeps the task table in parameter space).
+__device__ __forceinline__ void store_out(const M1Task& a, int64_t n, float v) {
   const int64_t e0 = a.seg[0].n_end, e1 = a.seg[1].n_end;
-  if (a.nseg < 2 || n < e0) return a.seg[0].y + n;
-  if (a.nseg < 3 || n < e1) return a.seg[1].y + (n - e0);
-  return a.seg[2].y + (n - e1);
+  const bool s0 = a.nseg < 2 || n < e0;
+  const bool s1 = !s0 && (a.nseg < 3 || n < e1);
+  const int64_t j = s0 ? n : (s1 ? n - e0 : n - e1);
+  uint16_t* y = s0 ? a.seg[0].y : (s1 ? a.seg[1].y : a.seg[2].y);
+  const uint16_t* b = s0 ? a.seg[0].bias : (s1 ? a.seg[1].bias : a.seg[2].bias);
+  if (b != nullptr) v += __half2float(__ushort_as_half(__ldg(b + j)));
+  y[j] = __half_as_ushort(__float2half_rn(v));
 }
 #endif
 
@@ -100,6 +124,10 @@ cudaError_t launch_gemv_rows(const GemvArgs& a, const DeviceInfo& d, cudaStream_
 // M = 8..16: mma.sync tensor-core kernel with cluster split-K.
 cudaError_t launch_gemv_mma(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 
+// h[m][j] = fp16_RN(silu(g[m*ld + j]) u[m*ld + j]) for j < n, rows of h with
+// stride n (the SwiGLU step of an unfused layer sequence).
+cudaError_t launch_swiglu(const uint16_t* g, const uint16_t* u, int64_t ld, uint16_t* h, int M, int n,
+                          bool pdl, cudaStream_t st);
 cudaError_t launch_dequant(const uint32_t* qweight, const uint16_t* scales, uint16_t* w_out,
                            int N, int K, cudaStream_t st);
 cudaError_t launch_quantize(const float* w, uint32_t* qweight, uint16_t* scales, int N, int K,

@@ -165,3 +165,44 @@ cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, uint32_t* status, cu
 }
 
 }  // namespace w4a16
+
+namespace w4a16 {
+namespace {
+
+// The SwiGLU step of a decoder layer's feed-forward (the page on hipfire,
+// "Overview of hipfire-arch-qwen2", "Key Technical Specifications": SwiGLU
+// FFN): h = fp16_RN(silu(g) u) with silu(g) = g / (1 + e^-g) in FP32, one
+// thread per element.  Runs between the [gate; up] and down GEMVs of a layer
+// sequence when it is not fused into the down GEMV.
+__global__ void swiglu_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u, int64_t ld,
+                              uint16_t* __restrict__ h, int M, int n) {
+  pdl_launch_dependents();
+  pdl_wait();  // g and u are the previous kernel's output
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(M) * n) return;
+  const int64_t m = i / n, j = i % n;
+  const float gv = __half2float(__ushort_as_half(g[m * ld + j]));
+  const float uv = __half2float(__ushort_as_half(u[m * ld + j]));
+  h[i] = __half_as_ushort(__float2half_rn(gv / (1.f + expf(-gv)) * uv));
+}
+
+}  // namespace
+
+cudaError_t launch_swiglu(const uint16_t* g, const uint16_t* u, int64_t ld, uint16_t* h, int M, int n,
+                          bool pdl, cudaStream_t st) {
+  const int64_t total = static_cast<int64_t>(M) * n;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((total + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, swiglu_kernel, g, u, ld, h, M, n);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

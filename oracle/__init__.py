@@ -61,6 +61,10 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.orc_dequant_f64.argtypes = [p, p, i64, i64, i64, p]
     L.orc_gemv.argtypes = [p, p, p, i64, i64, i64, i64, p]
     L.orc_gemv_rows.argtypes = [p, p, p, i64, i64, i64, i64, p, i64, p]
+    L.orc_silu.argtypes = [ctypes.c_double]
+    L.orc_silu.restype = ctypes.c_double
+    L.orc_swiglu.argtypes = [p, p, i64, p]
+    L.orc_swiglu.restype = None
     for f in ("orc_quantize", "orc_unpack", "orc_dequant", "orc_dequant_f64", "orc_gemv",
               "orc_gemv_rows"):
         getattr(L, f).restype = ctypes.c_int
@@ -173,6 +177,23 @@ def gemv_rows(qweight: np.ndarray, scales: np.ndarray, x: np.ndarray, rows: np.n
     _check(L.orc_gemv_rows(_ptr(qweight), _ptr(scales), _ptr(x), M, N, K8 * 8, group,
                            _ptr(rows), rows.size, _ptr(y)), "gemv_rows")
     return y
+
+
+def silu(v: float, L=None) -> float:
+    """silu(v) = v / (1 + e^-v) in double (the SwiGLU activation)."""
+    return float((L or lib()).orc_silu(float(v)))
+
+
+def swiglu(g: np.ndarray, u: np.ndarray, L=None) -> np.ndarray:
+    """h = fp16_RN(silu(g) * u) elementwise from fp16 bit patterns (uint16),
+    in double with one rounding."""
+    g = np.ascontiguousarray(g, dtype=np.uint16)
+    u = np.ascontiguousarray(u, dtype=np.uint16)
+    if g.shape != u.shape:
+        raise ValueError("g and u differ in shape")
+    h = np.empty(g.shape, dtype=np.uint16)
+    (L or lib()).orc_swiglu(_ptr(g), _ptr(u), g.size, _ptr(h))
+    return h
 
 
 def row_norms(qweight: np.ndarray, scales: np.ndarray, group: int = 128, L=None) -> np.ndarray:

@@ -250,3 +250,20 @@ int orc_gemv(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
   }
   return ORC_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * Layer epilogues around the GEMV (the page on hipfire, "Overview of
+ * hipfire-arch-qwen2", "Key Technical Specifications": a SwiGLU feed-forward
+ * and attention_bias on the Q, K and V projections).  A bias is added to the
+ * GEMV's unrounded FP64 sum by the caller; SwiGLU is defined here.
+ * ------------------------------------------------------------------------- */
+
+/* silu(v) = v * sigmoid(v) = v / (1 + e^-v), in double. */
+double orc_silu(double v) { return v / (1.0 + exp(-v)); }
+
+/* h[i] = fp16_RN(silu(g[i]) * u[i]) from fp16 g and u, in double with one
+ * rounding to fp16 at the end. */
+void orc_swiglu(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* h) {
+  for (int64_t i = 0; i < n; ++i)
+    h[i] = orc_double_to_half(orc_silu(orc_half_to_double(g[i])) * orc_half_to_double(u[i]));
+}

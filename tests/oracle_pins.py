@@ -310,13 +310,48 @@ def pin_gemv_fused_equals_separate(L):
     assert np.array_equal(y, np.hstack([oracle.gemv(qg, sg, x, 128, L), oracle.gemv(qu, su, x, 128, L)]))
 
 
+def pin_silu_closed_forms(L):
+    """silu(v) = v sigmoid(v): silu(0) = 0; silu(v) - silu(-v) = v (because
+    sigmoid(v) + sigmoid(-v) = 1); silu tends to v for large positive v and to
+    0 for large negative v; it is positive for v > 0 and negative for v < 0;
+    its minimum lies at v = -1.27846... where the derivative
+    sigmoid(v) (1 + v (1 - sigmoid(v))) vanishes, so silu there is below both
+    neighbours."""
+    assert oracle.silu(0.0, L) == 0.0
+    for v in (1e-3, 0.5, 1.0, 2.75, 7.0, 13.5):
+        assert abs((oracle.silu(v, L) - oracle.silu(-v, L)) - v) <= 1e-15 * max(1.0, v)
+        assert oracle.silu(v, L) > 0.0 > oracle.silu(-v, L)
+    assert abs(oracle.silu(40.0, L) - 40.0) < 1e-12
+    assert abs(oracle.silu(-40.0, L)) < 1e-12
+    vmin = -1.2784645427610738  # the minimum: sigmoid(v)(1 + v(1 - sigmoid(v))) = 0
+    assert oracle.silu(vmin, L) < oracle.silu(vmin - 0.01, L)
+    assert oracle.silu(vmin, L) < oracle.silu(vmin + 0.01, L)
+
+
+def pin_swiglu_vs_numpy(L):
+    """h = fp16_RN(silu(g) u) against numpy float64 arithmetic rounded by
+    numpy's float16 conversion, on random and special fp16 inputs; u = 1 and
+    a large g give h = g exactly, g = 0 gives 0."""
+    rng = np.random.default_rng(7)
+    g = rng.standard_normal(20000).astype(np.float16)
+    u = (rng.standard_normal(20000) * 2).astype(np.float16)
+    g[:6] = np.array([0.0, -0.0, 30.0, -30.0, 1e-4, 65504.0], dtype=np.float16)
+    u[:6] = np.array([1.0, 1.0, 1.0, 1.0, 3.0, 1.0], dtype=np.float16)
+    h = oracle.swiglu(g.view(np.uint16), u.view(np.uint16), L).view(np.float16)
+    gd, ud = g.astype(np.float64), u.astype(np.float64)
+    with np.errstate(over="ignore"):
+        want = (gd / (1.0 + np.exp(-gd)) * ud).astype(np.float16)
+    assert np.array_equal(h.view(np.uint16), want.view(np.uint16))
+    assert h[2] == np.float16(30.0) and h[0] == 0.0
+
+
 ALL_PINS = [
     pin_half_to_double_exhaustive, pin_half_roundtrip, pin_half_midpoints_ties_to_even,
     pin_half_overflow_and_specials, pin_half_vs_numpy_random, pin_hand_words,
     pin_dequant_half_scale, pin_hand_gemvs, pin_quantizer_properties,
     pin_quantizer_exact_recovery, pin_quantizer_rounding_ties, pin_quantizer_zero_group,
     pin_quantizer_errors, pin_gemv_vs_numpy_matmul, pin_gemv_m_consistency,
-    pin_gemv_fused_equals_separate,
+    pin_gemv_fused_equals_separate, pin_silu_closed_forms, pin_swiglu_vs_numpy,
 ]
 
 

@@ -22,7 +22,7 @@ def L():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(w4a16_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(w4a16_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declarations_match_binding_list():
@@ -144,6 +144,26 @@ def test_layer_seq_run_static_argument_checks(L):
     assert L.w4a16_layer_seq_run_static(layers(1, 128, 128, 28800), 1, 128, 128, 28800, 128,
                                         ctypes.byref(io), None) == 11
     assert L.w4a16_status_str(11) and b"limit" in L.w4a16_status_str(11)
+
+
+def test_layer_seq_create2_argument_checks(L):
+    """Epilogue options are checked on the host: unknown flag bits, misaligned
+    biases and biases overlapping an output are rejected before any device
+    work."""
+    lw = (w4._LayerWeights * 1)()
+    for pj in range(7):
+        lw[0].qweight[pj] = 0x10_0000_0000 + pj * 0x100_0000
+        lw[0].scales[pj] = 0x10_0000_0000 + pj * 0x100_0000 + 0x80_0000
+    io = w4._SeqIO(*[0x20_0000_0000 + 0x1000_0000 * i for i in range(7)])
+    out = ctypes.c_void_p(None)
+    args = (1, 1, 256, 128, 512, 128, ctypes.byref(io), ctypes.byref(out))
+    assert L.w4a16_layer_seq_create2(lw, None, 0x2, *args) == 2
+    b = (w4._LayerBias * 1)()
+    b[0].bias[0] = 0x30_0000_0008  # not 16-byte aligned
+    assert L.w4a16_layer_seq_create2(lw, b, 0, *args) == 3
+    b[0].bias[0] = 0x20_0000_0000 + 0x1000_0000 * 5 + 64  # inside y_gu
+    assert L.w4a16_layer_seq_create2(lw, b, 1, *args) == 6
+    assert L.w4a16_layer_seq_create2(lw, None, 0, 1, 1, 256, 128, 512, 128, ctypes.byref(io), None) == 1
 
 
 def test_device_status_null(L):

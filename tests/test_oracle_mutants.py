@@ -34,6 +34,11 @@ MUTANTS = [
     ("exponent_bias", "v = ldexp((double)(1024 + f), e - 25);", "v = ldexp((double)(1024 + f), e - 24);"),
     ("x_index_transposed", "acc += orc_half_to_double(x[m * K + k]) * w_hat(qweight, scales, K, G, n, k);\n      y[m * N + n]",
      "acc += orc_half_to_double(x[k * M + m]) * w_hat(qweight, scales, K, G, n, k);\n      y[m * N + n]"),
+    ("silu_exp_sign", "return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
+    ("silu_missing_one", "return v / (1.0 + exp(-v));", "return v / exp(-v);"),
+    ("swiglu_gate_up_swapped",
+     "orc_silu(orc_half_to_double(g[i])) * orc_half_to_double(u[i])",
+     "orc_silu(orc_half_to_double(u[i])) * orc_half_to_double(g[i])"),
 ]
 
 
