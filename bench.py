@@ -397,7 +397,35 @@ def per_config_table(layers, dev, reps=20):
     b = gemv_bytes(cfg.N, cfg.K, 1)
     out["tiny"] = {"M": 1, "N": cfg.N, "K": cfg.K, "us_per_gemv": round(us, 3),
                    "GBps": round(b / us / 1e3, 1), "bytes": b, "note": "L2-resident, latency-bound"}
+    out["layer_seq_qkv_bias_swiglu"] = epilogue_step(layers, dev, reps, ("q", "k", "v"))
+    out["layer_seq_bias_swiglu"] = epilogue_step(layers, dev, reps, synth.PROJ_NAMES)
     return out
+
+
+def epilogue_step(layers, dev, reps, bias_on):
+    """The 28-layer M = 1 step with the fused epilogues (output biases on the
+    projections bias_on, SwiGLU between [gate; up] and down): ms per step
+    and GB/s over the same algorithmic bytes plus the bias bytes."""
+    import torch
+
+    import int4_weight_only_gemv_gb300 as w4
+    import synth
+    H, KV, F = synth.HIDDEN, synth.KV_DIM, synth.FFN
+    width = {"q": H, "k": KV, "v": KV, "o": H, "gate": F, "up": F, "down": H}
+    g = torch.Generator().manual_seed(5)
+    biases = [{n: (torch.randn(width[n], generator=g) * 0.1).to(torch.float16).to(dev) for n in bias_on}
+              for _ in layers]
+    io = make_io(dev)
+    seq = w4.LayerSeq([{k: lw[k] for k in synth.PROJ_NAMES} for lw in layers], io, 1, H, KV, F,
+                      biases=biases, swiglu=True)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        seq.run(stream)
+    ms = time_graph_replays(seq, stream, reps, lambda: None) / reps
+    seq.close()
+    b = config_block()["bytes_per_step"] + 2 * sum(width[n] for n in bias_on) * len(layers)
+    return {"M": 1, "layers": len(layers), "ms_per_step": round(ms, 4), "GBps": round(b / ms / 1e6, 1),
+            "bytes": b, "note": "biases on " + "/".join(bias_on) + ", SwiGLU fused into down"}
 
 
 def bench_ours(args, rank, world):

@@ -148,14 +148,15 @@ __device__ __forceinline__ bool wait_count(const int* counter, int target, uint6
 }
 
 // SwiGLU of 8 packed fp16 values: fp16_RN(silu(g) u), silu(g) = g / (1 + e^-g),
-// computed in FP32 from the fp16 inputs.
+// computed in FP32 from the fp16 inputs with the fast exponential and
+// division (relative error ~1e-6, far below the fp16 result's 2^-11).
 __device__ __forceinline__ uint4 swiglu8(uint4 g, uint4 u) {
   uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w}, hw[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float g0 = half_lo(gw[i]), g1 = half_hi(gw[i]);
-    const float h0 = g0 / (1.f + expf(-g0)) * half_lo(uw[i]);
-    const float h1 = g1 / (1.f + expf(-g1)) * half_hi(uw[i]);
+    const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * half_lo(uw[i]);
+    const float h1 = __fdividef(g1, 1.f + __expf(-g1)) * half_hi(uw[i]);
     hw[i] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(h0))) |
             (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(h1))) << 16);
   }

@@ -171,8 +171,8 @@ namespace {
 
 // The SwiGLU step of a decoder layer's feed-forward (the page on hipfire,
 // "Overview of hipfire-arch-qwen2", "Key Technical Specifications": SwiGLU
-// FFN): h = fp16_RN(silu(g) u) with silu(g) = g / (1 + e^-g) in FP32, one
-// thread per element.  Runs between the [gate; up] and down GEMVs of a layer
+// FFN): h = fp16_RN(silu(g) u) with silu(g) = g / (1 + e^-g) in FP32 (fast
+// exponential and division, as the fused M = 1 path), one thread per element.  Runs between the [gate; up] and down GEMVs of a layer
 // sequence when it is not fused into the down GEMV.
 __global__ void swiglu_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u, int64_t ld,
                               uint16_t* __restrict__ h, int M, int n) {
@@ -183,7 +183,7 @@ __global__ void swiglu_kernel(const uint16_t* __restrict__ g, const uint16_t* __
   const int64_t m = i / n, j = i % n;
   const float gv = __half2float(__ushort_as_half(g[m * ld + j]));
   const float uv = __half2float(__ushort_as_half(u[m * ld + j]));
-  h[i] = __half_as_ushort(__float2half_rn(gv / (1.f + expf(-gv)) * uv));
+  h[i] = __half_as_ushort(__float2half_rn(__fdividef(gv, 1.f + __expf(-gv)) * uv));
 }
 
 }  // namespace
