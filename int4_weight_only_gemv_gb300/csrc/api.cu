@@ -57,8 +57,7 @@ w4a16_status device_state(DeviceState** out) {
     d.info.sms = sms;
     d.info.max_smem_optin = smem;
     d.status = static_cast<uint32_t*>(addr);
-    if (prepare_gemv_m1(d.info) != cudaSuccess || prepare_gemv_mma(d.info) != cudaSuccess ||
-        prepare_gemv_tc(d.info) != cudaSuccess) {
+    if (prepare_gemv_m1(d.info) != cudaSuccess || prepare_gemv_mma(d.info) != cudaSuccess) {
       cudaGetLastError();
       return W4A16_ERR_CUDA;
     }
@@ -114,8 +113,6 @@ w4a16_status enqueue(const DeviceState& d, GemvArgs a, cudaStream_t st) {
     e = launch_gemv_m1(a, d.info, st);
   else if (a.M <= 7)
     e = launch_gemv_rows(a, d.info, st);
-  else if (gemv_tc_supported(a))
-    e = launch_gemv_tc(a, d.info, st);
   else
     e = launch_gemv_mma(a, d.info, st);
   if (e != cudaSuccess) {

@@ -372,6 +372,26 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+namespace {
+
 // Tensor map of the packed weight as uint32 [N][K/8], box 32 words x rows,
 // 128-byte swizzle.
 bool weight_tensor_map(CUtensorMap* m, const uint32_t* qweight, int N, int K, int box_rows) {

@@ -125,11 +125,6 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
 cudaError_t launch_gemv_rows(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 // M = 8..16: mma.sync tensor-core kernel with cluster split-K.
 cudaError_t launch_gemv_mma(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
-// M <= 16 on the tcgen05 tensor cores (unpacked weights and accumulators in
-// tensor memory), cluster split-K; needs ldx % 8 == 0 and 16-byte aligned x
-// and weights (TMA).
-bool gemv_tc_supported(const GemvArgs& a);
-cudaError_t launch_gemv_tc(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 // cuTensorMapEncodeTiled from the driver (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
@@ -149,7 +144,6 @@ cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, uint32_t* status, cu
 // must run once per device before the first launch and outside stream capture.
 cudaError_t prepare_gemv_m1(const DeviceInfo& d);
 cudaError_t prepare_gemv_mma(const DeviceInfo& d);
-cudaError_t prepare_gemv_tc(const DeviceInfo& d);
 
 // Wall-clock bound on any in-kernel wait (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
