@@ -65,6 +65,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.orc_silu.restype = ctypes.c_double
     L.orc_swiglu.argtypes = [p, p, i64, p]
     L.orc_swiglu.restype = None
+    L.orc_attn_decode.argtypes = [p, p, p, i64, i64, i64, i64, i64, p]
+    L.orc_attn_decode.restype = ctypes.c_int
     for f in ("orc_quantize", "orc_unpack", "orc_dequant", "orc_dequant_f64", "orc_gemv",
               "orc_gemv_rows"):
         getattr(L, f).restype = ctypes.c_int
@@ -194,6 +196,45 @@ def swiglu(g: np.ndarray, u: np.ndarray, L=None) -> np.ndarray:
     h = np.empty(g.shape, dtype=np.uint16)
     (L or lib()).orc_swiglu(_ptr(g), _ptr(u), g.size, _ptr(h))
     return h
+
+
+def attn_decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, T: int | None = None, L=None) -> np.ndarray:
+    """Decode attention of one token (see orc_attn_decode): q uint16 (fp16 bits)
+    [H][D], k and v uint16 [Hkv][t_stride][D] (keys t < T used, default all);
+    returns o float64 [H][D]."""
+    L = L or lib()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    H, D = q.shape
+    Hkv, t_stride, Dk = k.shape
+    assert Dk == D and v.shape == k.shape
+    T = t_stride if T is None else T
+    o = np.empty((H, D), np.float64)
+    _check(L.orc_attn_decode(_ptr(q), _ptr(k), _ptr(v), H, Hkv, D, T, t_stride, _ptr(o)), "attn_decode")
+    return o
+
+
+# Tolerance of the decode-attention check, per query head h reading KV head g:
+#   max_d |o - o_ref| <= ATTN_SLOPE * max_{t < T, d} |v_g[t][d]| + ATTN_FLOOR.
+# The GPU rounds the softmax weights to fp16 for the P.V product (relative
+# error <= 2^-11 per weight, so <= 2^-11 max|v| on o) and o to fp16 (another
+# 2^-11 max|v|); scores and sums are FP32.  2e-3 is about twice their sum.
+ATTN_SLOPE = 2e-3
+ATTN_FLOOR = 1e-5
+
+
+def check_attn(o: np.ndarray, o_ref: np.ndarray, v: np.ndarray, n_heads: int, T: int) -> dict:
+    """o, o_ref [H][D] float64; v uint16 [Hkv][t_stride][D].  Returns a report
+    with 'ok'."""
+    Hkv = v.shape[0]
+    group = n_heads // Hkv
+    vmax = np.abs(half_to_double(v[:, :T, :])).reshape(Hkv, -1).max(axis=1)
+    bound = ATTN_SLOPE * vmax[np.arange(n_heads) // group] + ATTN_FLOOR
+    err = np.abs(o - o_ref).max(axis=1)
+    finite = bool(np.isfinite(o).all())
+    return {"ok": finite and bool((err <= bound).all()), "finite": finite,
+            "max_err": err.tolist(), "bound": bound.tolist()}
 
 
 def row_norms(qweight: np.ndarray, scales: np.ndarray, group: int = 128, L=None) -> np.ndarray:

@@ -40,6 +40,7 @@
  * aarch64, so the oracle gives the same bits on both hosts.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -266,4 +267,56 @@ double orc_silu(double v) { return v / (1.0 + exp(-v)); }
 void orc_swiglu(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* h) {
   for (int64_t i = 0; i < n; ++i)
     h[i] = orc_double_to_half(orc_silu(orc_half_to_double(g[i])) * orc_half_to_double(u[i]));
+}
+
+/* ---------------------------------------------------------------------------
+ * Decode attention over an fp16 KV cache (the page "LLM170", README of the
+ * LLM170 engine: the paragraph on its HIP attention path, whose decode kernel
+ * reads an f16 copy of the KV cache, and the long-context benchmark paragraph,
+ * where that decode attention is bandwidth-bound on the f16 KV).  The pages
+ * print no formula; this is the standard scaled dot-product attention of one
+ * query token with grouped-query heads, the model shape of the page "Costruire
+ * un runtime di inference LLM da zero", last paragraph of "Tre bug che
+ * insegnano" (28 query heads sharing 4 KV heads, head dimension 128).
+ *
+ * Query head h (of n_heads) reads KV head g = h / (n_heads / n_kv_heads):
+ *   s_t = (q_h . k_{g,t}) / sqrt(D)                     for t = 0 .. T-1
+ *   p_t = exp(s_t - max_u s_u) / sum_u exp(s_u - max_u s_u)
+ *   o_h = sum_t p_t v_{g,t}
+ * in double from the fp16 inputs, sums in ascending t (and d).  Layout:
+ * q [n_heads][D], k and v [n_kv_heads][t_stride][D] (keys t < T used),
+ * o [n_heads][D] as double.
+ * ------------------------------------------------------------------------- */
+int orc_attn_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t n_heads,
+                    int64_t n_kv_heads, int64_t D, int64_t T, int64_t t_stride, double* o) {
+  if (n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 || D <= 0 || T <= 0 ||
+      t_stride < T)
+    return ORC_ERR_SHAPE;
+  const int64_t group = n_heads / n_kv_heads;
+  double* s = (double*)malloc(sizeof(double) * (size_t)T);
+  if (s == NULL) return ORC_ERR_SHAPE;
+  const double scale = 1.0 / sqrt((double)D);
+  for (int64_t h = 0; h < n_heads; ++h) {
+    const int64_t g = h / group;
+    double smax = -INFINITY;
+    for (int64_t t = 0; t < T; ++t) {
+      double dot = 0.0;
+      for (int64_t d = 0; d < D; ++d)
+        dot += orc_half_to_double(q[h * D + d]) * orc_half_to_double(k[(g * t_stride + t) * D + d]);
+      s[t] = dot * scale;
+      if (s[t] > smax) smax = s[t];
+    }
+    double sum = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+      s[t] = exp(s[t] - smax);
+      sum += s[t];
+    }
+    for (int64_t d = 0; d < D; ++d) {
+      double acc = 0.0;
+      for (int64_t t = 0; t < T; ++t) acc += s[t] * orc_half_to_double(v[(g * t_stride + t) * D + d]);
+      o[h * D + d] = acc / sum;
+    }
+  }
+  free(s);
+  return ORC_OK;
 }

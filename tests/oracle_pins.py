@@ -14,6 +14,8 @@ from __future__ import annotations
 
 import os
 
+import math
+
 import numpy as np
 
 import oracle
@@ -345,6 +347,84 @@ def pin_swiglu_vs_numpy(L):
     assert h[2] == np.float16(30.0) and h[0] == 0.0
 
 
+def _attn_inputs(seed, H, Hkv, T, D=128, t_stride=None):
+    rng = np.random.default_rng(seed)
+    t_stride = T if t_stride is None else t_stride
+    q = rng.standard_normal((H, D)).astype(np.float16).view(np.uint16)
+    k = rng.standard_normal((Hkv, t_stride, D)).astype(np.float16).view(np.uint16)
+    v = rng.standard_normal((Hkv, t_stride, D)).astype(np.float16).view(np.uint16)
+    return q, k, v
+
+
+def pin_attn_single_key(L):
+    """T = 1: every softmax weight is 1, so o_h is exactly the value row of
+    the KV head its group reads (h / 7 for 28 query heads over 4 KV heads)."""
+    q, k, v = _attn_inputs(1, 28, 4, 1)
+    o = oracle.attn_decode(q, k, v, L=L)
+    vd = v.view(np.float16).astype(np.float64)
+    for h in range(28):
+        assert np.array_equal(o[h], vd[h // 7, 0]), h
+
+
+def pin_attn_two_keys_scale(L):
+    """T = 2 with q = e0, k0 = 8 e0, k1 = 0 (D = 128): the scores are
+    8 / sqrt(128) = 1/sqrt(2) and 0, so p0 is the logistic function of
+    1/sqrt(2) and o = p0 v0 + (1 - p0) v1."""
+    D = 128
+    q = np.zeros((1, D), np.float16)
+    q[0, 0] = 1.0
+    k = np.zeros((1, 2, D), np.float16)
+    k[0, 0, 0] = 8.0
+    v = np.random.default_rng(2).standard_normal((1, 2, D)).astype(np.float16)
+    o = oracle.attn_decode(q.view(np.uint16), k.view(np.uint16), v.view(np.uint16), L=L)
+    p0 = 1.0 / (1.0 + math.exp(-1.0 / math.sqrt(2.0)))
+    vd = v.astype(np.float64)
+    assert np.allclose(o[0], p0 * vd[0, 0] + (1.0 - p0) * vd[0, 1], rtol=0, atol=1e-13)
+
+
+def pin_attn_uniform_and_constant(L):
+    """Identical keys give uniform weights, so o is the mean of the value
+    rows; identical value rows give o equal to that row whatever q is."""
+    q, k, v = _attn_inputs(3, 4, 2, 9)
+    k[:, :, :] = k[:, :1, :]
+    o = oracle.attn_decode(q, k, v, L=L)
+    vd = v.view(np.float16).astype(np.float64)
+    for h in range(4):
+        assert np.allclose(o[h], vd[h // 2].mean(axis=0), rtol=0, atol=1e-13)
+    q, k, v = _attn_inputs(4, 4, 2, 9)
+    v[:, :, :] = v[:, :1, :]
+    o = oracle.attn_decode(q, k, v, L=L)
+    vd = v.view(np.float16).astype(np.float64)
+    for h in range(4):
+        assert np.allclose(o[h], vd[h // 2, 0], rtol=0, atol=1e-13)
+
+
+def pin_attn_permutation_and_dominance(L):
+    """Permuting the (key, value) pairs together leaves o unchanged; a key
+    with a score far above the others takes all the weight."""
+    q, k, v = _attn_inputs(5, 7, 1, 33)
+    o = oracle.attn_decode(q, k, v, L=L)
+    perm = np.random.default_rng(5).permutation(33)
+    o2 = oracle.attn_decode(q, k[:, perm].copy(), v[:, perm].copy(), L=L)
+    assert np.allclose(o, o2, rtol=0, atol=1e-12)
+    qd = q.view(np.float16)
+    k2 = k.view(np.float16).copy()
+    k2[0, 17] = (qd[0] * 8).astype(np.float16)  # score of key 17 for head 0: ~ 8 |q|^2 / sqrt(D)
+    o3 = oracle.attn_decode(q, k2.view(np.uint16), v, L=L)
+    assert np.allclose(o3[0], v.view(np.float16)[0, 17].astype(np.float64), rtol=0, atol=1e-9)
+
+
+def pin_attn_stride_and_prefix(L):
+    """Keys at t >= T are never read (poisoned with NaN there), and a cache
+    of T keys inside a larger stride gives the same o as the compact one."""
+    q, k, v = _attn_inputs(6, 8, 2, 24, t_stride=40)
+    k[:, 24:] = np.float16(np.nan).view(np.uint16)
+    v[:, 24:] = np.float16(np.nan).view(np.uint16)
+    o = oracle.attn_decode(q, k, v, T=24, L=L)
+    o2 = oracle.attn_decode(q, k[:, :24].copy(), v[:, :24].copy(), L=L)
+    assert np.isfinite(o).all() and np.array_equal(o, o2)
+
+
 ALL_PINS = [
     pin_half_to_double_exhaustive, pin_half_roundtrip, pin_half_midpoints_ties_to_even,
     pin_half_overflow_and_specials, pin_half_vs_numpy_random, pin_hand_words,
@@ -352,6 +432,8 @@ ALL_PINS = [
     pin_quantizer_exact_recovery, pin_quantizer_rounding_ties, pin_quantizer_zero_group,
     pin_quantizer_errors, pin_gemv_vs_numpy_matmul, pin_gemv_m_consistency,
     pin_gemv_fused_equals_separate, pin_silu_closed_forms, pin_swiglu_vs_numpy,
+    pin_attn_single_key, pin_attn_two_keys_scale, pin_attn_uniform_and_constant,
+    pin_attn_permutation_and_dominance, pin_attn_stride_and_prefix,
 ]
 
 

@@ -36,6 +36,14 @@ MUTANTS = [
      "acc += orc_half_to_double(x[k * M + m]) * w_hat(qweight, scales, K, G, n, k);\n      y[m * N + n]"),
     ("silu_exp_sign", "return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
     ("silu_missing_one", "return v / (1.0 + exp(-v));", "return v / exp(-v);"),
+    ("attn_missing_scale", "s[t] = dot * scale;", "s[t] = dot;"),
+    ("attn_gqa_mapping_modulo", "const int64_t g = h / group;", "const int64_t g = h % n_kv_heads;"),
+    ("attn_values_from_keys", "acc += s[t] * orc_half_to_double(v[(g * t_stride + t) * D + d]);",
+     "acc += s[t] * orc_half_to_double(k[(g * t_stride + t) * D + d]);"),
+    ("attn_dropped_last_key", "for (int64_t t = 0; t < T; ++t) {\n      s[t] = exp(s[t] - smax);",
+     "for (int64_t t = 0; t < T - 1; ++t) {\n      s[t] = exp(s[t] - smax);"),
+    ("attn_stride_ignored", "dot += orc_half_to_double(q[h * D + d]) * orc_half_to_double(k[(g * t_stride + t) * D + d]);",
+     "dot += orc_half_to_double(q[h * D + d]) * orc_half_to_double(k[(g * T + t) * D + d]);"),
     ("swiglu_gate_up_swapped",
      "orc_silu(orc_half_to_double(g[i])) * orc_half_to_double(u[i])",
      "orc_silu(orc_half_to_double(u[i])) * orc_half_to_double(g[i])"),
