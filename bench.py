@@ -397,9 +397,53 @@ def per_config_table(layers, dev, reps=20):
     b = gemv_bytes(cfg.N, cfg.K, 1)
     out["tiny"] = {"M": 1, "N": cfg.N, "K": cfg.K, "us_per_gemv": round(us, 3),
                    "GBps": round(b / us / 1e3, 1), "bytes": b, "note": "L2-resident, latency-bound"}
+    out["attn_decode_T8192"] = attn_decode_line(dev, reps)
     out["layer_seq_qkv_bias_swiglu"] = epilogue_step(layers, dev, reps, ("q", "k", "v"))
     out["layer_seq_bias_swiglu"] = epilogue_step(layers, dev, reps, synth.PROJ_NAMES)
     return out
+
+
+def attn_decode_line(dev, reps, T=8192):
+    """Decode attention of one token over an fp16 KV cache of T keys with the
+    Qwen-7B head layout (28 query heads over 4 KV heads, head dimension 128):
+    a CUDA graph of 28 calls over 28 distinct caches (cold L2: 28 x 16.8 MB),
+    us per call and GB/s over the cache bytes plus q and o."""
+    import torch
+
+    import int4_weight_only_gemv_gb300 as w4
+    import synth
+    H, Hkv, D = synth.HIDDEN // 128, synth.KV_DIM // 128, 128
+    g = torch.Generator(device=dev).manual_seed(8192)
+    caches = [(torch.randn((Hkv, T, D), generator=g, device=dev).half(),
+               torch.randn((Hkv, T, D), generator=g, device=dev).half()) for _ in range(synth.N_LAYERS)]
+    qs = [torch.randn((H, D), generator=g, device=dev).half() for _ in caches]
+    os_ = [torch.empty((H, D), dtype=torch.float16, device=dev) for _ in caches]
+    ws = torch.empty(w4.attn_decode_workspace(H, Hkv, T) // 4 + 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for (k, v), q, o in zip(caches, qs, os_):
+            w4.w4a16_attn_decode(q, k, v, T, o=o, workspace=ws)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for (k, v), q, o in zip(caches, qs, os_):
+            w4.w4a16_attn_decode(q, k, v, T, o=o, workspace=ws)
+    for _ in range(3):
+        gr.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    s.record(cur)
+    for _ in range(reps):
+        gr.replay()
+    e.record(cur)
+    torch.cuda.synchronize()
+    if w4.w4a16_device_status(clear=True):
+        raise RuntimeError("a kernel flagged a failure")
+    us = 1e3 * s.elapsed_time(e) / (reps * len(caches))
+    b = 2 * Hkv * T * D * 2 + 2 * H * D * 2
+    return {"H": H, "Hkv": Hkv, "T": T, "us_per_call": round(us, 3), "GBps": round(b / us / 1e3, 1),
+            "bytes": b, "note": "fp16 KV cache, 28 rotated caches (cold L2), partial + merge launches"}
 
 
 def epilogue_step(layers, dev, reps, bias_on):
@@ -540,6 +584,28 @@ def run_case(args):
                           "replays": args.launches, "bytes_per_replay": per_layer * n,
                           "us_per_replay": 1e3 * s.elapsed_time(e) / args.launches}))
         seq.close()
+        return
+    if args.case == "attn":
+        # one decode-attention call (Qwen-7B heads, T = 8192), launched `launches` times
+        dev = torch.device("cuda", 0)
+        H, Hkv, D, T = synth.HIDDEN // 128, synth.KV_DIM // 128, 128, 8192
+        gen = torch.Generator(device=dev).manual_seed(1)
+        k = torch.randn((Hkv, T, D), generator=gen, device=dev).half()
+        v = torch.randn((Hkv, T, D), generator=gen, device=dev).half()
+        q = torch.randn((H, D), generator=gen, device=dev).half()
+        o = torch.empty((H, D), dtype=torch.float16, device=dev)
+        ws = torch.empty(w4.attn_decode_workspace(H, Hkv, T) // 4 + 4, dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(args.launches):
+            w4.w4a16_attn_decode(q, k, v, T, o=o, workspace=ws)
+        e.record()
+        torch.cuda.synchronize()
+        if w4.w4a16_device_status(clear=True):
+            raise RuntimeError("a kernel flagged a failure")
+        print(json.dumps({"case": "attn", "H": H, "Hkv": Hkv, "T": T, "launches": args.launches,
+                          "us_per_call_warm_l2": 1e3 * s.elapsed_time(e) / args.launches}))
         return
     cfg = {c.name: c for c in synth.ALL_GEMVS}[args.case]
     dev = torch.device("cuda", 0)

@@ -303,6 +303,37 @@ w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* layers, int n
                                         int hidden, int kv_dim, int ffn, int group,
                                         const w4a16_seq_io* io, void* stream);
 
+/*
+ * Decode attention over an fp16 KV cache -- the bandwidth-bound kernel next
+ * to the GEMV in a decode step (the page "LLM170", README of the LLM170
+ * engine: its HIP decode attention reads an f16 copy of the KV cache and is
+ * bound by that read at long context).  For one query token and query head h
+ * reading KV head g = h / (n_heads / n_kv_heads) (grouped-query attention):
+ *   o_h = sum_{t < T} softmax_t(q_h . k_{g,t} / sqrt(head_dim)) v_{g,t}
+ * with FP32 scores, FP32 softmax statistics, the softmax weights rounded to
+ * fp16 for the product with V (FP32 accumulation) and o rounded to fp16.
+ *   q          fp16 [n_heads][head_dim]
+ *   k_cache,   fp16 [n_kv_heads][t_stride][head_dim]; keys 0 .. T-1 of each
+ *   v_cache    head are read, rows T .. t_stride-1 are never touched
+ *   o          fp16 [n_heads][head_dim]; must not overlap q, the caches or
+ *              the workspace
+ *   workspace  device scratch of at least the size that
+ *              w4a16_attn_decode_workspace returns for the same shape, owned
+ *              by the caller; must not overlap q or the caches.  Two calls
+ *              that overlap on the GPU must not share it.
+ * Limits: head_dim == 128, n_heads a multiple of n_kv_heads with at most 16
+ * query heads per KV head, 1 <= T <= t_stride <= 2^24 (W4A16_ERR_SHAPE
+ * otherwise, also for a workspace smaller than required); every pointer
+ * 16-byte aligned (W4A16_ERR_ALIGN).  Two kernel launches on `stream` (the
+ * second a programmatic dependent of the first); never allocates, never
+ * synchronises, deterministic.
+ */
+w4a16_status w4a16_attn_decode_workspace(int n_heads, int n_kv_heads, int head_dim, int T,
+                                         size_t* bytes);
+w4a16_status w4a16_attn_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                               uint16_t* o, int n_heads, int n_kv_heads, int head_dim, int T,
+                               int t_stride, float* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

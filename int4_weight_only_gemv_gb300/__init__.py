@@ -19,7 +19,7 @@ __all__ = [
     "W4A16Error", "lib", "w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
     "w4a16_selftest_wait_timeout", "w4a16_layer_seq_run_static", "STATIC_MAX_GEMVS",
     "LayerSeq", "GROUP", "MAX_M", "MAX_K", "DEV_NONFINITE", "DEV_SCALE_OVERFLOW",
-    "DEV_PIPE_TIMEOUT", "STATUS", "EXPORTED_SYMBOLS",
+    "DEV_PIPE_TIMEOUT", "STATUS", "EXPORTED_SYMBOLS", "w4a16_attn_decode", "attn_decode_workspace",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -47,6 +47,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_device_status", "w4a16_selftest_wait_timeout", "w4a16_layer_seq_create", "w4a16_layer_seq_num_launches",
     "w4a16_layer_seq_run", "w4a16_layer_seq_run_host", "w4a16_layer_seq_sync",
     "w4a16_layer_seq_destroy", "w4a16_layer_seq_run_static", "w4a16_layer_seq_create2",
+    "w4a16_attn_decode_workspace", "w4a16_attn_decode",
 )
 
 
@@ -105,10 +106,13 @@ def lib() -> ctypes.CDLL:
         L.w4a16_layer_seq_destroy.restype = None
         L.w4a16_layer_seq_run_static.argtypes = [ctypes.POINTER(_LayerWeights), i, i, i, i, i,
                                                  ctypes.POINTER(_SeqIO), p]
+        L.w4a16_attn_decode_workspace.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        L.w4a16_attn_decode.argtypes = [p, p, p, p, i, i, i, i, i, p, ctypes.c_size_t, p]
         for f in ("w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
                   "w4a16_selftest_wait_timeout",
                   "w4a16_layer_seq_create", "w4a16_layer_seq_run", "w4a16_layer_seq_run_host",
-                  "w4a16_layer_seq_sync", "w4a16_layer_seq_run_static", "w4a16_layer_seq_create2"):
+                  "w4a16_layer_seq_sync", "w4a16_layer_seq_run_static", "w4a16_layer_seq_create2",
+                  "w4a16_attn_decode_workspace", "w4a16_attn_decode"):
             getattr(L, f).restype = i
         _LIB = L
     return _LIB
@@ -145,6 +149,41 @@ def w4a16_gemv(qweight, scales, x, y=None, stream=None):
 def w4a16_gemv_raw(qw_ptr, sc_ptr, x_ptr, y_ptr, M, N, K, group=GROUP, stream=None) -> int:
     """Unchecked status passthrough (tests of the argument checks use it)."""
     return lib().w4a16_gemv(qw_ptr, sc_ptr, x_ptr, y_ptr, M, N, K, group, stream)
+
+
+def attn_decode_workspace(n_heads, n_kv_heads, T, head_dim=128) -> int:
+    """Bytes of device scratch w4a16_attn_decode needs for this shape."""
+    n = ctypes.c_size_t(0)
+    _check(lib().w4a16_attn_decode_workspace(n_heads, n_kv_heads, head_dim, T, ctypes.byref(n)),
+           "w4a16_attn_decode_workspace")
+    return n.value
+
+
+def w4a16_attn_decode(q, k_cache, v_cache, T=None, o=None, workspace=None, stream=None):
+    """Decode attention of one token: q float16 [H][128], caches float16
+    [Hkv][t_stride][128] (keys t < T, default all), o float16 [H][128]
+    (allocated if not given); workspace a CUDA tensor of at least
+    attn_decode_workspace(...) bytes (allocated if not given)."""
+    import torch
+    H, D = q.shape
+    Hkv, t_stride, _ = k_cache.shape
+    T = t_stride if T is None else T
+    if o is None:
+        o = torch.empty((H, D), dtype=torch.float16, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(attn_decode_workspace(H, Hkv, T, D) // 4 + 4, dtype=torch.float32,
+                                device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().w4a16_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), H, Hkv, D, T, t_stride,
+                                   _ptr(workspace), nbytes, _stream(stream)), "w4a16_attn_decode")
+    return o
+
+
+def w4a16_attn_decode_raw(q_ptr, k_ptr, v_ptr, o_ptr, H, Hkv, D, T, t_stride, ws_ptr, ws_bytes,
+                          stream=None) -> int:
+    """Unchecked status passthrough (tests of the argument checks use it)."""
+    return lib().w4a16_attn_decode(q_ptr, k_ptr, v_ptr, o_ptr, H, Hkv, D, T, t_stride, ws_ptr, ws_bytes,
+                                   stream)
 
 
 def w4a16_dequant(qweight, scales, w_out=None, stream=None):

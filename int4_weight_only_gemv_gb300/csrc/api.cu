@@ -57,7 +57,8 @@ w4a16_status device_state(DeviceState** out) {
     d.info.sms = sms;
     d.info.max_smem_optin = smem;
     d.status = static_cast<uint32_t*>(addr);
-    if (prepare_gemv_m1(d.info) != cudaSuccess || prepare_gemv_mma(d.info) != cudaSuccess) {
+    if (prepare_gemv_m1(d.info) != cudaSuccess || prepare_gemv_mma(d.info) != cudaSuccess ||
+        prepare_attn_decode(d.info) != cudaSuccess) {
       cudaGetLastError();
       return W4A16_ERR_CUDA;
     }
@@ -175,6 +176,67 @@ w4a16_status w4a16_gemv(const uint32_t* qweight, const uint16_t* scales, const u
   if ((s = device_state(&d)) != W4A16_OK) return s;
   return enqueue(*d, plain_args(qweight, scales, x, y, M, N, K, K, N),
                  static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+constexpr int kAttnMaxT = 1 << 24;
+
+w4a16_status check_attn_shape(int n_heads, int n_kv_heads, int head_dim, int T) {
+  if (head_dim != 128 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 ||
+      n_heads / n_kv_heads > 16 || T < 1 || T > kAttnMaxT)
+    return W4A16_ERR_SHAPE;
+  return W4A16_OK;
+}
+}  // namespace
+
+w4a16_status w4a16_attn_decode_workspace(int n_heads, int n_kv_heads, int head_dim, int T,
+                                         size_t* bytes) {
+  if (!bytes) return W4A16_ERR_NULL;
+  *bytes = 0;
+  w4a16_status s = check_attn_shape(n_heads, n_kv_heads, head_dim, T);
+  if (s != W4A16_OK) return s;
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != W4A16_OK) return s;
+  *bytes = attn_workspace_bytes(n_kv_heads, attn_splits(n_kv_heads, T, d->info));
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_attn_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                               uint16_t* o, int n_heads, int n_kv_heads, int head_dim, int T,
+                               int t_stride, float* workspace, size_t workspace_bytes, void* stream) {
+  w4a16_status s = check_attn_shape(n_heads, n_kv_heads, head_dim, T);
+  if (s != W4A16_OK) return s;
+  if (t_stride < T || t_stride > kAttnMaxT) return W4A16_ERR_SHAPE;
+  if (!q || !k_cache || !v_cache || !o || !workspace) return W4A16_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace))
+    return W4A16_ERR_ALIGN;
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != W4A16_OK) return s;
+  const size_t need = attn_workspace_bytes(n_kv_heads, attn_splits(n_kv_heads, T, d->info));
+  if (workspace_bytes < need) return W4A16_ERR_SHAPE;
+  const size_t qo = static_cast<size_t>(n_heads) * head_dim * 2;
+  const size_t cache = static_cast<size_t>(n_kv_heads) * t_stride * head_dim * 2;
+  if (overlaps(o, qo, q, qo) || overlaps(o, qo, k_cache, cache) || overlaps(o, qo, v_cache, cache) ||
+      overlaps(o, qo, workspace, need) || overlaps(workspace, need, q, qo) ||
+      overlaps(workspace, need, k_cache, cache) || overlaps(workspace, need, v_cache, cache))
+    return W4A16_ERR_ALIAS;
+  AttnArgs a;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.o = o;
+  a.workspace = workspace;
+  a.n_heads = n_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.T = T;
+  a.t_stride = t_stride;
+  a.pdl = false;
+  a.status = d->status;
+  if (launch_attn_decode(a, d->info, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
 }
 
 w4a16_status w4a16_dequant(const uint32_t* qweight, const uint16_t* scales, uint16_t* w_out,

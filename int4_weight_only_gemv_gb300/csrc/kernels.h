@@ -125,6 +125,21 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
 cudaError_t launch_gemv_rows(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 // M = 8..16: mma.sync tensor-core kernel with cluster split-K.
 cudaError_t launch_gemv_mma(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
+// Decode attention (attn_decode.cu): head dimension 128, at most 16 query
+// heads per KV head; arguments checked by the caller.
+struct AttnArgs {
+  const uint16_t* q;   // [n_heads][128]
+  const uint16_t* k;   // [n_kv_heads][t_stride][128]
+  const uint16_t* v;
+  uint16_t* o;         // [n_heads][128]
+  float* workspace;    // attn_workspace_bytes(n_kv_heads, attn_splits(...))
+  int n_heads, n_kv_heads, T, t_stride;
+  bool pdl;
+  uint32_t* status;
+};
+int attn_splits(int n_kv_heads, int T, const DeviceInfo& d);
+size_t attn_workspace_bytes(int n_kv_heads, int splits);
+cudaError_t launch_attn_decode(const AttnArgs& a, const DeviceInfo& d, cudaStream_t st);
 // cuTensorMapEncodeTiled from the driver (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
@@ -144,6 +159,7 @@ cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, uint32_t* status, cu
 // must run once per device before the first launch and outside stream capture.
 cudaError_t prepare_gemv_m1(const DeviceInfo& d);
 cudaError_t prepare_gemv_mma(const DeviceInfo& d);
+cudaError_t prepare_attn_decode(const DeviceInfo& d);
 
 // Wall-clock bound on any in-kernel wait (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -175,3 +175,23 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(w4, "_LIB", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         w4.lib()
+
+
+def test_attn_decode_argument_checks(L):
+    """Shape, null and alignment checks come before any CUDA call.  Q, K, V, O
+    and the workspace are fake 16-byte aligned addresses far apart (never
+    dereferenced: each call below fails its checks first)."""
+    Q, K, V, O, W = 1 << 20, 1 << 30, 1 << 31, 1 << 32, 1 << 33
+    f = L.w4a16_attn_decode
+    assert f(Q, K, V, O, 28, 4, 64, 100, 100, W, 1 << 20, None) == 2     # head_dim != 128
+    assert f(Q, K, V, O, 28, 5, 128, 100, 100, W, 1 << 20, None) == 2    # heads not a multiple
+    assert f(Q, K, V, O, 34, 2, 128, 100, 100, W, 1 << 20, None) == 2    # 17 heads per KV head
+    assert f(Q, K, V, O, 28, 4, 128, 0, 100, W, 1 << 20, None) == 2      # T = 0
+    assert f(Q, K, V, O, 28, 4, 128, 100, 99, W, 1 << 20, None) == 2     # t_stride < T
+    assert f(0, K, V, O, 28, 4, 128, 100, 100, W, 1 << 20, None) == 1    # null q
+    assert f(Q, K, V, O, 28, 4, 128, 100, 100, 0, 1 << 20, None) == 1    # null workspace
+    assert f(Q, K + 2, V, O, 28, 4, 128, 100, 100, W, 1 << 20, None) == 3  # misaligned k
+    assert f(Q, K, V, O + 8, 28, 4, 128, 100, 100, W, 1 << 20, None) == 3  # misaligned o
+    n = ctypes.c_size_t(7)
+    assert L.w4a16_attn_decode_workspace(28, 4, 128, 0, ctypes.byref(n)) == 2 and n.value == 0
+    assert L.w4a16_attn_decode_workspace(28, 4, 128, 10, None) == 1
