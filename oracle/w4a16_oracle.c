@@ -1,5 +1,6 @@
 /*
- * w4a16_oracle.c -- the CPU oracle for the INT4 weight-only (W4A16) GEMV.
+ * w4a16_oracle.c -- the CPU oracle for the INT4 weight-only (W4A16) GEMV, its
+ * layer epilogues and the fp16-KV decode attention next to it.
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain, single-threaded
  * statement of what the GPU library computes.  Only the test suite, the smoke
