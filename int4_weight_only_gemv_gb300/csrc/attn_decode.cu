@@ -18,11 +18,11 @@
 //   attn_partial_kernel   one CTA per (KV head, key range).  Warp 4 streams
 //       tiles of 64 keys through an S-stage ring: per tile four 3-D TMA loads
 //       (K and V, dimensions 0..63 and 64..127; 128-byte swizzle; keys at or
-//       past T read as zero, so they never reach P.V as garbage).  Warps 0..3
-//       take 16 keys of each tile: S = Q K^T (ldmatrix from the swizzled
+//       past T read as zero, so they never reach P.V as garbage).  Two groups
+//       of four warps take alternate tiles, each warp 16 keys of a tile: S = Q K^T (ldmatrix from the swizzled
 //       tile), scale by 1/sqrt(128), mask t >= T, an online softmax in FP32
 //       (running max and sum per query head), P rounded to fp16 and
-//       O += P V (ldmatrix.trans).  At the end the four warps' (max, sum, O)
+//       O += P V (ldmatrix.trans).  At the end the eight warps' (max, sum, O)
 //       are merged through shared memory and written to the workspace.
 //   attn_combine_kernel   one CTA per query head: merges the key ranges in
 //       their order (max, rescale, sum) and writes o in fp16.
@@ -40,7 +40,8 @@ namespace {
 
 constexpr int kAD = 128;                    // head dimension
 constexpr int kAKeys = 64;                  // keys per tile
-constexpr int kAWarps = 4;                  // consumer warps, 16 keys of a tile each
+constexpr int kAGroups = 2;                 // consumer groups, alternate tiles
+constexpr int kAWarps = 4 * kAGroups;       // consumer warps, 16 keys of their group's tile each
 constexpr int kAThreads = 32 * (kAWarps + 1);
 constexpr int kABox = kAKeys * 128;         // one box: 64 keys x 64 dimensions fp16
 constexpr int kATileBytes = 4 * kABox;      // K (two halves of the dimensions), then V
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kAWarps);
+      mbar_init(empty0 + 8 * s, kAWarps / kAGroups);
     }
     fence_barrier_init();
   }
@@ -183,9 +184,10 @@ __global__ void __launch_bounds__(kAThreads, 1)
 #pragma unroll
     for (int c = 0; c < 4; ++c) o[nd][c] = 0.f;
   bool ok = true;
-  const int kr = 16 * warp;  // this warp's first key row in a tile
+  const int grp = warp / 4;         // tiles i = grp (mod kAGroups)
+  const int kr = 16 * (warp % 4);   // this warp's first key row in a tile
 
-  for (int i = 0; i < nt; ++i) {
+  for (int i = grp; i < nt; i += kAGroups) {
     const int s = i % kAStages;
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * s, (i / kAStages) & 1, kWaitLimitNs));
     if (!ok) {
@@ -304,8 +306,9 @@ __global__ void __launch_bounds__(kAThreads, 1)
     wo[(g8 + 8) * kAD + d + 1] = o[nd][3];
   }
   asm volatile("bar.sync 1, %0;" ::"r"(32 * kAWarps) : "memory");
-  // thread d of the consumers merges dimension d of every query head
-  const int d = threadIdx.x;  // 0..127
+  // thread d < 128 of the consumers merges dimension d of every query head
+  if (threadIdx.x >= kAD) return;
+  const int d = threadIdx.x;
   const int64_t slot = static_cast<int64_t>(g) * p.splits + sp;
   for (int r = 0; r < p.group; ++r) {
     float M = -INFINITY;
@@ -330,26 +333,31 @@ __global__ void __launch_bounds__(kAThreads, 1)
 
 constexpr int kAMaxSplits = 256;  // key ranges per KV head (at most the SM count)
 
-// One CTA (128 threads, one per dimension) per query head: merge the key
-// ranges in order, o = fp16_RN(sum_sp O_sp e_sp / sum_sp l_sp e_sp) with
-// e_sp = 2^((m_sp - M) log2 e), M = max_sp m_sp.  The ranges' statistics are
-// loaded by all threads at once (one range per thread) and reduced through
-// shared memory; the weighted sum over ranges keeps several loads in flight.
-__global__ void __launch_bounds__(kAD) attn_combine_kernel(const float* __restrict__ ws_ml,
-                                                           const float* __restrict__ ws_o, uint16_t* o,
-                                                           int group, int splits) {
+constexpr int kAMergeParts = 4;  // threads per output dimension in the merge
+constexpr int kAMergeThreads = kAD * kAMergeParts;
+
+// One CTA per query head: merge the key ranges,
+//   o = fp16_RN(sum_sp O_sp e_sp / sum_sp l_sp e_sp),  e_sp = 2^((m_sp - M) log2 e),
+// M = max_sp m_sp.  The ranges' statistics are loaded one per thread and
+// reduced through shared memory; thread (part, d) sums the ranges
+// sp = part (mod 4) of dimension d with all its loads in flight, and the four
+// parts are added in order.  The result does not depend on timing.
+__global__ void __launch_bounds__(kAMergeThreads) attn_combine_kernel(const float* __restrict__ ws_ml,
+                                                                      const float* __restrict__ ws_o,
+                                                                      uint16_t* o, int group, int splits) {
   __shared__ float e_sh[kAMaxSplits];
-  __shared__ float red[kAD / 32];
+  __shared__ float red[kAMergeThreads / 32];
+  __shared__ float part_sh[kAMergeParts][kAD];
   pdl_wait();
   const int h = blockIdx.x;
   const int g = h / group, r = h % group;
-  const int d = threadIdx.x;
-  const int lane = d & 31, warp = d >> 5;
+  const int t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  constexpr int kW = kAMergeThreads / 32;
   constexpr float kLog2e = 1.4426950408889634f;
   const int64_t slot0 = static_cast<int64_t>(g) * splits;
-  // M = max over ranges
   float mloc = -INFINITY;
-  for (int sp = d; sp < splits; sp += kAD) {
+  for (int sp = t; sp < splits; sp += kAMergeThreads) {
     const float m = ws_ml[((slot0 + sp) * kARows + r) * 2];
     e_sh[sp] = m;
     mloc = fmaxf(mloc, m);
@@ -358,11 +366,10 @@ __global__ void __launch_bounds__(kAD) attn_combine_kernel(const float* __restri
   if (lane == 0) red[warp] = mloc;
   __syncthreads();
   float M = red[0];
-  for (int w = 1; w < kAD / 32; ++w) M = fmaxf(M, red[w]);
+  for (int w = 1; w < kW; ++w) M = fmaxf(M, red[w]);
   __syncthreads();
-  // e_sp and L = sum_sp l_sp e_sp (each thread its own ranges, then in order)
   float lloc = 0.f;
-  for (int sp = d; sp < splits; sp += kAD) {
+  for (int sp = t; sp < splits; sp += kAMergeThreads) {
     const float e = exp2f((e_sh[sp] - M) * kLog2e);
     e_sh[sp] = e;
     lloc += ws_ml[((slot0 + sp) * kARows + r) * 2 + 1] * e;
@@ -371,11 +378,31 @@ __global__ void __launch_bounds__(kAD) attn_combine_kernel(const float* __restri
   if (lane == 0) red[warp] = lloc;
   __syncthreads();
   float L = 0.f;
-  for (int w = 0; w < kAD / 32; ++w) L += red[w];
+  for (int w = 0; w < kW; ++w) L += red[w];
+  const int d = t % kAD, part = t / kAD;
   float acc = 0.f;
-#pragma unroll 8
-  for (int sp = 0; sp < splits; ++sp) acc += ws_o[((slot0 + sp) * kARows + r) * kAD + d] * e_sh[sp];
-  o[static_cast<int64_t>(h) * kAD + d] = __half_as_ushort(__float2half_rn(acc / L));
+  constexpr int kBatch = 16;  // loads in flight per thread
+  for (int s0 = part; s0 < splits; s0 += kBatch * kAMergeParts) {
+    float v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int sp = s0 + i * kAMergeParts;
+      v[i] = sp < splits ? ws_o[((slot0 + sp) * kARows + r) * kAD + d] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int sp = s0 + i * kAMergeParts;
+      if (sp < splits) acc += v[i] * e_sh[sp];
+    }
+  }
+  part_sh[part][d] = acc;
+  __syncthreads();
+  if (part == 0) {
+    float sum = part_sh[0][d];
+#pragma unroll
+    for (int q = 1; q < kAMergeParts; ++q) sum += part_sh[q][d];
+    o[static_cast<int64_t>(h) * kAD + d] = __half_as_ushort(__float2half_rn(sum / L));
+  }
 }
 
 // K or V cache as a 3-D tensor: [n_kv_heads][T][128] fp16 with head stride
@@ -440,7 +467,7 @@ cudaError_t launch_attn_decode(const AttnArgs& a, const DeviceInfo& d, cudaStrea
   // early and waits for it before reading the workspace
   cudaLaunchConfig_t c2 = {};
   c2.gridDim = dim3(a.n_heads);
-  c2.blockDim = dim3(kAD);
+  c2.blockDim = dim3(kAMergeThreads);
   c2.stream = st;
   cudaLaunchAttribute a2[1];
   a2[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
