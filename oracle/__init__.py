@@ -67,6 +67,10 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.orc_swiglu.restype = None
     L.orc_attn_decode.argtypes = [p, p, p, i64, i64, i64, i64, i64, p]
     L.orc_attn_decode.restype = ctypes.c_int
+    L.orc_quantize_act_a8.argtypes = [p, i64, p, p]
+    L.orc_quantize_act_a8.restype = ctypes.c_int
+    L.orc_gemv_w4a8.argtypes = [p, p, p, i64, i64, i64, i64, p]
+    L.orc_gemv_w4a8.restype = ctypes.c_int
     for f in ("orc_quantize", "orc_unpack", "orc_dequant", "orc_dequant_f64", "orc_gemv",
               "orc_gemv_rows"):
         getattr(L, f).restype = ctypes.c_int
@@ -213,6 +217,30 @@ def attn_decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, T: int | None = Non
     o = np.empty((H, D), np.float64)
     _check(L.orc_attn_decode(_ptr(q), _ptr(k), _ptr(v), H, Hkv, D, T, t_stride, _ptr(o)), "attn_decode")
     return o
+
+
+def quantize_act_a8(x: np.ndarray, L=None) -> tuple[np.ndarray, np.ndarray]:
+    """One fp16 activation row (uint16 bits [K]) -> (int8 codes [K], float32
+    block scales [K / 64]), see orc_quantize_act_a8."""
+    L = L or lib()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    xq = np.empty(x.shape, np.int8)
+    s = np.empty(x.size // 64, np.float32)
+    _check(L.orc_quantize_act_a8(_ptr(x), x.size, _ptr(xq), _ptr(s)), "quantize_act_a8")
+    return xq, s
+
+
+def gemv_w4a8(qweight: np.ndarray, scales: np.ndarray, x: np.ndarray, group: int = 128, L=None) -> np.ndarray:
+    """W4A8 GEMV (activations quantised per 64-element block), float64 [M][N]."""
+    L = L or lib()
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    N, K8 = qweight.shape
+    M = x.shape[0]
+    y = np.empty((M, N), np.float64)
+    _check(L.orc_gemv_w4a8(_ptr(qweight), _ptr(scales), _ptr(x), M, N, K8 * 8, group, _ptr(y)), "gemv_w4a8")
+    return y
 
 
 # Tolerance of the decode-attention check, per query head h reading KV head g:

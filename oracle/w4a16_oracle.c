@@ -321,3 +321,76 @@ int orc_attn_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, int
   free(s);
   return ORC_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * W4A8: the INT8-activation variant that the page "Costruire un runtime di
+ * inference LLM da zero", "Tre bug che insegnano" (third bug) describes
+ * trying with dp4a against the FP16-activation GEMV.  The page gives no
+ * activation format; the reading here is symmetric int8 per block of 64
+ * consecutive k of one activation row (half a weight group):
+ *   amax_b = max_{k in b} |x[k]|                  (exact, from fp16 values)
+ *   s_b    = amax_b / 127,  inv_b = 127 / amax_b  (each one FP32 division)
+ *   xq[k]  = clamp(round_half_away(x[k] * inv_b), -127, 127)  (FP32 product)
+ * with s_b = inv_b = 0 and xq = 0 for an all-zero block.  These steps are in
+ * FP32 because they decide integers: the GPU takes the same decisions in the
+ * same precision.  The GEMV is then
+ *   y[m][n] = sum_b s_w[n][b / 2] s_b sum_{k in b} q[n][k] xq[k]
+ * with exact integer inner sums, in FP64.
+ * ------------------------------------------------------------------------- */
+#define ORC_A8_BLOCK 64
+
+/* Quantise one activation row x[K] (K a multiple of 64): xq[K], s[K / 64]. */
+int orc_quantize_act_a8(const uint16_t* x, int64_t K, int8_t* xq, float* s) {
+  if (K <= 0 || K % ORC_A8_BLOCK != 0) return ORC_ERR_SHAPE;
+  for (int64_t b = 0; b < K / ORC_A8_BLOCK; ++b) {
+    float amax = 0.0f;
+    for (int64_t k = b * ORC_A8_BLOCK; k < (b + 1) * ORC_A8_BLOCK; ++k) {
+      const float v = fabsf((float)orc_half_to_double(x[k]));
+      if (!(v <= 3.0e38f)) return ORC_ERR_NONFINITE;
+      if (v > amax) amax = v;
+    }
+    const float sb = amax > 0.0f ? amax / 127.0f : 0.0f;
+    const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+    s[b] = sb;
+    for (int64_t k = b * ORC_A8_BLOCK; k < (b + 1) * ORC_A8_BLOCK; ++k) {
+      const float p = (float)orc_half_to_double(x[k]) * inv;
+      float r = roundf(p);
+      if (r > 127.0f) r = 127.0f;
+      if (r < -127.0f) r = -127.0f;
+      xq[k] = (int8_t)r;
+    }
+  }
+  return ORC_OK;
+}
+
+/* y[M][N] (double) of the W4A8 GEMV above, x fp16 [M][K]. */
+int orc_gemv_w4a8(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x, int64_t M,
+                  int64_t N, int64_t K, int64_t G, double* y) {
+  if (M <= 0 || !shape_ok(N, K, G) || G % ORC_A8_BLOCK != 0) return ORC_ERR_SHAPE;
+  int8_t* xq = (int8_t*)malloc((size_t)K);
+  float* sx = (float*)malloc(sizeof(float) * (size_t)(K / ORC_A8_BLOCK));
+  if (xq == NULL || sx == NULL) {
+    free(xq);
+    free(sx);
+    return ORC_ERR_SHAPE;
+  }
+  int rc = ORC_OK;
+  for (int64_t m = 0; m < M && rc == ORC_OK; ++m) {
+    rc = orc_quantize_act_a8(x + m * K, K, xq, sx);
+    for (int64_t n = 0; n < N && rc == ORC_OK; ++n) {
+      double acc = 0.0;
+      for (int64_t b = 0; b < K / ORC_A8_BLOCK; ++b) {
+        int64_t isum = 0;
+        for (int64_t k = b * ORC_A8_BLOCK; k < (b + 1) * ORC_A8_BLOCK; ++k) {
+          const uint32_t word = qweight[n * (K / 8) + k / 8];
+          isum += (int64_t)nibble_value(word >> (4 * (k % 8))) * (int64_t)xq[k];
+        }
+        acc += (double)isum * orc_half_to_double(scales[n * (K / G) + (b * ORC_A8_BLOCK) / G]) * (double)sx[b];
+      }
+      y[m * N + n] = acc;
+    }
+  }
+  free(xq);
+  free(sx);
+  return rc;
+}

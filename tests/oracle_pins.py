@@ -425,6 +425,69 @@ def pin_attn_stride_and_prefix(L):
     assert np.isfinite(o).all() and np.array_equal(o, o2)
 
 
+def _a8_reference(x_u16: np.ndarray):
+    """Block-64 int8 quantisation of one fp16 row with numpy: FP32 division
+    and product (IEEE single, as the definition states), rounding half away
+    from zero taken exactly in FP64."""
+    x = x_u16.view(np.float16).astype(np.float32).reshape(-1, 64)
+    amax = np.abs(x).max(axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s = np.where(amax > 0, amax / np.float32(127.0), np.float32(0.0)).astype(np.float32)
+        inv = np.where(amax > 0, np.float32(127.0) / amax, np.float32(0.0)).astype(np.float32)
+    p = (x * inv[:, None]).astype(np.float32).astype(np.float64)
+    q = np.clip(np.copysign(np.floor(np.abs(p) + 0.5), p), -127, 127).astype(np.int8)
+    return q.reshape(-1), s
+
+
+def pin_a8_quantize_vs_numpy(L):
+    """Codes and scales equal a numpy restatement bit for bit; every code of a
+    nonzero block is within half a step of x / s, and the block maximum maps
+    to +-127."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal(64 * 40) * np.repeat(rng.uniform(0.01, 30, 40), 64)).astype(np.float16)
+    xq, s = oracle.quantize_act_a8(x.view(np.uint16), L)
+    rq, rs = _a8_reference(x.view(np.uint16))
+    assert np.array_equal(xq, rq) and np.array_equal(s.view(np.uint32), rs.view(np.uint32))
+    xb = x.astype(np.float64).reshape(-1, 64)
+    err = np.abs(xb - xq.reshape(-1, 64) * s[:, None].astype(np.float64))
+    assert (err <= s[:, None] * (0.5 + 1e-6)).all()
+    assert (np.abs(xq.reshape(-1, 64)).max(axis=1) == 127).all()
+
+
+def pin_a8_ties_and_zero_block(L):
+    """With block maximum 127 the scale is 1: 2.5 -> 3 and -2.5 -> -3 (half
+    away from zero), integers map to themselves; an all-zero block has scale
+    0 and codes 0."""
+    x = np.zeros(128, np.float16)
+    x[0], x[1], x[2], x[3], x[4] = 127.0, 2.5, -2.5, 7.0, -0.5
+    xq, s = oracle.quantize_act_a8(x.view(np.uint16), L)
+    assert s[0] == 1.0 and list(xq[:5]) == [127, 3, -3, 7, -1]
+    assert s[1] == 0.0 and not xq[64:].any()
+
+
+def pin_a8_gemv_vs_numpy_and_exact_case(L):
+    """The W4A8 GEMV equals sum_b s_w s_b (q . xq) from numpy integer matmuls
+    per block; with activations that quantise exactly (integers, block
+    maximum 127) it equals the W4A16 GEMV."""
+    w = synth.weights(12, 384, 23).numpy()
+    qw, sc = oracle.quantize(w, 128, L)
+    x = synth.activations(3, 384, 23).numpy().view(np.uint16)
+    y = oracle.gemv_w4a8(qw, sc, x, 128, L)
+    q = oracle.unpack(qw, L).astype(np.int64)
+    sw = sc.view(np.float16).astype(np.float64)
+    for m in range(3):
+        xq, sx = _a8_reference(x[m])
+        ref = np.zeros(12)
+        for b in range(6):
+            isum = q[:, 64 * b:64 * b + 64] @ xq[64 * b:64 * b + 64].astype(np.int64)
+            ref += isum * sw[:, b // 2] * np.float64(sx[b])
+        assert np.allclose(y[m], ref, rtol=1e-13, atol=1e-13)
+    xi = np.random.default_rng(24).integers(-126, 127, (2, 384)).astype(np.float16)
+    xi[:, ::64] = 127.0
+    y8 = oracle.gemv_w4a8(qw, sc, xi.view(np.uint16), 128, L)
+    assert np.array_equal(y8, oracle.gemv(qw, sc, xi.view(np.uint16), 128, L))
+
+
 ALL_PINS = [
     pin_half_to_double_exhaustive, pin_half_roundtrip, pin_half_midpoints_ties_to_even,
     pin_half_overflow_and_specials, pin_half_vs_numpy_random, pin_hand_words,
@@ -434,6 +497,7 @@ ALL_PINS = [
     pin_gemv_fused_equals_separate, pin_silu_closed_forms, pin_swiglu_vs_numpy,
     pin_attn_single_key, pin_attn_two_keys_scale, pin_attn_uniform_and_constant,
     pin_attn_permutation_and_dominance, pin_attn_stride_and_prefix,
+    pin_a8_quantize_vs_numpy, pin_a8_ties_and_zero_block, pin_a8_gemv_vs_numpy_and_exact_case,
 ]
 
 
