@@ -348,19 +348,22 @@ def per_config_table(layers, dev, reps=20):
     shapes = [("q_proj", "q", H, 1), ("kv_proj", "k", H, 1), ("qkv", "qkv", H, 1),
               ("gate_up", "gate_up", H, 1)]
     shapes += [(f"down_m{m}", "down", F, m) for m in (1, 2, 4, 8, 16)]
+    # the W4A8 variant on the M = 1 shapes (activations quantised in-kernel)
+    shapes += [("q_proj_a8", "q", H, 1), ("gate_up_a8", "gate_up", H, 1), ("down_m1_a8", "down", F, 1)]
     stream = torch.cuda.Stream()
     for label, key, K, M in shapes:
+        gemv = w4.w4a16_gemv_a8 if label.endswith("_a8") else w4.w4a16_gemv
         xs = [synth.activations(M, K, 77 + l, dev) for l in range(len(layers))]
         N = layers[0][key][0].shape[0]
         ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in layers]
         with torch.cuda.stream(stream):
             for l, lw in enumerate(layers):  # warm-up, also outside capture
-                w4.w4a16_gemv(*lw[key], xs[l], ys[l])
+                gemv(*lw[key], xs[l], ys[l])
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for l, lw in enumerate(layers):
-                w4.w4a16_gemv(*lw[key], xs[l], ys[l])
+                gemv(*lw[key], xs[l], ys[l])
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
@@ -375,6 +378,8 @@ def per_config_table(layers, dev, reps=20):
         b = gemv_bytes(N, K, M)
         out[label] = {"M": M, "N": N, "K": K, "us_per_gemv": round(us, 3),
                       "GBps": round(b / us / 1e3, 1), "bytes": b}
+        if label.endswith("_a8"):
+            out[label]["note"] = "W4A8: int8 activations, per-64 block scales computed in the kernel"
     # the tiny workload fits in L2: latency-bound, measured warm
     cfg = synth.TINY
     wq, sc = w4.w4a16_quantize(synth.weights(cfg.N, cfg.K, cfg.seed, dev))
@@ -400,6 +405,7 @@ def per_config_table(layers, dev, reps=20):
     out["attn_decode_T8192"] = attn_decode_line(dev, reps)
     out["layer_seq_qkv_bias_swiglu"] = epilogue_step(layers, dev, reps, ("q", "k", "v"))
     out["layer_seq_bias_swiglu"] = epilogue_step(layers, dev, reps, synth.PROJ_NAMES)
+    out["layer_seq_w4a8"] = epilogue_step(layers, dev, reps, (), act_int8=True)
     return out
 
 
@@ -446,10 +452,11 @@ def attn_decode_line(dev, reps, T=8192):
             "bytes": b, "note": "fp16 KV cache, 28 rotated caches (cold L2), partial + merge launches"}
 
 
-def epilogue_step(layers, dev, reps, bias_on):
+def epilogue_step(layers, dev, reps, bias_on, act_int8=False):
     """The 28-layer M = 1 step with the fused epilogues (output biases on the
-    projections bias_on, SwiGLU between [gate; up] and down): ms per step
-    and GB/s over the same algorithmic bytes plus the bias bytes."""
+    projections bias_on, SwiGLU between [gate; up] and down), or with
+    act_int8 and nothing else the plain step as W4A8: ms per step and GB/s
+    over the same algorithmic bytes plus the bias bytes."""
     import torch
 
     import int4_weight_only_gemv_gb300 as w4
@@ -461,15 +468,17 @@ def epilogue_step(layers, dev, reps, bias_on):
               for _ in layers]
     io = make_io(dev)
     seq = w4.LayerSeq([{k: lw[k] for k in synth.PROJ_NAMES} for lw in layers], io, 1, H, KV, F,
-                      biases=biases, swiglu=True)
+                      biases=biases if bias_on else None, swiglu=not act_int8, act_int8=act_int8)
     stream = torch.cuda.current_stream()
     for _ in range(3):
         seq.run(stream)
     ms = time_graph_replays(seq, stream, reps, lambda: None) / reps
     seq.close()
     b = config_block()["bytes_per_step"] + 2 * sum(width[n] for n in bias_on) * len(layers)
+    note = ("W4A8: every GEMV with int8 activations quantised in-kernel" if act_int8 else
+            "biases on " + "/".join(bias_on) + ", SwiGLU fused into down")
     return {"M": 1, "layers": len(layers), "ms_per_step": round(ms, 4), "GBps": round(b / ms / 1e6, 1),
-            "bytes": b, "note": "biases on " + "/".join(bias_on) + ", SwiGLU fused into down"}
+            "bytes": b, "note": note}
 
 
 def bench_ours(args, rank, world):

@@ -100,6 +100,25 @@ w4a16_status w4a16_gemv(const uint32_t* qweight, const uint16_t* scales, const u
                         uint16_t* y, int M, int N, int K, int group, void* stream);
 
 /*
+ * w4a16_gemv_a8 -- the W4A8 variant of w4a16_gemv: INT4 weights against
+ * INT8 activations with int8 dot products (dp4a), the variant that the third
+ * bug of "Tre bug che insegnano" reports measuring against the FP16 path.
+ * x stays fp16 in memory; the kernel quantises each block of 64 consecutive
+ * activations of a row as it loads it:
+ *   s_b = max|x_b| / 127,  xq = round_to_nearest_even(x * (127 / max|x_b|))
+ * (FP32 divisions and product, |xq| <= 127; an all-zero block gives s_b = 0,
+ * xq = 0), and
+ *   y[n] = fp16_RN( sum_b s_w[n][b / 2] s_b sum_{k in b} q[n][k] xq[k] )
+ * with exact integer block sums and FP32 scaling and accumulation.  The
+ * result differs from w4a16_gemv by the activation rounding (about 1 % of
+ * |y| on Gaussian activations).  Arguments and checks as w4a16_gemv, plus:
+ * M must be 0 or 1 (W4A16_ERR_M_RANGE) and K within the M = 1 kernel's range
+ * (at most 28672; W4A16_ERR_SHAPE).  Deterministic; never allocates.
+ */
+w4a16_status w4a16_gemv_a8(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
+                           uint16_t* y, int M, int N, int K, int group, void* stream);
+
+/*
  * w4a16_dequant -- debugging aid: w_out fp16[N][K] = fp16_RN(q * s) (exact
  * product, one rounding).  w_out must not overlap qweight or scales.
  */
@@ -212,6 +231,10 @@ w4a16_status w4a16_layer_seq_create(const w4a16_layer_weights* layers, int n_lay
  * h[m][j] = fp16_RN(silu(g) u), g = y_gu[m][j], u = y_gu[m][ffn + j] (fp16),
  * silu(g) = g / (1 + e^-g), evaluated in FP32.  y_gu is still written. */
 #define W4A16_SEQ_SWIGLU 0x1u
+/* Flag: every GEMV of the sequence is the W4A8 variant (see w4a16_gemv_a8);
+ * M = 1 with every K within the M = 1 kernel's range only (W4A16_ERR_M_RANGE
+ * for M > 1, W4A16_ERR_SHAPE otherwise). */
+#define W4A16_SEQ_ACT_INT8 0x2u
 
 /* Optional per-layer output biases, fp16 bits, one per output row of a
  * projection (NULL: none), indexed by W4A16_Q .. W4A16_DOWN.  A bias is
@@ -223,8 +246,8 @@ typedef struct {
 
 /*
  * w4a16_layer_seq_create with epilogues: biases (n_layers entries, or NULL
- * for none) and flags (0 or W4A16_SEQ_SWIGLU; other bits return
- * W4A16_ERR_SHAPE).  At M = 1 (every K within the M = 1 kernel's range) the
+ * for none) and flags (W4A16_SEQ_SWIGLU, W4A16_SEQ_ACT_INT8 or both; other
+ * bits return W4A16_ERR_SHAPE).  At M = 1 (every K within the M = 1 kernel's range) the
  * SwiGLU is computed inside the down tasks as they load their activations, so
  * h is never written to memory; otherwise a separate kernel writes h to a
  * device buffer of n_layers x M x ffn fp16 values that the object allocates

@@ -20,6 +20,7 @@ __all__ = [
     "w4a16_selftest_wait_timeout", "w4a16_layer_seq_run_static", "STATIC_MAX_GEMVS",
     "LayerSeq", "GROUP", "MAX_M", "MAX_K", "DEV_NONFINITE", "DEV_SCALE_OVERFLOW",
     "DEV_PIPE_TIMEOUT", "STATUS", "EXPORTED_SYMBOLS", "w4a16_attn_decode", "attn_decode_workspace",
+    "w4a16_gemv_a8", "SEQ_ACT_INT8",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -32,6 +33,7 @@ DEV_NONFINITE = 0x1
 DEV_SCALE_OVERFLOW = 0x2
 DEV_PIPE_TIMEOUT = 0x4
 SEQ_SWIGLU = 0x1
+SEQ_ACT_INT8 = 0x2
 NPROJ = 7
 STATIC_MAX_GEMVS = 512
 
@@ -47,7 +49,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_device_status", "w4a16_selftest_wait_timeout", "w4a16_layer_seq_create", "w4a16_layer_seq_num_launches",
     "w4a16_layer_seq_run", "w4a16_layer_seq_run_host", "w4a16_layer_seq_sync",
     "w4a16_layer_seq_destroy", "w4a16_layer_seq_run_static", "w4a16_layer_seq_create2",
-    "w4a16_attn_decode_workspace", "w4a16_attn_decode",
+    "w4a16_attn_decode_workspace", "w4a16_attn_decode", "w4a16_gemv_a8",
 )
 
 
@@ -88,6 +90,7 @@ def lib() -> ctypes.CDLL:
         L.w4a16_abi_version.argtypes = []
         L.w4a16_abi_version.restype = i
         L.w4a16_gemv.argtypes = [p, p, p, p, i, i, i, i, p]
+        L.w4a16_gemv_a8.argtypes = [p, p, p, p, i, i, i, i, p]
         L.w4a16_dequant.argtypes = [p, p, p, i, i, i, p]
         L.w4a16_quantize.argtypes = [p, p, p, i, i, i, p]
         L.w4a16_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
@@ -108,7 +111,7 @@ def lib() -> ctypes.CDLL:
                                                  ctypes.POINTER(_SeqIO), p]
         L.w4a16_attn_decode_workspace.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         L.w4a16_attn_decode.argtypes = [p, p, p, p, i, i, i, i, i, p, ctypes.c_size_t, p]
-        for f in ("w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
+        for f in ("w4a16_gemv", "w4a16_gemv_a8", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
                   "w4a16_selftest_wait_timeout",
                   "w4a16_layer_seq_create", "w4a16_layer_seq_run", "w4a16_layer_seq_run_host",
                   "w4a16_layer_seq_sync", "w4a16_layer_seq_run_static", "w4a16_layer_seq_create2",
@@ -143,6 +146,19 @@ def w4a16_gemv(qweight, scales, x, y=None, stream=None):
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     _check(lib().w4a16_gemv(_ptr(qweight), _ptr(scales), _ptr(x), _ptr(y), M, N, K, GROUP,
                             _stream(stream)), "w4a16_gemv")
+    return y
+
+
+def w4a16_gemv_a8(qweight, scales, x, y=None, stream=None):
+    """W4A8 GEMV (M = 1): activations quantised to int8 per 64-element block
+    inside the kernel; y float16 [1][N] (allocated if not given)."""
+    import torch
+    M, K = x.shape
+    N = qweight.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check(lib().w4a16_gemv_a8(_ptr(qweight), _ptr(scales), _ptr(x), _ptr(y), M, N, K, GROUP,
+                               _stream(stream)), "w4a16_gemv_a8")
     return y
 
 
@@ -255,13 +271,14 @@ class LayerSeq:
     y_down, each [n_layers][M][width].  Optional epilogues
     (w4a16_layer_seq_create2): biases, a list of dicts name -> fp16 tensor of
     the projection's output width (missing names: no bias); swiglu=True makes
-    down read silu(gate) * up.  The tensors must outlive the object.
+    down read silu(gate) * up; act_int8=True runs every GEMV as the W4A8
+    variant (M = 1).  The tensors must outlive the object.
     """
 
     NAMES = ("q", "k", "v", "o", "gate", "up", "down")
     IO = ("x", "y_q", "y_k", "y_v", "y_o", "y_gu", "y_down")
 
-    def __init__(self, layers, io, M, hidden, kv_dim, ffn, biases=None, swiglu=False):
+    def __init__(self, layers, io, M, hidden, kv_dim, ffn, biases=None, swiglu=False, act_int8=False):
         arr = (_LayerWeights * len(layers))()
         for li, lw in enumerate(layers):
             for pj, name in enumerate(self.NAMES):
@@ -271,7 +288,7 @@ class LayerSeq:
         sio = _SeqIO(*[io[n].data_ptr() for n in self.IO])
         handle = ctypes.c_void_p(None)
         self._keep = (layers, io, biases)
-        if biases is None and not swiglu:
+        if biases is None and not swiglu and not act_int8:
             _check(lib().w4a16_layer_seq_create(arr, len(layers), M, hidden, kv_dim, ffn, GROUP,
                                                 ctypes.byref(sio), ctypes.byref(handle)),
                    "w4a16_layer_seq_create")
@@ -282,7 +299,8 @@ class LayerSeq:
                 for li, lb in enumerate(biases):
                     for pj, name in enumerate(self.NAMES):
                         barr[li].bias[pj] = _ptr(lb.get(name))
-            _check(lib().w4a16_layer_seq_create2(arr, barr, SEQ_SWIGLU if swiglu else 0, len(layers), M,
+            flags = (SEQ_SWIGLU if swiglu else 0) | (SEQ_ACT_INT8 if act_int8 else 0)
+            _check(lib().w4a16_layer_seq_create2(arr, barr, flags, len(layers), M,
                                                  hidden, kv_dim, ffn, GROUP, ctypes.byref(sio),
                                                  ctypes.byref(handle)),
                    "w4a16_layer_seq_create2")

@@ -239,6 +239,25 @@ w4a16_status w4a16_attn_decode(const uint16_t* q, const uint16_t* k_cache, const
   return W4A16_OK;
 }
 
+w4a16_status w4a16_gemv_a8(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
+                           uint16_t* y, int M, int N, int K, int group, void* stream) {
+  w4a16_status s = check_gemv(qweight, scales, x, y, M, N, K, group, K);
+  if (s != W4A16_OK) return s;
+  if (M > 1) return W4A16_ERR_M_RANGE;
+  if (!gemv_m1_supported(K)) return W4A16_ERR_SHAPE;
+  if (M == 0 || N == 0) return W4A16_OK;
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != W4A16_OK) return s;
+  GemvArgs a = plain_args(qweight, scales, x, y, M, N, K, K, N);
+  a.a8 = true;
+  a.status = d->status;
+  if (launch_gemv_m1(a, d->info, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
 w4a16_status w4a16_dequant(const uint32_t* qweight, const uint16_t* scales, uint16_t* w_out,
                            int N, int K, int group, void* stream) {
   w4a16_status s = check_weight_shape(N, K, group);
@@ -610,7 +629,7 @@ bool seq_uses_tasks(int M, const std::vector<GemvArgs>& gemvs) {
 // through *launches.
 w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs,
                                const std::vector<int>& dep, const std::vector<const uint16_t*>& x2,
-                               const std::vector<int>& layer_first, int* done, cudaStream_t st,
+                               const std::vector<int>& layer_first, int* done, bool a8, cudaStream_t st,
                                int* launches) {
   const int n_layers = static_cast<int>(layer_first.size()) - 1;
   std::vector<M1Task> tasks;
@@ -623,7 +642,7 @@ w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>
     if (t1 - t0 > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
     seq_tasks(gemvs, dep, x2, layer_first, l0, l1, &tasks);
     const cudaError_t e =
-        launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d.status, *launches > 0, d.info, st);
+        launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d.status, *launches > 0, a8, d.info, st);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return W4A16_ERR_CUDA;
@@ -649,10 +668,15 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
                                      int group, const w4a16_seq_io* io, w4a16_layer_seq** out) {
   if (!out) return W4A16_ERR_NULL;
   *out = nullptr;
-  if ((flags & ~static_cast<unsigned>(W4A16_SEQ_SWIGLU)) != 0) return W4A16_ERR_SHAPE;
+  if ((flags & ~static_cast<unsigned>(W4A16_SEQ_SWIGLU | W4A16_SEQ_ACT_INT8)) != 0) return W4A16_ERR_SHAPE;
   w4a16_status st = check_seq_args(layers, n_layers, M, hidden, kv_dim, ffn, group, io);
   if (st != W4A16_OK) return st;
   if ((st = check_seq_biases(biases, n_layers, M, hidden, kv_dim, ffn, io)) != W4A16_OK) return st;
+  // W4A8 runs only in the M = 1 task-list kernel
+  if ((flags & W4A16_SEQ_ACT_INT8) != 0) {
+    if (M != 1) return W4A16_ERR_M_RANGE;
+    if (!gemv_m1_supported(hidden) || !gemv_m1_supported(ffn)) return W4A16_ERR_SHAPE;
+  }
 
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != W4A16_OK) return st;
@@ -662,6 +686,7 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
   // separate activation step into a buffer this object owns
   const bool tasks = M == 1 && gemv_m1_supported(hidden) && gemv_m1_supported(ffn);
   const bool swiglu = (flags & W4A16_SEQ_SWIGLU) != 0;
+  const bool a8 = (flags & W4A16_SEQ_ACT_INT8) != 0;
   SeqOptions opt;
   opt.biases = biases;
   opt.flags = flags;
@@ -712,7 +737,8 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
     if (cudaMemsetAsync(s->task_done, 0, sizeof(int) * gemvs.size(), s->capture_stream) != cudaSuccess)
       cap = W4A16_ERR_CUDA;
     else
-      cap = enqueue_seq_tasks(*d, gemvs, dep, x2, layer_first, s->task_done, s->capture_stream, &launches);
+      cap = enqueue_seq_tasks(*d, gemvs, dep, x2, layer_first, s->task_done, a8, s->capture_stream,
+                              &launches);
   } else {
     for (size_t i = 0; i < gemvs.size() && cap == W4A16_OK; ++i) {
       if (act[i].h != nullptr) {
@@ -832,7 +858,7 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
     while (l1 < n_layers && layer_first[l1 + 1] - layer_first[l0] <= kM1MaxTasks) ++l1;
     const int t0 = layer_first[l0], t1 = layer_first[l1];
     seq_tasks(gemvs, dep, x2, layer_first, l0, l1, &tasks);
-    if (launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d->status, launches > 0, d->info, s) !=
+    if (launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d->status, launches > 0, false, d->info, s) !=
         cudaSuccess) {
       cudaGetLastError();
       return W4A16_ERR_CUDA;

@@ -31,6 +31,14 @@
 //               -> biased fp16, see ptx.cuh) and eight f16 x f16 -> f32 FMAs;
 //               the biases 1032 and 72 are removed once per unit and row with
 //               the precomputed C = 1032 sum x_even + 72 sum x_odd.
+// W4A8 variant (kA8, the INT8-activation GEMV that the same section's third
+// bug compares with): each consumer thread quantises its own 64-activation
+// unit when it loads it (scale max|x| / 127 and codes round(x 127 / max|x|)
+// in FP32, ties to even), so no pass over x runs first and x stays
+// fp16 in memory.  Per packed word: one shift, two LOP3s (nibbles + 8 as
+// bytes, even and odd k) and two dp4a against the unit's codes; the bias 8 is
+// removed once per unit and row with 8 sum(codes), and the integer sum is
+// scaled by group scale x activation scale in FP32.
 // Every wait is bounded; on a timeout the kernel sets W4A16_DEV_PIPE_TIMEOUT
 // and the CTA returns once its copies in flight have landed.
 #include <cuda_fp16.h>
@@ -187,6 +195,32 @@ __device__ __forceinline__ void dot_pair(const uint32_t (&wa)[8], const uint32_t
   rb = fmaf(0.0625f, ob0 + ob1, eb0 + eb1);
 }
 
+// W4A8: integer dot products of two rows (8 packed words each) with this
+// thread's 64 activation codes, xe[j] / xo[j] the codes of the even / odd k of
+// word j as 4 bytes.  Nibble n becomes n ^ 8 = q + 8 (0..15) in a byte, so the
+// sums are sum_k (q + 8) xq; the caller subtracts 8 sum(xq).
+__device__ __forceinline__ void dot_pair_a8(const uint32_t (&wa)[8], const uint32_t (&wb)[8],
+                                            const uint32_t (&xe)[8], const uint32_t (&xo)[8], int& ra,
+                                            int& rb) {
+  int a = 0, b = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    a = __dp4a(static_cast<int>(lop3_and_xor(wa[j], 0x0F0F0F0Fu, 0x08080808u)), static_cast<int>(xe[j]), a);
+    b = __dp4a(static_cast<int>(lop3_and_xor(wb[j], 0x0F0F0F0Fu, 0x08080808u)), static_cast<int>(xe[j]), b);
+    a = __dp4a(static_cast<int>(lop3_and_xor(wa[j] >> 4, 0x0F0F0F0Fu, 0x08080808u)), static_cast<int>(xo[j]), a);
+    b = __dp4a(static_cast<int>(lop3_and_xor(wb[j] >> 4, 0x0F0F0F0Fu, 0x08080808u)), static_cast<int>(xo[j]), b);
+  }
+  ra = a;
+  rb = b;
+}
+
+// The low bytes of four ints as one word (byte i from argument i).
+__device__ __forceinline__ uint32_t pack_bytes(int a, int b, int c, int d) {
+  const uint32_t lo = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040u);
+  const uint32_t hi = __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040u);
+  return __byte_perm(lo, hi, 0x5410u);
+}
+
 // The 8 packed words of one row at a stage address: two 16-byte shared loads,
 // the second chunk first when rot = 16.
 __device__ __forceinline__ void load_row(uint32_t addr, int rot, uint32_t (&w)[8]) {
@@ -198,8 +232,8 @@ __device__ __forceinline__ void load_row(uint32_t addr, int rot, uint32_t (&w)[8
 
 // kAct: some task of the list takes SwiGLU activations (x2 set).  The
 // instantiation without it carries no trace of that path, so the plain task
-// lists compile exactly as they would without the feature.
-template <int MAXT, bool kAct>
+// lists compile exactly as they would without the feature.  kA8: W4A8.
+template <int MAXT, bool kAct, bool kA8>
 __global__ void __launch_bounds__(kM1MaxThreads, 1)
     gemv_m1_kernel(const __grid_constant__ M1Params<MAXT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -467,7 +501,56 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     // this thread's 64 activations, paired to match the unpacked lanes
     XPairs X[8];
     float C = 0.f;
-    if (wact) {
+    // W4A8: the unit's int8 codes (even / odd k of each word as 4 bytes), 8
+    // times their sum, and the unit's activation scale
+    uint32_t xe[8], xo[8];
+    int C8 = 0;
+    float s_act = 0.f;
+    if (kA8 && wact) {
+      const uint16_t* xp = tk.x + u * 64;
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int jj = rot ? (j ^ 4) : j;
+        v[j] = ld_u4(xp + 8 * jj);
+        if (kAct && tk.x2 != nullptr) v[j] = swiglu8(v[j], ld_u4(tk.x2 + u * 64 + 8 * jj));
+      }
+      // max |x| with packed fp16 operations (exact), as a tree
+      __half2 m2[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const __half2 a = __habs2(*reinterpret_cast<const __half2*>(&v[j].x));
+        const __half2 b = __habs2(*reinterpret_cast<const __half2*>(&v[j].y));
+        const __half2 c = __habs2(*reinterpret_cast<const __half2*>(&v[j].z));
+        const __half2 d = __habs2(*reinterpret_cast<const __half2*>(&v[j].w));
+        m2[j] = __hmax2(__hmax2(a, b), __hmax2(c, d));
+      }
+      const __half2 mm = __hmax2(__hmax2(__hmax2(m2[0], m2[1]), __hmax2(m2[2], m2[3])),
+                                 __hmax2(__hmax2(m2[4], m2[5]), __hmax2(m2[6], m2[7])));
+      const float amax = fmaxf(__low2float(mm), __high2float(mm));
+      s_act = amax > 0.f ? amax / 127.f : 0.f;
+      const float inv = amax > 0.f ? 127.f / amax : 0.f;
+      // codes: one FP32 product and one round-to-nearest-even conversion each
+      // (|x inv| <= 127 (1 + 2^-23): no clamp), packed 4 to a word; their sum
+      // through dp4a with ones
+      int csum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        int ce[4], co[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ce[i] = __float2int_rn(half_lo(w4[i]) * inv);
+          co[i] = __float2int_rn(half_hi(w4[i]) * inv);
+        }
+        xe[j] = pack_bytes(ce[0], ce[1], ce[2], ce[3]);
+        xo[j] = pack_bytes(co[0], co[1], co[2], co[3]);
+        csum = __dp4a(static_cast<int>(xe[j]), 0x01010101, csum);
+        csum = __dp4a(static_cast<int>(xo[j]), 0x01010101, csum);
+      }
+      C8 = 8 * csum;
+    }
+    if (!kA8 && wact) {
       const uint16_t* xp = tk.x + u * 64;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -536,17 +619,31 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         float d0, d1;
         load_row(wa, rot, w0);
         load_row(wa + w_row_step, rot, w1);
-        dot_pair(w0, w1, X, d0, d1);
-        res[0] = (d0 - C) * sc[0];
-        res[1] = (d1 - C) * sc[1];
+        if (kA8) {
+          int i0, i1;
+          dot_pair_a8(w0, w1, xe, xo, i0, i1);
+          res[0] = static_cast<float>(i0 - C8) * (sc[0] * s_act);
+          res[1] = static_cast<float>(i1 - C8) * (sc[1] * s_act);
+        } else {
+          dot_pair(w0, w1, X, d0, d1);
+          res[0] = (d0 - C) * sc[0];
+          res[1] = (d1 - C) * sc[1];
+        }
         load_row(wa + 2 * w_row_step, rot, w0);
         load_row(wa + 3 * w_row_step, rot, w1);
         // the last reads of the stage are issued: release it (release order)
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
-        dot_pair(w0, w1, X, d0, d1);
-        res[2] = (d0 - C) * sc[2];
-        res[3] = (d1 - C) * sc[3];
+        if (kA8) {
+          int i0, i1;
+          dot_pair_a8(w0, w1, xe, xo, i0, i1);
+          res[2] = static_cast<float>(i0 - C8) * (sc[2] * s_act);
+          res[3] = static_cast<float>(i1 - C8) * (sc[3] * s_act);
+        } else {
+          dot_pair(w0, w1, X, d0, d1);
+          res[2] = (d0 - C) * sc[2];
+          res[3] = (d1 - C) * sc[3];
+        }
       } else {
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -578,7 +675,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
 }
 
 template <int MAXT>
-cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, bool pdl, bool act,
+cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, bool pdl, bool act, bool a8,
                          cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -590,8 +687,13 @@ cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true>, p)
-                      : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false>, p);
+  cudaError_t e;
+  if (a8)
+    e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, true>, p)
+            : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, true>, p);
+  else
+    e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, false>, p)
+            : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, false>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -629,11 +731,11 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   p.stage_bytes = rp.stage_bytes;
   p.red_bytes = rp.red_bytes;
   p.CW = rp.CW;
-  return launch_tasks(p, rp, grid, a.pdl, false, st);
+  return launch_tasks(p, rp, grid, a.pdl, false, a.a8, st);
 }
 
 cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uint32_t* status,
-                                 bool pdl, const DeviceInfo& d, cudaStream_t st) {
+                                 bool pdl, bool a8, const DeviceInfo& d, cudaStream_t st) {
   if (tasks == nullptr || ntasks <= 0 || ntasks > kM1MaxTasks) return cudaErrorInvalidValue;
   static thread_local M1Params<kM1MaxTasks> p;  // ~25 KB: kept off the stack
   int Ks[kM1MaxTasks];
@@ -661,19 +763,25 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
   p.red_bytes = rp.red_bytes;
   p.CW = rp.CW;
   // one CTA per SM: every CTA must be resident for the dependency counts
-  return launch_tasks(p, rp, d.sms, pdl, act, st);
+  return launch_tasks(p, rp, d.sms, pdl, act, a8, st);
 }
 
 cudaError_t prepare_gemv_m1(const DeviceInfo& d) {
   const int limit = d.max_smem_optin < kM1SmemBudget + 1024 ? d.max_smem_optin : kM1SmemBudget + 1024;
-  cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       limit);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemv_m1_kernel<kM1MaxTasks, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           limit);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemv_m1_kernel<kM1MaxTasks, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              limit);
+  const void* fns[] = {
+      reinterpret_cast<const void*>(gemv_m1_kernel<1, false, false>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<1, true, false>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<1, false, true>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<1, true, true>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, false, false>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, true, false>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, false, true>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, true, true>)};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace w4a16

@@ -38,6 +38,9 @@ struct GemvArgs {
   // kernel on the stream is still running; it reads only the (constant)
   // weights and scales before waiting for that kernel to finish.
   bool pdl;
+  // W4A8: int8 activations quantised per 64-element unit inside the M = 1
+  // kernel (gemv_m1.cu); only that kernel supports it.
+  bool a8;
 };
 
 #ifdef __CUDACC__
@@ -120,7 +123,7 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
 // (per-task completion counters); required when a task has a dependency,
 // may be null otherwise.  pdl: as GemvArgs::pdl.
 cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uint32_t* status,
-                                 bool pdl, const DeviceInfo& d, cudaStream_t st);
+                                 bool pdl, bool a8, const DeviceInfo& d, cudaStream_t st);
 // M = 1..7 (any K): warp-per-row-block CUDA-core kernel.
 cudaError_t launch_gemv_rows(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 // M = 8..16: mma.sync tensor-core kernel with cluster split-K.

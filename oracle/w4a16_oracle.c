@@ -330,10 +330,12 @@ int orc_attn_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, int
  * consecutive k of one activation row (half a weight group):
  *   amax_b = max_{k in b} |x[k]|                  (exact, from fp16 values)
  *   s_b    = amax_b / 127,  inv_b = 127 / amax_b  (each one FP32 division)
- *   xq[k]  = clamp(round_half_away(x[k] * inv_b), -127, 127)  (FP32 product)
+ *   xq[k]  = round_half_even(x[k] * inv_b)       (FP32 product; |xq| <= 127)
  * with s_b = inv_b = 0 and xq = 0 for an all-zero block.  These steps are in
  * FP32 because they decide integers: the GPU takes the same decisions in the
- * same precision.  The GEMV is then
+ * same precision.  Ties go to even, IEEE's default rounding (the page states
+ * no rule).  No clamp is needed: |x| <= amax gives |x inv| <= 127 (1 + 2^-23),
+ * which rounds to at most 127.  The GEMV is then
  *   y[m][n] = sum_b s_w[n][b / 2] s_b sum_{k in b} q[n][k] xq[k]
  * with exact integer inner sums, in FP64.
  * ------------------------------------------------------------------------- */
@@ -354,9 +356,8 @@ int orc_quantize_act_a8(const uint16_t* x, int64_t K, int8_t* xq, float* s) {
     s[b] = sb;
     for (int64_t k = b * ORC_A8_BLOCK; k < (b + 1) * ORC_A8_BLOCK; ++k) {
       const float p = (float)orc_half_to_double(x[k]) * inv;
-      float r = roundf(p);
-      if (r > 127.0f) r = 127.0f;
-      if (r < -127.0f) r = -127.0f;
+      const float r = nearbyintf(p); /* the default mode: to nearest, ties to even */
+      if (r > 127.0f || r < -127.0f) return ORC_ERR_SHAPE; /* cannot happen, see above */
       xq[k] = (int8_t)r;
     }
   }

@@ -427,15 +427,15 @@ def pin_attn_stride_and_prefix(L):
 
 def _a8_reference(x_u16: np.ndarray):
     """Block-64 int8 quantisation of one fp16 row with numpy: FP32 division
-    and product (IEEE single, as the definition states), rounding half away
-    from zero taken exactly in FP64."""
+    and product (IEEE single, as the definition states), rounding to nearest
+    with ties to even (numpy's rint)."""
     x = x_u16.view(np.float16).astype(np.float32).reshape(-1, 64)
     amax = np.abs(x).max(axis=1)
     with np.errstate(divide="ignore", invalid="ignore"):
         s = np.where(amax > 0, amax / np.float32(127.0), np.float32(0.0)).astype(np.float32)
         inv = np.where(amax > 0, np.float32(127.0) / amax, np.float32(0.0)).astype(np.float32)
-    p = (x * inv[:, None]).astype(np.float32).astype(np.float64)
-    q = np.clip(np.copysign(np.floor(np.abs(p) + 0.5), p), -127, 127).astype(np.int8)
+    p = (x * inv[:, None]).astype(np.float32)
+    q = np.rint(p).astype(np.int8)
     return q.reshape(-1), s
 
 
@@ -455,13 +455,13 @@ def pin_a8_quantize_vs_numpy(L):
 
 
 def pin_a8_ties_and_zero_block(L):
-    """With block maximum 127 the scale is 1: 2.5 -> 3 and -2.5 -> -3 (half
-    away from zero), integers map to themselves; an all-zero block has scale
-    0 and codes 0."""
+    """With block maximum 127 the scale is 1: ties go to even (2.5 -> 2,
+    -2.5 -> -2, 3.5 -> 4, -0.5 -> 0), integers map to themselves; an all-zero
+    block has scale 0 and codes 0."""
     x = np.zeros(128, np.float16)
-    x[0], x[1], x[2], x[3], x[4] = 127.0, 2.5, -2.5, 7.0, -0.5
+    x[0], x[1], x[2], x[3], x[4], x[5] = 127.0, 2.5, -2.5, 7.0, -0.5, 3.5
     xq, s = oracle.quantize_act_a8(x.view(np.uint16), L)
-    assert s[0] == 1.0 and list(xq[:5]) == [127, 3, -3, 7, -1]
+    assert s[0] == 1.0 and list(xq[:6]) == [127, 2, -2, 7, 0, 4]
     assert s[1] == 0.0 and not xq[64:].any()
 
 

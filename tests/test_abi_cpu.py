@@ -157,13 +157,26 @@ def test_layer_seq_create2_argument_checks(L):
     io = w4._SeqIO(*[0x20_0000_0000 + 0x1000_0000 * i for i in range(7)])
     out = ctypes.c_void_p(None)
     args = (1, 1, 256, 128, 512, 128, ctypes.byref(io), ctypes.byref(out))
-    assert L.w4a16_layer_seq_create2(lw, None, 0x2, *args) == 2
+    assert L.w4a16_layer_seq_create2(lw, None, 0x4, *args) == 2
     b = (w4._LayerBias * 1)()
     b[0].bias[0] = 0x30_0000_0008  # not 16-byte aligned
     assert L.w4a16_layer_seq_create2(lw, b, 0, *args) == 3
     b[0].bias[0] = 0x20_0000_0000 + 0x1000_0000 * 5 + 64  # inside y_gu
     assert L.w4a16_layer_seq_create2(lw, b, 1, *args) == 6
     assert L.w4a16_layer_seq_create2(lw, None, 0, 1, 1, 256, 128, 512, 128, ctypes.byref(io), None) == 1
+    # W4A8 sequences: M = 1 only, and every K within the M = 1 kernel's range
+    assert L.w4a16_layer_seq_create2(lw, None, 0x2, 1, 2, 256, 128, 512, 128, ctypes.byref(io),
+                                     ctypes.byref(out)) == 5
+    assert L.w4a16_layer_seq_create2(lw, None, 0x2, 1, 1, 256, 128, 32768, 128, ctypes.byref(io),
+                                     ctypes.byref(out)) == 2
+
+
+def test_gemv_a8_argument_checks(L):
+    assert L.w4a16_gemv_a8(0, B, C, D, 1, 8, 128, 128, None) == 1          # null qweight
+    assert L.w4a16_gemv_a8(A, B, C, D, 2, 8, 128, 128, None) == 5          # M > 1
+    assert L.w4a16_gemv_a8(A, B, C, D, 1, 8, 32768, 128, None) == 2        # K beyond the M = 1 kernel
+    assert L.w4a16_gemv_a8(A, B, C, C, 1, 8, 128, 128, None) == 6          # y overlaps x
+    assert L.w4a16_gemv_a8(0, 0, 0, 0, 0, 8, 128, 128, None) == 0          # M = 0
 
 
 def test_device_status_null(L):

@@ -44,7 +44,7 @@ MUTANTS = [
      "for (int64_t t = 0; t < T - 1; ++t) {\n      s[t] = exp(s[t] - smax);"),
     ("attn_stride_ignored", "dot += orc_half_to_double(q[h * D + d]) * orc_half_to_double(k[(g * t_stride + t) * D + d]);",
      "dot += orc_half_to_double(q[h * D + d]) * orc_half_to_double(k[(g * T + t) * D + d]);"),
-    ("a8_round_half_even", "float r = roundf(p);", "float r = rintf(p);"),
+    ("a8_round_half_away", "const float r = nearbyintf(p);", "const float r = roundf(p);"),
     ("a8_scale_128", "const float sb = amax > 0.0f ? amax / 127.0f : 0.0f;",
      "const float sb = amax > 0.0f ? amax / 128.0f : 0.0f;"),
     ("a8_weight_scale_index", "scales[n * (K / G) + (b * ORC_A8_BLOCK) / G]", "scales[n * (K / G) + b / G]"),
