@@ -26,16 +26,21 @@ namespace {
 
 constexpr int kRowsWarps = 8;
 constexpr int kRowsThreads = kRowsWarps * 32;
-constexpr int kDepth = 4;  // units of loads in flight per lane
 
-template <int M>
+// R rows per CTA, D units of loads in flight per lane (R x D x 8 bytes of
+// loads in flight per lane, 32 registers of ring either way).  Large K gives
+// each lane several units per row, so fewer rows and a deeper ring; small K
+// (a few units per row, about one per lane) gives each lane more rows.
+template <int M, bool kSmallK>
 struct RowsCfg {
-  static constexpr int R = M <= 2 ? 4 : 2;  // rows per CTA
+  static constexpr int R = kSmallK ? (M <= 3 ? 8 : 4) : (M <= 4 ? 4 : 2);
+  static constexpr int D = kSmallK ? (M <= 1 ? 2 : (M <= 3 ? 1 : 2)) : (M <= 4 ? 4 : 8);
 };
 
-template <int M>
+template <int M, bool kSmallK>
 __global__ void __launch_bounds__(kRowsThreads, 2) gemv_rows_kernel(const GemvArgs a) {
-  constexpr int R = RowsCfg<M>::R;
+  constexpr int R = RowsCfg<M, kSmallK>::R;
+  constexpr int kDepth = RowsCfg<M, kSmallK>::D;
   __shared__ float red[kRowsWarps][R * M];
   pdl_launch_dependents();
   pdl_wait();  // x may be the previous kernel's output
@@ -140,9 +145,9 @@ __global__ void __launch_bounds__(kRowsThreads, 2) gemv_rows_kernel(const GemvAr
   }
 }
 
-template <int M>
-cudaError_t launch_rows_m(const GemvArgs& a, cudaStream_t st) {
-  constexpr int R = RowsCfg<M>::R;
+template <int M, bool kSmallK>
+cudaError_t launch_rows_mk(const GemvArgs& a, cudaStream_t st) {
+  constexpr int R = RowsCfg<M, kSmallK>::R;
   const int64_t grid = (static_cast<int64_t>(a.N) + R - 1) / R;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -153,9 +158,15 @@ cudaError_t launch_rows_m(const GemvArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows_kernel<M>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows_kernel<M, kSmallK>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Small K: at most two 16-k units per lane of the 8 warps (K <= 8192).
+template <int M>
+cudaError_t launch_rows_m(const GemvArgs& a, cudaStream_t st) {
+  return a.K <= 2 * 16 * kRowsThreads ? launch_rows_mk<M, true>(a, st) : launch_rows_mk<M, false>(a, st);
 }
 
 }  // namespace
