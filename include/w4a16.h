@@ -88,13 +88,19 @@ int w4a16_abi_version(void);
  *   qweight, scales  the packed weight of N output rows and K inputs
  *   x                fp16 [M][K]
  *   y                fp16 [M][N]; must not overlap x, qweight or scales
- * Dispatch: M in 1..7 runs the CUDA-core kernel (nibble unpack in registers,
- * FP32 accumulation), M in 8..16 the tensor-core kernel (mma.sync over each
- * group of 128, FP32 accumulators).  The result is deterministic: the same
- * inputs give the same bits on every call.  Never allocates, never
- * synchronises.  The first call of any entry point on a device does a
- * one-time set-up (device queries, kernel attributes); make it outside
- * CUDA stream capture.  After that, w4a16_gemv may be captured.
+ * Dispatch: M = 1 with K <= 28672 runs the persistent TMA-fed CUDA-core
+ * kernel; other M in 1..7 the CUDA-core small-batch kernel (nibble unpack in
+ * registers, FP32 accumulation); M in 8..16 the tensor-core kernel (mma.sync
+ * over each group of 128, FP32 accumulators).  The result is deterministic:
+ * the same inputs give the same bits on every call.  Never allocates, never
+ * synchronises.  The kernel is launched as a programmatic dependent of the
+ * previous kernel on the stream: if that kernel lets dependents start early
+ * (griddepcontrol.launch_dependents), this one may read qweight and scales
+ * before it completes, but reads x and writes y only after it has completed
+ * (kernels that do not opt in are simply waited for).  The first call of any
+ * entry point on a device does a one-time set-up (device queries, kernel
+ * attributes); make it outside CUDA stream capture.  After that, w4a16_gemv
+ * may be captured.
  */
 w4a16_status w4a16_gemv(const uint32_t* qweight, const uint16_t* scales, const uint16_t* x,
                         uint16_t* y, int M, int N, int K, int group, void* stream);
@@ -347,9 +353,10 @@ w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* layers, int n
  * Limits: head_dim == 128, n_heads a multiple of n_kv_heads with at most 16
  * query heads per KV head, 1 <= T <= t_stride <= 2^24 (W4A16_ERR_SHAPE
  * otherwise, also for a workspace smaller than required); every pointer
- * 16-byte aligned (W4A16_ERR_ALIGN).  Two kernel launches on `stream` (the
- * second a programmatic dependent of the first); never allocates, never
- * synchronises, deterministic.
+ * 16-byte aligned (W4A16_ERR_ALIGN).  Two kernel launches on `stream`, each
+ * a programmatic dependent of the kernel before it (the first reads q and
+ * the caches only after the previous kernel has completed); never
+ * allocates, never synchronises, deterministic.
  */
 w4a16_status w4a16_attn_decode_workspace(int n_heads, int n_kv_heads, int head_dim, int T,
                                          size_t* bytes);

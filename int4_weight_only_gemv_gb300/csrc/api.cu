@@ -174,8 +174,11 @@ w4a16_status w4a16_gemv(const uint32_t* qweight, const uint16_t* scales, const u
   if (M == 0 || N == 0) return W4A16_OK;
   DeviceState* d = nullptr;
   if ((s = device_state(&d)) != W4A16_OK) return s;
-  return enqueue(*d, plain_args(qweight, scales, x, y, M, N, K, K, N),
-                 static_cast<cudaStream_t>(stream));
+  // a programmatic dependent of the previous kernel on the stream: the
+  // kernels read only the constant weights and scales before waiting for it
+  GemvArgs ga = plain_args(qweight, scales, x, y, M, N, K, K, N);
+  ga.pdl = true;
+  return enqueue(*d, ga, static_cast<cudaStream_t>(stream));
 }
 
 namespace {
@@ -230,7 +233,7 @@ w4a16_status w4a16_attn_decode(const uint16_t* q, const uint16_t* k_cache, const
   a.n_kv_heads = n_kv_heads;
   a.T = T;
   a.t_stride = t_stride;
-  a.pdl = false;
+  a.pdl = true;  // the partial kernel reads q and the caches only after its wait
   a.status = d->status;
   if (launch_attn_decode(a, d->info, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
@@ -250,6 +253,7 @@ w4a16_status w4a16_gemv_a8(const uint32_t* qweight, const uint16_t* scales, cons
   if ((s = device_state(&d)) != W4A16_OK) return s;
   GemvArgs a = plain_args(qweight, scales, x, y, M, N, K, K, N);
   a.a8 = true;
+  a.pdl = true;  // as w4a16_gemv
   a.status = d->status;
   if (launch_gemv_m1(a, d->info, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
