@@ -348,6 +348,9 @@ __global__ void __launch_bounds__(kAMergeThreads) attn_combine_kernel(const floa
   __shared__ float e_sh[kAMaxSplits];
   __shared__ float red[kAMergeThreads / 32];
   __shared__ float part_sh[kAMergeParts][kAD];
+  // the next kernel may be scheduled now: it reads and writes nothing of
+  // this one's before its own wait for this grid to complete
+  pdl_launch_dependents();
   pdl_wait();
   const int h = blockIdx.x;
   const int g = h / group, r = h % group;
