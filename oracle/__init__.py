@@ -71,6 +71,10 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.orc_quantize_act_a8.restype = ctypes.c_int
     L.orc_gemv_w4a8.argtypes = [p, p, p, i64, i64, i64, i64, p]
     L.orc_gemv_w4a8.restype = ctypes.c_int
+    L.orc_q4k_dequant.argtypes = [p, i64, i64, p]
+    L.orc_q4k_dequant.restype = ctypes.c_int
+    L.orc_q4k_gemv.argtypes = [p, p, i64, i64, i64, p]
+    L.orc_q4k_gemv.restype = ctypes.c_int
     for f in ("orc_quantize", "orc_unpack", "orc_dequant", "orc_dequant_f64", "orc_gemv",
               "orc_gemv_rows"):
         getattr(L, f).restype = ctypes.c_int
@@ -240,6 +244,28 @@ def gemv_w4a8(qweight: np.ndarray, scales: np.ndarray, x: np.ndarray, group: int
     M = x.shape[0]
     y = np.empty((M, N), np.float64)
     _check(L.orc_gemv_w4a8(_ptr(qweight), _ptr(scales), _ptr(x), M, N, K8 * 8, group, _ptr(y)), "gemv_w4a8")
+    return y
+
+
+def q4k_dequant(blocks: np.ndarray, N: int, K: int, L=None) -> np.ndarray:
+    """GGUF Q4_K blocks (uint8, N * K / 256 * 144 bytes) -> float32 [N][K]
+    (the FP32 reference dequantisation, see orc_q4k_dequant)."""
+    L = L or lib()
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    assert blocks.size == N * (K // 256) * 144
+    w = np.empty((N, K), np.float32)
+    _check(L.orc_q4k_dequant(_ptr(blocks), N, K, _ptr(w)), "q4k_dequant")
+    return w
+
+
+def q4k_gemv(blocks: np.ndarray, x: np.ndarray, N: int, K: int, L=None) -> np.ndarray:
+    """y[M][N] = x . w^T over GGUF Q4_K blocks with exact weights, FP64."""
+    L = L or lib()
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    M = x.shape[0]
+    y = np.empty((M, N), np.float64)
+    _check(L.orc_q4k_gemv(_ptr(blocks), _ptr(x), M, N, K, _ptr(y)), "q4k_gemv")
     return y
 
 

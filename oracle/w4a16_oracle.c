@@ -395,3 +395,92 @@ int orc_gemv_w4a8(const uint32_t* qweight, const uint16_t* scales, const uint16_
   free(sx);
   return rc;
 }
+
+/* ---------------------------------------------------------------------------
+ * GGUF Q4_K super-blocks (the page "VTE" (page 1), dequantisation of Q4_K /
+ * Q6_K / Q8_0 byte for byte in llama.cpp's reference layout, checked layer
+ * by layer against NumPy; the hipEngine page serves GGUF Q4_K_M files).  The
+ * pages print no layout; this is the GGUF Q4_K block as published with that
+ * format.  A row of K weights (K a multiple of 256) is K / 256 blocks of 144
+ * bytes:
+ *   bytes 0-1   d     (fp16)   scale of the sub-block scales
+ *   bytes 2-3   dmin  (fp16)   scale of the sub-block minima
+ *   bytes 4-15  eight 6-bit scales sc_j and eight 6-bit minima m_j:
+ *               j < 4:  sc_j = b[j] & 63,  m_j = b[j + 4] & 63
+ *               j >= 4: sc_j = (b[j + 4] & 15) | ((b[j - 4] >> 6) << 4)
+ *                       m_j  = (b[j + 4] >> 4) | ((b[j] >> 6) << 4)
+ *               (b = bytes 4-15)
+ *   bytes 16-143  256 unsigned 4-bit codes q: weight e of the block, with
+ *               c = e / 64 and i = e % 64, is the low nibble of byte
+ *               16 + 32 c + i for i < 32 (sub-block j = 2 c) and the high
+ *               nibble of byte 16 + 32 c + i - 32 for i >= 32 (j = 2 c + 1).
+ * The weight is w = d sc_j q - dmin m_j.  The reference dequantisation works
+ * in FP32 as d1 = d sc_j, m1 = dmin m_j, w = d1 q - m1 (three roundings,
+ * no fused multiply-add); the GEMV uses the exact value (every product fits
+ * FP64 exactly: 11 + 6 + 4 significand bits) in an FP64 sum.
+ * ------------------------------------------------------------------------- */
+#define ORC_QK 256
+#define ORC_QK_BYTES 144
+
+static void q4k_scale_min(int j, const uint8_t* b, int* sc, int* m) {
+  if (j < 4) {
+    *sc = b[j] & 63;
+    *m = b[j + 4] & 63;
+  } else {
+    *sc = (b[j + 4] & 15) | ((b[j - 4] >> 6) << 4);
+    *m = (b[j + 4] >> 4) | ((b[j] >> 6) << 4);
+  }
+}
+
+/* Code, sub-block of weight e (0..255) of one block. */
+static int q4k_code(const uint8_t* blk, int e, int* j) {
+  const int c = e / 64, i = e % 64;
+  if (i < 32) {
+    *j = 2 * c;
+    return blk[16 + 32 * c + i] & 15;
+  }
+  *j = 2 * c + 1;
+  return blk[16 + 32 * c + i - 32] >> 4;
+}
+
+static uint16_t rd_u16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* w[N][K] as float (the FP32 reference dequantisation above). */
+int orc_q4k_dequant(const uint8_t* blocks, int64_t N, int64_t K, float* w) {
+  if (N < 0 || K <= 0 || K % ORC_QK != 0) return ORC_ERR_SHAPE;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t s = 0; s < K / ORC_QK; ++s) {
+      const uint8_t* blk = blocks + (n * (K / ORC_QK) + s) * ORC_QK_BYTES;
+      const float d = (float)orc_half_to_double(rd_u16(blk));
+      const float dmin = (float)orc_half_to_double(rd_u16(blk + 2));
+      for (int e = 0; e < ORC_QK; ++e) {
+        int j, sc, m;
+        const int q = q4k_code(blk, e, &j);
+        q4k_scale_min(j, blk + 4, &sc, &m);
+        const float d1 = d * (float)sc;
+        const float m1 = dmin * (float)m;
+        const float dq = d1 * (float)q;
+        w[n * K + s * ORC_QK + e] = dq - m1;
+      }
+    }
+  return ORC_OK;
+}
+
+/* y[M][N] = x[M][K] . w^T with the exact weights, in FP64 (ascending k). */
+int orc_q4k_gemv(const uint8_t* blocks, const uint16_t* x, int64_t M, int64_t N, int64_t K, double* y) {
+  if (M <= 0 || N < 0 || K <= 0 || K % ORC_QK != 0) return ORC_ERR_SHAPE;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const uint8_t* blk = blocks + (n * (K / ORC_QK) + k / ORC_QK) * ORC_QK_BYTES;
+        int j, sc, mn;
+        const int q = q4k_code(blk, (int)(k % ORC_QK), &j);
+        q4k_scale_min(j, blk + 4, &sc, &mn);
+        const double wv = orc_half_to_double(rd_u16(blk)) * sc * q - orc_half_to_double(rd_u16(blk + 2)) * mn;
+        acc += orc_half_to_double(x[m * K + k]) * wv;
+      }
+      y[m * N + n] = acc;
+    }
+  return ORC_OK;
+}

@@ -488,6 +488,78 @@ def pin_a8_gemv_vs_numpy_and_exact_case(L):
     assert np.array_equal(y8, oracle.gemv(qw, sc, xi.view(np.uint16), 128, L))
 
 
+def _q4k_block(d, dmin, sc, mn, qs=None):
+    """One 144-byte Q4_K block from its parts: d, dmin (float, stored fp16),
+    eight 6-bit scales and minima (packed here into the 12 bytes the
+    decoding reads back: j < 4 in the low 6 bits of bytes j and j + 4, j >= 4
+    split into bytes j + 4 (low nibble: scale, high: minimum) and the top two
+    bits of bytes j - 4 (scale) and j (minimum)), 128 code bytes."""
+    b = np.zeros(144, np.uint8)
+    b[0:2] = np.frombuffer(np.array([d], np.float16).tobytes(), np.uint8)
+    b[2:4] = np.frombuffer(np.array([dmin], np.float16).tobytes(), np.uint8)
+    p = np.zeros(12, np.int64)
+    for j in range(4):
+        p[j] = sc[j] | ((sc[j + 4] >> 4) << 6)
+        p[j + 4] = mn[j] | ((mn[j + 4] >> 4) << 6)
+        p[j + 8] = (sc[j + 4] & 15) | ((mn[j + 4] & 15) << 4)
+    b[4:16] = p.astype(np.uint8)
+    if qs is not None:
+        b[16:] = qs
+    return b
+
+
+def pin_q4k_scales_and_minima(L):
+    """With d = dmin = 1: all-zero codes give w = -m_j on sub-block j, codes
+    of 1 give sc_j - m_j, for random 6-bit scales and minima (every bit of
+    the packing exercised)."""
+    rng = np.random.default_rng(31)
+    for _ in range(4):
+        sc = rng.integers(0, 64, 8)
+        mn = rng.integers(0, 64, 8)
+        w0 = oracle.q4k_dequant(_q4k_block(1.0, 1.0, sc, mn), 1, 256, L)[0]
+        w1 = oracle.q4k_dequant(_q4k_block(1.0, 1.0, sc, mn, np.full(128, 0x11, np.uint8)), 1, 256, L)[0]
+        for j in range(8):
+            assert (w0[32 * j:32 * j + 32] == -mn[j]).all(), j
+            assert (w1[32 * j:32 * j + 32] == sc[j] - mn[j]).all(), j
+
+
+def pin_q4k_element_order(L):
+    """Single nibbles land at the documented weights: low nibble of code byte
+    5 -> weight 5, its high nibble -> weight 37, high nibble of byte 64 + 9
+    (chunk 2) -> weight 128 + 32 + 9; scales 1..8 tell the sub-blocks apart."""
+    qs = np.zeros(128, np.uint8)
+    qs[5] = 0x73
+    qs[64 + 9] = 0x20
+    sc = np.arange(1, 9)
+    w = oracle.q4k_dequant(_q4k_block(1.0, 0.0, sc, np.zeros(8, np.int64), qs), 1, 256, L)[0]
+    want = np.zeros(256, np.float32)
+    want[5] = 3 * 1
+    want[37] = 7 * 2
+    want[169] = 2 * 6
+    assert np.array_equal(w, want)
+
+
+def pin_q4k_fp32_and_gemv(L):
+    """On random blocks the FP32 dequantisation is within three roundings of
+    the exact weights (read back as GEMV columns through one-hot
+    activations), and the GEMV equals x . w within the FP32 rounding of w."""
+    rng = np.random.default_rng(33)
+    N, K = 4, 512
+    b = rng.integers(0, 256, (N * 2, 144)).astype(np.uint8)
+    for i in range(N * 2):
+        b[i, 0:2] = np.frombuffer(np.array([rng.uniform(1e-3, 0.05)], np.float16).tobytes(), np.uint8)
+        b[i, 2:4] = np.frombuffer(np.array([rng.uniform(1e-3, 0.05)], np.float16).tobytes(), np.uint8)
+    w32 = oracle.q4k_dequant(b.reshape(-1), N, K, L).astype(np.float64)
+    eye = np.eye(K, dtype=np.float16)[::37]
+    cols = oracle.q4k_gemv(b.reshape(-1), eye.view(np.uint16), N, K, L)  # rows = exact w[:, k]
+    exact = cols.T
+    assert (np.abs(w32[:, ::37] - exact) <= 4 * np.spacing(np.abs(exact).astype(np.float32)) + 1e-12).all()
+    x = rng.standard_normal((2, K)).astype(np.float16)
+    y = oracle.q4k_gemv(b.reshape(-1), x.view(np.uint16), N, K, L)
+    ref = x.astype(np.float64) @ w32.T
+    assert np.allclose(y, ref, rtol=0, atol=1e-5 * np.abs(x).sum())
+
+
 ALL_PINS = [
     pin_half_to_double_exhaustive, pin_half_roundtrip, pin_half_midpoints_ties_to_even,
     pin_half_overflow_and_specials, pin_half_vs_numpy_random, pin_hand_words,
@@ -498,6 +570,7 @@ ALL_PINS = [
     pin_attn_single_key, pin_attn_two_keys_scale, pin_attn_uniform_and_constant,
     pin_attn_permutation_and_dominance, pin_attn_stride_and_prefix,
     pin_a8_quantize_vs_numpy, pin_a8_ties_and_zero_block, pin_a8_gemv_vs_numpy_and_exact_case,
+    pin_q4k_scales_and_minima, pin_q4k_element_order, pin_q4k_fp32_and_gemv,
 ]
 
 

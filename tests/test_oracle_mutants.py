@@ -49,6 +49,11 @@ MUTANTS = [
      "const float sb = amax > 0.0f ? amax / 128.0f : 0.0f;"),
     ("a8_weight_scale_index", "scales[n * (K / G) + (b * ORC_A8_BLOCK) / G]", "scales[n * (K / G) + b / G]"),
     ("a8_activation_scale_dropped", "* (double)sx[b];", ";"),
+    ("q4k_high_scale_bits_swapped", "*sc = (b[j + 4] & 15) | ((b[j - 4] >> 6) << 4);",
+     "*sc = (b[j + 4] & 15) | ((b[j] >> 6) << 4);"),
+    ("q4k_nibble_half_swapped", "return blk[16 + 32 * c + i] & 15;", "return blk[16 + 32 * c + i] >> 4;"),
+    ("q4k_min_sign", "w[n * K + s * ORC_QK + e] = dq - m1;", "w[n * K + s * ORC_QK + e] = dq + m1;"),
+    ("q4k_odd_subblock_index", "*j = 2 * c + 1;", "*j = 2 * c;"),
     ("swiglu_gate_up_swapped",
      "orc_silu(orc_half_to_double(g[i])) * orc_half_to_double(u[i])",
      "orc_silu(orc_half_to_double(u[i])) * orc_half_to_double(g[i])"),
