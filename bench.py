@@ -402,11 +402,57 @@ def per_config_table(layers, dev, reps=20):
     b = gemv_bytes(cfg.N, cfg.K, 1)
     out["tiny"] = {"M": 1, "N": cfg.N, "K": cfg.K, "us_per_gemv": round(us, 3),
                    "GBps": round(b / us / 1e3, 1), "bytes": b, "note": "L2-resident, latency-bound"}
+    out["gate_up_q4k"] = q4k_line(dev, reps)
     out["attn_decode_T8192"] = attn_decode_line(dev, reps)
     out["layer_seq_qkv_bias_swiglu"] = epilogue_step(layers, dev, reps, ("q", "k", "v"))
     out["layer_seq_bias_swiglu"] = epilogue_step(layers, dev, reps, synth.PROJ_NAMES)
     out["layer_seq_w4a8"] = epilogue_step(layers, dev, reps, (), act_int8=True)
     return out
+
+
+def q4k_line(dev, reps, N=None, K=None):
+    """The [gate; up] shape (N = 37888, K = 3584) as GGUF Q4_K blocks at M = 1:
+    a CUDA graph of 28 GEMVs over 28 distinct block sets (cold L2), us per
+    GEMV and GB/s over the block bytes plus x and y."""
+    import torch
+
+    import int4_weight_only_gemv_gb300 as w4
+    import synth
+    N = 2 * synth.FFN if N is None else N
+    K = synth.HIDDEN if K is None else K
+    nb = N * (K // 256)
+    g = torch.Generator(device=dev).manual_seed(4)
+    sets = []
+    for _ in range(synth.N_LAYERS):
+        b = torch.randint(0, 256, (nb, 144), generator=g, dtype=torch.uint8, device=dev)
+        d = (torch.rand((nb, 2), generator=g, device=dev) * 0.05 + 1e-3).half()
+        b[:, 0:4] = d.view(torch.uint8).view(nb, 4)
+        sets.append(b.view(-1))
+    xs = [synth.activations(1, K, 90 + i, dev).view(-1) for i in range(len(sets))]
+    ys = [torch.empty((N,), dtype=torch.float16, device=dev) for _ in sets]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for b, x, y in zip(sets, xs, ys):
+            w4.w4a16_q4k_gemv(b, x, N, K, y=y)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for b, x, y in zip(sets, xs, ys):
+            w4.w4a16_q4k_gemv(b, x, N, K, y=y)
+    for _ in range(3):
+        gr.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    s.record(cur)
+    for _ in range(reps):
+        gr.replay()
+    e.record(cur)
+    torch.cuda.synchronize()
+    us = 1e3 * s.elapsed_time(e) / (reps * len(sets))
+    bts = nb * 144 + 2 * K + 2 * N
+    return {"M": 1, "N": N, "K": K, "us_per_gemv": round(us, 3), "GBps": round(bts / us / 1e3, 1), "bytes": bts,
+            "note": "GGUF Q4_K blocks (4.5 bits per weight), read as stored"}
 
 
 def attn_decode_line(dev, reps, T=8192):

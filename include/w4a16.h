@@ -364,6 +364,35 @@ w4a16_status w4a16_attn_decode(const uint16_t* q, const uint16_t* k_cache, const
                                uint16_t* o, int n_heads, int n_kv_heads, int head_dim, int T,
                                int t_stride, float* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * GGUF Q4_K super-blocks (the format the page "VTE" dequantises byte for
+ * byte in llama.cpp's layout; the hipEngine page serves GGUF Q4_K_M files).
+ * A row of K weights (K a positive multiple of 256, at most W4A16_MAX_K) is
+ * K / 256 blocks of 144 bytes, rows back to back (`blocks` N * K / 256 * 144
+ * bytes, 16-byte aligned):
+ *   bytes 0-1 d, 2-3 dmin (fp16); bytes 4-15 eight 6-bit scales sc_j and
+ *   minima m_j (j < 4: sc_j = b[j] & 63, m_j = b[j + 4] & 63; j >= 4:
+ *   sc_j = (b[j + 4] & 15) | (b[j - 4] >> 6) << 4, m_j = (b[j + 4] >> 4) |
+ *   (b[j] >> 6) << 4, b = bytes 4-15); bytes 16-143 unsigned 4-bit codes,
+ *   chunk c of 32 bytes holding sub-block 2c in the low nibbles and 2c + 1
+ *   in the high nibbles (weight 64 c + i, i < 32: low nibble of byte i).
+ * The weight is w = d sc_j q - dmin m_j.  The blocks are read as stored (no
+ * repack).
+ *
+ * w4a16_q4k_gemv   y[n] = fp16_RN(sum_k x[k] w[n][k]) for one activation
+ *                  row x (fp16 [K]), y fp16 [N] (must not overlap x or the
+ *                  blocks); FP32 accumulation; a programmatic dependent of
+ *                  the previous kernel on the stream as w4a16_gemv.
+ * w4a16_q4k_dequant  w_out float [N][K] = (d sc_j) q - dmin m_j in FP32 with
+ *                  three roundings (the reference dequantisation; must not
+ *                  overlap the blocks).
+ * N == 0: OK, nothing launched.  Errors: W4A16_ERR_SHAPE, _NULL, _ALIGN,
+ * _ALIAS, _CUDA as for w4a16_gemv.  Never allocate, never synchronise.
+ */
+w4a16_status w4a16_q4k_gemv(const uint8_t* blocks, const uint16_t* x, uint16_t* y, int N, int K,
+                            void* stream);
+w4a16_status w4a16_q4k_dequant(const uint8_t* blocks, float* w_out, int N, int K, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

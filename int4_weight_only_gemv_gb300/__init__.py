@@ -20,7 +20,7 @@ __all__ = [
     "w4a16_selftest_wait_timeout", "w4a16_layer_seq_run_static", "STATIC_MAX_GEMVS",
     "LayerSeq", "GROUP", "MAX_M", "MAX_K", "DEV_NONFINITE", "DEV_SCALE_OVERFLOW",
     "DEV_PIPE_TIMEOUT", "STATUS", "EXPORTED_SYMBOLS", "w4a16_attn_decode", "attn_decode_workspace",
-    "w4a16_gemv_a8", "SEQ_ACT_INT8",
+    "w4a16_gemv_a8", "SEQ_ACT_INT8", "w4a16_q4k_gemv", "w4a16_q4k_dequant",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -49,7 +49,8 @@ EXPORTED_SYMBOLS = (
     "w4a16_device_status", "w4a16_selftest_wait_timeout", "w4a16_layer_seq_create", "w4a16_layer_seq_num_launches",
     "w4a16_layer_seq_run", "w4a16_layer_seq_run_host", "w4a16_layer_seq_sync",
     "w4a16_layer_seq_destroy", "w4a16_layer_seq_run_static", "w4a16_layer_seq_create2",
-    "w4a16_attn_decode_workspace", "w4a16_attn_decode", "w4a16_gemv_a8",
+    "w4a16_attn_decode_workspace", "w4a16_attn_decode", "w4a16_gemv_a8", "w4a16_q4k_gemv",
+    "w4a16_q4k_dequant",
 )
 
 
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.w4a16_abi_version.restype = i
         L.w4a16_gemv.argtypes = [p, p, p, p, i, i, i, i, p]
         L.w4a16_gemv_a8.argtypes = [p, p, p, p, i, i, i, i, p]
+        L.w4a16_q4k_gemv.argtypes = [p, p, p, i, i, p]
+        L.w4a16_q4k_dequant.argtypes = [p, p, i, i, p]
         L.w4a16_dequant.argtypes = [p, p, p, i, i, i, p]
         L.w4a16_quantize.argtypes = [p, p, p, i, i, i, p]
         L.w4a16_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
@@ -111,7 +114,7 @@ def lib() -> ctypes.CDLL:
                                                  ctypes.POINTER(_SeqIO), p]
         L.w4a16_attn_decode_workspace.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         L.w4a16_attn_decode.argtypes = [p, p, p, p, i, i, i, i, i, p, ctypes.c_size_t, p]
-        for f in ("w4a16_gemv", "w4a16_gemv_a8", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
+        for f in ("w4a16_gemv", "w4a16_gemv_a8", "w4a16_q4k_gemv", "w4a16_q4k_dequant", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
                   "w4a16_selftest_wait_timeout",
                   "w4a16_layer_seq_create", "w4a16_layer_seq_run", "w4a16_layer_seq_run_host",
                   "w4a16_layer_seq_sync", "w4a16_layer_seq_run_static", "w4a16_layer_seq_create2",
@@ -160,6 +163,25 @@ def w4a16_gemv_a8(qweight, scales, x, y=None, stream=None):
     _check(lib().w4a16_gemv_a8(_ptr(qweight), _ptr(scales), _ptr(x), _ptr(y), M, N, K, GROUP,
                                _stream(stream)), "w4a16_gemv_a8")
     return y
+
+
+def w4a16_q4k_gemv(blocks, x, N, K, y=None, stream=None):
+    """GGUF Q4_K GEMV (M = 1): blocks uint8 CUDA tensor of N * K / 256 * 144
+    bytes, x float16 [K] or [1][K]; returns y float16 [N]."""
+    import torch
+    if y is None:
+        y = torch.empty((N,), dtype=torch.float16, device=x.device)
+    _check(lib().w4a16_q4k_gemv(_ptr(blocks), _ptr(x), _ptr(y), N, K, _stream(stream)), "w4a16_q4k_gemv")
+    return y
+
+
+def w4a16_q4k_dequant(blocks, N, K, w_out=None, stream=None):
+    """GGUF Q4_K blocks -> float32 [N][K] (the FP32 reference dequantisation)."""
+    import torch
+    if w_out is None:
+        w_out = torch.empty((N, K), dtype=torch.float32, device=blocks.device)
+    _check(lib().w4a16_q4k_dequant(_ptr(blocks), _ptr(w_out), N, K, _stream(stream)), "w4a16_q4k_dequant")
+    return w_out
 
 
 def w4a16_gemv_raw(qw_ptr, sc_ptr, x_ptr, y_ptr, M, N, K, group=GROUP, stream=None) -> int:

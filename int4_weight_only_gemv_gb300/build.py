@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libw4a16.so")
-SOURCES = ["api.cu", "gemv_m1.cu", "gemv_rows.cu", "gemv_mma.cu", "quant.cu", "attn_decode.cu"]
+SOURCES = ["api.cu", "gemv_m1.cu", "gemv_rows.cu", "gemv_mma.cu", "quant.cu", "attn_decode.cu", "q4k.cu"]
 HEADERS = ["kernels.h", "ptx.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

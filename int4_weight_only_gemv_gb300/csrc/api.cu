@@ -58,7 +58,7 @@ w4a16_status device_state(DeviceState** out) {
     d.info.max_smem_optin = smem;
     d.status = static_cast<uint32_t*>(addr);
     if (prepare_gemv_m1(d.info) != cudaSuccess || prepare_gemv_mma(d.info) != cudaSuccess ||
-        prepare_attn_decode(d.info) != cudaSuccess) {
+        prepare_attn_decode(d.info) != cudaSuccess || prepare_q4k(d.info) != cudaSuccess) {
       cudaGetLastError();
       return W4A16_ERR_CUDA;
     }
@@ -256,6 +256,52 @@ w4a16_status w4a16_gemv_a8(const uint32_t* qweight, const uint16_t* scales, cons
   a.pdl = true;  // as w4a16_gemv
   a.status = d->status;
   if (launch_gemv_m1(a, d->info, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+namespace {
+w4a16_status check_q4k(const void* blocks, int N, int K) {
+  if (K <= 0 || K % 256 != 0 || K > W4A16_MAX_K || N < 0 || N > W4A16_MAX_N) return W4A16_ERR_SHAPE;
+  if (N > 0 && !blocks) return W4A16_ERR_NULL;
+  if (N > 0 && !aligned16(blocks)) return W4A16_ERR_ALIGN;
+  return W4A16_OK;
+}
+}  // namespace
+
+w4a16_status w4a16_q4k_gemv(const uint8_t* blocks, const uint16_t* x, uint16_t* y, int N, int K,
+                            void* stream) {
+  w4a16_status s = check_q4k(blocks, N, K);
+  if (s != W4A16_OK) return s;
+  if (N == 0) return W4A16_OK;
+  if (!x || !y) return W4A16_ERR_NULL;
+  if (!aligned16(x) || !aligned16(y)) return W4A16_ERR_ALIGN;
+  const size_t bbytes = static_cast<size_t>(N) * (K / 256) * 144;
+  if (overlaps(y, static_cast<size_t>(N) * 2, blocks, bbytes) ||
+      overlaps(y, static_cast<size_t>(N) * 2, x, static_cast<size_t>(K) * 2))
+    return W4A16_ERR_ALIAS;
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != W4A16_OK) return s;
+  if (launch_q4k_gemv(blocks, x, y, N, K, true, d->info, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_q4k_dequant(const uint8_t* blocks, float* w_out, int N, int K, void* stream) {
+  w4a16_status s = check_q4k(blocks, N, K);
+  if (s != W4A16_OK) return s;
+  if (N == 0) return W4A16_OK;
+  if (!w_out) return W4A16_ERR_NULL;
+  if (!aligned16(w_out)) return W4A16_ERR_ALIGN;
+  if (overlaps(w_out, static_cast<size_t>(N) * K * 4, blocks, static_cast<size_t>(N) * (K / 256) * 144))
+    return W4A16_ERR_ALIAS;
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != W4A16_OK) return s;
+  if (launch_q4k_dequant(blocks, w_out, N, K, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return W4A16_ERR_CUDA;
   }

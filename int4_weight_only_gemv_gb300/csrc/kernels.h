@@ -143,6 +143,12 @@ struct AttnArgs {
 int attn_splits(int n_kv_heads, int T, const DeviceInfo& d);
 size_t attn_workspace_bytes(int n_kv_heads, int splits);
 cudaError_t launch_attn_decode(const AttnArgs& a, const DeviceInfo& d, cudaStream_t st);
+// GGUF Q4_K (q4k.cu): K a multiple of 256, blocks 16-byte aligned.
+cudaError_t launch_q4k_dequant(const uint8_t* blocks, float* w, int N, int K, cudaStream_t st);
+cudaError_t launch_q4k_gemv(const uint8_t* blocks, const uint16_t* x, uint16_t* y, int N, int K, bool pdl,
+                            const DeviceInfo& d, cudaStream_t st);
+size_t q4k_gemv_smem(int K);
+cudaError_t prepare_q4k(const DeviceInfo& d);
 // cuTensorMapEncodeTiled from the driver (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 

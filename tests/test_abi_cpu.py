@@ -208,3 +208,14 @@ def test_attn_decode_argument_checks(L):
     n = ctypes.c_size_t(7)
     assert L.w4a16_attn_decode_workspace(28, 4, 128, 0, ctypes.byref(n)) == 2 and n.value == 0
     assert L.w4a16_attn_decode_workspace(28, 4, 128, 10, None) == 1
+
+
+def test_q4k_argument_checks(L):
+    assert L.w4a16_q4k_gemv(A, C, D, 8, 100, None) == 2        # K not a multiple of 256
+    assert L.w4a16_q4k_gemv(A, C, D, 8, 32768 + 256, None) == 2
+    assert L.w4a16_q4k_gemv(0, C, D, 8, 256, None) == 1        # null blocks
+    assert L.w4a16_q4k_gemv(A + 8, C, D, 8, 256, None) == 3    # misaligned blocks
+    assert L.w4a16_q4k_gemv(A, C, C, 8, 256, None) == 6        # y overlaps x
+    assert L.w4a16_q4k_gemv(0, 0, 0, 0, 256, None) == 0        # N = 0
+    assert L.w4a16_q4k_dequant(A, 0, 8, 256, None) == 1
+    assert L.w4a16_q4k_dequant(A, A, 8, 256, None) == 6        # output overlaps the blocks
