@@ -284,7 +284,13 @@ w4a16_status w4a16_q4k_gemv(const uint8_t* blocks, const uint16_t* x, uint16_t* 
     return W4A16_ERR_ALIAS;
   DeviceState* d = nullptr;
   if ((s = device_state(&d)) != W4A16_OK) return s;
-  if (launch_q4k_gemv(blocks, x, y, N, K, true, d->info, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+  // the persistent TMA-fed kernel where K fits its consumer threads, else the
+  // warp-per-row kernel
+  const cudaError_t e =
+      gemv_m1_q4k_supported(K)
+          ? launch_gemv_m1_q4k(blocks, x, y, N, K, true, d->status, d->info, static_cast<cudaStream_t>(stream))
+          : launch_q4k_gemv(blocks, x, y, N, K, true, d->info, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return W4A16_ERR_CUDA;
   }

@@ -31,7 +31,7 @@
 //               -> biased fp16, see ptx.cuh) and eight f16 x f16 -> f32 FMAs;
 //               the biases 1032 and 72 are removed once per unit and row with
 //               the precomputed C = 1032 sum x_even + 72 sum x_odd.
-// W4A8 variant (kA8, the INT8-activation GEMV that the same section's third
+// W4A8 variant (kFmt = kFmtW4A8, the INT8-activation GEMV that the same section's third
 // bug compares with): each consumer thread quantises its own 64-activation
 // unit when it loads it (scale max|x| / 127 and codes round(x 127 / max|x|)
 // in FP32, ties to even), so no pass over x runs first and x stays
@@ -39,6 +39,14 @@
 // bytes, even and odd k) and two dp4a against the unit's codes; the bias 8 is
 // removed once per unit and row with 8 sum(codes), and the integer sum is
 // scaled by group scale x activation scale in FP32.
+// Q4_K variant (kFmt = kFmtQ4K, a single GEMV): the tile is RB whole rows of
+// GGUF Q4_K super-blocks (144 bytes per 256 weights, scales inside the
+// blocks, so there is no scale window).  Unit u is chunk u mod 4 of block
+// u / 4; per row the thread reads the block's 16-byte header and the chunk's
+// 32 code bytes, forms D_j = sum (1024 + q) x for its two sub-blocks with
+// mask-and-OR unpacking (the high nibbles in place, as 1024 + 16 q), and
+// returns d sc_j (D_j - 1024 S_j) - dmin m_j S_j summed over them, S_j =
+// sum x over the sub-block computed once per task.
 // Every wait is bounded; on a timeout the kernel sets W4A16_DEV_PIPE_TIMEOUT
 // and the CTA returns once its copies in flight have landed.
 #include <cuda_fp16.h>
@@ -59,7 +67,14 @@ constexpr int kRR = 4;  // rows per consumer thread per tile
 constexpr int kM1MaxStages = 8;
 constexpr int kM1SmemBudget = 200 * 1024;
 
-// Per-task tiling, a pure function of K (U <= kM1MaxConsumers).
+// Weight formats of the kernel: the INT4 group-128 layout with FP16 or
+// in-kernel INT8 activations, and GGUF Q4_K blocks (144 bytes per 256
+// weights, scales inside the blocks).
+constexpr int kFmtW4A16 = 0;
+constexpr int kFmtW4A8 = 1;
+constexpr int kFmtQ4K = 2;
+
+// Per-task tiling, a pure function of K and the format (U <= kM1MaxConsumers).
 struct TaskPlan {
   int U;             // units (64 k) per row
   int RL;            // rows across consumer threads
@@ -70,14 +85,15 @@ struct TaskPlan {
   int red_stride;    // floats per row in a partial slot (U + 1)
 };
 
-__host__ __device__ inline TaskPlan task_plan(int K) {
+__host__ __device__ inline TaskPlan task_plan(int K, int fmt = kFmtW4A16) {
   TaskPlan p;
   p.U = K >> 6;
   p.RL = p.U >= kM1MaxConsumers ? 1 : kM1MaxConsumers / p.U;
   p.RB = p.RL * kRR;
   p.T = p.U * p.RL;
-  p.row_bytes = K >> 1;
-  p.sc_row_bytes = K >> 6;
+  // Q4_K: 144 bytes per 256 weights (a multiple of 16), no separate scales
+  p.row_bytes = fmt == kFmtQ4K ? (K >> 8) * 144 : K >> 1;
+  p.sc_row_bytes = fmt == kFmtQ4K ? 0 : K >> 6;
   p.red_stride = p.U + 1;
   return p;
 }
@@ -101,10 +117,10 @@ constexpr int kXReady = 4;          // dependency-signal barriers
 constexpr int kBarrierBytes = 512;  // [full S][empty S][redfull S][redempty S][xready kXReady]
 static_assert(32 * kM1MaxStages + 8 * kXReady <= kBarrierBytes, "barriers overflow their area");
 
-RingPlan make_ring_plan(const int* Ks, int n, int smem_limit) {
+RingPlan make_ring_plan(const int* Ks, int n, int smem_limit, int fmt = kFmtW4A16) {
   RingPlan r{};
   for (int i = 0; i < n; ++i) {
-    const TaskPlan tp = task_plan(Ks[i]);
+    const TaskPlan tp = task_plan(Ks[i], fmt);
     const int st = tp.RB * tp.row_bytes + sc_window_cap(tp);
     const int rb = tp.RB * tp.red_stride * 4;
     const int cw = (tp.T + 31) / 32;
@@ -214,6 +230,55 @@ __device__ __forceinline__ void dot_pair_a8(const uint32_t (&wa)[8], const uint3
   rb = b;
 }
 
+// Q4_K: dot products of one 64-weight unit (chunk c of a block: code word t
+// holds weights 4t .. 4t + 3 in its low nibbles and 32 + 4t .. + 3 in its
+// high nibbles) with this thread's activations, paired as X[t] = {x(4t),
+// x(4t+2)}, {x(4t+1), x(4t+3)}, {x(32+4t), x(32+4t+2)}, {x(32+4t+1),
+// x(32+4t+3)}.  A low nibble becomes fp16 1024 + q and a high nibble, left
+// in place, 1024 + 16 q (bits 4-7 are still mantissa), one LOP3 each.
+// Returns D0 = sum (1024 + q) x over sub-block 2c and D1 = sum (1024 + 16 q) x
+// over sub-block 2c + 1.
+__device__ __forceinline__ void q4k_dot(const uint32_t (&q)[8], const XPairs (&X)[8], float& D0, float& D1) {
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const uint32_t v = q[t], v8 = v >> 8;
+    fma_f32_f16x2(a0, a1, (v & 0x000F000Fu) | 0x64006400u, X[t].p0);
+    fma_f32_f16x2(a0, a1, (v8 & 0x000F000Fu) | 0x64006400u, X[t].p1);
+    fma_f32_f16x2(b0, b1, (v & 0x00F000F0u) | 0x64006400u, X[t].p2);
+    fma_f32_f16x2(b0, b1, (v8 & 0x00F000F0u) | 0x64006400u, X[t].p3);
+  }
+  D0 = a0 + a1;
+  D1 = b0 + b1;
+}
+
+// Q4_K: the 6-bit scales and minima of sub-blocks 2c and 2c + 1 from the
+// header words h.y, h.z, h.w (packed bytes 0-11) as bytes {sc0, sc1, m0, m1}
+// of one word.  Both cases start from bytes {2c', 2c'+1, 2c'+4, 2c'+5},
+// c' = c mod 2 (selector selp): for c < 2 these are the values' 6 bits;
+// for c >= 2 their top two bits are the values' bits 4-5, and the low four
+// come from the nibbles of bytes 8 + 2c', 9 + 2c' (selector selq: scale in
+// the low nibble, minimum in the high).
+__device__ __forceinline__ uint32_t q4k_scales_pair(const uint4 h, uint32_t selp, uint32_t selq, bool hi) {
+  const uint32_t p = __byte_perm(h.y, h.z, selp);
+  const uint32_t q = __byte_perm(h.w, h.w, selq);
+  const uint32_t low = (q & 0x00000F0Fu) | ((q >> 4) & 0x0F0F0000u);
+  return hi ? (low | ((p >> 2) & 0x30303030u)) : (p & 0x3F3F3F3Fu);
+}
+
+// Q4_K: one row's partial of the unit from its block header h:
+// d sc0 (D0 - 1024 S0) + d sc1 (D1 - 1024 S1) / 16 - dmin (m0 S0 + m1 S1).
+__device__ __forceinline__ float q4k_combine(const uint4 h, uint32_t selp, uint32_t selq, bool hi, float D0,
+                                             float D1, float S0, float S1) {
+  const uint32_t sm = q4k_scales_pair(h, selp, selq, hi);
+  const float sc0 = static_cast<float>(sm & 0xFFu), sc1 = static_cast<float>((sm >> 8) & 0xFFu);
+  const float m0 = static_cast<float>((sm >> 16) & 0xFFu), m1 = static_cast<float>(sm >> 24);
+  const float d = half_lo(h.x), dmin = half_hi(h.x);
+  float r = (d * sc0) * fmaf(-1024.f, S0, D0);
+  r = fmaf((d * 0.0625f) * sc1, fmaf(-1024.f, S1, D1), r);
+  return fmaf(-dmin, fmaf(m0, S0, m1 * S1), r);
+}
+
 // The low bytes of four ints as one word (byte i from argument i).
 __device__ __forceinline__ uint32_t pack_bytes(int a, int b, int c, int d) {
   const uint32_t lo = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040u);
@@ -232,8 +297,9 @@ __device__ __forceinline__ void load_row(uint32_t addr, int rot, uint32_t (&w)[8
 
 // kAct: some task of the list takes SwiGLU activations (x2 set).  The
 // instantiation without it carries no trace of that path, so the plain task
-// lists compile exactly as they would without the feature.  kA8: W4A8.
-template <int MAXT, bool kAct, bool kA8>
+// lists compile exactly as they would without the feature.  kFmt: the
+// weight format (kFmtW4A16, kFmtW4A8, kFmtQ4K).
+template <int MAXT, bool kAct, int kFmt>
 __global__ void __launch_bounds__(kM1MaxThreads, 1)
     gemv_m1_kernel(const __grid_constant__ M1Params<MAXT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -281,7 +347,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     bool ok = true;
     for (int i = 0; i < p.ntasks && ok; ++i) {
       const M1Task& tk = p.task[i];
-      const TaskPlan tp = task_plan(tk.K);
+      const TaskPlan tp = task_plan(tk.K, kFmt);
       int64_t row_begin;
       const int rows = cta_rows(tk, &row_begin);
       const int ntiles = (rows + tp.RB - 1) / tp.RB;
@@ -362,7 +428,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     };
     for (int i = 0; i < p.ntasks; ++i) {
       const M1Task& tk = p.task[i];
-      const TaskPlan tp = task_plan(tk.K);
+      const TaskPlan tp = task_plan(tk.K, kFmt);
       int64_t row_begin;
       const int rows = cta_rows(tk, &row_begin);
       const int ntiles = (rows + tp.RB - 1) / tp.RB;
@@ -472,7 +538,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
   uint32_t base = stage0, rs = red0;
   for (int i = 0; i < p.ntasks; ++i) {
     const M1Task& tk = p.task[i];
-    const TaskPlan tp = task_plan(tk.K);
+    const TaskPlan tp = task_plan(tk.K, kFmt);
     int64_t row_begin;
     const int rows = cta_rows(tk, &row_begin);
     const int ntiles = (rows + tp.RB - 1) / tp.RB;
@@ -506,7 +572,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     uint32_t xe[8], xo[8];
     int C8 = 0;
     float s_act = 0.f;
-    if (kA8 && wact) {
+    if (kFmt == kFmtW4A8 && wact) {
       const uint16_t* xp = tk.x + u * 64;
       uint4 v[8];
 #pragma unroll
@@ -550,7 +616,27 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       }
       C8 = 8 * csum;
     }
-    if (!kA8 && wact) {
+    // Q4_K: the pairs above and the two 32-activation sums
+    float S0 = 0.f, S1 = 0.f;
+    if (kFmt == kFmtQ4K && wact) {
+      const uint4* xp = reinterpret_cast<const uint4*>(tk.x + u * 64);
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = ld_u4(xp + j);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const uint4 lo = v[t >> 1], hi = v[4 + (t >> 1)];
+        const uint32_t la = (t & 1) ? lo.z : lo.x, lb = (t & 1) ? lo.w : lo.y;
+        const uint32_t ha = (t & 1) ? hi.z : hi.x, hb = (t & 1) ? hi.w : hi.y;
+        X[t].p0 = __byte_perm(la, lb, 0x5410u);
+        X[t].p1 = __byte_perm(la, lb, 0x7632u);
+        X[t].p2 = __byte_perm(ha, hb, 0x5410u);
+        X[t].p3 = __byte_perm(ha, hb, 0x7632u);
+        S0 += (half_lo(la) + half_hi(la)) + (half_lo(lb) + half_hi(lb));
+        S1 += (half_lo(ha) + half_hi(ha)) + (half_lo(hb) + half_hi(hb));
+      }
+    }
+    if (kFmt == kFmtW4A16 && wact) {
       const uint16_t* xp = tk.x + u * 64;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -609,7 +695,32 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         pending = false;
       }
       float res[kRR];
-      if (wact) {
+      if (kFmt == kFmtQ4K && wact) {
+        // rows rl + r RL: the unit's block header and 32 code bytes
+        const uint32_t ua = base + rl * tp.row_bytes + (u >> 2) * 144;
+        const int cc = u & 3;
+        const uint32_t selp = (cc & 1) ? 0x7632u : 0x5410u, selq = (cc & 1) ? 0x3232u : 0x1010u;
+        const bool hi = cc >= 2;
+        uint4 h[2], qa, qb;
+        uint32_t q[8];
+        float D0, D1;
+#pragma unroll
+        for (int r = 0; r < kRR; ++r) {
+          const uint32_t ra = ua + r * w_row_step;
+          h[r & 1] = lds_u4(ra);
+          qa = lds_u4(ra + 16 + 32 * cc);
+          qb = lds_u4(ra + 32 + 32 * cc);
+          if (r == kRR - 1) {
+            // the last reads of the stage are issued: release it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+          }
+          q[0] = qa.x; q[1] = qa.y; q[2] = qa.z; q[3] = qa.w;
+          q[4] = qb.x; q[5] = qb.y; q[6] = qb.z; q[7] = qb.w;
+          q4k_dot(q, X, D0, D1);
+          res[r] = q4k_combine(h[r & 1], selp, selq, hi, D0, D1, S0, S1);
+        }
+      } else if (kFmt != kFmtQ4K && wact) {
         const uint32_t sa = base + sc_off + sc_lo;
         float sc[kRR];
 #pragma unroll
@@ -619,7 +730,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         float d0, d1;
         load_row(wa, rot, w0);
         load_row(wa + w_row_step, rot, w1);
-        if (kA8) {
+        if (kFmt == kFmtW4A8) {
           int i0, i1;
           dot_pair_a8(w0, w1, xe, xo, i0, i1);
           res[0] = static_cast<float>(i0 - C8) * (sc[0] * s_act);
@@ -634,7 +745,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         // the last reads of the stage are issued: release it (release order)
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
-        if (kA8) {
+        if (kFmt == kFmtW4A8) {
           int i0, i1;
           dot_pair_a8(w0, w1, xe, xo, i0, i1);
           res[2] = static_cast<float>(i0 - C8) * (sc[2] * s_act);
@@ -675,7 +786,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
 }
 
 template <int MAXT>
-cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, bool pdl, bool act, bool a8,
+cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, bool pdl, bool act, int fmt,
                          cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -688,12 +799,22 @@ cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, 
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
-  if (a8)
-    e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, true>, p)
-            : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, true>, p);
+  if constexpr (MAXT == 1) {
+    // Q4_K runs as a single task without an activation epilogue
+    if (fmt == kFmtQ4K) {
+      if (act) return cudaErrorInvalidValue;
+      e = cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, kFmtQ4K>, p);
+      if (e != cudaSuccess) return e;
+      return cudaGetLastError();
+    }
+  }
+  if (fmt == kFmtQ4K) return cudaErrorInvalidValue;
+  if (fmt == kFmtW4A8)
+    e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, kFmtW4A8>, p)
+            : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, kFmtW4A8>, p);
   else
-    e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, false>, p)
-            : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, false>, p);
+    e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, kFmtW4A16>, p)
+            : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, kFmtW4A16>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -731,7 +852,42 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   p.stage_bytes = rp.stage_bytes;
   p.red_bytes = rp.red_bytes;
   p.CW = rp.CW;
-  return launch_tasks(p, rp, grid, a.pdl, false, a.a8, st);
+  return launch_tasks(p, rp, grid, a.pdl, false, a.a8 ? kFmtW4A8 : kFmtW4A16, st);
+}
+
+bool gemv_m1_q4k_supported(int K) {
+  return K > 0 && K % 256 == 0 && K / 64 <= kM1MaxConsumers;
+}
+
+cudaError_t launch_gemv_m1_q4k(const uint8_t* blocks, const uint16_t* x, uint16_t* y, int N, int K, bool pdl,
+                               uint32_t* status, const DeviceInfo& d, cudaStream_t st) {
+  if (!gemv_m1_q4k_supported(K) || N <= 0) return cudaErrorInvalidValue;
+  M1Params<1> p{};
+  p.ntasks = 1;
+  p.done = nullptr;
+  p.status = status;
+  M1Task& tk = p.task[0];
+  tk.qweight = reinterpret_cast<const uint32_t*>(blocks);
+  tk.scales = nullptr;
+  tk.x = x;
+  tk.N = N;
+  tk.K = K;
+  tk.x2 = nullptr;
+  tk.nseg = 1;
+  tk.dep = -1;
+  tk.publish = 0;
+  tk.seg[0] = M1Seg{y, nullptr, N};
+  for (int s = 1; s < kMaxSegs; ++s) tk.seg[s] = M1Seg{nullptr, nullptr, N};
+  const int grid = N < d.sms ? N : d.sms;
+  tk.rq = N / grid;
+  tk.rr = N % grid;
+  const RingPlan rp = make_ring_plan(&K, 1, d.max_smem_optin, kFmtQ4K);
+  if (rp.S < 2) return cudaErrorInvalidConfiguration;
+  p.S = rp.S;
+  p.stage_bytes = rp.stage_bytes;
+  p.red_bytes = rp.red_bytes;
+  p.CW = rp.CW;
+  return launch_tasks(p, rp, grid, pdl, false, kFmtQ4K, st);
 }
 
 cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uint32_t* status,
@@ -763,20 +919,21 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
   p.red_bytes = rp.red_bytes;
   p.CW = rp.CW;
   // one CTA per SM: every CTA must be resident for the dependency counts
-  return launch_tasks(p, rp, d.sms, pdl, act, a8, st);
+  return launch_tasks(p, rp, d.sms, pdl, act, a8 ? kFmtW4A8 : kFmtW4A16, st);
 }
 
 cudaError_t prepare_gemv_m1(const DeviceInfo& d) {
   const int limit = d.max_smem_optin < kM1SmemBudget + 1024 ? d.max_smem_optin : kM1SmemBudget + 1024;
   const void* fns[] = {
-      reinterpret_cast<const void*>(gemv_m1_kernel<1, false, false>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<1, true, false>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<1, false, true>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<1, true, true>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, false, false>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, true, false>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, false, true>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, true, true>)};
+      reinterpret_cast<const void*>(gemv_m1_kernel<1, false, kFmtW4A16>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<1, true, kFmtW4A16>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<1, false, kFmtW4A8>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<1, true, kFmtW4A8>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<1, false, kFmtQ4K>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, false, kFmtW4A16>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, true, kFmtW4A16>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, false, kFmtW4A8>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, true, kFmtW4A8>)};
   for (const void* f : fns) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
     if (e != cudaSuccess) return e;

@@ -118,6 +118,11 @@ struct DeviceInfo {
 // M = 1, K within the pipelined kernel's limit (see gemv_m1_supported).
 bool gemv_m1_supported(int K);
 cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
+// The same kernel on GGUF Q4_K blocks (K a multiple of 256, blocks 16-byte
+// aligned, one CTA per SM).
+bool gemv_m1_q4k_supported(int K);
+cudaError_t launch_gemv_m1_q4k(const uint8_t* blocks, const uint16_t* x, uint16_t* y, int N, int K, bool pdl,
+                               uint32_t* status, const DeviceInfo& d, cudaStream_t st);
 // A task list (1 <= ntasks <= kM1MaxTasks, every K supported, M = 1) in one
 // launch of one CTA per SM.  done: ntasks ints, zero before the launch
 // (per-task completion counters); required when a task has a dependency,

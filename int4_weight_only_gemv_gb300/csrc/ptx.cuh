@@ -312,6 +312,25 @@ __device__ __forceinline__ XPairs pair_activations(uint4 v) {
   return x;
 }
 
+// GGUF Q4_K: sub-block j's 6-bit scale and minimum from a block's 12 packed
+// bytes b (3 words, bytes 4-15 of the block): j < 4 in the low 6 bits of
+// bytes j and j + 4; j >= 4 in the nibbles of byte j + 4 (scale low, minimum
+// high) with their top two bits in bytes j - 4 (scale) and j (minimum).
+__device__ __forceinline__ void q4k_scale_min(const uint32_t (&b)[3], int j, int& sc, int& m) {
+  // word by selects, not by index: j may vary between threads
+  auto byte = [&](int i) {
+    const uint32_t w = i < 4 ? b[0] : (i < 8 ? b[1] : b[2]);
+    return static_cast<int>((w >> (8 * (i & 3))) & 0xFFu);
+  };
+  if (j < 4) {
+    sc = byte(j) & 63;
+    m = byte(j + 4) & 63;
+  } else {
+    sc = (byte(j + 4) & 15) | ((byte(j - 4) >> 6) << 4);
+    m = (byte(j + 4) >> 4) | ((byte(j) >> 6) << 4);
+  }
+}
+
 __device__ __forceinline__ float half_lo(uint32_t v) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
 }

@@ -35,18 +35,6 @@ constexpr int kQkBytes = 144;   // bytes per block
 constexpr int kQkWarps = 8;     // rows per CTA
 constexpr int kQkThreads = 32 * kQkWarps;
 
-// Sub-block j's 6-bit scale and minimum from the 12 packed bytes (3 words).
-__device__ __forceinline__ void scale_min(const uint32_t (&b)[3], int j, int& sc, int& m) {
-  auto byte = [&](int i) { return static_cast<int>((b[i >> 2] >> (8 * (i & 3))) & 0xFFu); };
-  if (j < 4) {
-    sc = byte(j) & 63;
-    m = byte(j + 4) & 63;
-  } else {
-    sc = (byte(j + 4) & 15) | ((byte(j - 4) >> 6) << 4);
-    m = (byte(j + 4) >> 4) | ((byte(j) >> 6) << 4);
-  }
-}
-
 // Two halves a (low) and b (high) of a word pair.
 __device__ __forceinline__ uint32_t pair_halves(uint32_t lo_word, uint32_t hi_word, uint32_t sel) {
   return __byte_perm(lo_word, hi_word, sel);
@@ -67,8 +55,8 @@ __global__ void q4k_dequant_kernel(const uint8_t* __restrict__ blocks, float* __
   const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu)));
   const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16)));
   int sc0, m0, sc1, m1;
-  scale_min(sb, 2 * c, sc0, m0);
-  scale_min(sb, 2 * c + 1, sc1, m1);
+  q4k_scale_min(sb, 2 * c, sc0, m0);
+  q4k_scale_min(sb, 2 * c + 1, sc1, m1);
   const float d0 = __fmul_rn(d, static_cast<float>(sc0)), n0 = __fmul_rn(dmin, static_cast<float>(m0));
   const float d1 = __fmul_rn(d, static_cast<float>(sc1)), n1 = __fmul_rn(dmin, static_cast<float>(m1));
   const uint32_t q = __ldg(reinterpret_cast<const uint32_t*>(p + 16 + 32 * c + i));
@@ -115,8 +103,8 @@ __device__ __forceinline__ float q4k_unit(const uint4 h, const uint32_t (&q)[8],
   const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu)));
   const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16)));
   int sc0, m0, sc1, m1;
-  scale_min(sb, 2 * c, sc0, m0);
-  scale_min(sb, 2 * c + 1, sc1, m1);
+  q4k_scale_min(sb, 2 * c, sc0, m0);
+  q4k_scale_min(sb, 2 * c + 1, sc1, m1);
   float r = d * static_cast<float>(sc0) * fmaf(-1024.f, s0, dlo0 + dlo1);
   r = fmaf(d * static_cast<float>(sc1), fmaf(-1024.f, s1, dhi0 + dhi1), r);
   return fmaf(-dmin, fmaf(static_cast<float>(m0), s0, static_cast<float>(m1) * s1), r);
