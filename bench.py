@@ -50,7 +50,8 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--case", default=None,
                     help="profiling mode: run one workload GEMV (tiny, q_proj, kv_proj, gate_up, "
-                         "down_m1 .. down_m16), or seqN (an N-layer M=1 layer sequence), "
+                         "down_m1 .. down_m16), seqN (an N-layer M=1 layer sequence), attn "
+                         "(decode attention, T = 8192) or q4k ([gate; up] as GGUF Q4_K blocks), "
                          "--launches times and exit")
     ap.add_argument("--launches", type=int, default=4)
     return ap.parse_args()
@@ -99,12 +100,19 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The sources the step's kernel (the M = 1 task-list launch) is built and
+# launched from: its kernel, the shared device helpers and declarations, the
+# host code that builds the task table, and the public header.
+STEP_KERNEL_SOURCES = ("int4_weight_only_gemv_gb300/csrc/gemv_m1.cu", "int4_weight_only_gemv_gb300/csrc/ptx.cuh",
+                       "int4_weight_only_gemv_gb300/csrc/kernels.h", "int4_weight_only_gemv_gb300/csrc/api.cu",
+                       "include/w4a16.h")
+
+
 def kernel_source_hash():
-    csrc = os.path.join(ROOT, "int4_weight_only_gemv_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    for rel in STEP_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(rel.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -661,6 +669,30 @@ def run_case(args):
             raise RuntimeError("a kernel flagged a failure")
         print(json.dumps({"case": "attn", "H": H, "Hkv": Hkv, "T": T, "launches": args.launches,
                           "us_per_call_warm_l2": 1e3 * s.elapsed_time(e) / args.launches}))
+        return
+    if args.case == "q4k":
+        # the [gate; up] shape as GGUF Q4_K blocks (random bytes, d and dmin
+        # in [1e-3, 0.051]), M = 1, launched `launches` times
+        dev = torch.device("cuda", 0)
+        N, K = 2 * synth.FFN, synth.HIDDEN
+        nb = N * (K // 256)
+        gen = torch.Generator(device=dev).manual_seed(4)
+        b = torch.randint(0, 256, (nb, 144), generator=gen, dtype=torch.uint8, device=dev)
+        d = (torch.rand((nb, 2), generator=gen, device=dev) * 0.05 + 1e-3).half()
+        b[:, 0:4] = d.view(torch.uint8).view(nb, 4)
+        x = synth.activations(1, K, 90, dev).view(-1)
+        y = torch.empty((N,), dtype=torch.float16, device=dev)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(args.launches):
+            w4.w4a16_q4k_gemv(b.view(-1), x, N, K, y=y)
+        e.record()
+        torch.cuda.synchronize()
+        if w4.w4a16_device_status(clear=True):
+            raise RuntimeError("a kernel flagged a failure")
+        print(json.dumps({"case": "q4k", "N": N, "K": K, "launches": args.launches, "bytes": nb * 144 + 2 * K + 2 * N,
+                          "us_per_gemv_warm_l2": 1e3 * s.elapsed_time(e) / args.launches}))
         return
     cfg = {c.name: c for c in synth.ALL_GEMVS}[args.case]
     dev = torch.device("cuda", 0)
