@@ -467,7 +467,8 @@ def attn_decode_line(dev, reps, T=8192):
     """Decode attention of one token over an fp16 KV cache of T keys with the
     Qwen-7B head layout (28 query heads over 4 KV heads, head dimension 128):
     a CUDA graph of 28 calls over 28 distinct caches (cold L2: 28 x 16.8 MB),
-    us per call and GB/s over the cache bytes plus q and o."""
+    one workspace for all of them, us per call and GB/s over the cache bytes
+    plus q and o."""
     import torch
 
     import int4_weight_only_gemv_gb300 as w4
@@ -478,7 +479,7 @@ def attn_decode_line(dev, reps, T=8192):
                torch.randn((Hkv, T, D), generator=g, device=dev).half()) for _ in range(synth.N_LAYERS)]
     qs = [torch.randn((H, D), generator=g, device=dev).half() for _ in caches]
     os_ = [torch.empty((H, D), dtype=torch.float16, device=dev) for _ in caches]
-    ws = torch.empty(w4.attn_decode_workspace(H, Hkv, T) // 4 + 4, dtype=torch.float32, device=dev)
+    ws = w4.attn_decode_new_workspace(H, Hkv, T, dev)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for (k, v), q, o in zip(caches, qs, os_):
@@ -657,7 +658,7 @@ def run_case(args):
         v = torch.randn((Hkv, T, D), generator=gen, device=dev).half()
         q = torch.randn((H, D), generator=gen, device=dev).half()
         o = torch.empty((H, D), dtype=torch.float16, device=dev)
-        ws = torch.empty(w4.attn_decode_workspace(H, Hkv, T) // 4 + 4, dtype=torch.float32, device=dev)
+        ws = w4.attn_decode_new_workspace(H, Hkv, T, dev)
         torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()

@@ -54,6 +54,9 @@ extern "C" {
 #define W4A16_MAX_M 16
 #define W4A16_MAX_K 32768
 #define W4A16_MAX_N (1 << 24)
+/* Decode attention: most KV heads per call (the workspace's counter block
+ * holds one counter per possible KV head). */
+#define W4A16_ATTN_MAX_KV_HEADS 256
 
 typedef enum {
   W4A16_OK = 0,
@@ -348,14 +351,20 @@ w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* layers, int n
  *              the workspace
  *   workspace  device scratch of at least the size that
  *              w4a16_attn_decode_workspace returns for the same shape, owned
- *              by the caller; must not overlap q or the caches.  Two calls
- *              that overlap on the GPU must not share it.
+ *              by the caller; must not overlap q or the caches.  It must be
+ *              zero-filled before its first use: its first
+ *              4 * W4A16_ATTN_MAX_KV_HEADS bytes count the finished key
+ *              ranges of each KV head, and every call leaves them zero
+ *              again, so it can be reused for any shape it is large enough
+ *              for.  After a call that set W4A16_DEV_PIPE_TIMEOUT, zero it
+ *              again.  Two calls that overlap on the GPU must not share it.
  * Limits: head_dim == 128, n_heads a multiple of n_kv_heads with at most 16
- * query heads per KV head, 1 <= T <= t_stride <= 2^24 (W4A16_ERR_SHAPE
+ * query heads per KV head, n_kv_heads <= W4A16_ATTN_MAX_KV_HEADS, 1 <= T <= t_stride <= 2^24 (W4A16_ERR_SHAPE
  * otherwise, also for a workspace smaller than required); every pointer
- * 16-byte aligned (W4A16_ERR_ALIGN).  Two kernel launches on `stream`, each
- * a programmatic dependent of the kernel before it (the first reads q and
- * the caches only after the previous kernel has completed); never
+ * 16-byte aligned (W4A16_ERR_ALIGN).  One kernel launch on `stream`, a
+ * programmatic dependent of the kernel before it (it reads q and the caches
+ * only after the previous kernel has completed): the key ranges of each KV
+ * head are merged, in a fixed order, by the CTA that finishes last.  Never
  * allocates, never synchronises, deterministic.
  */
 w4a16_status w4a16_attn_decode_workspace(int n_heads, int n_kv_heads, int head_dim, int T,

@@ -20,7 +20,7 @@ __all__ = [
     "w4a16_selftest_wait_timeout", "w4a16_layer_seq_run_static", "STATIC_MAX_GEMVS",
     "LayerSeq", "GROUP", "MAX_M", "MAX_K", "DEV_NONFINITE", "DEV_SCALE_OVERFLOW",
     "DEV_PIPE_TIMEOUT", "STATUS", "EXPORTED_SYMBOLS", "w4a16_attn_decode", "attn_decode_workspace",
-    "w4a16_gemv_a8", "SEQ_ACT_INT8", "w4a16_q4k_gemv", "w4a16_q4k_dequant",
+    "attn_decode_new_workspace", "w4a16_gemv_a8", "SEQ_ACT_INT8", "w4a16_q4k_gemv", "w4a16_q4k_dequant",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -197,11 +197,21 @@ def attn_decode_workspace(n_heads, n_kv_heads, T, head_dim=128) -> int:
     return n.value
 
 
+def attn_decode_new_workspace(n_heads, n_kv_heads, T, device, head_dim=128):
+    """A zero-filled workspace for w4a16_attn_decode of this shape (or any
+    shape needing no more bytes); calls leave it zero-filled where it must
+    be, so it can be reused."""
+    import torch
+    return torch.zeros(attn_decode_workspace(n_heads, n_kv_heads, T, head_dim) // 4, dtype=torch.float32,
+                       device=device)
+
+
 def w4a16_attn_decode(q, k_cache, v_cache, T=None, o=None, workspace=None, stream=None):
     """Decode attention of one token: q float16 [H][128], caches float16
     [Hkv][t_stride][128] (keys t < T, default all), o float16 [H][128]
     (allocated if not given); workspace a CUDA tensor of at least
-    attn_decode_workspace(...) bytes (allocated if not given)."""
+    attn_decode_workspace(...) bytes, zero-filled before its first use
+    (attn_decode_new_workspace; allocated if not given)."""
     import torch
     H, D = q.shape
     Hkv, t_stride, _ = k_cache.shape
@@ -209,8 +219,7 @@ def w4a16_attn_decode(q, k_cache, v_cache, T=None, o=None, workspace=None, strea
     if o is None:
         o = torch.empty((H, D), dtype=torch.float16, device=q.device)
     if workspace is None:
-        workspace = torch.empty(attn_decode_workspace(H, Hkv, T, D) // 4 + 4, dtype=torch.float32,
-                                device=q.device)
+        workspace = attn_decode_new_workspace(H, Hkv, T, q.device, D)
     nbytes = workspace.numel() * workspace.element_size()
     _check(lib().w4a16_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), H, Hkv, D, T, t_stride,
                                    _ptr(workspace), nbytes, _stream(stream)), "w4a16_attn_decode")

@@ -185,8 +185,8 @@ namespace {
 constexpr int kAttnMaxT = 1 << 24;
 
 w4a16_status check_attn_shape(int n_heads, int n_kv_heads, int head_dim, int T) {
-  if (head_dim != 128 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 ||
-      n_heads / n_kv_heads > 16 || T < 1 || T > kAttnMaxT)
+  if (head_dim != 128 || n_heads <= 0 || n_kv_heads <= 0 || n_kv_heads > W4A16_ATTN_MAX_KV_HEADS ||
+      n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > 16 || T < 1 || T > kAttnMaxT)
     return W4A16_ERR_SHAPE;
   return W4A16_OK;
 }

@@ -14,7 +14,7 @@
 // an m16n8k16 MMA (f16 x f16 -> f32), so every K/V byte read feeds all of
 // them from the tensor cores.
 //
-// Two launches (flash-decoding split over keys):
+// One launch (flash-decoding split over keys):
 //   attn_partial_kernel   one CTA per (KV head, key range).  Warp 4 streams
 //       tiles of 64 keys through an S-stage ring: per tile four 3-D TMA loads
 //       (K and V, dimensions 0..63 and 64..127; 128-byte swizzle; keys at or
@@ -24,8 +24,10 @@
 //       (running max and sum per query head), P rounded to fp16 and
 //       O += P V (ldmatrix.trans).  At the end the eight warps' (max, sum, O)
 //       are merged through shared memory and written to the workspace.
-//   attn_combine_kernel   one CTA per query head: merges the key ranges in
-//       their order (max, rescale, sum) and writes o in fp16.
+//       The CTA then counts itself in on its KV head's counter (after a
+//       fence); the one that completes the count merges the head's key ranges
+//       in their order (max, rescale, sum), writes o in fp16 and sets the
+//       counter back to zero.  No CTA waits for another.
 // Every wait is bounded; a timed-out wait sets W4A16_DEV_PIPE_TIMEOUT.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -47,13 +49,15 @@ constexpr int kABox = kAKeys * 128;         // one box: 64 keys x 64 dimensions 
 constexpr int kATileBytes = 4 * kABox;      // K (two halves of the dimensions), then V
 constexpr int kAStages = 4;
 constexpr int kARows = 16;                  // query heads per KV head, padded (MMA M)
-constexpr int kAHeader = 1024;              // barriers
+constexpr int kAHeader = 1024;              // barriers, then the merge flag
 // per-warp merge area: max[16], sum[16], O[16][128] floats
 constexpr int kAMergeBytes = kAWarps * (2 * kARows + kARows * kAD) * 4;
 constexpr int kASmem = kAHeader + kAStages * kATileBytes + kAMergeBytes + 1024;
 
 struct AttnParams {
   const uint16_t* q;  // [n_heads][128]
+  uint16_t* o;        // [n_heads][128]
+  unsigned* ctr;      // [n_kv_heads]: key ranges finished (zero between calls)
   float* ws_ml;       // [n_kv_heads][splits][16][2]: running max and sum
   float* ws_o;        // [n_kv_heads][splits][16][128]: unnormalised output
   int group;          // query heads per KV head (<= 16)
@@ -98,6 +102,85 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // of row r at chunk c ^ (r % 8)).
 __device__ __forceinline__ uint32_t box_addr(uint32_t box, int row, int d0) {
   return box + row * 128 + ((((d0 >> 3) & 7) ^ (row & 7)) << 4);
+}
+
+constexpr int kAMaxSplits = 256;  // key ranges per KV head (at most the SM count)
+static_assert(kAWarps * kAMaxSplits * 4 <= kAMergeBytes, "merge scratch exceeds the merge area");
+static_assert(kAMaxSplits % 32 == 0, "ranges are spread over the lanes of a warp");
+
+// Merge the key ranges of KV head g (run by the CTA that finished last):
+//   o_h = fp16_RN(sum_sp O_sp e_sp / sum_sp l_sp e_sp),  e_sp = 2^((m_sp - M) log2 e),
+// M = max_sp m_sp, for the group's query heads h = g group + r, every sum
+// in range order (the result does not depend on which CTA merges).  Warp w
+// merges heads r = w, w + 8 alone: lane l holds the statistics of ranges
+// l, l + 32, ... and sums dimensions 4 l .. 4 l + 3 over the ranges, with
+// the first kB ranges' loads issued together with the statistics (two
+// rounds of L2 loads for 38 ranges).  sh: kAWarps x kAMaxSplits floats.
+// The workspace is read past L1 (written by other CTAs of this launch).
+__device__ __forceinline__ void merge_ranges(const AttnParams& p, int g, float* sh, int t) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr int kB = 20;                      // ranges per round of loads
+  constexpr int kPer = kAMaxSplits / 32;      // statistics per lane
+  constexpr int kRangeF4 = kARows * kAD / 4;  // float4s per range
+  const int lane = t & 31, warp = t >> 5;
+  float* er = sh + warp * kAMaxSplits;
+  const float* ml = p.ws_ml + static_cast<int64_t>(g) * p.splits * kARows * 2;
+  const float* wo = p.ws_o + static_cast<int64_t>(g) * p.splits * kARows * kAD;
+  const int splits = p.splits;
+  for (int r = warp; r < p.group; r += kAWarps) {
+    const float4* src = reinterpret_cast<const float4*>(wo + r * kAD) + lane;
+    float4 v[kB];
+#pragma unroll
+    for (int i = 0; i < kB; ++i)
+      v[i] = i < splits ? __ldcg(src + static_cast<int64_t>(i) * kRangeF4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mv[kPer], lv[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int sp = lane + 32 * j;
+      mv[j] = sp < splits ? __ldcg(ml + (sp * kARows + r) * 2) : -INFINITY;
+      lv[j] = sp < splits ? __ldcg(ml + (sp * kARows + r) * 2 + 1) : 0.f;
+    }
+    float mloc = mv[0];
+#pragma unroll
+    for (int j = 1; j < kPer; ++j) mloc = fmaxf(mloc, mv[j]);
+    for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+    const float Mu = mloc == -INFINITY ? 0.f : mloc;
+    float lloc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int sp = lane + 32 * j;
+      if (sp < splits) {
+        const float e = exp2f((mv[j] - Mu) * kLog2e);
+        er[sp] = e;
+        lloc += lv[j] * e;
+      }
+    }
+    for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
+    __syncwarp();
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0;;) {
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        if (s0 + i < splits) {
+          const float e = er[s0 + i];
+          acc.x += v[i].x * e;
+          acc.y += v[i].y * e;
+          acc.z += v[i].z * e;
+          acc.w += v[i].w * e;
+        }
+      }
+      s0 += kB;
+      if (s0 >= splits) break;
+#pragma unroll
+      for (int i = 0; i < kB; ++i)
+        v[i] = s0 + i < splits ? __ldcg(src + static_cast<int64_t>(s0 + i) * kRangeF4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const uint32_t lo = pack_half2(acc.x / lloc, acc.y / lloc), hi = pack_half2(acc.z / lloc, acc.w / lloc);
+    uint2* dst = reinterpret_cast<uint2*>(p.o + (static_cast<int64_t>(g) * p.group + r) * kAD) + lane;
+    *dst = make_uint2(lo, hi);
+    __syncwarp();  // er is rewritten for the warp's next head
+  }
 }
 
 __global__ void __launch_bounds__(kAThreads, 1)
@@ -307,105 +390,49 @@ __global__ void __launch_bounds__(kAThreads, 1)
   }
   asm volatile("bar.sync 1, %0;" ::"r"(32 * kAWarps) : "memory");
   // thread d < 128 of the consumers merges dimension d of every query head
-  if (threadIdx.x >= kAD) return;
-  const int d = threadIdx.x;
+  // and writes the key range's statistics and output to the workspace
   const int64_t slot = static_cast<int64_t>(g) * p.splits + sp;
-  for (int r = 0; r < p.group; ++r) {
-    float M = -INFINITY;
+  if (threadIdx.x < kAD) {
+    const int d = threadIdx.x;
+    for (int r = 0; r < p.group; ++r) {
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, mg[w * (2 * kARows + kARows * kAD) + r]);
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float L = 0.f, acc = 0.f;
+      for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, mg[w * (2 * kARows + kARows * kAD) + r]);
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float L = 0.f, acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kAWarps; ++w) {
-      const float* b = mg + w * (2 * kARows + kARows * kAD);
-      const float e = exp2f((b[r] - Mu) * kLog2e);
-      L += b[kARows + r] * e;
-      acc += b[2 * kARows + r * kAD + d] * e;
-    }
-    p.ws_o[(slot * kARows + r) * kAD + d] = acc;
-    if (d == 0) {
-      p.ws_ml[(slot * kARows + r) * 2] = M;
-      p.ws_ml[(slot * kARows + r) * 2 + 1] = L;
-    }
-  }
-}
-
-constexpr int kAMaxSplits = 256;  // key ranges per KV head (at most the SM count)
-
-constexpr int kAMergeParts = 4;  // threads per output dimension in the merge
-constexpr int kAMergeThreads = kAD * kAMergeParts;
-
-// One CTA per query head: merge the key ranges,
-//   o = fp16_RN(sum_sp O_sp e_sp / sum_sp l_sp e_sp),  e_sp = 2^((m_sp - M) log2 e),
-// M = max_sp m_sp.  The ranges' statistics are loaded one per thread and
-// reduced through shared memory; thread (part, d) sums the ranges
-// sp = part (mod 4) of dimension d with all its loads in flight, and the four
-// parts are added in order.  The result does not depend on timing.
-__global__ void __launch_bounds__(kAMergeThreads) attn_combine_kernel(const float* __restrict__ ws_ml,
-                                                                      const float* __restrict__ ws_o,
-                                                                      uint16_t* o, int group, int splits) {
-  __shared__ float e_sh[kAMaxSplits];
-  __shared__ float red[kAMergeThreads / 32];
-  __shared__ float part_sh[kAMergeParts][kAD];
-  // the next kernel may be scheduled now: it reads and writes nothing of
-  // this one's before its own wait for this grid to complete
-  pdl_launch_dependents();
-  pdl_wait();
-  const int h = blockIdx.x;
-  const int g = h / group, r = h % group;
-  const int t = threadIdx.x;
-  const int lane = t & 31, warp = t >> 5;
-  constexpr int kW = kAMergeThreads / 32;
-  constexpr float kLog2e = 1.4426950408889634f;
-  const int64_t slot0 = static_cast<int64_t>(g) * splits;
-  float mloc = -INFINITY;
-  for (int sp = t; sp < splits; sp += kAMergeThreads) {
-    const float m = ws_ml[((slot0 + sp) * kARows + r) * 2];
-    e_sh[sp] = m;
-    mloc = fmaxf(mloc, m);
-  }
-  for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-  if (lane == 0) red[warp] = mloc;
-  __syncthreads();
-  float M = red[0];
-  for (int w = 1; w < kW; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-  float lloc = 0.f;
-  for (int sp = t; sp < splits; sp += kAMergeThreads) {
-    const float e = exp2f((e_sh[sp] - M) * kLog2e);
-    e_sh[sp] = e;
-    lloc += ws_ml[((slot0 + sp) * kARows + r) * 2 + 1] * e;
-  }
-  for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
-  if (lane == 0) red[warp] = lloc;
-  __syncthreads();
-  float L = 0.f;
-  for (int w = 0; w < kW; ++w) L += red[w];
-  const int d = t % kAD, part = t / kAD;
-  float acc = 0.f;
-  constexpr int kBatch = 16;  // loads in flight per thread
-  for (int s0 = part; s0 < splits; s0 += kBatch * kAMergeParts) {
-    float v[kBatch];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int sp = s0 + i * kAMergeParts;
-      v[i] = sp < splits ? ws_o[((slot0 + sp) * kARows + r) * kAD + d] : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int sp = s0 + i * kAMergeParts;
-      if (sp < splits) acc += v[i] * e_sh[sp];
+      for (int w = 0; w < kAWarps; ++w) {
+        const float* b = mg + w * (2 * kARows + kARows * kAD);
+        const float e = exp2f((b[r] - Mu) * kLog2e);
+        L += b[kARows + r] * e;
+        acc += b[2 * kARows + r * kAD + d] * e;
+      }
+      p.ws_o[(slot * kARows + r) * kAD + d] = acc;
+      if (d == 0) {
+        p.ws_ml[(slot * kARows + r) * 2] = M;
+        p.ws_ml[(slot * kARows + r) * 2 + 1] = L;
+      }
     }
   }
-  part_sh[part][d] = acc;
-  __syncthreads();
-  if (part == 0) {
-    float sum = part_sh[0][d];
-#pragma unroll
-    for (int q = 1; q < kAMergeParts; ++q) sum += part_sh[q][d];
-    o[static_cast<int64_t>(h) * kAD + d] = __half_as_ushort(__float2half_rn(sum / L));
+  // Count the range in: after the CTA barrier one thread adds to the counter
+  // with release and acquire semantics at GPU scope (cumulative over the
+  // CTA's stores ordered before it by the barrier); the CTA that completes
+  // the count (exactly one per KV head) has then acquired every range's
+  // stores, and its barrier orders its threads' loads after that.
+  // The flag sits in the header, past the pipeline barriers.
+  volatile unsigned* s_last = reinterpret_cast<volatile unsigned*>(smem + 16 * kAStages);
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * kAWarps) : "memory");
+  if (threadIdx.x == 0) {
+    unsigned done;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(done) : "l"(p.ctr + g) : "memory");
+    const bool last = done == static_cast<unsigned>(p.splits - 1);
+    *s_last = last ? 1u : 0u;
+    // every range of this call has counted: ready for the next call
+    if (last) atomicExch(p.ctr + g, 0u);
   }
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * kAWarps) : "memory");
+  if (*s_last == 0) return;
+  merge_ranges(p, g, mg, threadIdx.x);
 }
 
 // K or V cache as a 3-D tensor: [n_kv_heads][T][128] fp16 with head stride
@@ -435,8 +462,12 @@ int attn_splits(int n_kv_heads, int T, const DeviceInfo& d) {
   return ntiles < per_head ? ntiles : per_head;
 }
 
+// [counters: one per possible KV head, at a fixed place for every shape][ws_ml][ws_o]
+constexpr size_t kACtrBytes = W4A16_ATTN_MAX_KV_HEADS * sizeof(unsigned);
+static_assert(kACtrBytes % 16 == 0, "the statistics must stay 16-byte aligned");
+
 size_t attn_workspace_bytes(int n_kv_heads, int splits) {
-  return static_cast<size_t>(n_kv_heads) * splits * kARows * (2 + kAD) * sizeof(float);
+  return kACtrBytes + static_cast<size_t>(n_kv_heads) * splits * kARows * (2 + kAD) * sizeof(float);
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, const DeviceInfo& d, cudaStream_t st) {
@@ -447,8 +478,11 @@ cudaError_t launch_attn_decode(const AttnArgs& a, const DeviceInfo& d, cudaStrea
     return cudaErrorInvalidValue;
   AttnParams p;
   p.q = a.q;
-  p.ws_ml = a.workspace;
-  p.ws_o = a.workspace + static_cast<size_t>(a.n_kv_heads) * splits * kARows * 2;
+  p.o = a.o;
+  p.ctr = reinterpret_cast<unsigned*>(a.workspace);
+  if (a.n_kv_heads > W4A16_ATTN_MAX_KV_HEADS) return cudaErrorInvalidValue;
+  p.ws_ml = a.workspace + kACtrBytes / sizeof(float);
+  p.ws_o = p.ws_ml + static_cast<size_t>(a.n_kv_heads) * splits * kARows * 2;
   p.group = a.n_heads / a.n_kv_heads;
   p.T = a.T;
   p.splits = splits;
@@ -465,20 +499,6 @@ cudaError_t launch_attn_decode(const AttnArgs& a, const DeviceInfo& d, cudaStrea
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_partial_kernel, kmap, vmap, p);
-  if (e != cudaSuccess) return e;
-  // the merge is a programmatic dependent of the partial kernel: it launches
-  // early and waits for it before reading the workspace
-  cudaLaunchConfig_t c2 = {};
-  c2.gridDim = dim3(a.n_heads);
-  c2.blockDim = dim3(kAMergeThreads);
-  c2.stream = st;
-  cudaLaunchAttribute a2[1];
-  a2[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  a2[0].val.programmaticStreamSerializationAllowed = 1;
-  c2.attrs = a2;
-  c2.numAttrs = 1;
-  e = cudaLaunchKernelEx(&c2, attn_combine_kernel, static_cast<const float*>(p.ws_ml),
-                         static_cast<const float*>(p.ws_o), a.o, p.group, splits);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

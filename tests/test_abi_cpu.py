@@ -199,6 +199,7 @@ def test_attn_decode_argument_checks(L):
     assert f(Q, K, V, O, 28, 4, 64, 100, 100, W, 1 << 20, None) == 2     # head_dim != 128
     assert f(Q, K, V, O, 28, 5, 128, 100, 100, W, 1 << 20, None) == 2    # heads not a multiple
     assert f(Q, K, V, O, 34, 2, 128, 100, 100, W, 1 << 20, None) == 2    # 17 heads per KV head
+    assert f(Q, K, V, O, 257, 257, 128, 100, 100, W, 1 << 20, None) == 2  # KV heads past the counter block
     assert f(Q, K, V, O, 28, 4, 128, 0, 100, W, 1 << 20, None) == 2      # T = 0
     assert f(Q, K, V, O, 28, 4, 128, 100, 99, W, 1 << 20, None) == 2     # t_stride < T
     assert f(0, K, V, O, 28, 4, 128, 100, 100, W, 1 << 20, None) == 1    # null q

@@ -101,7 +101,7 @@ def test_attn_rejects_bad_workspace_and_alias():
     need = w4.attn_decode_workspace(28, 4, 500)
     assert need > 0
     o = torch.empty((28, 128), dtype=torch.float16, device=DEV)
-    ws = torch.empty(need // 4, dtype=torch.float32, device=DEV)
+    ws = w4.attn_decode_new_workspace(28, 4, 500, DEV)
     rc = w4.w4a16_attn_decode_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), 28, 4, 128, 500,
                                   500, ws.data_ptr(), need - 16)
     assert rc == 2  # workspace too small
@@ -113,3 +113,51 @@ def test_attn_rejects_bad_workspace_and_alias():
     assert rc == 0
     torch.cuda.synchronize()
     _check(q, k, v, 500, o)
+
+
+def test_attn_workspace_reused_and_left_zero():
+    """The workspace's range counters are zero after every call: one zeroed
+    workspace serves calls of different shapes in turn, each matching the
+    oracle and a fresh workspace bit for bit."""
+    big = w4.attn_decode_new_workspace(28, 4, 8192, DEV)
+    ws_u32 = big.view(torch.int32)
+    for H, Hkv, T in ((28, 4, 8192), (8, 8, 300), (16, 1, 777), (28, 4, 65), (28, 4, 8192)):
+        assert w4.attn_decode_workspace(H, Hkv, T) <= big.numel() * 4
+        q, k, v = _inputs(H, Hkv, T, T, seed=7 * T + H, poison=False)
+        qd, kd, vd = (torch.from_numpy(a).to(DEV) for a in (q, k, v))
+        a = w4.w4a16_attn_decode(qd, kd, vd, T, workspace=big)
+        b = w4.w4a16_attn_decode(qd, kd, vd, T)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert int(ws_u32[:256].abs().sum()) == 0  # the whole counter block
+        _check(q, k, v, T, a)
+
+
+def test_attn_graph_of_calls_sharing_a_workspace():
+    """28 calls captured in one CUDA graph over distinct caches with one
+    workspace (the bench's layout), replayed twice: every output equals its
+    call made alone."""
+    H, Hkv, T = 28, 4, 1000
+    ins = [_inputs(H, Hkv, T, T, seed=1000 + i, poison=False) for i in range(28)]
+    dev_ins = [tuple(torch.from_numpy(a).to(DEV) for a in t) for t in ins]
+    ws = w4.attn_decode_new_workspace(H, Hkv, T, DEV)
+    outs = [torch.empty((H, 128), dtype=torch.float16, device=DEV) for _ in ins]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for (q, k, v), o in zip(dev_ins, outs):
+            w4.w4a16_attn_decode(q, k, v, T, o=o, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for (q, k, v), o in zip(dev_ins, outs):
+            w4.w4a16_attn_decode(q, k, v, T, o=o, workspace=ws)
+    for _ in range(2):
+        for o in outs:
+            o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for (q, k, v), o in zip(dev_ins, outs):
+            alone = w4.w4a16_attn_decode(q, k, v, T)
+            torch.cuda.synchronize()
+            assert torch.equal(o.view(torch.int16), alone.view(torch.int16))
+    _check(*ins[5], T, outs[5])
