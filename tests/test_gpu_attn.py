@@ -56,10 +56,13 @@ def _check(q, k, v, T, o):
     return rep
 
 
+# The key ranges per KV head are min(tiles of 64 keys, SMs / n_kv_heads):
+# 1 (T <= 64) up to 38 for 4 KV heads; 76 for 2 KV heads (2 x 9000) and
+# every SM for one KV head (16 x 1 x 16384: 152 ranges merged by one CTA).
 @pytest.mark.parametrize("H,Hkv,T,t_stride", [
     (28, 4, 1, 1), (28, 4, 63, 64), (28, 4, 64, 64), (28, 4, 65, 100), (28, 4, 129, 129),
     (28, 4, 1000, 1024), (8, 8, 300, 300), (16, 1, 777, 800), (7, 1, 5000, 5000),
-    (28, 4, 8192, 8192),
+    (28, 4, 8192, 8192), (2, 2, 9000, 9000), (16, 1, 16384, 16384),
 ])
 def test_attn_against_oracle(H, Hkv, T, t_stride):
     q, k, v = _inputs(H, Hkv, T, t_stride, seed=H * 100003 + T)
