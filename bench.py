@@ -411,6 +411,7 @@ def per_config_table(layers, dev, reps=20):
     out["tiny"] = {"M": 1, "N": cfg.N, "K": cfg.K, "us_per_gemv": round(us, 3),
                    "GBps": round(b / us / 1e3, 1), "bytes": b, "note": "L2-resident, latency-bound"}
     out["gate_up_q4k"] = q4k_line(dev, reps)
+    out["down_q4k"] = q4k_line(dev, reps, N=synth.HIDDEN, K=synth.FFN)
     out["attn_decode_T8192"] = attn_decode_line(dev, reps)
     out["layer_seq_qkv_bias_swiglu"] = epilogue_step(layers, dev, reps, ("q", "k", "v"))
     out["layer_seq_bias_swiglu"] = epilogue_step(layers, dev, reps, synth.PROJ_NAMES)
@@ -419,9 +420,10 @@ def per_config_table(layers, dev, reps=20):
 
 
 def q4k_line(dev, reps, N=None, K=None):
-    """The [gate; up] shape (N = 37888, K = 3584) as GGUF Q4_K blocks at M = 1:
-    a CUDA graph of 28 GEMVs over 28 distinct block sets (cold L2), us per
-    GEMV and GB/s over the block bytes plus x and y."""
+    """A projection as GGUF Q4_K blocks at M = 1, by default the [gate; up]
+    shape (N = 37888, K = 3584): a CUDA graph of 28 GEMVs over 28 distinct
+    block sets (cold L2), us per GEMV and GB/s over the block bytes plus x
+    and y."""
     import torch
 
     import int4_weight_only_gemv_gb300 as w4
