@@ -278,13 +278,15 @@ ATTN_SLOPE = 2e-3
 ATTN_FLOOR = 1e-5
 
 
-def check_attn(o: np.ndarray, o_ref: np.ndarray, v: np.ndarray, n_heads: int, T: int) -> dict:
+def check_attn(o: np.ndarray, o_ref: np.ndarray, v: np.ndarray, n_heads: int, T: int,
+               slope: float = ATTN_SLOPE, floor: float = ATTN_FLOOR) -> dict:
     """o, o_ref [H][D] float64; v uint16 [Hkv][t_stride][D].  Returns a report
-    with 'ok'."""
+    with 'ok'.  Query head h reads KV head h / (n_heads / Hkv); its bound is
+    slope * max|v| over that KV head's keys t < T, plus floor."""
     Hkv = v.shape[0]
     group = n_heads // Hkv
     vmax = np.abs(half_to_double(v[:, :T, :])).reshape(Hkv, -1).max(axis=1)
-    bound = ATTN_SLOPE * vmax[np.arange(n_heads) // group] + ATTN_FLOOR
+    bound = slope * vmax[np.arange(n_heads) // group] + floor
     err = np.abs(o - o_ref).max(axis=1)
     finite = bool(np.isfinite(o).all())
     return {"ok": finite and bool((err <= bound).all()), "finite": finite,

@@ -560,6 +560,167 @@ def pin_q4k_fp32_and_gemv(L):
     assert np.allclose(y, ref, rtol=0, atol=1e-5 * np.abs(x).sum())
 
 
+
+# --------------------------------------------------------------------------- tolerance machinery
+#
+# Every GPU parity test is judged by the GEMV bound (per activation row m,
+# max_n |y - y_ref| <= 2e-3 ||x_m||_2 max_n ||w_hat_n||_2 + 1e-3, and the
+# relative L2 error over the whole output <= 1e-3) and by the attention bound
+# (per query head, max_d |o - o_ref| <= 2e-3 max|v| + 1e-5 over the keys t < T
+# of the KV head it reads).  These pins fix the functions that evaluate them
+# (the exact weights behind the row norms, the norms, both checkers) to values
+# worked out by hand, so that a mistake in any of them cannot loosen every
+# parity test at once.  They take O, the module providing the Python-level
+# functions, so that planted mistakes in those functions can be checked too.
+
+def _hand_two_group_matrix():
+    """N = 3, K = 256: group 0 of every row holds 16 words 0x76543210 (q = 0..7)
+    at scale 2^-n, group 1 holds 16 words 0x89ABCDEF (q = -1..-8) at scale
+    2^-(n+4).  Returns (qweight, scales, dense exact w_hat from the hand-decoded
+    golden words)."""
+    words = dict(read_hand_words())
+    qa, qb = np.array(words[0x76543210], np.float64), np.array(words[0x89ABCDEF], np.float64)
+    N, K = 3, 256
+    qw = np.zeros((N, K // 8), np.uint32)
+    qw[:, :16] = 0x76543210
+    qw[:, 16:] = 0x89ABCDEF
+    sc = np.zeros((N, 2), np.uint16)
+    dense = np.zeros((N, K))
+    for n in range(N):
+        sc[n] = np.array([2.0 ** -n, 2.0 ** -(n + 4)], np.float16).view(np.uint16)
+        dense[n, :128] = np.tile(qa, 16) * 2.0 ** -n
+        dense[n, 128:] = np.tile(qb, 16) * 2.0 ** -(n + 4)
+    return qw, sc, dense
+
+
+def pin_dequant_f64_hand(L, O=oracle):
+    """The exact weights behind the row norms: element by element equal to
+    the hand-decoded words times their group scale, on a 3 x 256 matrix whose
+    rows and groups all differ (a transposed index or a wrong group scale
+    moves values)."""
+    qw, sc, dense = _hand_two_group_matrix()
+    got = O.dequant_f64(qw, sc, 128, L)
+    assert got.shape == dense.shape and np.array_equal(got, dense)
+
+
+def pin_row_norms_closed_form(L, O=oracle):
+    """||w_hat_n||_2 in closed form.  16 words 0x76543210 at s = 1: q = 0..7
+    sixteen times, sum q^2 = 16 * 140 = 2240.  The two-group matrix: row n
+    has 16 * 140 * 4^-n from group 0 and 16 * 204 * 4^-(n+4) from group 1,
+    so ||w_hat_n||^2 = 4^-n (2240 + 3264 / 256) = 2252.75 * 4^-n, and the norm
+    is sqrt(2252.75) 2^-n (both sums are exact, and a power of 4 leaves the
+    square root exact)."""
+    one = O.row_norms(np.full((1, 16), 0x76543210, np.uint32), np.array([[0x3C00]], np.uint16), 128, L)
+    assert one.shape == (1,) and one[0] == math.sqrt(2240.0)
+    qw, sc, _ = _hand_two_group_matrix()
+    got = O.row_norms(qw, sc, 128, L)
+    want = np.array([math.sqrt(2252.75) * 2.0 ** -n for n in range(3)])
+    assert got.shape == (3,) and np.array_equal(got, want)
+
+
+def pin_check_gemv_abs_bound(L, O=oracle):
+    """The per-row absolute bound, with slope 2^-9 and floor 2^-10 so that
+    every bound is exact: x rows of norm 1, 2 and 5 ([1,0,0,0], [1,1,1,1],
+    [0,0,3,4]) and max row norm 4 give bounds 2^-7 + 2^-10 = 0.0087890625,
+    2^-6 + 2^-10 = 0.0166015625 and 20 2^-9 + 2^-10 = 0.0400390625.  An error
+    exactly at a row's bound passes; one unit in the last place above it
+    fails; a larger row's bound planted in a smaller row fails; a NaN
+    fails."""
+    x = np.array([[1, 0, 0, 0], [1, 1, 1, 1], [0, 0, 3, 4]], np.float64)
+    bounds = [0.0087890625, 0.0166015625, 0.0400390625]
+    y_ref = np.zeros((3, 5))
+
+    def run(row, col, err):
+        y = y_ref.copy()
+        y[row, col] = err
+        return O.check_gemv(y, y_ref, x, 4.0, rel_l2=np.inf, abs_slope=2.0 ** -9, abs_floor=2.0 ** -10)
+
+    for m in range(3):
+        assert run(m, 2, bounds[m])["ok"], m
+        assert run(m, 2, -bounds[m])["ok"], m
+        assert not run(m, 2, np.nextafter(bounds[m], np.inf))["ok"], m
+    assert not run(0, 4, bounds[2])["ok"]
+    assert not run(1, 0, bounds[2])["ok"]
+    assert run(2, 0, bounds[0])["ok"]
+    # every row at its own bound at once
+    y = np.array([[bounds[0], 0, 0, 0, 0], [0, -bounds[1], 0, 0, 0], [0, 0, 0, 0, bounds[2]]])
+    assert O.check_gemv(y, y_ref, x, 4.0, rel_l2=np.inf, abs_slope=2.0 ** -9, abs_floor=2.0 ** -10)["ok"]
+    y[1, 3] = np.nan
+    assert not O.check_gemv(y, y_ref, x, 4.0, rel_l2=np.inf, abs_slope=2.0 ** -9,
+                            abs_floor=2.0 ** -10)["ok"]
+    # the default constants: ||x|| = 3 ([1, 2, 2]), max row norm 5:
+    # 2e-3 * 3 * 5 + 1e-3 = 0.031 (y_ref of norm 100 keeps the L2 test loose)
+    x1 = np.array([[1.0, 2.0, 2.0]])
+    y_ref1 = np.array([[100.0, 0.0]])
+    assert O.check_gemv(np.array([[100.0, 0.0309]]), y_ref1, x1, 5.0)["ok"]
+    assert not O.check_gemv(np.array([[100.0, 0.0311]]), y_ref1, x1, 5.0)["ok"]
+
+
+def pin_check_gemv_rel_l2(L, O=oracle):
+    """The relative L2 bound over the whole [M][N] output.  y_ref has norm
+    1024 (one entry), the planted error norm 1, so the relative error is
+    exactly 2^-10: it passes at rel_l2 = 2^-10 and fails one unit in the last
+    place above; the error may sit in another activation row (the norm is over
+    the whole output, not per row).  With the default 1e-3: 0.999 over a
+    reference of norm 1000 passes, 1.001 fails."""
+    x = np.array([[4096.0], [4096.0]])  # abs bound far away
+    y_ref = np.array([[1024.0, 0.0], [0.0, 0.0]])
+    for (r, c) in ((0, 1), (1, 0), (1, 1)):
+        y = y_ref.copy()
+        y[r, c] = 1.0
+        assert O.check_gemv(y, y_ref, x, 1.0, rel_l2=2.0 ** -10)["ok"], (r, c)
+        y[r, c] = np.nextafter(1.0, 2.0)
+        assert not O.check_gemv(y, y_ref, x, 1.0, rel_l2=2.0 ** -10)["ok"], (r, c)
+    # two errors of norm 2^-1/2 each combine in quadrature to 1 (not 2^1/2 or 2^-1/2)
+    y = y_ref.copy()
+    y[0, 1] = y[1, 1] = math.sqrt(0.5)
+    rep = O.check_gemv(y, y_ref, x, 1.0, rel_l2=2.0 ** -10)
+    assert abs(rep["rel_l2"] - 2.0 ** -10) <= 2.0 ** -60
+    x1 = np.array([[1000.0]])
+    y_ref1 = np.array([[1000.0, 0.0]])
+    assert O.check_gemv(np.array([[1000.0, 0.999]]), y_ref1, x1, 1000.0)["ok"]
+    assert not O.check_gemv(np.array([[1000.0, 1.001]]), y_ref1, x1, 1000.0)["ok"]
+
+
+def pin_check_attn_bound(L, O=oracle):
+    """The attention bound: 4 query heads over 2 KV heads (heads 0, 1 read
+    KV head 0; heads 2, 3 read KV head 1), T = 3 keys of a stride of 5, whose
+    rows past T hold 1000 (never part of the bound).  max|v| is 2 for KV head
+    0 and 8 for KV head 1, so with slope 2^-8 and floor 2^-12 the bounds are
+    2^-7 + 2^-12 and 2^-5 + 2^-12.  An error at a head's bound passes, one
+    unit in the last place above fails, KV head 1's bound planted in head 1
+    fails and KV head 0's in head 2 passes.  With the default constants and
+    max|v| = 1 the bound is 2e-3 + 1e-5 = 0.00201."""
+    D = 4
+    v = np.zeros((2, 5, D), np.float16)
+    v[0, 1, 2] = -2.0
+    v[0, 0, 0] = 1.5
+    v[1, 2, 3] = 8.0
+    v[1, 0, 1] = -7.5
+    v[:, 3:, :] = 1000.0
+    v = v.view(np.uint16)
+    o_ref = np.zeros((4, D))
+    b0, b1 = 2.0 ** -7 + 2.0 ** -12, 2.0 ** -5 + 2.0 ** -12
+
+    def run(h, d, err):
+        o = o_ref.copy()
+        o[h, d] = err
+        return O.check_attn(o, o_ref, v, 4, 3, slope=2.0 ** -8, floor=2.0 ** -12)
+
+    for h, b in ((0, b0), (1, b0), (2, b1), (3, b1)):
+        assert run(h, 1, b)["ok"] and run(h, 3, -b)["ok"], h
+        assert not run(h, 1, np.nextafter(b, np.inf))["ok"], h
+    assert not run(1, 0, b1)["ok"]
+    assert run(2, 0, b0)["ok"]
+    o = o_ref.copy()
+    o[3, 2] = np.nan
+    assert not O.check_attn(o, o_ref, v, 4, 3, slope=2.0 ** -8, floor=2.0 ** -12)["ok"]
+    v1 = np.ones((1, 2, D), np.float16).view(np.uint16)
+    o_ref1 = np.zeros((2, D))
+    assert O.check_attn(np.full((2, D), 0.002), o_ref1, v1, 2, 2)["ok"]
+    assert not O.check_attn(np.full((2, D), 0.00202), o_ref1, v1, 2, 2)["ok"]
+
+
 ALL_PINS = [
     pin_half_to_double_exhaustive, pin_half_roundtrip, pin_half_midpoints_ties_to_even,
     pin_half_overflow_and_specials, pin_half_vs_numpy_random, pin_hand_words,
@@ -574,12 +735,23 @@ ALL_PINS = [
 ]
 
 
-def failing_pins(L) -> list[str]:
-    """Names of the pins that fail (or crash) against oracle library L."""
+# The pins of the tolerance machinery (they also take the Python-level module).
+CHECK_PINS = [
+    pin_dequant_f64_hand, pin_row_norms_closed_form, pin_check_gemv_abs_bound,
+    pin_check_gemv_rel_l2, pin_check_attn_bound,
+]
+
+
+def failing_pins(L, O=oracle) -> list[str]:
+    """Names of the pins that fail (or crash) against oracle library L, with
+    the Python-level functions of module O."""
     bad = []
-    for pin in ALL_PINS:
+    for pin in ALL_PINS + CHECK_PINS:
         try:
-            pin(L)
+            if pin in CHECK_PINS:
+                pin(L, O)
+            else:
+                pin(L)
         except Exception as e:  # noqa: BLE001 -- a crash is a failure too
             bad.append(f"{pin.__name__}: {type(e).__name__}")
     return bad

@@ -4,6 +4,7 @@ fails against that broken build (and that the unbroken build passes them all).
 No GPU is involved."""
 import os
 import subprocess
+import types
 
 import pytest
 
@@ -57,6 +58,29 @@ MUTANTS = [
     ("swiglu_gate_up_swapped",
      "orc_silu(orc_half_to_double(g[i])) * orc_half_to_double(u[i])",
      "orc_silu(orc_half_to_double(u[i])) * orc_half_to_double(g[i])"),
+    ("dequant_f64_transposed",
+     "for (int64_t k = 0; k < K; ++k) w_out[n * K + k] = w_hat(qweight, scales, K, G, n, k);",
+     "for (int64_t k = 0; k < K; ++k) w_out[k * N + n] = w_hat(qweight, scales, K, G, n, k);"),
+]
+
+# (name, text in oracle/__init__.py, replacement) -- planted mistakes in the
+# Python-level tolerance machinery (row norms and the two checkers)
+PY_MUTANTS = [
+    ("row_norms_per_column", "return np.sqrt(np.sum(w * w, axis=1))", "return np.sqrt(np.sum(w * w, axis=0))"),
+    ("row_norms_squared", "return np.sqrt(np.sum(w * w, axis=1))", "return np.sum(w * w, axis=1)"),
+    ("check_gemv_strict_abs", "bool(np.all(max_err <= bound))", "bool(np.all(max_err < bound))"),
+    ("check_gemv_strict_rel", "and rel <= rel_l2", "and rel < rel_l2"),
+    ("check_gemv_x_norm_axis", "np.sqrt(np.sum(x_f64 * x_f64, axis=1))", "np.sqrt(np.sum(x_f64 * x_f64))"),
+    ("check_gemv_max_per_column", "max_err = err.max(axis=1)", "max_err = err.max(axis=0).max() + 0 * err.max(axis=1)"),
+    ("check_gemv_bound_one_row", "bound = abs_slope * np.sqrt(np.sum(x_f64 * x_f64, axis=1)) * max_row_norm + abs_floor",
+     "bound = abs_slope * np.sqrt(np.sum(x_f64 * x_f64, axis=1)).max() * max_row_norm + abs_floor"),
+    ("check_gemv_rel_per_row_max", "rel = float(np.sqrt(np.sum(err * err)) / denom)",
+     "rel = float(np.sqrt(np.sum(err * err, axis=1)).max() / denom)"),
+    ("check_attn_strict", "bool((err <= bound).all())", "bool((err < bound).all())"),
+    ("check_attn_head_mapping_modulo", "vmax[np.arange(n_heads) // group]", "vmax[np.arange(n_heads) % Hkv]"),
+    ("check_attn_whole_stride", "half_to_double(v[:, :T, :])", "half_to_double(v)"),
+    ("check_attn_max_over_heads", "vmax = np.abs(half_to_double(v[:, :T, :])).reshape(Hkv, -1).max(axis=1)",
+     "vmax = np.abs(half_to_double(v[:, :T, :])).reshape(Hkv, -1).max(axis=1).max() + 0 * np.arange(Hkv)"),
 ]
 
 
@@ -79,4 +103,23 @@ def test_unbroken_oracle_passes_every_pin():
 def test_planted_mistake_is_caught(tmp_path, name, old, new):
     L = _build_mutant(tmp_path, old, new)
     failing = oracle_pins.failing_pins(L)
+    assert failing, f"no pin caught the planted mistake {name}"
+
+
+def _load_py_mutant(old, new):
+    """A copy of the oracle's Python module with one planted mistake (it still
+    loads the unbroken C library)."""
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "__init__.py")).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    mod = types.ModuleType("oracle_mutant")
+    mod.__package__ = "oracle"
+    mod.__file__ = oracle.__file__
+    exec(compile(src.replace(old, new, 1), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_planted_checker_mistake_is_caught(name, old, new):
+    O = _load_py_mutant(old, new)
+    failing = oracle_pins.failing_pins(oracle.lib(), O)
     assert failing, f"no pin caught the planted mistake {name}"

@@ -10,6 +10,6 @@ def L():
     return oracle.lib()
 
 
-@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda p: p.__name__)
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS + oracle_pins.CHECK_PINS, ids=lambda p: p.__name__)
 def test_pin(pin, L):
     pin(L)
