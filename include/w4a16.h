@@ -215,11 +215,15 @@ typedef struct {
  *           shaped layers with stacked weights: one launch), after a memset
  *           node that zeroes one completion counter per GEMV.  A GEMV that
  *           reads another's output (o, down) starts once every CTA has
- *           written that output.
+ *           written that output.  Such a launch is cooperative (one CTA per
+ *           SM, all resident at once): where that cannot be had (fewer free
+ *           SMs, e.g. under MPS limits), the launch fails and so does the
+ *           replay, instead of CTAs waiting on ones that never start.
  *   M > 1:  one launch per GEMV, each a programmatic dependent of the
  *           previous one.
  * The library allocates the graph, a stream, an event and, for M = 1, one
- * int of device memory per GEMV (the counters); nothing else.  The pointers
+ * int of device memory per task (the counters: one per GEMV, two for a GEMV
+ * whose K the M = 1 kernel splits in halves); nothing else.  The pointers
  * are recorded in the graph and must outlive the object.  Blocks until
  * instantiation is done (a set-up call, not a hot-path call).  *out is NULL
  * on failure.
@@ -288,7 +292,13 @@ w4a16_status w4a16_layer_seq_run_host(w4a16_layer_seq* seq, const w4a16_seq_io* 
  * Wait for the most recent run / run_host of `seq`: timeout_ms < 0 waits
  * without bound, timeout_ms >= 0 polls and returns W4A16_ERR_TIMEOUT if the
  * replay has not finished in that time (the replay keeps running; call again
- * to keep waiting).
+ * to keep waiting).  Once it has finished, the device status word of the
+ * sequence's device is read (on the sequence's own stream): if it holds
+ * W4A16_DEV_PIPE_TIMEOUT -- a pipeline or dependency wait inside a GEMV ran
+ * past its bound, so outputs may be wrong -- the call returns
+ * W4A16_ERR_DEVICE.  The word is shared by every call on the device and is
+ * left set (later syncs return W4A16_ERR_DEVICE too) until
+ * w4a16_device_status reads and clears it.
  */
 w4a16_status w4a16_layer_seq_sync(w4a16_layer_seq* seq, int timeout_ms);
 
@@ -312,12 +322,17 @@ void w4a16_layer_seq_destroy(w4a16_layer_seq* seq);
  * Arguments and checks are those of w4a16_layer_seq_create with M = 1; the
  * work is the same task-list launches (one per up to 224 GEMVs), enqueued on
  * `stream` directly, so the outputs are the same bits.  Limits: at most
- * W4A16_STATIC_MAX_GEMVS GEMVs per call (4 per layer with stacked [q; k; v]
- * and [gate; up], up to 7 otherwise) and every K at most 28672 (the M = 1
- * kernel's range); beyond either the call returns W4A16_ERR_LIMIT and
- * enqueues nothing.
+ * W4A16_STATIC_MAX_GEMVS tasks per call -- one per GEMV (4 per layer with
+ * stacked [q; k; v] and [gate; up], up to 7 otherwise), two for a GEMV whose
+ * K the M = 1 kernel splits in halves (a K = 18944 down projection) -- and
+ * every K at most 28672 (the M = 1 kernel's range); beyond either the call
+ * returns W4A16_ERR_LIMIT and
+ * enqueues nothing.  Every task table is also checked against the kernel's
+ * limits on this device before anything is enqueued; W4A16_ERR_CUDA after
+ * that means a launch itself failed, and the memset and any launches before
+ * it may have been enqueued (the outputs are then undefined).
  *
- * Scratch: the per-GEMV completion counters are one fixed device array of
+ * Scratch: the per-task completion counters are one fixed device array of
  * W4A16_STATIC_MAX_GEMVS ints (2 KB) inside the library, held on every device
  * that loads the library until the process exits.  Each call zeroes the
  * counters it uses with a memset on `stream` before its launches.  All calls

@@ -634,29 +634,29 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
 // The GEMVs of layers [l0, l1) as one task table, in launch order.  Layers
 // are independent of each other, so the table interleaves them: stage A of
 // a layer (the GEMVs that read the layer's x) runs one layer ahead of its
-// stage B (o and down, which read stage A's outputs):
-//   A(l0) A(l0+1) B(l0) A(l0+2) B(l0+1) ... B(l1-1)
-// A dependent GEMV then finds its producer finished one stage earlier by the
-// whole grid, instead of waiting for the grid to finish it.  Stage A runs in
-// reverse GEMV order ([gate; up] before [q; k; v]), so a cycle is
-// gate_up(l+1) qkv(l+1) o(l) down(l).  A task's activation set-up is hidden
-// behind the weight ring when the task before it was bound by the memory
-// stream (ring nearly empty), and exposed when it was bound by the CUDA cores
-// (down at K = 18944 leaves the ring full); this order puts the shortest
-// set-up after down.  Of the six cyclic orders it measured fastest on the
-// 28-layer Qwen-7B-shaped step (0.751 ms against 0.767-0.801 ms).
+// stage B (o and down, which read stage A's outputs), so that a dependent
+// GEMV finds its producer finished a whole cycle earlier by the whole grid.
+// W4A16 alternates the two stages, largest first:
+//   gate_up(l+1) down(l) qkv(l+1) o(l)
+// (the M = 1 kernel stages each task's activations into shared memory while
+// the task before it runs; down's, K = 18944, take the longest to stage and
+// follow [gate; up], the longest task; with separate q, k, v or gate, up
+// weights the longer stage continues after the shorter one runs out).  W4A8,
+// whose consumer threads load their own activations, runs
+//   gate_up(l+1) qkv(l+1) o(l) down(l)
+// which puts the shortest set-up after down, its most CUDA-core-bound task.
 // Dependencies become task indices within the table (the done counters are
-// per table slot); a producer before l0 is met by the launch order.
-void seq_tasks(const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep,
+// per table slot); a producer before l0 is met by the launch order.  A GEMV
+// whose K the M = 1 kernel splits becomes two consecutive tasks; a GEMV that
+// reads its output depends on the second.
+void seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep,
                const std::vector<const uint16_t*>& x2, const std::vector<int>& layer_first, int l0, int l1,
-               std::vector<M1Task>* tasks) {
+               bool a8, std::vector<M1Task>* tasks) {
   tasks->clear();
   static thread_local std::vector<int> slot;  // table slot of each emitted GEMV (capacity kept)
   slot.assign(gemvs.size(), -1);
-  auto emit = [&](int l, bool stage_b) {
-    for (int k = layer_first[l]; k < layer_first[l + 1]; ++k) {
-      const int i = stage_b ? k : layer_first[l] + layer_first[l + 1] - 1 - k;  // stage A reversed
-      if ((dep[i] >= 0) != stage_b) continue;
+  auto emit_one = [&](int i) {
+    {
       const GemvArgs& a = gemvs[i];
       M1Task tk{};
       tk.qweight = a.qweight;
@@ -665,17 +665,41 @@ void seq_tasks(const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep,
       tk.x2 = x2[i];
       tk.N = a.N;
       tk.K = a.K;
-      tk.nseg = a.nseg;
+      tk.nseg = static_cast<uint8_t>(a.nseg);
       tk.dep = dep[i] < 0 ? -1 : slot[dep[i]];
       for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = M1Seg{a.seg[g].y, a.seg[g].bias, a.seg[g].n_end};
-      slot[i] = static_cast<int>(tasks->size());
-      tasks->push_back(tk);
+      M1Task parts[2];
+      const int np = gemv_m1_split_tasks(tk, a8, d.info, parts);
+      for (int q = 0; q < np; ++q) tasks->push_back(parts[q]);
+      slot[i] = static_cast<int>(tasks->size()) - 1;
     }
   };
-  emit(l0, false);
+  // a layer's stage A (reads x) and stage B (reads stage A), each in reverse
+  // GEMV order: [gate; up] before [q; k; v], down before o
+  static thread_local std::vector<int> stage_a, stage_b;
+  auto stage = [&](int l, bool b, std::vector<int>* out) {
+    out->clear();
+    for (int i = layer_first[l + 1] - 1; i >= layer_first[l]; --i)
+      if ((dep[i] >= 0) == b) out->push_back(i);
+  };
+  stage(l0, false, &stage_a);
+  for (int i : stage_a) emit_one(i);
   for (int l = l0; l < l1; ++l) {
-    if (l + 1 < l1) emit(l + 1, false);
-    emit(l, true);
+    if (l + 1 < l1)
+      stage(l + 1, false, &stage_a);
+    else
+      stage_a.clear();
+    stage(l, true, &stage_b);
+    if (a8) {
+      for (int i : stage_a) emit_one(i);
+      for (auto it = stage_b.rbegin(); it != stage_b.rend(); ++it) emit_one(*it);  // o, down
+      continue;
+    }
+    const size_t n = stage_a.size() > stage_b.size() ? stage_a.size() : stage_b.size();
+    for (size_t k = 0; k < n; ++k) {
+      if (k < stage_a.size()) emit_one(stage_a[k]);
+      if (k < stage_b.size()) emit_one(stage_b[k]);
+    }
   }
 }
 
@@ -687,26 +711,57 @@ bool seq_uses_tasks(int M, const std::vector<GemvArgs>& gemvs) {
   return true;
 }
 
+// The task lists of a checked M = 1 sequence: task_first[l] is the index of
+// layer l's first task (task_first[n_layers] = tasks, one completion counter
+// each), every layer within one task table, every task within the M = 1
+// kernel's limits on this device.  Host-only: nothing is enqueued.
+// scratch: the caller's buffer (its capacity is reused).
+w4a16_status check_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs,
+                             const std::vector<int>& dep, const std::vector<const uint16_t*>& x2,
+                             const std::vector<int>& layer_first, bool a8, std::vector<M1Task>* scratch,
+                             std::vector<int>* task_first) {
+  const int n_layers = static_cast<int>(layer_first.size()) - 1;
+  for (const GemvArgs& a : gemvs)
+    if (a.N <= 0) return W4A16_ERR_SHAPE;
+  task_first->assign(1, 0);
+  for (int l = 0; l < n_layers; ++l) {
+    int n = 0;
+    for (int i = layer_first[l]; i < layer_first[l + 1]; ++i) {
+      M1Task t{};
+      t.K = gemvs[i].K;
+      t.N = gemvs[i].N;
+      M1Task parts[2];
+      n += gemv_m1_split_tasks(t, a8, d.info, parts);
+    }
+    if (n > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
+    task_first->push_back(task_first->back() + n);
+  }
+  seq_tasks(d, gemvs, dep, x2, layer_first, 0, n_layers, a8, scratch);
+  return gemv_m1_tasks_fit(scratch->data(), static_cast<int>(scratch->size()), a8, d.info) ? W4A16_OK
+                                                                                          : W4A16_ERR_SHAPE;
+}
+
 // Enqueue a sequence's task lists: as many whole layers per launch as fit in
 // one task table, each launch after the first a programmatic dependent of the
-// previous one.  done: one zeroed counter per GEMV.  Returns the launch count
-// through *launches.
+// previous one.  done: one zeroed counter per task (task_first from
+// check_seq_tasks, which must have passed: a launch that fails here leaves
+// the launches before it enqueued); tasks: the caller's table buffer (its
+// capacity is reused).  Returns the launch count through *launches.
 w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs,
                                const std::vector<int>& dep, const std::vector<const uint16_t*>& x2,
-                               const std::vector<int>& layer_first, int* done, bool a8, cudaStream_t st,
-                               int* launches) {
+                               const std::vector<int>& layer_first, const std::vector<int>& task_first,
+                               int* done, bool a8, cudaStream_t st, std::vector<M1Task>* tasks, int* launches) {
   const int n_layers = static_cast<int>(layer_first.size()) - 1;
-  std::vector<M1Task> tasks;
   int l0 = 0;
   *launches = 0;
   while (l0 < n_layers) {
     int l1 = l0 + 1;
-    while (l1 < n_layers && layer_first[l1 + 1] - layer_first[l0] <= kM1MaxTasks) ++l1;
-    const int t0 = layer_first[l0], t1 = layer_first[l1];
+    while (l1 < n_layers && task_first[l1 + 1] - task_first[l0] <= kM1MaxTasks) ++l1;
+    const int t0 = task_first[l0], t1 = task_first[l1];
     if (t1 - t0 > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
-    seq_tasks(gemvs, dep, x2, layer_first, l0, l1, &tasks);
+    seq_tasks(d, gemvs, dep, x2, layer_first, l0, l1, a8, tasks);
     const cudaError_t e =
-        launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d.status, *launches > 0, a8, d.info, st);
+        launch_gemv_m1_tasks(tasks->data(), t1 - t0, done + t0, d.status, *launches > 0, a8, d.info, st);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return W4A16_ERR_CUDA;
@@ -779,7 +834,15 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
   std::vector<ActOp> act;
   build_seq_gemvs(layers, opt, n_layers, M, hidden, kv_dim, ffn, io, tasks, &gemvs, &dep, &x2, &act,
                   &layer_first);
-  if (tasks && cudaMalloc(&s->task_done, sizeof(int) * gemvs.size()) != cudaSuccess) {
+  // M = 1: the task lists, checked on the host before anything is captured
+  std::vector<M1Task> table;
+  std::vector<int> task_first;
+  if (tasks && (st = check_seq_tasks(*d, gemvs, dep, x2, layer_first, a8, &table, &task_first)) != W4A16_OK) {
+    seq_free(s);
+    return st;
+  }
+  const size_t ntasks = tasks ? static_cast<size_t>(task_first.back()) : 0;
+  if (tasks && cudaMalloc(&s->task_done, sizeof(int) * ntasks) != cudaSuccess) {
     cudaGetLastError();
     seq_free(s);
     return W4A16_ERR_CUDA;
@@ -798,11 +861,11 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
   w4a16_status cap = W4A16_OK;
   int launches = 0;
   if (tasks) {
-    if (cudaMemsetAsync(s->task_done, 0, sizeof(int) * gemvs.size(), s->capture_stream) != cudaSuccess)
+    if (cudaMemsetAsync(s->task_done, 0, sizeof(int) * ntasks, s->capture_stream) != cudaSuccess)
       cap = W4A16_ERR_CUDA;
     else
-      cap = enqueue_seq_tasks(*d, gemvs, dep, x2, layer_first, s->task_done, a8, s->capture_stream,
-                              &launches);
+      cap = enqueue_seq_tasks(*d, gemvs, dep, x2, layer_first, task_first, s->task_done, a8,
+                              s->capture_stream, &table, &launches);
   } else {
     for (size_t i = 0; i < gemvs.size() && cap == W4A16_OK; ++i) {
       if (act[i].h != nullptr) {
@@ -898,39 +961,28 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
   static thread_local std::vector<const uint16_t*> x2;
   static thread_local std::vector<ActOp> act;
   static thread_local std::vector<M1Task> tasks;
+  static thread_local std::vector<int> task_first;
   build_seq_gemvs(layers, SeqOptions{}, n_layers, 1, hidden, kv_dim, ffn, io, true, &gemvs, &dep, &x2, &act,
                   &layer_first);
-  const int n = static_cast<int>(gemvs.size());
-  if (n > W4A16_STATIC_MAX_GEMVS || !seq_uses_tasks(1, gemvs)) return W4A16_ERR_LIMIT;
+  if (!seq_uses_tasks(1, gemvs)) return W4A16_ERR_LIMIT;
 
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != W4A16_OK) return st;
   int* done = nullptr;
   if ((st = static_task_done(&done)) != W4A16_OK) return st;
 
+  // every task table is checked on the host before anything is enqueued
+  if ((st = check_seq_tasks(*d, gemvs, dep, x2, layer_first, false, &tasks, &task_first)) != W4A16_OK) return st;
+  const int n = task_first.back();  // one counter per task
+  if (n > W4A16_STATIC_MAX_GEMVS) return W4A16_ERR_LIMIT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the counters keep the previous call's values: zero the ones this call uses
   if (cudaMemsetAsync(done, 0, sizeof(int) * n, s) != cudaSuccess) {
     cudaGetLastError();
     return W4A16_ERR_CUDA;
   }
-  // whole layers per launch, up to one task table each; every launch after
-  // the first is a programmatic dependent of the previous one
   int launches = 0;
-  for (int l0 = 0; l0 < n_layers;) {
-    int l1 = l0 + 1;
-    while (l1 < n_layers && layer_first[l1 + 1] - layer_first[l0] <= kM1MaxTasks) ++l1;
-    const int t0 = layer_first[l0], t1 = layer_first[l1];
-    seq_tasks(gemvs, dep, x2, layer_first, l0, l1, &tasks);
-    if (launch_gemv_m1_tasks(tasks.data(), t1 - t0, done + t0, d->status, launches > 0, false, d->info, s) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return W4A16_ERR_CUDA;
-    }
-    ++launches;
-    l0 = l1;
-  }
-  return W4A16_OK;
+  return enqueue_seq_tasks(*d, gemvs, dep, x2, layer_first, task_first, done, false, s, &tasks, &launches);
 }
 
 extern "C" {
@@ -974,6 +1026,34 @@ w4a16_status w4a16_layer_seq_run_host(w4a16_layer_seq* seq, const w4a16_seq_io* 
   return W4A16_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// After a replay has completed: W4A16_ERR_DEVICE if the device status word of
+// the sequence's device holds W4A16_DEV_PIPE_TIMEOUT (a pipeline or
+// dependency wait inside a GEMV ran out, so outputs may be wrong), else OK.
+// The word is read on the sequence's own stream and left as it is.
+w4a16_status seq_device_check(w4a16_layer_seq* seq) {
+  uint32_t* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (seq->device >= 0 && seq->device < kMaxDevices) status = g_dev[seq->device].status;
+  }
+  if (status == nullptr) return W4A16_ERR_STATE;
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, status, sizeof(v), cudaMemcpyDeviceToHost, seq->capture_stream) != cudaSuccess ||
+      cudaStreamSynchronize(seq->capture_stream) != cudaSuccess) {
+    cudaGetLastError();
+    return W4A16_ERR_CUDA;
+  }
+  return (v & W4A16_DEV_PIPE_TIMEOUT) ? W4A16_ERR_DEVICE : W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 w4a16_status w4a16_layer_seq_sync(w4a16_layer_seq* seq, int timeout_ms) {
   if (!seq || !seq->done) return W4A16_ERR_STATE;
   if (timeout_ms < 0) {
@@ -981,12 +1061,12 @@ w4a16_status w4a16_layer_seq_sync(w4a16_layer_seq* seq, int timeout_ms) {
       cudaGetLastError();
       return W4A16_ERR_CUDA;
     }
-    return W4A16_OK;
+    return seq_device_check(seq);
   }
   const auto t0 = std::chrono::steady_clock::now();
   for (;;) {
     const cudaError_t e = cudaEventQuery(seq->done);
-    if (e == cudaSuccess) return W4A16_OK;
+    if (e == cudaSuccess) return seq_device_check(seq);
     if (e != cudaErrorNotReady) {
       cudaGetLastError();
       return W4A16_ERR_CUDA;

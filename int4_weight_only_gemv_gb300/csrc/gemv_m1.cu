@@ -58,14 +58,14 @@
 namespace w4a16 {
 namespace {
 
-// 16 warps: producer, reducer and up to 14 consumer warps.  Registers are
-// handed out to warps in groups of four, so 16 warps leave up to 128
-// registers per thread.
+// 16 warps: the producer (lane 0 of warp 0; for W4A16, lanes 1..31 of the
+// same warp stage the activations of the next task into shared memory), the
+// reducer and 14 consumer warps.  Registers are handed out to warps in groups
+// of four, so 16 warps leave up to 128 registers per thread.
 constexpr int kM1MaxThreads = 512;
 constexpr int kM1MaxConsumers = kM1MaxThreads - 64;
-constexpr int kRR = 4;  // rows per consumer thread per tile
 constexpr int kM1MaxStages = 8;
-constexpr int kM1SmemBudget = 200 * 1024;
+constexpr int kM1SmemBudget = 227 * 1024;
 
 // Weight formats of the kernel: the INT4 group-128 layout with FP16 or
 // in-kernel INT8 activations, and GGUF Q4_K blocks (144 bytes per 256
@@ -74,75 +74,138 @@ constexpr int kFmtW4A16 = 0;
 constexpr int kFmtW4A8 = 1;
 constexpr int kFmtQ4K = 2;
 
-// Per-task tiling, a pure function of K and the format (U <= kM1MaxConsumers).
+// First consumer warp and consumer threads.
+__host__ __device__ constexpr int first_consumer_warp(int) { return 2; }
+__host__ __device__ constexpr int max_consumers(int fmt) { return kM1MaxThreads - 32 * first_consumer_warp(fmt); }
+
+// A consumer thread's unit of K and its rows per tile, by format.  W4A16:
+// one whole 128-k group (its 128 activations in 64 registers, the group scale
+// applied once per row), two rows per tile.  W4A8: 64 k, one activation
+// block; Q4_K: 64 k, one chunk of a block; four rows per tile.
+__host__ __device__ constexpr int unit_k(int fmt) { return fmt == kFmtW4A16 ? 128 : 64; }
+__host__ __device__ constexpr int rows_per_thread(int fmt) { return fmt == kFmtW4A16 ? 2 : 4; }
+
+// Rows of one CTA a K-split task may have (its first part's sums wait in
+// shared memory for the second part).
+constexpr int kM1PartRows = 256;
+
+// Per-task tiling, a pure function of the task's K, its format and whether
+// it is half of a K-split GEMV (U <= max_consumers(fmt)).
 struct TaskPlan {
-  int U;             // units (64 k) per row
+  int U;             // units (unit_k(fmt) k) per row
   int RL;            // rows across consumer threads
-  int RB;            // rows per tile = RL * kRR
-  int T;             // consumer threads = U * RL (<= kM1MaxConsumers)
-  int row_bytes;     // K / 2: packed bytes per row, also the row pitch in a stage
-  int sc_row_bytes;  // K / 64: scale bytes per row
+  int RB;            // rows per tile = RL * rows_per_thread(fmt)
+  int T;             // consumer threads = U * RL
+  int row_bytes;     // K / 2: packed bytes of a row's K range, also the row pitch in a stage
+  int sc_row_bytes;  // K / 64: scale bytes of a row's K range
+  int pitch;         // bytes between rows in memory (row_bytes times the parts of the split)
+  int sc_pitch;      // scale bytes between rows in memory
   int red_stride;    // floats per row in a partial slot (U + 1)
 };
 
-__host__ __device__ inline TaskPlan task_plan(int K, int fmt = kFmtW4A16) {
+__host__ __device__ inline TaskPlan task_plan(int K, int fmt, int parts = 1) {
   TaskPlan p;
-  p.U = K >> 6;
-  p.RL = p.U >= kM1MaxConsumers ? 1 : kM1MaxConsumers / p.U;
-  p.RB = p.RL * kRR;
+  const int cons = max_consumers(fmt);
+  p.U = K / unit_k(fmt);
+  p.RL = p.U >= cons ? 1 : cons / p.U;
+  p.RB = p.RL * rows_per_thread(fmt);
   p.T = p.U * p.RL;
   // Q4_K: 144 bytes per 256 weights (a multiple of 16), no separate scales
   p.row_bytes = fmt == kFmtQ4K ? (K >> 8) * 144 : K >> 1;
   p.sc_row_bytes = fmt == kFmtQ4K ? 0 : K >> 6;
+  p.pitch = p.row_bytes * parts;
+  p.sc_pitch = p.sc_row_bytes * parts;
   p.red_stride = p.U + 1;
   return p;
 }
 
-// Bytes of a stage's scale window: RB rows plus up to 15 bytes of alignment
-// slack on each side, rounded to 16.
+__host__ __device__ inline int task_parts(const M1Task& tk) { return tk.split ? 2 : 1; }
+
+// Bytes of a stage's scale window: RB rows at the task's scale pitch plus up
+// to 15 bytes of alignment slack on each side, rounded to 16.
 __host__ __device__ inline int sc_window_cap(const TaskPlan& tp) {
-  return (tp.RB * tp.sc_row_bytes + 32 + 15) & ~15;
+  return (tp.RB * tp.sc_pitch + 32 + 15) & ~15;
+}
+
+// Bytes of one W4A16 activation slot for a task of U units: per unit its 128
+// activations paired as the consumers use them (256 bytes), then one FP32
+// bias sum per unit.
+__host__ __device__ inline int xslot_bytes(int U) { return (U * 260 + 15) & ~15; }
+
+// Units the stager converts in one pass (one per lane 1..31).
+constexpr int kStagers = 31;
+
+// W4A16: whether the stager may stage task i of a list (its activations come
+// through the shared-memory slot), given whether it is the first task with
+// rows on the CTA.  SwiGLU tasks never are: their elementwise work is spread
+// over the consumer threads.  The first task is only when one pass of the
+// stager converts it: nothing runs before it to hide a longer staging.
+__host__ __device__ inline bool may_stage(const M1Task& tk, int U, bool first) {
+  return tk.x2 == nullptr && (!first || U <= kStagers);
 }
 
 // Sizes shared by every task of a launch.
 struct RingPlan {
   int stage_bytes;  // max over tasks of RB * row_bytes + scale window, 128-aligned
   int red_bytes;    // max over tasks of RB * red_stride * 4, 16-aligned
+  int xslot;        // bytes of one activation slot (W4A16 tasks the stager may stage), 16-aligned; or 0
   int CW;           // consumer warps = max over tasks of ceil(T / 32)
   int S;            // stages
   int smem;         // dynamic shared memory, bytes
 };
 
 constexpr int kXReady = 4;          // dependency-signal barriers
-constexpr int kBarrierBytes = 512;  // [full S][empty S][redfull S][redempty S][xready kXReady]
-static_assert(32 * kM1MaxStages + 8 * kXReady <= kBarrierBytes, "barriers overflow their area");
+constexpr int kXSlots = 1;          // activation slots (W4A16)
+constexpr unsigned kStagerYieldNs = 64;  // the stager's pause between pieces of work
+// [full S][empty S][redfull S][redempty S][xready kXReady][xfull kXSlots][xempty kXSlots]
+constexpr int kBarrierBytes = 512;
+static_assert(32 * kM1MaxStages + 8 * kXReady + 16 * kXSlots <= kBarrierBytes, "barriers overflow their area");
+constexpr int kPartBytes = 4 * kM1PartRows;
 
-RingPlan make_ring_plan(const int* Ks, int n, int smem_limit, int fmt = kFmtW4A16) {
+// Shared layout: barriers | K-split partial sums | xslots | S partial slots |
+// S stages (128-aligned).
+RingPlan make_ring_plan(const M1Task* tasks, int n, int smem_limit, int fmt) {
   RingPlan r{};
   for (int i = 0; i < n; ++i) {
-    const TaskPlan tp = task_plan(Ks[i], fmt);
+    const TaskPlan tp = task_plan(tasks[i].K, fmt, task_parts(tasks[i]));
     const int st = tp.RB * tp.row_bytes + sc_window_cap(tp);
     const int rb = tp.RB * tp.red_stride * 4;
     const int cw = (tp.T + 31) / 32;
+    // any task but the list's first may be some CTA's first with rows
+    const int xs = fmt == kFmtW4A16 && may_stage(tasks[i], tp.U, i == 0) ? xslot_bytes(tp.U) : 0;
     if (st > r.stage_bytes) r.stage_bytes = st;
     if (rb > r.red_bytes) r.red_bytes = rb;
     if (cw > r.CW) r.CW = cw;
+    if (xs > r.xslot) r.xslot = xs;
   }
   r.stage_bytes = (r.stage_bytes + 127) & ~127;
   r.red_bytes = (r.red_bytes + 15) & ~15;
   const int per_stage = r.stage_bytes + r.red_bytes;
-  // 128 bytes of slack: the stages start at the next 128-byte boundary
-  const int budget = (smem_limit < kM1SmemBudget ? smem_limit : kM1SmemBudget) - kBarrierBytes - 128;
+  const int fixed = kBarrierBytes + kPartBytes + kXSlots * r.xslot + 128;  // 128: stage alignment slack
+  const int budget = (smem_limit < kM1SmemBudget ? smem_limit : kM1SmemBudget) - fixed;
   r.S = budget / per_stage;
   if (r.S > kM1MaxStages) r.S = kM1MaxStages;
-  r.smem = kBarrierBytes + r.S * per_stage + 128;
+  r.smem = fixed + r.S * per_stage;
   return r;
+}
+
+// K-split of a W4A16 GEMV: two tasks over the two halves of each row's K
+// when that fills the consumer threads markedly better (K = 18944: 148
+// units use 2 x 148 = 296 of 416 threads, 74 use 5 x 74 = 370) and a CTA's
+// rows fit the partial-sum buffer.  A pure function of K, N and the grid, so
+// a GEMV is split the same way alone and inside a task list.
+int split_parts(int K, int N, int grid) {
+  const int cons = max_consumers(kFmtW4A16);
+  if (K % 256 != 0 || (N + grid - 1) / grid > kM1PartRows) return 1;
+  auto used = [&](int U) { return U >= cons ? cons : (cons / U) * U; };
+  const int U = K / 128;
+  return 10 * used(U / 2) > 11 * used(U) ? 2 : 1;
 }
 
 template <int MAXT>
 struct M1Params {
   int ntasks;
-  int S, stage_bytes, red_bytes, CW;
+  int S, stage_bytes, red_bytes, xslot, CW;
   int* done;         // per-task completion counters (null: no task has a dependency)
   uint32_t* status;  // device status word
   M1Task task[MAXT];
@@ -187,28 +250,91 @@ __device__ __forceinline__ uint4 swiglu8(uint4 g, uint4 u) {
   return make_uint4(hw[0], hw[1], hw[2], hw[3]);
 }
 
-// Dot products of two rows (8 packed words each, registers wa, wb) with this
-// thread's 64 activations.  Returns sum_k (1032 + q or 1152 + 16 q) x, the
-// second kind scaled back by 1/16, i.e. sum_k q x + C.
-__device__ __forceinline__ void dot_pair(const uint32_t (&wa)[8], const uint32_t (&wb)[8],
-                                         const XPairs (&X)[8], float& ra, float& rb) {
-  float ea0 = 0.f, ea1 = 0.f, oa0 = 0.f, oa1 = 0.f;
-  float eb0 = 0.f, eb1 = 0.f, ob0 = 0.f, ob1 = 0.f;
+// Bias sums of a W4A16 unit, C = 1032 sum x(k even) + 72 sum x(k odd) (the
+// dot product of its activations with a word of zero nibbles), in one
+// canonical order: each 4-word chunk (32 activations, words in natural
+// order) into its own even and odd sums, then the chunks in natural order.
+// Both ways of staging a unit's activations (the stager, or each consumer
+// thread for itself) use it, so a row's sum does not depend on the way.
+__device__ __forceinline__ void chunk_bias(const XPairs* q, float& e, float& o) {
+  float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const Unpacked a = unpack_biased(wa[j]);
-    const Unpacked b = unpack_biased(wb[j]);
-    fma_f32_f16x2(ea0, ea1, a.h0, X[j].p0);
-    fma_f32_f16x2(eb0, eb1, b.h0, X[j].p0);
-    fma_f32_f16x2(oa0, oa1, a.h1, X[j].p1);
-    fma_f32_f16x2(ob0, ob1, b.h1, X[j].p1);
-    fma_f32_f16x2(ea0, ea1, a.h2, X[j].p2);
-    fma_f32_f16x2(eb0, eb1, b.h2, X[j].p2);
-    fma_f32_f16x2(oa0, oa1, a.h3, X[j].p3);
-    fma_f32_f16x2(ob0, ob1, b.h3, X[j].p3);
+  for (int i = 0; i < 4; ++i) {
+    fma_f32_f16x2(e0, e1, 0x64086408u, q[i].p0);
+    fma_f32_f16x2(o0, o1, 0x64806480u, q[i].p1);
+    fma_f32_f16x2(e0, e1, 0x64086408u, q[i].p2);
+    fma_f32_f16x2(o0, o1, 0x64806480u, q[i].p3);
   }
-  ra = fmaf(0.0625f, oa0 + oa1, ea0 + ea1);
-  rb = fmaf(0.0625f, ob0 + ob1, eb0 + eb1);
+  e = e0 + e1;
+  o = o0 + o1;
+}
+__device__ __forceinline__ float unit_bias(const float (&e)[4], const float (&o)[4]) {
+  return fmaf(0.0625f, (o[0] + o[1]) + (o[2] + o[3]), (e[0] + e[1]) + (e[2] + e[3]));
+}
+
+// The stager's conversion of one W4A16 unit in shared memory: its 128 raw
+// activations at dst become pairs as dot_unit128 uses them, word w of the
+// unit (activations 8 w .. 8 w + 7) at 16-byte slot w ^ (u mod 16) of the
+// same 256 bytes (so that the consumers' rotated reads of consecutive units
+// hit distinct bank groups).  Returns the unit's bias sum.
+__device__ __forceinline__ float convert_unit128(uint32_t dst, int u) {
+  uint4 v[16];
+#pragma unroll
+  for (int w = 0; w < 16; ++w) v[w] = lds_u4(dst + 16 * w);
+  float e[4], o[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    XPairs q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int w = 4 * c + i;
+      q[i] = pair_activations(v[w]);
+      sts_u4(dst + ((w ^ (u & 15)) << 4), q[i].p0, q[i].p1, q[i].p2, q[i].p3);
+    }
+    chunk_bias(q, e[c], o[c]);
+  }
+  return unit_bias(e, o);
+}
+
+// x[(c - f) mod 4] for c = 0..3 (a runtime rotation of four registers).
+__device__ __forceinline__ void unrotate4(const float (&x)[4], int f, float (&out)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int j = (c - f) & 3;
+    out[c] = j == 0 ? x[0] : (j == 1 ? x[1] : (j == 2 ? x[2] : x[3]));
+  }
+}
+
+// The 16 packed words of one row's 128-k unit at a stage address: four
+// 16-byte shared loads, chunk (j + f) mod 4 into words 4j .. 4j + 3.
+__device__ __forceinline__ void load_unit128(uint32_t addr, int f, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 v = lds_u4(addr + 16 * ((j + f) & 3));
+    w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+  }
+}
+
+// Dot product of one row's 128-k unit (16 packed words) with this thread's
+// 128 activations: sum_k (1032 + q or 1152 + 16 q) x, the second kind scaled
+// back by 1/16, i.e. sum_k q x + C.
+__device__ __forceinline__ float dot_unit128(const uint32_t (&w)[16], const XPairs (&X)[16]) {
+  float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;
+  float e2 = 0.f, e3 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const Unpacked a = unpack_biased(w[j]);
+    const Unpacked b = unpack_biased(w[j + 1]);
+    fma_f32_f16x2(e0, e1, a.h0, X[j].p0);
+    fma_f32_f16x2(e2, e3, b.h0, X[j + 1].p0);
+    fma_f32_f16x2(o0, o1, a.h1, X[j].p1);
+    fma_f32_f16x2(o2, o3, b.h1, X[j + 1].p1);
+    fma_f32_f16x2(e0, e1, a.h2, X[j].p2);
+    fma_f32_f16x2(e2, e3, b.h2, X[j + 1].p2);
+    fma_f32_f16x2(o0, o1, a.h3, X[j].p3);
+    fma_f32_f16x2(o2, o3, b.h3, X[j + 1].p3);
+  }
+  return fmaf(0.0625f, (o0 + o1) + (o2 + o3), (e0 + e1) + (e2 + e3));
 }
 
 // W4A8: integer dot products of two rows (8 packed words each) with this
@@ -304,21 +430,29 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     gemv_m1_kernel(const __grid_constant__ M1Params<MAXT> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = p.S;
-  // shared layout: barriers | S partial slots of red_bytes | S stages of
-  // stage_bytes (128-aligned).  All hot accesses use 32-bit shared addresses.
+  constexpr int CW0 = first_consumer_warp(kFmt);
+  // shared layout: barriers | K-split row sums | activation slots (W4A16) |
+  // S partial slots of red_bytes | S stages of stage_bytes (128-aligned).
+  // All hot accesses use 32-bit shared addresses.
   //   full[s]      producer -> consumers: the tile's bytes landed (tx count)
   //   empty[s]     consumers -> producer: the stage may be refilled
   //   redfull[s]   consumers -> reducer: the tile's partial sums are written
   //   redempty[s]  reducer -> consumers: partial slot s may be rewritten
-  //   xready[4]    reducer -> consumers: a dependent task's input is
-  //                complete (a ring of kXReady barriers, so the reducer may
-  //                signal up to kXReady - 1 dependent tasks ahead)
+  //   xready[4]    reducer -> stager (W4A16) or consumers: a dependent task's
+  //                input is complete (a ring of kXReady barriers, so the
+  //                reducer may signal up to kXReady - 1 dependent tasks ahead)
+  //   xfull[2]     stager -> consumers: activation slot written (W4A16)
+  //   xempty[2]    consumers -> stager: activation slot read (W4A16)
   const uint32_t full0 = smem_addr(smem);
   const uint32_t empty0 = full0 + 8 * S;
   const uint32_t redfull0 = full0 + 16 * S;
   const uint32_t redempty0 = full0 + 24 * S;
   const uint32_t xready0 = full0 + 32 * S;
-  const uint32_t red0 = full0 + kBarrierBytes;
+  const uint32_t xfull0 = xready0 + 8 * kXReady;
+  const uint32_t xempty0 = xfull0 + 8 * kXSlots;
+  const uint32_t part0 = full0 + kBarrierBytes;
+  const uint32_t xslot0 = part0 + kPartBytes;
+  const uint32_t red0 = xslot0 + kXSlots * p.xslot;
   const uint32_t stage0 = (red0 + S * p.red_bytes + 127) & ~127u;
 
   const int tid = threadIdx.x;
@@ -333,12 +467,24 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       mbar_init(redempty0 + 8 * s, 1);
     }
     for (int b = 0; b < kXReady; ++b) mbar_init(xready0 + 8 * b, 1);
+    for (int b = 0; b < kXSlots; ++b) {
+      mbar_init(xfull0 + 8 * b, 1);
+      mbar_init(xempty0 + 8 * b, p.CW);
+    }
     fence_barrier_init();
   }
   __syncthreads();
   pdl_launch_dependents();
 
-  if (warp == 0) {
+  // W4A16: whether task i's activations come through the stager's slot
+  // (may_stage) or each consumer thread loads its own
+  int first_task = 0;
+  while (first_task < p.ntasks && !cta_has_rows(p.task[first_task])) ++first_task;
+  auto staged = [&](const M1Task& tk, int i) {
+    return kFmt == kFmtW4A16 && may_stage(tk, tk.K / unit_k(kFmt), i == first_task);
+  };
+
+  if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
     int s = 0, g = 0;  // stage, tiles issued so far (all tasks)
@@ -347,14 +493,17 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     bool ok = true;
     for (int i = 0; i < p.ntasks && ok; ++i) {
       const M1Task& tk = p.task[i];
-      const TaskPlan tp = task_plan(tk.K, kFmt);
+      const TaskPlan tp = task_plan(tk.K, kFmt, task_parts(tk));
       int64_t row_begin;
       const int rows = cta_rows(tk, &row_begin);
       const int ntiles = (rows + tp.RB - 1) / tp.RB;
-      const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(tk.qweight) + row_begin * tp.row_bytes;
+      const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(tk.qweight) + row_begin * tp.pitch;
+      // the task's scales: rows sc_pitch apart from its first one; the buffer
+      // they sit in ends N rows after its start (a second half starts
+      // sc_row_bytes into it)
       const uint8_t* scb = reinterpret_cast<const uint8_t*>(tk.scales);
-      const int64_t sc_total = static_cast<int64_t>(tk.N) * tp.sc_row_bytes;
-      int64_t sb0 = row_begin * tp.sc_row_bytes;  // first scale byte of the tile
+      const uintptr_t sc_end = reinterpret_cast<uintptr_t>(scb) - (tk.split == 2 ? tp.sc_row_bytes : 0) +
+                               static_cast<uintptr_t>(tk.N) * tp.sc_pitch;
       for (int t = 0; t < ntiles; ++t) {
         // stage s still holds tile g - S until every consumer warp is done with it
         if (g >= S && !mbar_wait_bounded(empty0 + 8 * s, phase ^ 1u, kWaitLimitNs)) {
@@ -363,27 +512,31 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         }
         const int lr0 = t * tp.RB;
         const int nr = rows - lr0 < tp.RB ? rows - lr0 : tp.RB;
-        const int64_t sb1 = sb0 + static_cast<int64_t>(nr) * tp.sc_row_bytes;
-        const int64_t a = sb0 & ~int64_t(15);
-        int64_t e = (sb1 + 15) & ~int64_t(15);
-        if (e > sc_total) e = sc_total & ~int64_t(15);  // never read past the buffer
-        const int64_t ecopy = e > a ? e : a;
+        // scale window: from the tile's first scale byte to past its last,
+        // widened to 16-byte boundaries but never past the buffer
+        const uintptr_t f = reinterpret_cast<uintptr_t>(scb) + static_cast<uintptr_t>(row_begin + lr0) * tp.sc_pitch;
+        const uintptr_t l = f + static_cast<uintptr_t>(nr - 1) * tp.sc_pitch + tp.sc_row_bytes;
+        const uintptr_t a = f & ~uintptr_t(15);
+        uintptr_t e = (l + 15) & ~uintptr_t(15);
+        if (e > sc_end) e = sc_end & ~uintptr_t(15);
+        const uintptr_t ecopy = e > a ? e : a;
         const uint32_t scw = base + tp.RB * tp.row_bytes;
         const uint32_t bar = full0 + 8 * s;
-        if (lane == 0) {
-          // the last few scale bytes of the matrix, where the aligned copy stops short
-          for (int64_t b = ecopy; b < sb1; b += 2)
-            sts_u16(scw + static_cast<uint32_t>(b - a), ld_nc_u16(scb + b));
-          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * tp.row_bytes + (ecopy - a)));
+        // the last few scale bytes of the matrix, where the aligned copy stops short
+        for (uintptr_t b = ecopy; b < l; b += 2)
+          sts_u16(scw + static_cast<uint32_t>(b - a), ld_nc_u16(reinterpret_cast<const void*>(b)));
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * tp.row_bytes + (ecopy - a)));
+        if (tk.split) {
+          // a half of each row: one copy per row
+          for (int r = 0; r < nr; ++r)
+            bulk_g2s(base + r * tp.row_bytes, wsrc + static_cast<int64_t>(lr0 + r) * tp.pitch,
+                     static_cast<uint32_t>(tp.row_bytes), bar, pol);
+        } else {
+          // consecutive rows are contiguous in memory: one copy for the whole tile
+          bulk_g2s(base, wsrc + static_cast<int64_t>(lr0) * tp.row_bytes, static_cast<uint32_t>(nr * tp.row_bytes),
+                   bar, pol);
         }
-        __syncwarp();
-        // consecutive rows are contiguous in memory: one copy for the whole tile
-        if (lane == 0)
-          bulk_g2s(base, wsrc + static_cast<int64_t>(lr0) * tp.row_bytes,
-                   static_cast<uint32_t>(nr * tp.row_bytes), bar, pol);
-        if (lane == 1 && ecopy > a)
-          bulk_g2s(scw, scb + a, static_cast<uint32_t>(ecopy - a), bar, pol);
-        sb0 = sb1;
+        if (ecopy > a) bulk_g2s(scw, reinterpret_cast<const void*>(a), static_cast<uint32_t>(ecopy - a), bar, pol);
         ++g;
         base += p.stage_bytes;
         if (++s == S) {
@@ -394,7 +547,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       }
     }
     if (!ok) {
-      if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+      atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
       // let the copies in flight land before the CTA exits: the last S tiles
       // issued sit in stages s, s + 1, ... (mod S)
       for (int v = 0; v < S; ++v) {
@@ -405,21 +558,82 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     return;
   }
 
+  if (warp == 0) {
+    // ------------------------------------------------------------ stager
+    // Lanes 1..31 of the producer's warp (W4A16; idle for the other
+    // formats): the activations of each task it stages (may_stage), one task
+    // ahead of the consumers (the slot is refilled once they have read it).
+    // After the task's dependency signal, the raw activations come in with
+    // 16-byte asynchronous copies from every lane at once (through L2: the
+    // reducer's acquire made the other CTAs' writes visible), then each unit
+    // is paired in place and its bias sum stored.
+    if (kFmt != kFmtW4A16) return;
+    constexpr unsigned kStagerMask = 0xFFFFFFFEu;  // lanes 1..31
+    const int sl0 = lane - 1;
+    pdl_wait();  // x may be the previous kernel's output
+    int n = 0, nw = 0;  // slot uses, dependency signals waited on
+    const uint16_t* xprev = nullptr;
+    int kprev = 0;
+    for (int i = 0; i < p.ntasks; ++i) {
+      const M1Task& tk = p.task[i];
+      if (!cta_has_rows(tk)) continue;
+      const TaskPlan tp = task_plan(tk.K, kFmt, task_parts(tk));
+      if (tk.dep >= 0 && p.done != nullptr) {
+        // every dependent task's signal, in order, staged here or not
+        if (!mbar_wait_bounded(xready0 + 8 * (nw % kXReady), (nw / kXReady) & 1, kWaitLimitNs)) {
+          if (lane == 1) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+          return;
+        }
+        ++nw;
+      }
+      if (!staged(tk, i)) continue;
+      const int sl = n % kXSlots;
+      if (n >= kXSlots && !mbar_wait_bounded(xempty0 + 8 * sl, ((n / kXSlots) - 1) & 1, kWaitLimitNs)) {
+        if (lane == 1) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+        return;
+      }
+      const uint32_t xs = xslot0 + sl * p.xslot;
+      // the slot already holds these activations (the previous task staged
+      // here read the same vector over the same K): keep it
+      const bool same = n > 0 && tk.x == xprev && tk.K == kprev;
+      xprev = tk.x;
+      kprev = tk.K;
+      if (!same) {
+        const int chunks = tp.U * 16;  // 16-byte chunks of the task's activations
+        for (int q = sl0; q < chunks; q += kStagers) cp_async_16(xs + 16 * q, tk.x + 8 * q);
+        cp_async_wait_all();
+        __syncwarp(kStagerMask);
+        // the producer shares this warp: after the launch's first task, a
+        // short sleep after each unit lets its lane issue the next weight
+        // copies
+        const bool yield = i != first_task;
+        for (int u = sl0; u < tp.U; u += kStagers) {
+          sts_f32(xs + tp.U * 256 + 4 * u, convert_unit128(xs + u * 256, u));
+          if (yield) __nanosleep(kStagerYieldNs);
+        }
+        __syncwarp(kStagerMask);
+      }
+      if (lane == 1) mbar_arrive(xfull0 + 8 * sl);
+      ++n;
+    }
+    return;
+  }
+
   if (warp == 1) {
     // ------------------------------------------------------------ reducer
     pdl_wait();  // y may still be read by the previous kernel on the stream
     int s = 0;
     uint32_t phase = 0;
     uint32_t rs = red0;
-    // Consumers start a task that reads task dep's output once every CTA has
-    // published dep.  The reducer checks (acquire) and tells them (release),
-    // the n-th such task with rows here on xready[n % kXReady], in task
-    // order.  At the start of task i it signals, ahead of time, every next
-    // such task whose producer is older than i (so this CTA has published
-    // it), up to kXReady - 1 signals beyond what the consumers have used;
-    // the polls of one batch run in parallel lanes.  In an interleaved layer
-    // sequence a dependent task is signalled a few tasks early, off the
-    // consumers' path.
+    // A task that reads task dep's output starts once every CTA has
+    // published dep.  The reducer checks (acquire) and tells the stager
+    // (W4A16) or the consumers (release), the n-th such task with rows here
+    // on xready[n % kXReady], in task order.  At the start of task i it
+    // signals, ahead of time, every next such task whose producer is older
+    // than i (so this CTA has published it), up to kXReady - 1 signals beyond
+    // what has been used; the polls of one batch run in parallel lanes.  In
+    // an interleaved layer sequence a dependent task is signalled a few tasks
+    // early, off the consumers' path.
     int nsig = 0;    // signals sent
     int nused = 0;   // dependent tasks with rows here before task i (consumed)
     int jnext = 0;   // next task that may need a signal
@@ -428,7 +642,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     };
     for (int i = 0; i < p.ntasks; ++i) {
       const M1Task& tk = p.task[i];
-      const TaskPlan tp = task_plan(tk.K, kFmt);
+      const TaskPlan tp = task_plan(tk.K, kFmt, task_parts(tk));
       int64_t row_begin;
       const int rows = cta_rows(tk, &row_begin);
       const int ntiles = (rows + tp.RB - 1) / tp.RB;
@@ -495,18 +709,24 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
           }
           float sum = (s0 + s1) + (s2 + s3);
           for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-          if (part == 0 && row < nr)
-          {
-            // y[n] = fp16_RN(sum + bias), routed to n's segment
-            const int64_t n = row_begin + lr0 + row;
-            const int seg = n < e0 ? 0 : (n < e1 ? 1 : 2);
-            const int64_t j = seg == 0 ? n : (seg == 1 ? n - e0 : n - e1);
-            if (has_bias) {
-              const uint16_t* b = seg == 0 ? b0 : (seg == 1 ? b1 : b2);
-              if (b != nullptr) sum += __half2float(__ushort_as_half(__ldg(b + j)));
+          if (part == 0 && row < nr) {
+            const uint32_t pa = part0 + 4 * static_cast<uint32_t>(lr0 + row);
+            if (tk.split == 1) {
+              // the first half of a K-split row: kept for the second half
+              sts_f32(pa, sum);
+            } else {
+              // y[n] = fp16_RN(first half + sum + bias), routed to n's segment
+              if (tk.split == 2) sum = lds_f32(pa) + sum;
+              const int64_t n = row_begin + lr0 + row;
+              const int seg = n < e0 ? 0 : (n < e1 ? 1 : 2);
+              const int64_t j = seg == 0 ? n : (seg == 1 ? n - e0 : n - e1);
+              if (has_bias) {
+                const uint16_t* b = seg == 0 ? b0 : (seg == 1 ? b1 : b2);
+                if (b != nullptr) sum += __half2float(__ushort_as_half(__ldg(b + j)));
+              }
+              uint16_t* y = seg == 0 ? y0 : (seg == 1 ? y1 : y2);
+              y[j] = __half_as_ushort(__float2half_rn(sum));
             }
-            uint16_t* y = seg == 0 ? y0 : (seg == 1 ? y1 : y2);
-            y[j] = __half_as_ushort(__float2half_rn(sum));
           }
         }
         __syncwarp();
@@ -529,50 +749,117 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  const int c = tid - 64;
-  const int cw = warp - 2;
+  const int c = tid - 32 * CW0;
+  const int cw = warp - CW0;
   pdl_wait();  // x may be the previous kernel's output
   int s = 0, g = 0;  // stage, tiles consumed so far (all tasks)
   uint32_t phase = 0;
-  int nwait = 0;  // dependent tasks with rows here waited on so far
+  int nwait = 0;  // dependent tasks with rows here so far (the next one's signal index)
+  int nx = 0;     // activation slots used (W4A16)
   uint32_t base = stage0, rs = red0;
   for (int i = 0; i < p.ntasks; ++i) {
     const M1Task& tk = p.task[i];
-    const TaskPlan tp = task_plan(tk.K, kFmt);
+    const TaskPlan tp = task_plan(tk.K, kFmt, task_parts(tk));
     int64_t row_begin;
     const int rows = cta_rows(tk, &row_begin);
     const int ntiles = (rows + tp.RB - 1) / tp.RB;
     if (ntiles == 0) continue;
-    if (tk.dep >= 0 && p.done != nullptr) {
-      if (!mbar_wait_bounded(xready0 + 8 * (nwait % kXReady), (nwait / kXReady) & 1, kWaitLimitNs)) {
-        if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
-        return;
-      }
-      ++nwait;
-    }
 
-    // Consecutive threads take consecutive 64-k units of one row, so a warp
-    // reads 32 x 32 contiguous bytes of a stage; threads whose unit index has
-    // bit 2 set read their two 16-byte chunks in the opposite order, which
-    // puts every quarter-warp phase of the 16-byte shared loads on 8
-    // distinct bank groups.  Threads past T (in a partly used warp) compute
-    // on unit 0 of row 0 and store nothing; wholly unused warps only keep
-    // the barrier counts.
+    // Consecutive threads take consecutive units of one row, so a warp reads
+    // 32 units' contiguous bytes of a stage.  The 16-byte chunks of a unit
+    // are read in a rotated order so that every quarter-warp phase of the
+    // 16-byte shared loads touches 8 distinct bank groups (except where the
+    // quarter-warp spans two rows): W4A16 (four chunks of a 64-byte unit)
+    // starts at chunk f = (u / 2) mod 4; the 64-k formats (two chunks of a
+    // 32-byte unit) swap them when bit 2 of the unit is set.  The order is a
+    // function of the unit alone, so a row's sum is the same whichever
+    // thread and CTA compute it.  Threads past T (in a partly used warp)
+    // compute on unit 0 of row 0 and store nothing; wholly unused warps only
+    // keep the barrier counts.
+    constexpr int kR = rows_per_thread(kFmt);
     const bool wact = cw * 32 < tp.T;
     const bool active = c < tp.T;
     const int u = active ? c % tp.U : 0;
     const int rl = active ? c / tp.U : 0;
     const int rot = ((u >> 2) & 1) * 16;
+    const int f = (u >> 1) & 3;
 
-    // this thread's 64 activations, paired to match the unpacked lanes
-    XPairs X[8];
+    // this thread's activations (W4A16: 128, else 64), paired to match the
+    // unpacked lanes
+    XPairs X[kFmt == kFmtW4A16 ? 16 : 8];
     float C = 0.f;
+    // the index of this task's dependency signal (every dependent task with
+    // rows here has one, in order)
+    const int sig = tk.dep >= 0 && p.done != nullptr ? nwait++ : -1;
+    if constexpr (kFmt == kFmtW4A16) if (!staged(tk, i)) {
+      // this thread's own 128 activations (or their SwiGLU), loaded from
+      // global memory: X[4 j + i] pairs with word 4 ((j + f) mod 4) + i of
+      // the unit, the order in which the tiles' words are read.  Plain loads
+      // through L1: x of a dependent task is read after the reducer's
+      // acquire.
+      if (sig >= 0 && !mbar_wait_bounded(xready0 + 8 * (sig % kXReady), (sig / kXReady) & 1, kWaitLimitNs)) {
+        if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+        return;
+      }
+      if (wact) {
+        const uint16_t* xp = tk.x + u * 128;
+        const uint16_t* x2p = kAct && tk.x2 != nullptr ? tk.x2 + u * 128 : nullptr;
+        float es[4], os[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ch = (j + f) & 3;
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            uint4 v = ld_u4(xp + 32 * ch + 8 * i4);
+            if (kAct && x2p != nullptr) v = swiglu8(v, ld_u4(x2p + 32 * ch + 8 * i4));
+            X[4 * j + i4] = pair_activations(v);
+          }
+          chunk_bias(&X[4 * j], es[j], os[j]);
+        }
+        float e[4], o[4];
+        unrotate4(es, f, e);
+        unrotate4(os, f, o);
+        C = unit_bias(e, o);
+      }
+    } else {
+      // from the stager's slot: X[4 j + i] pairs with word 4 ((j + f) mod 4) + i
+      // of the unit, the order in which the tiles' words are read
+      const int sl = nx % kXSlots;
+      if (!mbar_wait_bounded(xfull0 + 8 * sl, (nx / kXSlots) & 1, kWaitLimitNs)) {
+        if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+        return;
+      }
+      const uint32_t xs = xslot0 + sl * p.xslot;
+      if (wact) {
+        const uint32_t xu = xs + u * 256;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int w0 = 4 * ((j + f) & 3);
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            const uint4 v = lds_u4(xu + (((w0 + i4) ^ (u & 15)) << 4));
+            X[4 * j + i4] = XPairs{v.x, v.y, v.z, v.w};
+          }
+        }
+        C = lds_f32(xs + tp.U * 256 + 4 * u);
+      }
+      // the slot's values are in registers once these reads are issued
+      // (release order): the stager may refill it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xempty0 + 8 * sl);
+      ++nx;
+    }
+    if (kFmt != kFmtW4A16 && sig >= 0 &&
+        !mbar_wait_bounded(xready0 + 8 * (sig % kXReady), (sig / kXReady) & 1, kWaitLimitNs)) {
+      if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
+      return;
+    }
     // W4A8: the unit's int8 codes (even / odd k of each word as 4 bytes), 8
     // times their sum, and the unit's activation scale
     uint32_t xe[8], xo[8];
     int C8 = 0;
     float s_act = 0.f;
-    if (kFmt == kFmtW4A8 && wact) {
+    if constexpr (kFmt == kFmtW4A8) if (wact) {
       const uint16_t* xp = tk.x + u * 64;
       uint4 v[8];
 #pragma unroll
@@ -618,7 +905,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     }
     // Q4_K: the pairs above and the two 32-activation sums
     float S0 = 0.f, S1 = 0.f;
-    if (kFmt == kFmtQ4K && wact) {
+    if constexpr (kFmt == kFmtQ4K) if (wact) {
       const uint4* xp = reinterpret_cast<const uint4*>(tk.x + u * 64);
       uint4 v[8];
 #pragma unroll
@@ -636,43 +923,27 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         S1 += (half_lo(ha) + half_hi(ha)) + (half_lo(hb) + half_hi(hb));
       }
     }
-    if (kFmt == kFmtW4A16 && wact) {
-      const uint16_t* xp = tk.x + u * 64;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        // X[j] pairs with the j-th word as this thread loads them: with the
-        // chunk order rotated, words 4..7 come first
-        const int jj = rot ? (j ^ 4) : j;
-        // plain loads through L1: x of a dependent task is read after the
-        // reducer's acquire, and the line may have been prefetched (below)
-        uint4 v = ld_u4(xp + 8 * jj);
-        if (kAct && tk.x2 != nullptr) v = swiglu8(v, ld_u4(tk.x2 + u * 64 + 8 * jj));
-        X[j] = pair_activations(v);
-        const float even = (half_lo(X[j].p0) + half_hi(X[j].p0)) + (half_lo(X[j].p2) + half_hi(X[j].p2));
-        const float odd = (half_lo(X[j].p1) + half_hi(X[j].p1)) + (half_lo(X[j].p3) + half_hi(X[j].p3));
-        C = fmaf(1032.f, even, fmaf(72.f, odd, C));
-      }
-    }
-
     // per-thread offsets inside a stage and a partial slot: rows rl + r RL
-    const int w_off = rl * tp.row_bytes + u * 32;
+    const int w_off = rl * tp.row_bytes + u * (unit_k(kFmt) / 2);
     const int w_row_step = tp.RL * tp.row_bytes;
-    const int sc_off = tp.RB * tp.row_bytes + rl * tp.sc_row_bytes + (u >> 1) * 2;
-    const int sc_row_step = tp.RL * tp.sc_row_bytes;
+    const int sc_off = tp.RB * tp.row_bytes + rl * tp.sc_pitch + (kFmt == kFmtW4A16 ? u : (u >> 1)) * 2;
+    const int sc_row_step = tp.RL * tp.sc_pitch;
     const int red_off = 4 * (rl * tp.red_stride + u);
     const int red_row_step = 4 * tp.RL * tp.red_stride;
-    const int sc_tile_step = tp.RB * tp.sc_row_bytes;
-    int sc_lo = static_cast<int>((row_begin * tp.sc_row_bytes) & 15);  // window offset of the tile
+    const int sc_tile_step = tp.RB * tp.sc_pitch;
+    // offset of the tile's first scale byte in its 16-byte-aligned window
+    int sc_lo = static_cast<int>((reinterpret_cast<uintptr_t>(tk.scales) + row_begin * tp.sc_pitch) & 15);
 
-    // The next task with rows here: its activations go to L1 ahead of time,
-    // one 128-byte line per thread (K / 64 lines), right away when it reads
-    // nothing written in this launch, else once its signal has arrived.
+    // 64-k formats: the next task with rows here has its activations go to
+    // L1 ahead of time, one 128-byte line per thread (K / 64 lines), right
+    // away when it reads nothing written in this launch, else once its
+    // signal has arrived (W4A16: the stager loads them).
     int inext = i + 1;
     while (inext < p.ntasks && !cta_has_rows(p.task[inext])) ++inext;
     const uint16_t* xnext = nullptr;
     bool pending = false;
     const uint16_t* x2next = nullptr;
-    if (inext < p.ntasks && c < (p.task[inext].K >> 6)) {
+    if (kFmt != kFmtW4A16 && inext < p.ntasks && c < (p.task[inext].K >> 6)) {
       xnext = p.task[inext].x + c * 64;
       if (kAct && p.task[inext].x2 != nullptr) x2next = p.task[inext].x2 + c * 64;
       if (p.task[inext].dep < 0 || p.done == nullptr) {
@@ -694,8 +965,11 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         if (kAct && x2next != nullptr) prefetch_l1(x2next);
         pending = false;
       }
-      float res[kRR];
-      if (kFmt == kFmtQ4K && wact) {
+      float res[kR];
+      if (!wact) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      } else if constexpr (kFmt == kFmtQ4K) {
         // rows rl + r RL: the unit's block header and 32 code bytes
         const uint32_t ua = base + rl * tp.row_bytes + (u >> 2) * 144;
         const int cc = u & 3;
@@ -705,12 +979,12 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         uint32_t q[8];
         float D0, D1;
 #pragma unroll
-        for (int r = 0; r < kRR; ++r) {
+        for (int r = 0; r < kR; ++r) {
           const uint32_t ra = ua + r * w_row_step;
           h[r & 1] = lds_u4(ra);
           qa = lds_u4(ra + 16 + 32 * cc);
           qb = lds_u4(ra + 32 + 32 * cc);
-          if (r == kRR - 1) {
+          if (r == kR - 1) {
             // the last reads of the stage are issued: release it
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -720,44 +994,44 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
           q4k_dot(q, X, D0, D1);
           res[r] = q4k_combine(h[r & 1], selp, selq, hi, D0, D1, S0, S1);
         }
-      } else if (kFmt != kFmtQ4K && wact) {
+      } else if constexpr (kFmt == kFmtW4A16) {
+        // rows rl and rl + RL: one scale and 16 words each.  The second row
+        // is skipped by a warp none of whose threads has it in this tile (a
+        // tile's last rows).
         const uint32_t sa = base + sc_off + sc_lo;
-        float sc[kRR];
+        const uint32_t wa = base + w_off;
+        const float sc0 = __half2float(__ushort_as_half(lds_u16(sa)));
+        const float sc1 = __half2float(__ushort_as_half(lds_u16(sa + sc_row_step)));
+        uint32_t w[16];
+        load_unit128(wa, f, w);
+        res[0] = (dot_unit128(w, X) - C) * sc0;
+        const bool any1 = __any_sync(0xffffffffu, active && rl + tp.RL < nr);
+        if (any1) load_unit128(wa + w_row_step, f, w);
+        // the last reads of the stage are issued: release it (release order)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        res[1] = any1 ? (dot_unit128(w, X) - C) * sc1 : 0.f;
+      } else {
+        const uint32_t sa = base + sc_off + sc_lo;
+        float sc[kR];
 #pragma unroll
-        for (int r = 0; r < kRR; ++r) sc[r] = __half2float(__ushort_as_half(lds_u16(sa + r * sc_row_step)));
+        for (int r = 0; r < kR; ++r) sc[r] = __half2float(__ushort_as_half(lds_u16(sa + r * sc_row_step)));
         const uint32_t wa = base + w_off;
         uint32_t w0[8], w1[8];
-        float d0, d1;
         load_row(wa, rot, w0);
         load_row(wa + w_row_step, rot, w1);
-        if (kFmt == kFmtW4A8) {
-          int i0, i1;
-          dot_pair_a8(w0, w1, xe, xo, i0, i1);
-          res[0] = static_cast<float>(i0 - C8) * (sc[0] * s_act);
-          res[1] = static_cast<float>(i1 - C8) * (sc[1] * s_act);
-        } else {
-          dot_pair(w0, w1, X, d0, d1);
-          res[0] = (d0 - C) * sc[0];
-          res[1] = (d1 - C) * sc[1];
-        }
+        int i0, i1;
+        dot_pair_a8(w0, w1, xe, xo, i0, i1);
+        res[0] = static_cast<float>(i0 - C8) * (sc[0] * s_act);
+        res[1] = static_cast<float>(i1 - C8) * (sc[1] * s_act);
         load_row(wa + 2 * w_row_step, rot, w0);
         load_row(wa + 3 * w_row_step, rot, w1);
         // the last reads of the stage are issued: release it (release order)
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
-        if (kFmt == kFmtW4A8) {
-          int i0, i1;
-          dot_pair_a8(w0, w1, xe, xo, i0, i1);
-          res[2] = static_cast<float>(i0 - C8) * (sc[2] * s_act);
-          res[3] = static_cast<float>(i1 - C8) * (sc[3] * s_act);
-        } else {
-          dot_pair(w0, w1, X, d0, d1);
-          res[2] = (d0 - C) * sc[2];
-          res[3] = (d1 - C) * sc[3];
-        }
-      } else {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        dot_pair_a8(w0, w1, xe, xo, i0, i1);
+        res[2] = static_cast<float>(i0 - C8) * (sc[2] * s_act);
+        res[3] = static_cast<float>(i1 - C8) * (sc[3] * s_act);
       }
       // partial slot s still holds tile g - S until the reducer has read it
       if (g >= S && !mbar_wait_bounded(redempty0 + 8 * s, phase ^ 1u, kWaitLimitNs)) {
@@ -766,7 +1040,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       }
       if (active) {
 #pragma unroll
-        for (int r = 0; r < kRR; ++r)
+        for (int r = 0; r < kR; ++r)
           if (rl + r * tp.RL < nr) sts_f32(rs + red_off + r * red_row_step, res[r]);
       }
       __syncwarp();
@@ -790,33 +1064,54 @@ cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, 
                          cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(64 + rp.CW * 32);
+  cfg.blockDim = dim3(32 * (first_consumer_warp(fmt) + rp.CW));
   cfg.dynamicSmemBytes = rp.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (p.done != nullptr) {
+    // CTAs wait on each other's completion counters: the launch must make
+    // every CTA resident at once, or fail (e.g. when fewer SMs are free)
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   cudaError_t e;
   if constexpr (MAXT == 1) {
     // Q4_K runs as a single task without an activation epilogue
-    if (fmt == kFmtQ4K) {
-      if (act) return cudaErrorInvalidValue;
-      e = cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, kFmtQ4K>, p);
-      if (e != cudaSuccess) return e;
-      return cudaGetLastError();
-    }
+    if (fmt != kFmtQ4K || act) return cudaErrorInvalidValue;
+    e = cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, kFmtQ4K>, p);
+  } else {
+    if (fmt == kFmtQ4K) return cudaErrorInvalidValue;
+    if (fmt == kFmtW4A8)
+      e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, kFmtW4A8>, p)
+              : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, kFmtW4A8>, p);
+    else
+      e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, kFmtW4A16>, p)
+              : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, kFmtW4A16>, p);
   }
-  if (fmt == kFmtQ4K) return cudaErrorInvalidValue;
-  if (fmt == kFmtW4A8)
-    e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, kFmtW4A8>, p)
-            : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, kFmtW4A8>, p);
-  else
-    e = act ? cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, true, kFmtW4A16>, p)
-            : cudaLaunchKernelEx(&cfg, gemv_m1_kernel<MAXT, false, kFmtW4A16>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Shared checks and plan of a task list; fills the launch fields of p.
+template <int MAXT>
+bool plan_tasks(M1Params<MAXT>& p, const M1Task* tasks, int ntasks, int fmt, const DeviceInfo& d, RingPlan* rp) {
+  *rp = make_ring_plan(tasks, ntasks, d.max_smem_optin, fmt);
+  if (rp->S < 2) return false;
+  p.S = rp->S;
+  p.stage_bytes = rp->stage_bytes;
+  p.red_bytes = rp->red_bytes;
+  p.xslot = rp->xslot;
+  p.CW = rp->CW;
+  return true;
 }
 
 }  // namespace
@@ -825,34 +1120,51 @@ bool gemv_m1_supported(int K) {
   return K > 0 && K % 128 == 0 && K / 64 <= kM1MaxConsumers;
 }
 
+int gemv_m1_split_tasks(const M1Task& t, bool a8, const DeviceInfo& d, M1Task* out) {
+  out[0] = t;
+  out[0].split = 0;
+  if (a8 || split_parts(t.K, t.N, d.sms) == 1) return 1;
+  const int h = t.K / 2;
+  out[0].K = h;
+  out[0].split = 1;
+  out[0].publish = 0;
+  out[1] = t;
+  out[1].K = h;
+  out[1].split = 2;
+  out[1].qweight = t.qweight + h / 8;
+  out[1].scales = t.scales + h / 128;
+  out[1].x = t.x + h;
+  out[1].x2 = t.x2 != nullptr ? t.x2 + h : nullptr;
+  return 2;
+}
+
 cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
   if (!gemv_m1_supported(a.K) || a.M != 1) return cudaErrorInvalidValue;
-  M1Params<1> p{};
-  p.ntasks = 1;
+  M1Task t{};
+  t.qweight = a.qweight;
+  t.scales = a.scales;
+  t.x = a.x;
+  t.N = a.N;
+  t.K = a.K;
+  t.x2 = nullptr;
+  t.nseg = static_cast<uint8_t>(a.nseg);
+  t.dep = -1;
+  t.publish = 0;
+  for (int s = 0; s < kMaxSegs; ++s) t.seg[s] = M1Seg{a.seg[s].y, a.seg[s].bias, a.seg[s].n_end};
+  M1Params<2> p{};
+  p.ntasks = gemv_m1_split_tasks(t, a.a8, d, p.task);
   p.done = nullptr;
   p.status = a.status;
-  M1Task& tk = p.task[0];
-  tk.qweight = a.qweight;
-  tk.scales = a.scales;
-  tk.x = a.x;
-  tk.N = a.N;
-  tk.K = a.K;
-  tk.x2 = nullptr;
-  tk.nseg = a.nseg;
-  tk.dep = -1;
-  tk.publish = 0;
-  for (int s = 0; s < kMaxSegs; ++s) tk.seg[s] = M1Seg{a.seg[s].y, a.seg[s].bias, a.seg[s].n_end};
   // no dependency counting: CTAs beyond N would have no rows
   const int grid = a.N < d.sms ? a.N : d.sms;
-  tk.rq = a.N / grid;
-  tk.rr = a.N % grid;
-  const RingPlan rp = make_ring_plan(&a.K, 1, d.max_smem_optin);
-  if (rp.S < 2) return cudaErrorInvalidConfiguration;
-  p.S = rp.S;
-  p.stage_bytes = rp.stage_bytes;
-  p.red_bytes = rp.red_bytes;
-  p.CW = rp.CW;
-  return launch_tasks(p, rp, grid, a.pdl, false, a.a8 ? kFmtW4A8 : kFmtW4A16, st);
+  for (int i = 0; i < p.ntasks; ++i) {
+    p.task[i].rq = a.N / grid;
+    p.task[i].rr = a.N % grid;
+  }
+  const int fmt = a.a8 ? kFmtW4A8 : kFmtW4A16;
+  RingPlan rp;
+  if (!plan_tasks(p, p.task, p.ntasks, fmt, d, &rp)) return cudaErrorInvalidConfiguration;
+  return launch_tasks(p, rp, grid, a.pdl, false, fmt, st);
 }
 
 bool gemv_m1_q4k_supported(int K) {
@@ -876,33 +1188,35 @@ cudaError_t launch_gemv_m1_q4k(const uint8_t* blocks, const uint16_t* x, uint16_
   tk.nseg = 1;
   tk.dep = -1;
   tk.publish = 0;
+  tk.split = 0;
   tk.seg[0] = M1Seg{y, nullptr, N};
   for (int s = 1; s < kMaxSegs; ++s) tk.seg[s] = M1Seg{nullptr, nullptr, N};
   const int grid = N < d.sms ? N : d.sms;
   tk.rq = N / grid;
   tk.rr = N % grid;
-  const RingPlan rp = make_ring_plan(&K, 1, d.max_smem_optin, kFmtQ4K);
-  if (rp.S < 2) return cudaErrorInvalidConfiguration;
-  p.S = rp.S;
-  p.stage_bytes = rp.stage_bytes;
-  p.red_bytes = rp.red_bytes;
-  p.CW = rp.CW;
+  RingPlan rp;
+  if (!plan_tasks(p, p.task, 1, kFmtQ4K, d, &rp)) return cudaErrorInvalidConfiguration;
   return launch_tasks(p, rp, grid, pdl, false, kFmtQ4K, st);
 }
 
 cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uint32_t* status,
                                  bool pdl, bool a8, const DeviceInfo& d, cudaStream_t st) {
   if (tasks == nullptr || ntasks <= 0 || ntasks > kM1MaxTasks) return cudaErrorInvalidValue;
-  static thread_local M1Params<kM1MaxTasks> p;  // ~25 KB: kept off the stack
-  int Ks[kM1MaxTasks];
+  static thread_local M1Params<kM1MaxTasks> p;  // ~28 KB: kept off the stack
   for (int i = 0; i < ntasks; ++i) {
-    if (!gemv_m1_supported(tasks[i].K) || tasks[i].N <= 0) return cudaErrorInvalidValue;
-    if (tasks[i].dep >= i || (tasks[i].dep >= 0 && done == nullptr)) return cudaErrorInvalidValue;
-    p.task[i] = tasks[i];
-    p.task[i].rq = tasks[i].N / d.sms;
-    p.task[i].rr = tasks[i].N % d.sms;
+    const M1Task& t = tasks[i];
+    if (!gemv_m1_supported(t.K * task_parts(t)) || t.N <= 0) return cudaErrorInvalidValue;
+    if (t.dep >= i || (t.dep >= 0 && done == nullptr)) return cudaErrorInvalidValue;
+    // a K split is two consecutive halves of one GEMV, small enough per CTA
+    if (t.split > 2 || (t.split != 0 && (a8 || (t.N + d.sms - 1) / d.sms > kM1PartRows))) return cudaErrorInvalidValue;
+    if (t.split == 1 && (i + 1 >= ntasks || tasks[i + 1].split != 2 || tasks[i + 1].N != t.N ||
+                         tasks[i + 1].K != t.K))
+      return cudaErrorInvalidValue;
+    if (t.split == 2 && (i == 0 || tasks[i - 1].split != 1)) return cudaErrorInvalidValue;
+    p.task[i] = t;
+    p.task[i].rq = t.N / d.sms;
+    p.task[i].rr = t.N % d.sms;
     p.task[i].publish = 0;
-    Ks[i] = tasks[i].K;
   }
   bool act = false;
   for (int i = 0; i < ntasks; ++i) {
@@ -912,24 +1226,30 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
   p.ntasks = ntasks;
   p.done = done;
   p.status = status;
-  const RingPlan rp = make_ring_plan(Ks, ntasks, d.max_smem_optin);
-  if (rp.S < 2) return cudaErrorInvalidConfiguration;
-  p.S = rp.S;
-  p.stage_bytes = rp.stage_bytes;
-  p.red_bytes = rp.red_bytes;
-  p.CW = rp.CW;
+  const int fmt = a8 ? kFmtW4A8 : kFmtW4A16;
+  RingPlan rp;
+  if (!plan_tasks(p, p.task, ntasks, fmt, d, &rp)) return cudaErrorInvalidConfiguration;
   // one CTA per SM: every CTA must be resident for the dependency counts
-  return launch_tasks(p, rp, d.sms, pdl, act, a8 ? kFmtW4A8 : kFmtW4A16, st);
+  return launch_tasks(p, rp, d.sms, pdl, act, fmt, st);
+}
+
+bool gemv_m1_tasks_fit(const M1Task* tasks, int n, bool a8, const DeviceInfo& d) {
+  if (tasks == nullptr || n <= 0) return false;
+  for (int i = 0; i < n; ++i)
+    if (!gemv_m1_supported(tasks[i].K * task_parts(tasks[i]))) return false;
+  // a table's plan takes the largest stage of its tasks: the plan over all of
+  // them bounds every subset's
+  return make_ring_plan(tasks, n, d.max_smem_optin, a8 ? kFmtW4A8 : kFmtW4A16).S >= 2;
 }
 
 cudaError_t prepare_gemv_m1(const DeviceInfo& d) {
-  const int limit = d.max_smem_optin < kM1SmemBudget + 1024 ? d.max_smem_optin : kM1SmemBudget + 1024;
+  const int limit = d.max_smem_optin < kM1SmemBudget ? d.max_smem_optin : kM1SmemBudget;
   const void* fns[] = {
-      reinterpret_cast<const void*>(gemv_m1_kernel<1, false, kFmtW4A16>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<1, true, kFmtW4A16>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<1, false, kFmtW4A8>),
-      reinterpret_cast<const void*>(gemv_m1_kernel<1, true, kFmtW4A8>),
       reinterpret_cast<const void*>(gemv_m1_kernel<1, false, kFmtQ4K>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<2, false, kFmtW4A16>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<2, true, kFmtW4A16>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<2, false, kFmtW4A8>),
+      reinterpret_cast<const void*>(gemv_m1_kernel<2, true, kFmtW4A8>),
       reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, false, kFmtW4A16>),
       reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, true, kFmtW4A16>),
       reinterpret_cast<const void*>(gemv_m1_kernel<kM1MaxTasks, false, kFmtW4A8>),

@@ -88,6 +88,12 @@ struct M1Task {
   int rq, rr;               // rows per CTA (set by the launcher): rq, one more for CTAs < rr
   uint8_t nseg;             // 1..kMaxSegs
   uint8_t publish;          // a later task reads this one's output (set by the launcher)
+  // K-split of one GEMV into two consecutive tasks over the halves of each
+  // row's K (rows of pitch 2 K): 1 = the first half (its row sums wait in
+  // shared memory, nothing is written), 2 = the second half (adds them, then
+  // the bias and the rounding; qweight, scales, x and x2 point at the half).
+  // 0 = a whole GEMV.
+  uint8_t split;
   M1Seg seg[kMaxSegs];
 };
 static_assert(sizeof(M1Task) == 128, "a task record is 128 bytes (the table is kernel parameters)");
@@ -126,9 +132,19 @@ cudaError_t launch_gemv_m1_q4k(const uint8_t* blocks, const uint16_t* x, uint16_
 // A task list (1 <= ntasks <= kM1MaxTasks, every K supported, M = 1) in one
 // launch of one CTA per SM.  done: ntasks ints, zero before the launch
 // (per-task completion counters); required when a task has a dependency,
-// may be null otherwise.  pdl: as GemvArgs::pdl.
+// may be null otherwise.  pdl: as GemvArgs::pdl.  A K-split GEMV is two
+// consecutive tasks (M1Task::split), made by gemv_m1_split_tasks.
 cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uint32_t* status,
                                  bool pdl, bool a8, const DeviceInfo& d, cudaStream_t st);
+// Host-only: whether task lists over these tasks (any subset of them, in
+// tables of up to kM1MaxTasks) pass launch_gemv_m1_tasks's own checks of K
+// and the shared-memory plan on this device.
+bool gemv_m1_tasks_fit(const M1Task* tasks, int n, bool a8, const DeviceInfo& d);
+// Host-only: the tasks of one M = 1 GEMV (its K, N, pointers in t, split 0):
+// one task, or (W4A16 only, when split_parts says so) its two K halves.
+// Writes 1 or 2 tasks to out and returns the count; dep and publish are
+// copied to both.
+int gemv_m1_split_tasks(const M1Task& t, bool a8, const DeviceInfo& d, M1Task* out);
 // M = 1..7 (any K): warp-per-row-block CUDA-core kernel.
 cudaError_t launch_gemv_rows(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 // M = 8..16: mma.sync tensor-core kernel with cluster split-K.

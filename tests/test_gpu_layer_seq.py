@@ -1,7 +1,7 @@
 """GPU tests of layer_seq: the seven projections of a Qwen-7B-shaped layer,
 28 layers, captured as one CUDA graph.
 
-Layers 0 and 27 are drawn on the CPU and checked against the oracle on
+Layers 0, 14 and 27 are drawn on the CPU and checked against the oracle on
 sampled rows (each GEMV alone: o and down take the GPU's own fp16
 intermediate as their input); every layer is checked bit for bit against
 separate w4a16_gemv calls; run_host, the fused/unfused gate+up paths, M > 1
@@ -19,7 +19,7 @@ from gpu_helpers import sample_rows, to_np_u16, to_np_u32
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 H, KV, F, L = synth.HIDDEN, synth.KV_DIM, synth.FFN, synth.N_LAYERS
-CHECKED_LAYERS = (0, L - 1)
+CHECKED_LAYERS = (0, L // 2, L - 1)
 
 
 def _layer_weights(layer, fused=True, cpu=False, qkv=False):
@@ -175,6 +175,40 @@ def test_layer_seq_sync_timeout(seq28):
         seq.run()
     assert seq.sync(0) == 8
     assert seq.sync(-1) == 0
+
+
+def test_layer_seq_sync_reports_device_failure():
+    """A bounded wait that ran out on the device (here the self-test's wait on
+    a barrier nothing arrives on) makes the next sync return
+    W4A16_ERR_DEVICE instead of OK; once the status word is cleared, a replay
+    syncs OK again.  No kernel is left waiting: the self-test's wait ends at
+    its 20 ms bound."""
+    h, kv, ffn, n = 256, 128, 512, 2
+    layers = []
+    for l in range(n):
+        lw = {}
+        for pj, name in enumerate(synth.PROJ_NAMES):
+            N, K = {"q": (h, h), "k": (kv, h), "v": (kv, h), "o": (h, h), "gate": (ffn, h), "up": (ffn, h),
+                    "down": (h, ffn)}[name]
+            lw[name] = w4.w4a16_quantize(synth.weights(N, K, 81000 + 8 * l + pj).to(DEV))
+        layers.append(lw)
+    io = {"x": synth.activations(n, h, 81999).view(n, 1, h).to(DEV)}
+    for name, width in (("y_q", h), ("y_k", kv), ("y_v", kv), ("y_o", h), ("y_gu", 2 * ffn), ("y_down", h)):
+        io[name] = torch.empty((n, 1, width), dtype=torch.float16, device=DEV)
+    seq = w4.LayerSeq(layers, io, 1, h, kv, ffn)
+    assert w4.w4a16_device_status(clear=True) == 0
+    seq.run()
+    assert seq.sync() == 0
+    w4.w4a16_selftest_wait_timeout(20000)
+    seq.run()
+    with pytest.raises(w4.W4A16Error, match="DEVICE"):
+        seq.sync()
+    with pytest.raises(w4.W4A16Error, match="DEVICE"):
+        seq.sync(1000)  # the word stays set until it is read and cleared
+    assert w4.w4a16_device_status(clear=True) == w4.DEV_PIPE_TIMEOUT
+    seq.run()
+    assert seq.sync() == 0
+    seq.close()
 
 
 @pytest.mark.parametrize("M,fused,qkv", [(1, False, False), (3, True, True), (3, False, False),

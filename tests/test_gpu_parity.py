@@ -117,17 +117,21 @@ def test_gemv_small_configs_full(cfg):
 
 
 def test_gemv_gate_up_full_size():
+    """[gate; up] at full size, every one of the 37,888 outputs against the
+    oracle (about 136 M multiply-adds on the host)."""
     cfg = synth.GATE_UP
     c = Case(cfg.N, cfg.K, cfg.M, seed=cfg.seed)
     assert c.packed_equal()
-    _run_and_check(c, rows=sample_rows(cfg.N, 2048, 1))
+    _run_and_check(c)
 
 
 @pytest.mark.parametrize("cfg", synth.DOWN_SWEEP, ids=lambda c: c.name)
 def test_gemv_down_sweep_full_size(cfg):
+    """down at full size: every output for M = 1 and 2, sampled rows (first,
+    last, ragged tail, random) for the larger batches."""
     c = Case(cfg.N, cfg.K, cfg.M, seed=cfg.seed)
     assert c.packed_equal()
-    _run_and_check(c, rows=sample_rows(cfg.N, 384 // cfg.M + 16, 2))
+    _run_and_check(c, rows=None if cfg.M <= 2 else sample_rows(cfg.N, 384 // cfg.M + 16, 2))
 
 
 @pytest.mark.parametrize("M", list(range(1, 17)))

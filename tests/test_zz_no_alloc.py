@@ -102,6 +102,69 @@ def test_run_static_matches_layer_seq_on_two_calls(model):
     assert w4.w4a16_device_status(clear=True) == 0
 
 
+def test_run_static_takes_no_device_memory(model):
+    """The property the entry point exists for: after a first round of calls
+    (which may set up the library on this device, and lets torch cache what
+    the comparisons below need), further calls -- with another layer count,
+    and on another stream -- leave both the device's free memory and torch's
+    allocator untouched, and give the same bits on a side stream as on the
+    default stream."""
+    layers, x = model
+    io = _poisoned_io(x)
+    side = torch.cuda.Stream()
+    io2 = {k: v[:2] for k, v in io.items()}
+    w4.w4a16_layer_seq_run_static(layers, io, H, KV, F)
+    torch.cuda.synchronize()
+    ref = {name: io[name].clone() for name, _ in OUTS}
+
+    def one_call(kind):
+        for name, _ in OUTS:
+            io[name].fill_(float("nan"))
+        torch.cuda.synchronize()
+        if kind == "fewer_layers":
+            w4.w4a16_layer_seq_run_static(layers[:2], io2, H, KV, F)
+        elif kind == "side_stream":
+            with torch.cuda.stream(side):
+                w4.w4a16_layer_seq_run_static(layers, io, H, KV, F, stream=side)
+            side.synchronize()
+        else:
+            w4.w4a16_layer_seq_run_static(layers, io, H, KV, F)
+        torch.cuda.synchronize()
+        n = 2 if kind == "fewer_layers" else N_LAYERS
+        return all(torch.equal(io[name][:n].view(torch.int16), ref[name][:n].view(torch.int16))
+                   for name, _ in OUTS)
+
+    kinds = ("default", "fewer_layers", "side_stream", "default")
+    for kind in kinds:  # warm-up round: first use of every path
+        assert one_call(kind), kind
+    free0 = torch.cuda.mem_get_info()[0]
+    alloc0 = torch.cuda.memory_allocated()
+    for kind in kinds:
+        assert one_call(kind), kind
+        assert torch.cuda.mem_get_info()[0] == free0, kind
+        assert torch.cuda.memory_allocated() == alloc0, kind
+    assert w4.w4a16_device_status(clear=True) == 0
+
+
+def test_run_static_rejects_k_beyond_the_kernel(model):
+    """An FFN width whose down projection (K = 28800) is beyond the M = 1
+    kernel's K range: W4A16_ERR_LIMIT, and the outputs keep their NaN."""
+    h, kv, ffn = 128, 128, 28800
+    lw = {}
+    for pj, name in enumerate(synth.PROJ_NAMES):
+        N, K = {"q": (h, h), "k": (kv, h), "v": (kv, h), "o": (h, h), "gate": (ffn, h), "up": (ffn, h),
+                "down": (h, ffn)}[name]
+        lw[name] = w4.w4a16_quantize(synth.weights(N, K, 71000 + pj, DEV))
+    io = {"x": synth.activations(1, h, 71999).view(1, 1, h).to(DEV)}
+    for name, width in (("y_q", h), ("y_k", kv), ("y_v", kv), ("y_o", h), ("y_gu", 2 * ffn), ("y_down", h)):
+        io[name] = torch.full((1, 1, width), float("nan"), dtype=torch.float16, device=DEV)
+    with pytest.raises(w4.W4A16Error, match="LIMIT"):
+        w4.w4a16_layer_seq_run_static([lw], io, h, kv, ffn)
+    torch.cuda.synchronize()
+    for name in ("y_q", "y_k", "y_v", "y_o", "y_gu", "y_down"):
+        assert torch.isnan(io[name]).all(), name
+
+
 def test_run_static_rejects_beyond_its_limits(model):
     """More GEMVs than the fixed scratch holds, or a K beyond the M = 1
     kernel: W4A16_ERR_LIMIT, and nothing is written."""
