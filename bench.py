@@ -12,8 +12,10 @@ Prints ONE JSON line (rank 0).  Besides the contract keys it reports
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
   e2e           the same metric through w4a16_layer_seq_run_host: host x in,
                 every output back, copies inside the timed region
-  configs       per-workload-shape us/GEMV and GB/s (28 rotated instances
-                per CUDA graph, cold L2), including the M = 1..16 down sweep
+  configs       per-workload-shape us/GEMV and GB/s with cold L2 (weights
+                rotated over >= 4 x L2), warm L2 and single-launch latency,
+                as fractions of the measured peak and the nominal 8 TB/s,
+                including the M = 1..16 down sweep
   clocks        SM clock and throttle reasons sampled during the timed region
 
 --impl reference times the CPU oracle (the only reference implementation
@@ -255,10 +257,13 @@ def cpu_baseline(budget_s=15.0):
     passes = max(1, int(budget_s / t)) if frac >= 1.0 else 1
     if passes > 1:
         t += sum(run_oracle_steps(plan, passes - 1))
-    return {"value": nbytes * passes / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+    line = {"value": nbytes * passes / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"single-threaded C oracle (FP64) on {frac:.4f} of the rows of each of "
                       f"layer 0's 7 projections ({nbytes} algorithmic bytes), {passes} pass(es), "
-                      f"{t:.1f} s"}
+                      f"{t:.1f} s; the oracle uses 1 of the host's cores"}
+    line.update(host_cpu())
+    line["per_config"] = oracle_config_timing()
+    return line
 
 
 def bench_reference(args, rank, world):
@@ -278,7 +283,7 @@ def bench_reference(args, rank, world):
         "data": "synthetic", "config": config_block(),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"each step: {frac:.5f} of the rows of each of layer 0's "
-                                   f"7 projections ({nbytes} algorithmic bytes)"},
+                                   f"7 projections ({nbytes} algorithmic bytes)", **host_cpu()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
@@ -344,35 +349,73 @@ def time_graph_replays(seq, stream, steps, dist_barrier):
     return start.elapsed_time(end)
 
 
-def per_config_table(layers, dev, reps=20):
-    """us/GEMV and GB/s per workload shape: a CUDA graph of 28 GEMVs over the
-    28 layers' distinct weights (cold L2), replayed `reps` times."""
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
+
+
+def host_cpu():
+    """Model name and logical core count of this host."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:  # noqa: BLE001
+            pass
+    import platform
+    return {"host_cores": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
+def gemv_line(qw, sc, M, dev, gemv=None, reps=5, seed=77):
+    """One GEMV shape measured three ways:
+      cold     -- a CUDA graph of max(200, R) GEMVs cycling over R distinct
+                  copies of the weights with R * weight bytes >= 4 x L2, so
+                  every launch streams its weights from HBM;
+      warm     -- a graph of 200 GEMVs on one copy (L2-resident when it fits);
+      single   -- an event pair around one launch outside any graph (median
+                  of 20), the per-call latency a caller sees.
+    Returns us per GEMV and GB/s of algorithmic bytes, with the fraction of
+    the measured HBM peak and of the nominal 8 TB/s."""
+    import math
+
     import torch
 
     import int4_weight_only_gemv_gb300 as w4
     import synth
-    H, F = synth.HIDDEN, synth.FFN
-    out = {}
-    shapes = [("q_proj", "q", H, 1), ("kv_proj", "k", H, 1), ("qkv", "qkv", H, 1),
-              ("gate_up", "gate_up", H, 1)]
-    shapes += [(f"down_m{m}", "down", F, m) for m in (1, 2, 4, 8, 16)]
-    # the W4A8 variant on the M = 1 shapes (activations quantised in-kernel)
-    shapes += [("q_proj_a8", "q", H, 1), ("gate_up_a8", "gate_up", H, 1), ("down_m1_a8", "down", F, 1)]
+    gemv = gemv or w4.w4a16_gemv
+    N, K = qw.shape[0], qw.shape[1] * 8
+    wbytes = qw.numel() * 4 + sc.numel() * 2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, math.ceil(4 * l2 / wbytes))
+    G = max(200, R)
+    copies = [(qw.clone(), sc.clone()) for _ in range(R)]
+    xs = [synth.activations(M, K, seed + i, dev) for i in range(8)]
+    ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in range(8)]
     stream = torch.cuda.Stream()
-    for label, key, K, M in shapes:
-        gemv = w4.w4a16_gemv_a8 if label.endswith("_a8") else w4.w4a16_gemv
-        xs = [synth.activations(M, K, 77 + l, dev) for l in range(len(layers))]
-        N = layers[0][key][0].shape[0]
-        ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in layers]
+
+    def graph_of(which):
         with torch.cuda.stream(stream):
-            for l, lw in enumerate(layers):  # warm-up, also outside capture
-                gemv(*lw[key], xs[l], ys[l])
+            for i in range(min(G, 8)):
+                gemv(*copies[which(i)], xs[i % 8], ys[i % 8])
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for l, lw in enumerate(layers):
-                gemv(*lw[key], xs[l], ys[l])
-        for _ in range(3):
+            for i in range(G):
+                gemv(*copies[which(i)], xs[i % 8], ys[i % 8])
+        return g
+
+    def time_graph(g, n):
+        for _ in range(2):
             g.replay()
         torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -382,40 +425,80 @@ def per_config_table(layers, dev, reps=20):
             g.replay()
         e.record(cur)
         torch.cuda.synchronize()
-        us = 1e3 * s.elapsed_time(e) / (reps * len(layers))
-        b = gemv_bytes(N, K, M)
-        out[label] = {"M": M, "N": N, "K": K, "us_per_gemv": round(us, 3),
-                      "GBps": round(b / us / 1e3, 1), "bytes": b}
-        if label.endswith("_a8"):
-            out[label]["note"] = "W4A8: int8 activations, per-64 block scales computed in the kernel"
-    # the tiny workload fits in L2: latency-bound, measured warm
-    cfg = synth.TINY
-    wq, sc = w4.w4a16_quantize(synth.weights(cfg.N, cfg.K, cfg.seed, dev))
-    x = synth.activations(1, cfg.K, cfg.seed, dev)
-    y = torch.empty((1, cfg.N), dtype=torch.float16, device=dev)
-    w4.w4a16_gemv(wq, sc, x, y)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(28):
-            w4.w4a16_gemv(wq, sc, x, y)
-    g.replay()
-    torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(reps):
-        g.replay()
-    e.record()
-    torch.cuda.synchronize()
-    us = 1e3 * s.elapsed_time(e) / (reps * 28)
-    b = gemv_bytes(cfg.N, cfg.K, 1)
-    out["tiny"] = {"M": 1, "N": cfg.N, "K": cfg.K, "us_per_gemv": round(us, 3),
-                   "GBps": round(b / us / 1e3, 1), "bytes": b, "note": "L2-resident, latency-bound"}
-    out["gate_up_q4k"] = q4k_line(dev, reps)
-    out["down_q4k"] = q4k_line(dev, reps, N=synth.HIDDEN, K=synth.FFN)
-    out["attn_decode_T8192"] = attn_decode_line(dev, reps)
-    out["layer_seq_qkv_bias_swiglu"] = epilogue_step(layers, dev, reps, ("q", "k", "v"))
-    out["layer_seq_bias_swiglu"] = epilogue_step(layers, dev, reps, synth.PROJ_NAMES)
-    out["layer_seq_w4a8"] = epilogue_step(layers, dev, reps, (), act_int8=True)
+        return 1e3 * s.elapsed_time(e) / (reps * n)
+
+    cold = time_graph(graph_of(lambda i: i % R), G)
+    warm = time_graph(graph_of(lambda i: 0), G)
+    singles = []
+    cur = torch.cuda.current_stream()
+    for i in range(20):
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(cur)
+        gemv(*copies[i % R], xs[i % 8], ys[i % 8])
+        e.record(cur)
+        torch.cuda.synchronize()
+        singles.append(1e3 * s.elapsed_time(e))
+    b = gemv_bytes(N, K, M)
+    peak, _ = measured_peak()
+    gbps = b / cold / 1e3
+    del copies
+    return {"M": M, "N": N, "K": K, "bytes": b, "us_per_gemv": round(cold, 3), "GBps": round(gbps, 1),
+            "frac_measured": round(gbps / peak, 4), "frac_nominal_8TBps": round(gbps / NOMINAL_HBM_GBS, 4),
+            "warm_us": round(warm, 3), "single_launch_us": round(statistics.median(singles), 3),
+            "rotation": f"{R} weight copies ({R * wbytes / 1e6:.0f} MB >= 4 x {l2 / 1e6:.0f} MB L2), "
+                        f"graph of {G} GEMVs"}
+
+
+def oracle_config_timing(budget_s=0.25):
+    """The single-threaded C oracle on each workload GEMV shape, timed on a
+    row sample sized to take about budget_s seconds, median of 3 runs, and
+    extrapolated to us per full GEMV (the oracle's cost is linear in rows)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    rate = _oracle_mac_rate()
+    out = {}
+    for cfg in synth.ALL_GEMVS:
+        nrows = max(1, min(cfg.N, int(rate * budget_s / (cfg.M * cfg.K))))
+        w = synth.weights(nrows, cfg.K, cfg.seed).numpy()
+        qw, sc = oracle.quantize(w)
+        x = synth.activations(cfg.M, cfg.K, cfg.seed).numpy().view(np.uint16)
+        times = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            oracle.gemv(qw, sc, x)
+            times.append(time.perf_counter() - t0)
+        t = statistics.median(times) * cfg.N / nrows
+        out[cfg.name] = {"us_per_gemv": round(1e6 * t, 1), "rows_timed": nrows,
+                         "GBps": round(gemv_bytes(cfg.N, cfg.K, cfg.M) / t / 1e9, 4)}
+    return out
+
+
+def per_config_table(layers, dev, reps=5):
+    """Per workload shape: us/GEMV and GB/s with cold L2 (rotation over >= 4 x
+    L2 of weight copies), warm L2, and single-launch latency (gemv_line); the
+    configured shapes use their own seeds, the stacked [q; k; v] and the W4A8
+    lines the step's layer-0 weights."""
+    import int4_weight_only_gemv_gb300 as w4
+    import synth
+    out = {}
+    for cfg in synth.ALL_GEMVS:
+        qw, sc = w4.w4a16_quantize(synth.weights(cfg.N, cfg.K, cfg.seed, dev))
+        out[cfg.name] = gemv_line(qw, sc, cfg.M, dev, reps=reps, seed=cfg.seed)
+        del qw, sc
+    out["qkv"] = gemv_line(*layers[0]["qkv"], 1, dev, reps=reps)
+    # the W4A8 variant on the M = 1 shapes (activations quantised in-kernel)
+    for label, key in (("q_proj_a8", "q"), ("gate_up_a8", "gate_up"), ("down_m1_a8", "down")):
+        out[label] = gemv_line(*layers[0][key], 1, dev, gemv=w4.w4a16_gemv_a8, reps=reps)
+        out[label]["note"] = "W4A8: int8 activations, per-64 block scales computed in the kernel"
+    out["gate_up_q4k"] = q4k_line(dev, 20)
+    out["down_q4k"] = q4k_line(dev, 20, N=synth.HIDDEN, K=synth.FFN)
+    out["attn_decode_T8192"] = attn_decode_line(dev, 20)
+    out["layer_seq_qkv_bias_swiglu"] = epilogue_step(layers, dev, 20, ("q", "k", "v"))
+    out["layer_seq_bias_swiglu"] = epilogue_step(layers, dev, 20, synth.PROJ_NAMES)
+    out["layer_seq_w4a8"] = epilogue_step(layers, dev, 20, (), act_int8=True)
     return out
 
 
