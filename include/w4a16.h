@@ -77,6 +77,10 @@ typedef enum {
 #define W4A16_DEV_NONFINITE 0x1u     /* w4a16_quantize met a non-finite weight   */
 #define W4A16_DEV_SCALE_OVERFLOW 0x2u /* w4a16_quantize: max|w|/7 overflows fp16 */
 #define W4A16_DEV_PIPE_TIMEOUT 0x4u  /* a GEMV pipeline wait ran past its bound  */
+/* Only in the index-checked build of the library (compiled with
+ * W4A16_CHECKED, for tests): a kernel's index or address check failed and the
+ * access was skipped instead of made (the results are then undefined). */
+#define W4A16_DEV_INDEX 0x8u
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* w4a16_status_str(w4a16_status s);

@@ -19,12 +19,15 @@ __all__ = [
     "W4A16Error", "lib", "w4a16_gemv", "w4a16_dequant", "w4a16_quantize", "w4a16_device_status",
     "w4a16_selftest_wait_timeout", "w4a16_layer_seq_run_static", "STATIC_MAX_GEMVS",
     "LayerSeq", "GROUP", "MAX_M", "MAX_K", "DEV_NONFINITE", "DEV_SCALE_OVERFLOW",
-    "DEV_PIPE_TIMEOUT", "STATUS", "EXPORTED_SYMBOLS", "w4a16_attn_decode", "attn_decode_workspace",
+    "DEV_PIPE_TIMEOUT", "DEV_INDEX", "STATUS", "EXPORTED_SYMBOLS", "w4a16_attn_decode", "attn_decode_workspace",
     "attn_decode_new_workspace", "w4a16_gemv_a8", "SEQ_ACT_INT8", "w4a16_q4k_gemv", "w4a16_q4k_dequant",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_lib", "libw4a16.so")
+# W4A16_LIBRARY=checked selects the index-checked build (build(checked=True)),
+# whose kernels record W4A16_DEV_INDEX instead of an out-of-range access.
+LIB_PATH = (os.path.join(HERE, "_lib", "checked", "libw4a16_checked.so")
+            if os.environ.get("W4A16_LIBRARY") == "checked" else os.path.join(HERE, "_lib", "libw4a16.so"))
 
 GROUP = 128
 MAX_M = 16
@@ -32,6 +35,7 @@ MAX_K = 32768
 DEV_NONFINITE = 0x1
 DEV_SCALE_OVERFLOW = 0x2
 DEV_PIPE_TIMEOUT = 0x4
+DEV_INDEX = 0x8
 SEQ_SWIGLU = 0x1
 SEQ_ACT_INT8 = 0x2
 NPROJ = 7

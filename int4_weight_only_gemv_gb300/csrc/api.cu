@@ -525,7 +525,8 @@ struct ActOp {
 // one GEMV when the three weights are stacked in one allocation (outputs
 // still go to y_q, y_k, y_v), o, [gate; up] as one GEMV when stacked, down.
 // dep[i] is the GEMV whose output GEMV i reads (o reads y_q, down the gate
-// half of y_gu, or with SwiGLU both halves: the later of gate and up), or -1;
+// half of y_gu, or with SwiGLU both halves: then dep2[i] is the other of gate
+// and up when they are separate GEMVs), or -1;
 // x2[i] is the SwiGLU partner of GEMV i's x (the up half) when the sequence
 // fuses SwiGLU into the M = 1 task, else null; act[i] the separate SwiGLU
 // step before GEMV i (unfused path); layer_first[l] is the index of layer l's
@@ -533,11 +534,12 @@ struct ActOp {
 // output segments.
 void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, int n_layers, int M,
                      int hidden, int kv_dim, int ffn, const w4a16_seq_io* io, bool fuse_swiglu,
-                     std::vector<GemvArgs>* gemvs, std::vector<int>* dep,
+                     std::vector<GemvArgs>* gemvs, std::vector<int>* dep, std::vector<int>* dep2,
                      std::vector<const uint16_t*>* x2, std::vector<ActOp>* act,
                      std::vector<int>* layer_first) {
   gemvs->clear();
   dep->clear();
+  dep2->clear();
   x2->clear();
   act->clear();
   layer_first->clear();
@@ -552,6 +554,7 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
   auto add = [&](const GemvArgs& a, int d) {
     gemvs->push_back(a);
     dep->push_back(d);
+    dep2->push_back(-1);
     x2->push_back(nullptr);
     act->push_back(ActOp{});
     return static_cast<int>(gemvs->size()) - 1;
@@ -594,7 +597,8 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
       add(a, iq);
     }
     // y_gu rows are [gate | up]: row stride 2 ffn
-    int ilast;  // the GEMV down waits for
+    int ilast;       // the GEMV down waits for
+    int ialso = -1;  // and, with SwiGLU over separate gate and up, the other one
     const int64_t ldgu = 2 * static_cast<int64_t>(ffn);
     if (stacked(w, W4A16_GATE, W4A16_UP, ffn)) {
       GemvArgs a = plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, 2 * ffn, hidden,
@@ -611,7 +615,12 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
       a = plain_args(w.qweight[W4A16_UP], w.scales[W4A16_UP], xl, ygu + ffn, M, ffn, hidden, hidden, ldgu);
       a.seg[0].bias = b(W4A16_UP);
       const int iu = add(a, -1);
-      if (swiglu) ilast = iu;  // down reads both halves; publication is in task order
+      if (swiglu) {
+        // down reads both halves: it waits for whichever of the two a task
+        // table runs later (each CTA publishes its tasks in table order)
+        ialso = ilast;
+        ilast = iu;
+      }
     }
     {
       GemvArgs a = plain_args(w.qweight[W4A16_DOWN], w.scales[W4A16_DOWN], ygu, io->y_down + l * Mh, M,
@@ -624,6 +633,7 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
         a.ldx = ffn;
       }
       const int id = add(a, ilast);
+      (*dep2)[id] = ialso;
       if (swiglu && fuse_swiglu) (*x2)[id] = ygu + ffn;
       (*act)[id] = op;
     }
@@ -650,8 +660,8 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
 // whose K the M = 1 kernel splits becomes two consecutive tasks; a GEMV that
 // reads its output depends on the second.
 void seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep,
-               const std::vector<const uint16_t*>& x2, const std::vector<int>& layer_first, int l0, int l1,
-               bool a8, std::vector<M1Task>* tasks) {
+               const std::vector<int>& dep2, const std::vector<const uint16_t*>& x2,
+               const std::vector<int>& layer_first, int l0, int l1, bool a8, std::vector<M1Task>* tasks) {
   tasks->clear();
   static thread_local std::vector<int> slot;  // table slot of each emitted GEMV (capacity kept)
   slot.assign(gemvs.size(), -1);
@@ -666,7 +676,10 @@ void seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs, const s
       tk.N = a.N;
       tk.K = a.K;
       tk.nseg = static_cast<uint8_t>(a.nseg);
+      // with two producers, the one later in the table (its publication on
+      // every CTA implies the other's)
       tk.dep = dep[i] < 0 ? -1 : slot[dep[i]];
+      if (dep2[i] >= 0 && slot[dep2[i]] > tk.dep) tk.dep = slot[dep2[i]];
       for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = M1Seg{a.seg[g].y, a.seg[g].bias, a.seg[g].n_end};
       M1Task parts[2];
       const int np = gemv_m1_split_tasks(tk, a8, d.info, parts);
@@ -717,7 +730,8 @@ bool seq_uses_tasks(int M, const std::vector<GemvArgs>& gemvs) {
 // kernel's limits on this device.  Host-only: nothing is enqueued.
 // scratch: the caller's buffer (its capacity is reused).
 w4a16_status check_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs,
-                             const std::vector<int>& dep, const std::vector<const uint16_t*>& x2,
+                             const std::vector<int>& dep, const std::vector<int>& dep2,
+                             const std::vector<const uint16_t*>& x2,
                              const std::vector<int>& layer_first, bool a8, std::vector<M1Task>* scratch,
                              std::vector<int>* task_first) {
   const int n_layers = static_cast<int>(layer_first.size()) - 1;
@@ -736,7 +750,7 @@ w4a16_status check_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& 
     if (n > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
     task_first->push_back(task_first->back() + n);
   }
-  seq_tasks(d, gemvs, dep, x2, layer_first, 0, n_layers, a8, scratch);
+  seq_tasks(d, gemvs, dep, dep2, x2, layer_first, 0, n_layers, a8, scratch);
   return gemv_m1_tasks_fit(scratch->data(), static_cast<int>(scratch->size()), a8, d.info) ? W4A16_OK
                                                                                           : W4A16_ERR_SHAPE;
 }
@@ -748,7 +762,8 @@ w4a16_status check_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& 
 // the launches before it enqueued); tasks: the caller's table buffer (its
 // capacity is reused).  Returns the launch count through *launches.
 w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs,
-                               const std::vector<int>& dep, const std::vector<const uint16_t*>& x2,
+                               const std::vector<int>& dep, const std::vector<int>& dep2,
+                               const std::vector<const uint16_t*>& x2,
                                const std::vector<int>& layer_first, const std::vector<int>& task_first,
                                int* done, bool a8, cudaStream_t st, std::vector<M1Task>* tasks, int* launches) {
   const int n_layers = static_cast<int>(layer_first.size()) - 1;
@@ -759,7 +774,7 @@ w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>
     while (l1 < n_layers && task_first[l1 + 1] - task_first[l0] <= kM1MaxTasks) ++l1;
     const int t0 = task_first[l0], t1 = task_first[l1];
     if (t1 - t0 > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
-    seq_tasks(d, gemvs, dep, x2, layer_first, l0, l1, a8, tasks);
+    seq_tasks(d, gemvs, dep, dep2, x2, layer_first, l0, l1, a8, tasks);
     const cudaError_t e =
         launch_gemv_m1_tasks(tasks->data(), t1 - t0, done + t0, d.status, *launches > 0, a8, d.info, st);
     if (e != cudaSuccess) {
@@ -829,15 +844,15 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
   }
   opt.hbuf = s->hbuf;
   std::vector<GemvArgs> gemvs;
-  std::vector<int> dep, layer_first;
+  std::vector<int> dep, dep2, layer_first;
   std::vector<const uint16_t*> x2;
   std::vector<ActOp> act;
-  build_seq_gemvs(layers, opt, n_layers, M, hidden, kv_dim, ffn, io, tasks, &gemvs, &dep, &x2, &act,
+  build_seq_gemvs(layers, opt, n_layers, M, hidden, kv_dim, ffn, io, tasks, &gemvs, &dep, &dep2, &x2, &act,
                   &layer_first);
   // M = 1: the task lists, checked on the host before anything is captured
   std::vector<M1Task> table;
   std::vector<int> task_first;
-  if (tasks && (st = check_seq_tasks(*d, gemvs, dep, x2, layer_first, a8, &table, &task_first)) != W4A16_OK) {
+  if (tasks && (st = check_seq_tasks(*d, gemvs, dep, dep2, x2, layer_first, a8, &table, &task_first)) != W4A16_OK) {
     seq_free(s);
     return st;
   }
@@ -864,7 +879,7 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
     if (cudaMemsetAsync(s->task_done, 0, sizeof(int) * ntasks, s->capture_stream) != cudaSuccess)
       cap = W4A16_ERR_CUDA;
     else
-      cap = enqueue_seq_tasks(*d, gemvs, dep, x2, layer_first, task_first, s->task_done, a8,
+      cap = enqueue_seq_tasks(*d, gemvs, dep, dep2, x2, layer_first, task_first, s->task_done, a8,
                               s->capture_stream, &table, &launches);
   } else {
     for (size_t i = 0; i < gemvs.size() && cap == W4A16_OK; ++i) {
@@ -957,13 +972,13 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
 
   // host tables: thread-local, their capacity kept from call to call
   static thread_local std::vector<GemvArgs> gemvs;
-  static thread_local std::vector<int> dep, layer_first;
+  static thread_local std::vector<int> dep, dep2, layer_first;
   static thread_local std::vector<const uint16_t*> x2;
   static thread_local std::vector<ActOp> act;
   static thread_local std::vector<M1Task> tasks;
   static thread_local std::vector<int> task_first;
-  build_seq_gemvs(layers, SeqOptions{}, n_layers, 1, hidden, kv_dim, ffn, io, true, &gemvs, &dep, &x2, &act,
-                  &layer_first);
+  build_seq_gemvs(layers, SeqOptions{}, n_layers, 1, hidden, kv_dim, ffn, io, true, &gemvs, &dep, &dep2, &x2,
+                  &act, &layer_first);
   if (!seq_uses_tasks(1, gemvs)) return W4A16_ERR_LIMIT;
 
   DeviceState* d = nullptr;
@@ -972,7 +987,8 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
   if ((st = static_task_done(&done)) != W4A16_OK) return st;
 
   // every task table is checked on the host before anything is enqueued
-  if ((st = check_seq_tasks(*d, gemvs, dep, x2, layer_first, false, &tasks, &task_first)) != W4A16_OK) return st;
+  if ((st = check_seq_tasks(*d, gemvs, dep, dep2, x2, layer_first, false, &tasks, &task_first)) != W4A16_OK)
+    return st;
   const int n = task_first.back();  // one counter per task
   if (n > W4A16_STATIC_MAX_GEMVS) return W4A16_ERR_LIMIT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -982,7 +998,7 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
     return W4A16_ERR_CUDA;
   }
   int launches = 0;
-  return enqueue_seq_tasks(*d, gemvs, dep, x2, layer_first, task_first, done, false, s, &tasks, &launches);
+  return enqueue_seq_tasks(*d, gemvs, dep, dep2, x2, layer_first, task_first, done, false, s, &tasks, &launches);
 }
 
 extern "C" {

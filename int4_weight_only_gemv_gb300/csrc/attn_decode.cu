@@ -178,7 +178,7 @@ __device__ __forceinline__ void merge_ranges(const AttnParams& p, int g, float* 
     }
     const uint32_t lo = pack_half2(acc.x / lloc, acc.y / lloc), hi = pack_half2(acc.z / lloc, acc.w / lloc);
     uint2* dst = reinterpret_cast<uint2*>(p.o + (static_cast<int64_t>(g) * p.group + r) * kAD) + lane;
-    *dst = make_uint2(lo, hi);
+    if (W4A16_IN(p.status, r < p.group && g < static_cast<int>(gridDim.x) / p.splits)) *dst = make_uint2(lo, hi);
     __syncwarp();  // er is rewritten for the warp's next head
   }
 }
@@ -407,6 +407,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
         L += b[kARows + r] * e;
         acc += b[2 * kARows + r * kAD + d] * e;
       }
+      if (!W4A16_IN(p.status, slot < static_cast<int>(gridDim.x) && r < kARows)) break;
       p.ws_o[(slot * kARows + r) * kAD + d] = acc;
       if (d == 0) {
         p.ws_ml[(slot * kARows + r) * 2] = M;

@@ -522,11 +522,17 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         const uintptr_t ecopy = e > a ? e : a;
         const uint32_t scw = base + tp.RB * tp.row_bytes;
         const uint32_t bar = full0 + 8 * s;
+        // checked build: the tile's rows and its scale window inside the
+        // task and the stage (else nothing is copied and the tile is garbage)
+        const bool in = W4A16_IN(p.status, row_begin + lr0 + nr <= tk.N && nr <= tp.RB &&
+                                               tp.RB * tp.row_bytes + (l - a) <= static_cast<uintptr_t>(p.stage_bytes) &&
+                                               a + (tk.split == 2 ? tp.sc_row_bytes : 0) >= reinterpret_cast<uintptr_t>(scb));
         // the last few scale bytes of the matrix, where the aligned copy stops short
-        for (uintptr_t b = ecopy; b < l; b += 2)
+        for (uintptr_t b = ecopy; in && b < l; b += 2)
           sts_u16(scw + static_cast<uint32_t>(b - a), ld_nc_u16(reinterpret_cast<const void*>(b)));
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * tp.row_bytes + (ecopy - a)));
-        if (tk.split) {
+        mbar_arrive_expect_tx(bar, in ? static_cast<uint32_t>(nr * tp.row_bytes + (ecopy - a)) : 0u);
+        if (!in) {
+        } else if (tk.split) {
           // a half of each row: one copy per row
           for (int r = 0; r < nr; ++r)
             bulk_g2s(base + r * tp.row_bytes, wsrc + static_cast<int64_t>(lr0 + r) * tp.pitch,
@@ -536,7 +542,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
           bulk_g2s(base, wsrc + static_cast<int64_t>(lr0) * tp.row_bytes, static_cast<uint32_t>(nr * tp.row_bytes),
                    bar, pol);
         }
-        if (ecopy > a) bulk_g2s(scw, reinterpret_cast<const void*>(a), static_cast<uint32_t>(ecopy - a), bar, pol);
+        if (in && ecopy > a) bulk_g2s(scw, reinterpret_cast<const void*>(a), static_cast<uint32_t>(ecopy - a), bar, pol);
         ++g;
         base += p.stage_bytes;
         if (++s == S) {
@@ -600,7 +606,8 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       kprev = tk.K;
       if (!same) {
         const int chunks = tp.U * 16;  // 16-byte chunks of the task's activations
-        for (int q = sl0; q < chunks; q += kStagers) cp_async_16(xs + 16 * q, tk.x + 8 * q);
+        for (int q = sl0; q < chunks; q += kStagers)
+          if (W4A16_IN(p.status, 16 * q + 16 <= p.xslot && 8 * q + 8 <= tk.K)) cp_async_16(xs + 16 * q, tk.x + 8 * q);
         cp_async_wait_all();
         __syncwarp(kStagerMask);
         // the producer shares this warp: after the launch's first task, a
@@ -709,7 +716,8 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
           }
           float sum = (s0 + s1) + (s2 + s3);
           for (int o = lpr >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-          if (part == 0 && row < nr) {
+          if (part == 0 && row < nr &&
+              W4A16_IN(p.status, row_begin + lr0 + row < tk.N && (tk.split == 0 || lr0 + row < kM1PartRows))) {
             const uint32_t pa = part0 + 4 * static_cast<uint32_t>(lr0 + row);
             if (tk.split == 1) {
               // the first half of a K-split row: kept for the second half
@@ -778,7 +786,12 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     // keep the barrier counts.
     constexpr int kR = rows_per_thread(kFmt);
     const bool wact = cw * 32 < tp.T;
-    const bool active = c < tp.T;
+    // checked build: a thread whose rows, unit and partial slot do not fit
+    // the stage and the slots computes on unit 0 of row 0 and stores nothing
+    const bool active =
+        c < tp.T && W4A16_IN(p.status, (c / tp.U + (kR - 1) * tp.RL + 1) * tp.row_bytes <= tp.RB * tp.row_bytes &&
+                                           4 * ((c / tp.U + (kR - 1) * tp.RL) * tp.red_stride + c % tp.U + 1) <= p.red_bytes &&
+                                           (kFmt != kFmtW4A16 || !staged(tk, i) || tp.U * 260 <= p.xslot));
     const int u = active ? c % tp.U : 0;
     const int rl = active ? c / tp.U : 0;
     const int rot = ((u >> 2) & 1) * 16;

@@ -140,8 +140,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           }
           if (lane == 0) {
             const uint32_t bar = full0 + 8 * s;
-            mbar_arrive_expect_tx(bar, stage_bytes);
-            tma_load_2d(stage0 + s * stage_bytes, &tmap, (box_first + b) * kBoxWords, cb * 16, bar, pol);
+            // checked build: the box starts inside the matrix (TMA fills the
+            // part of a box past the matrix with zeros)
+            const bool in = W4A16_IN(a.status, (box_first + b) * kBoxWords < a.K / 8 && cb * 16 < a.N);
+            mbar_arrive_expect_tx(bar, in ? stage_bytes : 0u);
+            if (in) tma_load_2d(stage0 + s * stage_bytes, &tmap, (box_first + b) * kBoxWords, cb * 16, bar, pol);
           }
           __syncwarp();
           ++g;
@@ -219,7 +222,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const int m = nt * 8 + (ln >> 2);
         const int k0 = (gb + gl) * 128 + 32 * (ln & 3) + 8 * j;
         v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (e < entries && m < a.M) v[i] = ld_u4(a.x + m * a.ldx + k0);
+        if (e < entries && m < a.M && W4A16_IN(a.status, k0 + 8 <= a.K && 16 * e + 16 <= p.x_bytes))
+          v[i] = ld_u4(a.x + m * a.ldx + k0);
       }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
@@ -335,7 +339,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           auto push = [&](int row, int m, float v) {
             const int e = (row - 16 * pb) * 8 * NT + m;
             const uint32_t local = part0 + 4 * static_cast<uint32_t>((e / KS) * KS + rank);
-            st_cluster_f32(map_to_rank(local, static_cast<uint32_t>(e % KS)), v);
+            if (W4A16_IN(a.status, 4 * ((e / KS) * KS + rank) + 4 <= p.part_bytes))
+              st_cluster_f32(map_to_rank(local, static_cast<uint32_t>(e % KS)), v);
           };
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {

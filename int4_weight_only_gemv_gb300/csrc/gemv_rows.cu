@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(kRowsThreads, 2) gemv_rows_kernel(const GemvAr
 #pragma unroll
         for (int r = 0; r < R; ++r) sc[r] = __half2float(__ushort_as_half(ld_nc_u16(srow[r] + g)));
         XPairs xp[M][2];
+        // checked build: the unit's activations inside every row of x
+        if (!W4A16_IN(a.status, 16 * u + 16 <= K && (M - 1) * a.ldx + K <= static_cast<int64_t>(M) * a.ldx)) continue;
 #pragma unroll
         for (int m = 0; m < M; ++m) {
           const uint16_t* xr = a.x + m * a.ldx + 16 * u;
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2) gemv_rows_kernel(const GemvAr
     float v = 0.f;
 #pragma unroll
     for (int w = 0; w < kRowsWarps; ++w) v += red[w][threadIdx.x];
-    if (r0 + r < N) store_out(a, m, r0 + r, v);
+    if (r0 + r < N && W4A16_IN(a.status, m < a.M)) store_out(a, m, r0 + r, v);
   }
 }
 

@@ -8,6 +8,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "w4a16.h"
+
 namespace w4a16 {
 
 // Where output row n of activation row m goes.  A GEMV over a weight made of
@@ -193,5 +195,21 @@ cudaError_t prepare_attn_decode(const DeviceInfo& d);
 
 // Wall-clock bound on any in-kernel wait (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+#ifdef __CUDACC__
+// Index checks of the checked build (compiled with W4A16_CHECKED): when cond
+// is false, W4A16_DEV_INDEX is set in the device status word and the caller
+// skips the access.  In the normal build every check is the constant true and
+// compiles to nothing.
+#ifdef W4A16_CHECKED
+__device__ __forceinline__ bool w4a16_check(uint32_t* status, bool cond) {
+  if (!cond) atomicOr(status, W4A16_DEV_INDEX);
+  return cond;
+}
+#define W4A16_IN(status, cond) ::w4a16::w4a16_check((status), (cond))
+#else
+#define W4A16_IN(status, cond) true
+#endif
+#endif
 
 }  // namespace w4a16

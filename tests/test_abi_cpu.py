@@ -220,3 +220,14 @@ def test_q4k_argument_checks(L):
     assert L.w4a16_q4k_gemv(0, 0, 0, 0, 256, None) == 0        # N = 0
     assert L.w4a16_q4k_dequant(A, 0, 8, 256, None) == 1
     assert L.w4a16_q4k_dequant(A, A, 8, 256, None) == 6        # output overlaps the blocks
+
+
+def test_checked_build_compiles_and_exports_every_declared_symbol():
+    """The index-checked build (W4A16_CHECKED: kernels record
+    W4A16_DEV_INDEX instead of an out-of-range access) compiles for sm_103a
+    and exports the same entry points."""
+    path = wbuild.build(checked=True)
+    assert path.endswith("libw4a16_checked.so") and os.path.exists(path)
+    Lc = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(Lc, name), name

@@ -143,3 +143,45 @@ def test_create2_without_options_equals_create(M):
         assert torch.equal(io_a[name].view(torch.int16), io_b[name].view(torch.int16)), name
     a.close()
     b.close()
+
+
+def test_swiglu_waits_for_both_halves_small_layers():
+    """SwiGLU over separate gate and up GEMVs: down reads both halves of y_gu,
+    so it must wait for both producers, whichever order the task table runs
+    them in.  Small layers make each cycle of the table short, so a down task
+    that waited for only one of them would read NaN from the poisoned half.
+    Every output of every layer, on several replays, within tolerance of the
+    oracle (h from the GPU's own y_gu)."""
+    h, kv, ffn, n = 256, 128, 512, 6
+    widths = {"q": (h, h), "k": (kv, h), "v": (kv, h), "o": (h, h), "gate": (ffn, h), "up": (ffn, h),
+              "down": (h, ffn)}
+    layers, keep = [], []
+    for l in range(n):
+        lw = {}
+        for pj, name in enumerate(synth.PROJ_NAMES):
+            lw[name] = w4.w4a16_quantize(synth.weights(*widths[name], 82000 + 8 * l + pj).to(DEV))
+            keep.append(torch.empty(4096, dtype=torch.uint8, device=DEV))  # no two weights adjacent
+        layers.append(lw)
+    io = {"x": synth.activations(n, h, 82999).view(n, 1, h).to(DEV)}
+    for name, width in (("y_q", h), ("y_k", kv), ("y_v", kv), ("y_o", h), ("y_gu", 2 * ffn), ("y_down", h)):
+        io[name] = torch.empty((n, 1, width), dtype=torch.float16, device=DEV)
+    seq = w4.LayerSeq(layers, io, 1, h, kv, ffn, swiglu=True)
+    assert seq.num_launches == 1
+    for rep in range(4):
+        for name in ("y_q", "y_k", "y_v", "y_o", "y_gu", "y_down"):
+            io[name].fill_(float("nan"))
+        seq.run()
+        assert seq.sync() == 0
+        for name in ("y_q", "y_k", "y_v", "y_o", "y_gu", "y_down"):
+            assert not torch.isnan(io[name]).any(), (rep, name)
+        for l in range(n):
+            ygu = io["y_gu"][l]
+            hh = oracle.swiglu(to_np_u16(ygu[:, :ffn]), to_np_u16(ygu[:, ffn:]))
+            qw, sc = layers[l]["down"]
+            qw_np, sc_np = to_np_u32(qw), to_np_u16(sc)
+            y_ref = oracle.gemv(qw_np, sc_np, hh)
+            rep_ = oracle.check_gemv(io["y_down"][l].double().cpu().numpy(), y_ref,
+                                     hh.view(np.float16).astype(np.float64),
+                                     float(oracle.row_norms(qw_np, sc_np).max()))
+            assert rep_["ok"], (rep, l, rep_)
+    seq.close()
