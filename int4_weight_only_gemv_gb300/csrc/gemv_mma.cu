@@ -1,46 +1,58 @@
-// gemv_mma.cu -- small-batch GEMV for M = 8..16 on the tensor cores.
+// gemv_mma.cu -- small-batch GEMV (M = 2..16) on the tensor cores.
 //
 // Same operation as the other GEMV kernels ("Costruire un runtime di
 // inference LLM da zero", "Tre bug che insegnano": INT4 group-128 weights x
-// FP16 activations, FP32 accumulation).  From M = 8 on, each weight feeds
-// eight or more products, so the contraction is dense enough for mma.sync
-// m16n8k16 (f16 x f16 -> f32).  W is the A operand (16 rows per warp), the
-// activations the B operand (8 activation rows per n-tile), so M = 16 is two
-// n-tiles sharing every unpacked A fragment.
+// FP16 activations, FP32 accumulation).  With M activation rows each weight
+// feeds M products, so the contraction runs on mma.sync m16n8k16
+// (f16 x f16 -> f32): W is the A operand (16 weight rows), the activations
+// the B operand (8 activation rows per n-tile; M <= 8 is one n-tile, M <= 16
+// two sharing every unpacked A fragment).  Below M = 8 the n-tile is padded
+// with zero columns: the tensor core has cycles to spare, the weight stream
+// is the bound.
 //
-// Layout of the work.  A cluster of KS CTAs owns a contiguous range of
-// 16-row blocks; CTA rank r of the cluster covers the r-th slice [gb, ge) of
-// the K groups, so it stages only that slice of x (once, in fragment order)
-// and reads every weight byte of its slice exactly once.
-//   warp 0      producer.  Streams the cluster's rows, W blocks (16 W rows)
-//               at a time, through an S-stage shared-memory ring with one
-//               2-D TMA load per stage: a box of 16 W rows x 32 packed words
-//               (two groups, 128 bytes per row), 128-byte swizzled, rows past
-//               N filled with zeros by the copy.
-//   warps 1..W  consumers.  Warp w takes rows 16 w .. 16 w + 15 of each box;
-//               lane (g, t) reads the 16 bytes of its rows g' = pi(g) and
-//               g' + 8 at word offset 4 t of each group (pi = 0 4 1 5 2 6 3 7
-//               puts the 8 lanes of every quarter-warp load on 8 distinct
-//               swizzled 16-byte chunks: no bank conflicts).  Word j of those
-//               16 bytes is super-step j: its exact-q halves {q0,q4},{q2,q6}
-//               are the A registers of one mma and {q1,q5},{q3,q7} those of a
-//               second (the order of k inside a contraction is free; the
-//               staged B fragments follow it).  Per group the mma partial is
-//               scaled by the group scales (read through L1) and added to
-//               FP32 accumulators that stay in registers over the K slice.
-// Split-K reduction.  Each CTA keeps its partial sums of every row of a pass
-// (a bounded number of the cluster's blocks) in shared memory; after the
-// pass the cluster synchronises and rank r finalises the entries r, r + KS,
-// ... by summing the KS partials through distributed shared memory in rank
-// order (deterministic, no atomics, no global workspace).  With KS = 1 the
-// consumers write y directly.  Every wait is bounded.
+// Layout of the work.  K is cut into 256-k ranges (two groups; 128 bytes of
+// a row; with an odd number of groups the last range is one group).  A
+// cluster of KS CTAs owns a contiguous run of 16-row blocks; CTA rank r of
+// the cluster owns ranges [r R, min(nr, (r + 1) R)), one per consumer warp,
+// so the warp's activations (its B fragments for every k-step and n-tile)
+// are loaded once into registers and reused for every block.
+//   warp 0      producer (one lane).  Per block: ONE 3-D TMA load of the
+//               rank's full ranges through a view of the packed weight as
+//               [row][range][32 words] (a box of 16 rows x R ranges x 128
+//               bytes, 128-byte swizzled; ranges past the row and rows past
+//               N are filled with zeros, not read), a 2-D load of the last
+//               half range (odd group count, last rank), and one bulk copy
+//               of the block's scale rows.  A copy per block and not per
+//               range: a thread's copy instructions, not the bytes, bound
+//               the stream at 2 KB per copy.  S stages in flight.
+//   warp 1      reducer.  Sums the consumer warps' partials of a block in
+//               warp order; stores y (KS = 1) or pushes the CTA's partial to
+//               the block's owner rank in the cluster (KS > 1).
+//   warps 2..   consumers.  Warp w, lane (g, t) reads the 16 bytes at word
+//               4 t of each group of its range in its rows pi(g) and
+//               pi(g) + 8.  Rows pi(2q), pi(2q + 1) of a quarter-warp are d
+//               apart with d R = 4 (mod 8): their 128-byte lines then differ
+//               in bit 2 of the swizzle and the 8 lanes of every 16-byte load
+//               hit 8 distinct chunks (no bank conflicts; R a multiple of 8
+//               leaves a 2-way conflict).  Word j of those 16 bytes gives
+//               two mma k-steps: exact-q halves {q0,q4},{q2,q6} are the A
+//               registers of one and {q1,q5},{q3,q7} of the other (the order
+//               of k inside a contraction is free; the B fragments follow
+//               it).  The two groups' mma chains are interleaved; each
+//               group's partial is scaled by its scales and summed.
+// Split-K (KS > 1): owner rank of the cluster's i-th block is i mod KS; each
+// rank's partial lands in its own slot of the owner's shared memory, and
+// after one cluster barrier at the end the owners add the KS slots in rank
+// order.  Deterministic (fixed orders, no atomics, no global workspace);
+// every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include <map>
 #include <mutex>
-#include <utility>
+#include <tuple>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -49,42 +61,58 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kMmaMaxW = 16;            // consumer warps (16-row blocks per box)
-constexpr int kMmaThreads = 32 * (kMmaMaxW + 1);
-constexpr int kBoxWords = 32;           // box width: 32 packed words = 2 groups = 128 bytes
+constexpr int kMmaMaxRanges = 14;  // consumer warps: 16 warps of at most 128 registers fill the register file
+constexpr int kMmaMaxThreads = 32 * (2 + kMmaMaxRanges);
 constexpr int kMmaMaxStages = 8;
-constexpr int kMmaBarrierBytes = 256;   // [full S][empty S]
+constexpr int kMmaMaxCluster = 16;  // above the portable 8 only when K needs it
+constexpr int kRangeBytes = 2048;   // one TMA box: 16 rows x 32 packed words
+constexpr int kMmaBarrierBytes = 256;
+constexpr int kPartialBytes = 512;  // one warp's (or CTA's) partial of a block and n-tile: 32 lanes x float4
+constexpr int kRedBufs = 3;         // consumer partial buffers: consumers run up to 3 blocks ahead of the reducer
+constexpr uint32_t kTailBytes = 1024;  // the half range of a block: 16 rows x 64 bytes
 
 struct MmaParams {
   GemvArgs a;
-  int KS;            // CTAs per cluster = K slices
-  int W;             // consumer warps = 16-row blocks per box
-  int S;             // ring stages
-  int pass_blocks;   // 16-row blocks per reduction pass (KS > 1)
-  int x_bytes;       // bytes of the staged B fragments (max over ranks)
-  int part_bytes;    // bytes of the partial buffer (KS > 1)
-  int sc_bytes;      // bytes of the per-warp scale buffers (W x 16 rows x groups of a slice)
+  int KS;           // CTAs per cluster = K slices
+  int R;            // ranges per rank (the last rank may have fewer) = consumer warps
+  int Rb;           // ranges of the 3-D box: min(R, ranges of two groups)
+  int S;            // ring stages
+  int stage_bytes;  // Rb x 2048 (weights) [+ 1024: the half range] + scale rows of 16 weight rows, 1024-aligned
+  int red_bytes;    // kRedBufs x R x NT x 512: consumer partials
+  int part_bytes;   // owner slots (KS > 1): blocks owned x NT x KS x 512
 };
 
+// Not volatile: a pure function of its operands, so the compiler may
+// interleave independent accumulator chains.
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void named_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  const uint4 u = lds_u4(addr);
+  return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+}
+
+__device__ __forceinline__ void add4(float4& s, const float4 v) {
+  s.x += v.x;
+  s.y += v.y;
+  s.z += v.z;
+  s.w += v.w;
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kMmaThreads, 1)
-    gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ MmaParams p) {
+__global__ void __launch_bounds__(kMmaMaxThreads, 1)
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_tail,
+                    const __grid_constant__ MmaParams p) {
+  constexpr int kCorrBytes = 64 * NT;  // a consumer warp's odd-lane corrections (two n-tiles): [group][nt][8] floats
   extern __shared__ __align__(1024) uint8_t smem[];
   const GemvArgs& a = p.a;
-  const int KS = p.KS, W = p.W, S = p.S;
+  const int KS = p.KS, S = p.S, R = p.R, Rb = p.Rb;
   const int rank = KS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int cluster = blockIdx.x / KS;
   const int nclusters = gridDim.x / KS;
@@ -93,284 +121,405 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   const int N = a.N;
   const int G = a.K / 128;
+  const int nr = (G + 1) / 2;               // 256-k ranges
+  const int nfull = G / 2;                  // ranges of two groups (the last one is half when G is odd)
+  const int rb = rank * R;                  // this rank's ranges [rb, rb + nw)
+  const int nw = (nr - rb < R ? nr - rb : R);
+  const int nwf = nfull - rb < 0 ? 0 : (nfull - rb < nw ? nfull - rb : nw);  // full ones among them
+  const bool has_tail = nwf < nw;           // the half range is this rank's last
   const int T16 = (N + 15) / 16;
-  const int blk_begin = static_cast<int>((static_cast<int64_t>(T16) * cluster) / nclusters);
-  const int blk_end = static_cast<int>((static_cast<int64_t>(T16) * (cluster + 1)) / nclusters);
-  const int gb = (G * rank) / KS;
-  const int ge = (G * (rank + 1)) / KS;
-  const int box_first = gb / 2;                   // boxes covering groups [gb, ge)
-  const int box_last = ge > gb ? (ge - 1) / 2 : box_first - 1;
-  const int nbox = box_last - box_first + 1;
-  const int pass_blocks = KS > 1 ? p.pass_blocks : (blk_end - blk_begin);
+  const int blk0 = static_cast<int>((static_cast<int64_t>(T16) * cluster) / nclusters);
+  const int nblk = static_cast<int>((static_cast<int64_t>(T16) * (cluster + 1)) / nclusters) - blk0;
 
-  // shared layout: barriers | B fragments | partials | scales | stages (1024-aligned)
-  const uint32_t full0 = smem_addr(smem);
-  const uint32_t empty0 = full0 + 8 * S;
-  const uint32_t xf0 = full0 + kMmaBarrierBytes;
-  const uint32_t part0 = xf0 + p.x_bytes;
-  const uint32_t sc0 = part0 + p.part_bytes;
-  const uint32_t stage0 = (sc0 + p.sc_bytes + 1023) & ~1023u;
-  const uint32_t stage_bytes = 16 * W * 128;
+  // shared layout: barriers | consumer partials | corrections | owner slots | stages (1024-aligned)
+  // stage: [16 rows][Rb ranges][128 bytes] swizzled | [16 rows][64 bytes] half range (odd G) | scale rows
+  const uint32_t bar0 = smem_addr(smem);
+  const uint32_t full0 = bar0;
+  const uint32_t empty0 = bar0 + 8 * S;
+  const uint32_t rfull0 = bar0 + 16 * S;
+  const uint32_t rempty0 = rfull0 + 8 * kRedBufs;
+  const uint32_t red0 = bar0 + kMmaBarrierBytes;
+  const uint32_t corr0 = red0 + p.red_bytes;
+  const uint32_t part0 = corr0 + static_cast<uint32_t>(R * kCorrBytes);
+  const uint32_t stage0 = (part0 + p.part_bytes + 1023) & ~1023u;
+  const uint32_t tail_off = static_cast<uint32_t>(Rb) * kRangeBytes;
+  const uint32_t sc_off = tail_off + ((G & 1) ? kTailBytes : 0u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, W);
+      mbar_init(empty0 + 8 * s, nw);
+    }
+    for (int b = 0; b < kRedBufs; ++b) {
+      mbar_init(rfull0 + 8 * b, nw);
+      mbar_init(rempty0 + 8 * b, 1);
     }
     fence_barrier_init();
   }
   __syncthreads();
+  // Every CTA of the cluster must have started before shared memory of
+  // another is written: the reducer waits for this before its first push.
+  if (KS > 1) cluster_arrive_relaxed();
   pdl_launch_dependents();
+
+  // A wait whose outcome every lane of the warp shares (the cluster barriers
+  // at the end are executed by whole warps).
+  auto warp_wait = [](uint32_t bar, uint32_t parity) {
+    const bool r = mbar_wait_bounded(bar, parity, kWaitLimitNs);
+    return __all_sync(0xffffffffu, r);
+  };
+
+  // lane's place in the mma fragments: row group g8 holds weight rows
+  // pi, pi + 8 of the block; the two rows of a quarter-warp are d apart,
+  // d Rb = 4 (mod 8)
+  const int g8 = lane >> 2;
+  const int t4 = lane & 3;
+  const int pi = (Rb & 1) ? (((g8 & 1) << 2) | (g8 >> 1))                                // d = 4: 0 4 1 5 2 6 3 7
+                          : ((Rb & 3) == 2 ? ((g8 & 4) | ((g8 & 1) << 1) | ((g8 >> 1) & 1))  // d = 2: 0 2 1 3 4 6 5 7
+                                           : g8);                                        // d = 1
+
+  // Where y[m][n] goes for every m: n's segment, pointer to its element of
+  // activation row 0, row stride, bias (0 without); null past N.
+  struct RowOut {
+    uint16_t* y;
+    int64_t ldy;
+    float bias;
+  };
+  auto row_out = [&](int64_t n) {
+    RowOut r{nullptr, 0, 0.f};
+    if (n >= N) return r;
+    int sg = 0;
+    int64_t n0 = 0;
+    if (a.nseg > 1 && n >= a.seg[0].n_end) {
+      n0 = a.seg[0].n_end;
+      sg = 1;
+      if (a.nseg > 2 && n >= a.seg[1].n_end) {
+        n0 = a.seg[1].n_end;
+        sg = 2;
+      }
+    }
+    r.y = a.seg[sg].y + (n - n0);
+    r.ldy = a.seg[sg].ldy;
+    if (a.seg[sg].bias != nullptr) r.bias = __half2float(__ushort_as_half(__ldg(a.seg[sg].bias + (n - n0))));
+    return r;
+  };
+  // y of one block from the sums of lane's four fragment entries per
+  // n-tile: rows pi, pi + 8 of the block, activation rows 8 nt + 2 t4, + 1;
+  // y = fp16_RN(sum + bias)
+  auto store_block = [&](int blk, const float4 (&v)[NT]) {
+    const RowOut ra = row_out(16 * static_cast<int64_t>(blk) + pi);
+    const RowOut rc = row_out(16 * static_cast<int64_t>(blk) + pi + 8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int m0 = nt * 8 + 2 * t4;
+      if (m0 < a.M) {
+        if (ra.y) ra.y[m0 * ra.ldy] = __half_as_ushort(__float2half_rn(v[nt].x + ra.bias));
+        if (rc.y) rc.y[m0 * rc.ldy] = __half_as_ushort(__float2half_rn(v[nt].z + rc.bias));
+      }
+      if (m0 + 1 < a.M) {
+        if (ra.y) ra.y[(m0 + 1) * ra.ldy] = __half_as_ushort(__float2half_rn(v[nt].y + ra.bias));
+        if (rc.y) rc.y[(m0 + 1) * rc.ldy] = __half_as_ushort(__float2half_rn(v[nt].w + rc.bias));
+      }
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol = policy_evict_first();
-    int s = 0, g = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    // After a failed wait the producer issues nothing more but still takes
-    // part in every cluster barrier, so no CTA of the cluster waits forever.
-    for (int pb = blk_begin; pb < blk_end; pb += pass_blocks) {
-      const int pe = pb + pass_blocks < blk_end ? pb + pass_blocks : blk_end;
-      for (int cb = pb; cb < pe && ok; cb += W) {
-        for (int b = 0; b < nbox; ++b) {
-          if (g >= S && !mbar_wait_bounded(empty0 + 8 * s, phase ^ 1u, kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            const uint32_t bar = full0 + 8 * s;
-            // checked build: the box starts inside the matrix (TMA fills the
-            // part of a box past the matrix with zeros)
-            const bool in = W4A16_IN(a.status, (box_first + b) * kBoxWords < a.K / 8 && cb * 16 < a.N);
-            mbar_arrive_expect_tx(bar, in ? stage_bytes : 0u);
-            if (in) tma_load_2d(stage0 + s * stage_bytes, &tmap, (box_first + b) * kBoxWords, cb * 16, bar, pol);
-          }
-          __syncwarp();
-          ++g;
-          if (++s == S) {
-            s = 0;
-            phase ^= 1u;
-          }
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const uint64_t pol_sc = policy_evict_normal();  // scale rows: every rank of the cluster reads them
+      const uint32_t tx = (nwf > 0 ? static_cast<uint32_t>(Rb) * kRangeBytes : 0u) + (has_tail ? kTailBytes : 0u);
+      bool ok = true;
+      int i = 0;
+      int s = 0;        // stage of block i
+      uint32_t ph = 0;  // parity of the stage's round (i / S)
+      uint32_t st = stage0;
+      for (; i < nblk; ++i) {
+        if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const int blk = blk0 + i;
+        const uint32_t bar = full0 + 8 * s;
+        // scale rows of the block: 16 rows x G fp16 (a whole multiple of 16
+        // bytes except in a last block of fewer rows, whose last few bytes
+        // are copied here before the barrier's arrival publishes them)
+        const int rows = N - 16 * blk < 16 ? N - 16 * blk : 16;
+        const uint32_t sc_bytes = static_cast<uint32_t>(rows) * G * 2;
+        const uint32_t sc_bulk = sc_bytes & ~15u;
+        const uint16_t* sc_src = a.scales + static_cast<int64_t>(blk) * 16 * G;
+        for (uint32_t b = sc_bulk; b < sc_bytes; b += 2)
+          sts_u16(st + sc_off + b, ld_nc_u16(sc_src + b / 2));
+        mbar_arrive_expect_tx(bar, tx + sc_bulk);
+        // checked build: the boxes start inside the matrix
+        if (nwf > 0 && W4A16_IN(a.status, rb < nfull && 16 * blk < N))
+          tma_load_3d(st, &tmap, 0, rb, 16 * blk, bar, pol);
+        if (has_tail && W4A16_IN(a.status, 16 * (G - 1) < a.K / 8 && 16 * blk < N))
+          tma_load_2d(st + tail_off, &tmap_tail, 16 * (G - 1), 16 * blk, bar, pol);
+        if (sc_bulk > 0) bulk_g2s(st + sc_off, sc_src, sc_bulk, bar, pol_sc);
+        st += p.stage_bytes;
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+          st = stage0;
         }
       }
-      if (KS > 1) {
-        cluster_sync();  // the pass's partials have been pushed to their owners
-        if (pe < blk_end) cluster_sync();  // and summed: the buffers may be reused
+      if (!ok) {
+        atomicOr(a.status, W4A16_DEV_PIPE_TIMEOUT);
+        // the copies in flight land before the CTA may exit
+        for (int j = i - S > 0 ? i - S : 0; j < i; ++j)
+          mbar_wait_bounded(full0 + 8 * (j % S), (j / S) & 1, kWaitLimitNs);
       }
     }
-    if (!ok) {
-      if (lane == 0) atomicOr(a.status, W4A16_DEV_PIPE_TIMEOUT);
-      for (int v = 0; v < S; ++v) {
-        const int gg = g - S + v;
-        if (gg >= 0) mbar_wait_bounded(full0 + 8 * ((s + v) % S), (gg / S) & 1, kWaitLimitNs);
-      }
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int w = warp - 1;
-  const int g8 = lane >> 2;  // fragment row group
-  const int t4 = lane & 3;   // thread in group
-  const int pi = ((g8 & 1) << 2) | (g8 >> 1);  // 0 4 1 5 2 6 3 7
-  const int ct = threadIdx.x - 32;              // consumer thread index
-  const int nct = 32 * W;
-
-  const int ngs = ge - gb;  // groups of this rank's slice
-  const uint16_t* scales = a.scales;
-  // Scales of a warp's 16 rows x the slice's groups go to its own buffer:
-  // [row in block][group - gb] fp16 (rows past N read row N - 1).  The
-  // loads are issued in batches of 16 per lane before any of them is used.
-  auto stage_scales = [&](int blk, uint32_t scw) {
-    for (int i0 = lane; i0 < 16 * ngs; i0 += 16 * 32) {
-      uint16_t v[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int i = i0 + 32 * q;
-        const int r = blk * 16 + i / ngs;
-        v[q] = i < 16 * ngs ? ld_nc_u16(scales + static_cast<int64_t>(r < N ? r : N - 1) * G + gb + i % ngs)
-                            : static_cast<uint16_t>(0);
-      }
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        if (i0 + 32 * q < 16 * ngs) sts_u16(scw + 2 * (i0 + 32 * q), v[q]);
-    }
-  };
-  const uint32_t scw = sc0 + static_cast<uint32_t>(w * 16 * ngs) * 2;
-  // the first chunk's scales (weights and scales are constant: no need to
-  // wait for the previous kernel)
-  if (blk_begin + w < (blk_begin + pass_blocks < blk_end ? blk_begin + pass_blocks : blk_end))
-    stage_scales(blk_begin + w, scw);
-
-  pdl_wait();  // x may be the previous kernel's output
-  // ---- stage this rank's slice of x as B fragments:
-  // [group][nt][super-step j][lane] x 16 bytes = {x0,x4} {x2,x6} {x1,x5} {x3,x7}
-  // of column m = 8 nt + lane / 4, k = 128 group + 32 (lane % 4) + 8 j
-  {
-    const int entries = (ge - gb) * NT * 4 * 32;
-    constexpr int kBatch = 8;  // loads in flight per thread
-    for (int e0 = ct; e0 < entries; e0 += kBatch * nct) {
-      uint4 v[kBatch];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int e = e0 + i * nct;
-        const int ln = e & 31;
-        const int j = (e >> 5) & 3;
-        const int nt = (e >> 7) % NT;
-        const int gl = (e >> 7) / NT;
-        const int m = nt * 8 + (ln >> 2);
-        const int k0 = (gb + gl) * 128 + 32 * (ln & 3) + 8 * j;
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (e < entries && m < a.M && W4A16_IN(a.status, k0 + 8 <= a.K && 16 * e + 16 <= p.x_bytes))
-          v[i] = ld_u4(a.x + m * a.ldx + k0);
-      }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int e = e0 + i * nct;
-        if (e >= entries) break;
-        uint4 f;
-        f.x = __byte_perm(v[i].x, v[i].z, 0x5410);  // {x0, x4}
-        f.y = __byte_perm(v[i].y, v[i].w, 0x5410);  // {x2, x6}
-        f.z = __byte_perm(v[i].x, v[i].z, 0x7632);  // {x1, x5}
-        f.w = __byte_perm(v[i].y, v[i].w, 0x7632);  // {x3, x7}
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xf0 + 16 * e), "r"(f.x), "r"(f.y),
-                     "r"(f.z), "r"(f.w)
-                     : "memory");
-      }
-    }
-  }
-  named_sync(1, nct);
-
-  int s = 0;
-  uint32_t phase = 0;
-  // after a failed wait the warp computes nothing more but still takes part
-  // in every cluster barrier
-  bool ok = true;
-  for (int pb = blk_begin; pb < blk_end; pb += pass_blocks) {
-    const int pe = pb + pass_blocks < blk_end ? pb + pass_blocks : blk_end;
-    for (int cb = pb; cb < pe; cb += W) {
-      // rows of this warp in the box: 16 w + pi and 16 w + pi + 8
-      const int blk = cb + w;
-      const int ra = blk * 16 + pi;
-      const int rb = ra + 8;
-      const bool live = blk < pe;  // block inside the pass (rows < N checked at the store)
-      float acc[NT][4];
+    __syncwarp();
+  } else if (warp >= 2) {
+    // -------------------------------------------------------------- consumers
+    const int w = warp - 2;
+    const int rg = rb + w;  // this warp's range
+    // TWO: a range of two groups; else the half range (one group) at the end
+    // of a row with an odd group count.  Two copies of the loop, so that the
+    // hot one tests nothing about it.
+    auto consume = [&](auto two_tag) {
+      constexpr bool TWO = decltype(two_tag)::value;
+      constexpr int NG = TWO ? 2 : 1;
+      pdl_wait();  // x may be the previous kernel's output
+      // B fragments of the range: [nt][group jj][super-step j] =
+      // {x0,x4} {x2,x6} {x1,x5} {x3,x7} of activation row 8 nt + g8 at
+      // k = 128 (2 rg + jj) + 32 t4 + 8 j (zero past M); the odd-k halves
+      // {x1,x5} {x3,x7} divided by 16 (unpack_mma leaves their weights as
+      // 1152 + 16 q): exact in fp16 down to |x| = 2^-10, below it rounded to
+      // a subnormal.
+      const __half2 sixteenth = __half2half2(__ushort_as_half(0x2C00));
+      uint4 bx[NT][NG][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-      // scales of this chunk (the first chunk's were staged up front)
-      if (live && cb != blk_begin) {
-        __syncwarp();  // the previous chunk's scales have been read
-        stage_scales(blk, scw);
-      }
-      __syncwarp();
-      for (int b = 0; b < nbox; ++b) {
-        if (ok && !mbar_wait_bounded(full0 + 8 * s, phase, kWaitLimitNs)) {
-          if (lane == 0) atomicOr(a.status, W4A16_DEV_PIPE_TIMEOUT);
-          ok = false;
-        }
-        const uint32_t base = stage0 + s * stage_bytes + (16 * w + pi) * 128;
-        if (live && ok) {
+        for (int jj = 0; jj < NG; ++jj)
 #pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            const int grp = 2 * (box_first + b) + jj;
-            if (grp < gb || grp >= ge) continue;  // the other rank's half of a shared box
-            const int c = ((4 * jj + t4) ^ pi) << 4;
-            const uint4 va = lds_u4(base + c);
-            const uint4 vb = lds_u4(base + 8 * 128 + c);
-            const float s_a = __half2float(__ushort_as_half(lds_u16(scw + 2 * (pi * ngs + grp - gb))));
-            const float s_b = __half2float(__ushort_as_half(lds_u16(scw + 2 * ((pi + 8) * ngs + grp - gb))));
-            float d[NT][4];
+          for (int j = 0; j < 4; ++j) {
+            const int m = nt * 8 + g8;
+            const int k0 = 128 * (2 * rg + jj) + 32 * t4 + 8 * j;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (m < a.M && W4A16_IN(a.status, k0 + 8 <= a.K)) v = ld_u4(a.x + m * a.ldx + k0);
+            bx[nt][jj][j].x = __byte_perm(v.x, v.z, 0x5410);
+            bx[nt][jj][j].y = __byte_perm(v.y, v.w, 0x5410);
+            uint32_t o = __byte_perm(v.x, v.z, 0x7632);
+            __half2 h = __hmul2(*reinterpret_cast<__half2*>(&o), sixteenth);
+            bx[nt][jj][j].z = *reinterpret_cast<uint32_t*>(&h);
+            o = __byte_perm(v.y, v.w, 0x7632);
+            h = __hmul2(*reinterpret_cast<__half2*>(&o), sixteenth);
+            bx[nt][jj][j].w = *reinterpret_cast<uint32_t*>(&h);
+          }
+      // What the biased odd lanes add per group: 1152 (x / 16) summed over
+      // the group's odd k, for each activation row (FP32, exact products):
+      // this lane's odd k, then the 4 lanes of row group g8.  Each block's
+      // mma chains start from minus it, for the two activation rows of this
+      // lane's D entries (8 nt + 2 t4, + 1): kept in registers with one
+      // n-tile, in shared memory with two (registers are short there).
+      float corr[NG][NT][2];
+#pragma unroll
+      for (int jj = 0; jj < NG; ++jj)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float c = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            c += 1152.f * (half_lo(bx[nt][jj][j].z) + half_hi(bx[nt][jj][j].z));
+            c += 1152.f * (half_lo(bx[nt][jj][j].w) + half_hi(bx[nt][jj][j].w));
+          }
+          c += __shfl_xor_sync(0xffffffffu, c, 1);
+          c += __shfl_xor_sync(0xffffffffu, c, 2);
+          if (NT == 1) {
+            corr[jj][nt][0] = __shfl_sync(0xffffffffu, c, 8 * t4);
+            corr[jj][nt][1] = __shfl_sync(0xffffffffu, c, 8 * t4 + 4);
+          } else if (t4 == 0) {
+            sts_f32(corr0 + static_cast<uint32_t>(w * kCorrBytes + ((jj * NT + nt) * 8 + g8) * 4), c);
+          }
+        }
+      __syncwarp();
+      const uint32_t corr_lane = corr0 + static_cast<uint32_t>(w * kCorrBytes + 8 * t4);
+      // this lane's 16 bytes of rows pi and pi + 8 in a stage, per group
+      const uint32_t line = static_cast<uint32_t>(pi * Rb + w);
+      const uint32_t row_a = TWO ? line * 128 : tail_off + pi * 64;
+      const uint32_t row_b = TWO ? row_a + 8 * Rb * 128 : row_a + 8 * 64;
+      uint32_t chunk[NG];
+#pragma unroll
+      for (int jj = 0; jj < NG; ++jj)
+        chunk[jj] = TWO ? ((static_cast<uint32_t>(4 * jj + t4) ^ (line & 7u)) << 4) : static_cast<uint32_t>(t4) << 4;
+      const uint32_t sc_a = sc_off + 2 * (pi * G + 2 * rg);  // scale of row pi, group 2 rg
+      const uint32_t sc_b = sc_a + 16 * G;                   // row pi + 8
+      int s = 0;         // stage of block i
+      uint32_t ph = 0;   // parity of its round
+      uint32_t st = stage0;
+      int b = 0;         // partial buffer of block i
+      uint32_t rph = 0;  // parity of its round
+      for (int i = 0; i < nblk; ++i) {
+        if (!warp_wait(full0 + 8 * s, ph)) {
+          if (lane == 0) atomicOr(a.status, W4A16_DEV_PIPE_TIMEOUT);
+          break;
+        }
+        uint4 va[NG], vb[NG];
+        float s_a[NG], s_b[NG];
+#pragma unroll
+        for (int jj = 0; jj < NG; ++jj) {
+          va[jj] = lds_u4(st + row_a + chunk[jj]);
+          vb[jj] = lds_u4(st + row_b + chunk[jj]);
+          s_a[jj] = __half2float(__ushort_as_half(lds_u16(st + sc_a + 2 * jj)));
+          s_b[jj] = __half2float(__ushort_as_half(lds_u16(st + sc_b + 2 * jj)));
+        }
+        // Accumulator chains: per group and n-tile, and with one n-tile the
+        // two k-steps of a word apart too (four chains either way).  The
+        // odd-k chain starts from minus the group's correction.
+        constexpr int kH = NT == 1 ? 2 : 1;
+        float d[kH][NG][NT][4];
+#pragma unroll
+        for (int jj = 0; jj < NG; ++jj)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float c0, c1;
+            if (NT == 1) {
+              c0 = corr[jj][nt][0];
+              c1 = corr[jj][nt][1];
+            } else {
+              const uint2 c = lds_u2(corr_lane + static_cast<uint32_t>((jj * NT + nt) * 32));
+              c0 = __uint_as_float(c.x);
+              c1 = __uint_as_float(c.y);
+            }
+            d[kH - 1][jj][nt][0] = -c0;
+            d[kH - 1][jj][nt][1] = -c1;
+            d[kH - 1][jj][nt][2] = -c0;
+            d[kH - 1][jj][nt][3] = -c1;
+            if (kH == 2) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) d[0][jj][nt][q] = 0.f;
+            }
+          }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          Unpacked qa[NG], qb[NG];
+#pragma unroll
+          for (int jj = 0; jj < NG; ++jj) {
+            const uint32_t wa = j == 0 ? va[jj].x : (j == 1 ? va[jj].y : (j == 2 ? va[jj].z : va[jj].w));
+            const uint32_t wb = j == 0 ? vb[jj].x : (j == 1 ? vb[jj].y : (j == 2 ? vb[jj].z : vb[jj].w));
+            qa[jj] = unpack_mma(wa);
+            qb[jj] = unpack_mma(wb);
+          }
+#pragma unroll
+          for (int jj = 0; jj < NG; ++jj)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
+              mma_16816(d[0][jj][nt], qa[jj].h0, qb[jj].h0, qa[jj].h2, qb[jj].h2, bx[nt][jj][j].x, bx[nt][jj][j].y);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) d[nt][q] = 0.f;
-            const uint32_t wa4[4] = {va.x, va.y, va.z, va.w};
-            const uint32_t wb4[4] = {vb.x, vb.y, vb.z, vb.w};
-            const uint32_t xg = xf0 + static_cast<uint32_t>(grp - gb) * NT * 4 * 32 * 16 + 16 * lane;
+          for (int jj = 0; jj < NG; ++jj)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const Unpacked qa = unpack_exact(wa4[j]);
-              const Unpacked qb = unpack_exact(wb4[j]);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                const uint4 bf = lds_u4(xg + (nt * 4 + j) * 32 * 16);
-                mma_16816(d[nt], qa.h0, qb.h0, qa.h2, qb.h2, bf.x, bf.y);
-                mma_16816(d[nt], qa.h1, qb.h1, qa.h3, qb.h3, bf.z, bf.w);
-              }
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              acc[nt][0] = fmaf(s_a, d[nt][0], acc[nt][0]);
-              acc[nt][1] = fmaf(s_a, d[nt][1], acc[nt][1]);
-              acc[nt][2] = fmaf(s_b, d[nt][2], acc[nt][2]);
-              acc[nt][3] = fmaf(s_b, d[nt][3], acc[nt][3]);
-            }
-          }
+            for (int nt = 0; nt < NT; ++nt)
+              mma_16816(d[kH - 1][jj][nt], qa[jj].h1, qb[jj].h1, qa[jj].h3, qb[jj].h3, bx[nt][jj][j].z,
+                        bx[nt][jj][j].w);
         }
         __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(empty0 + 8 * s);
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        st += p.stage_bytes;
         if (++s == S) {
           s = 0;
-          phase ^= 1u;
+          ph ^= 1u;
+          st = stage0;
+        }
+        // the block's partial: per D entry, the groups' sums times their scales
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float v = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < NG; ++jj) {
+              const float g = kH == 2 ? d[0][jj][nt][q] + d[kH - 1][jj][nt][q] : d[0][jj][nt][q];
+              v = fmaf(q < 2 ? s_a[jj] : s_b[jj], g, v);
+            }
+            acc[nt][q] = v;
+          }
+        if (i >= kRedBufs && !warp_wait(rempty0 + 8 * b, rph ^ 1u)) {
+          if (lane == 0) atomicOr(a.status, W4A16_DEV_PIPE_TIMEOUT);
+          break;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t off = static_cast<uint32_t>(((b * R + w) * NT + nt) * kPartialBytes + 16 * lane);
+          if (W4A16_IN(a.status, off + 16 <= static_cast<uint32_t>(p.red_bytes)))
+            sts_u4(red0 + off, __float_as_uint(acc[nt][0]), __float_as_uint(acc[nt][1]),
+                   __float_as_uint(acc[nt][2]), __float_as_uint(acc[nt][3]));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rfull0 + 8 * b);
+        if (++b == kRedBufs) {
+          b = 0;
+          rph ^= 1u;
         }
       }
-      // D layout: d[0], d[1] = row g', columns 2 t, 2 t + 1; d[2], d[3] = row g' + 8
-      if (live) {
-        if (KS == 1) {
+    };
+    if (w < nwf)
+      consume(std::true_type{});
+    else if (w < nw)
+      consume(std::false_type{});
+  } else {
+    // ---------------------------------------------------------------- reducer
+    pdl_wait();  // y may still be read by the previous kernel
+    if (KS > 1) cluster_wait();
+    for (int i = 0; i < nblk; ++i) {
+      const int b = i % kRedBufs;
+      if (!warp_wait(rfull0 + 8 * b, (i / kRedBufs) & 1)) {
+        if (lane == 0) atomicOr(a.status, W4A16_DEV_PIPE_TIMEOUT);
+        break;
+      }
+      // all partials loaded, then summed in a fixed order:
+      // (p0 + p2 + p4 + ...) + (p1 + p3 + ...)
+      float4 v[NT];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const int m0 = nt * 8 + 2 * t4;
-            if (ra < N) {
-              if (m0 < a.M) store_out(a, m0, ra, acc[nt][0]);
-              if (m0 + 1 < a.M) store_out(a, m0 + 1, ra, acc[nt][1]);
-            }
-            if (rb < N) {
-              if (m0 < a.M) store_out(a, m0, rb, acc[nt][2]);
-              if (m0 + 1 < a.M) store_out(a, m0 + 1, rb, acc[nt][3]);
-            }
-          }
-        } else {
-          // Entry e = (row - 16 pb) 8 NT + m of the pass belongs to rank
-          // e mod KS; its partial from rank q goes to slot (e / KS) KS + q of
-          // the owner's buffer (remote stores, no waiting on them).
-          auto push = [&](int row, int m, float v) {
-            const int e = (row - 16 * pb) * 8 * NT + m;
-            const uint32_t local = part0 + 4 * static_cast<uint32_t>((e / KS) * KS + rank);
-            if (W4A16_IN(a.status, 4 * ((e / KS) * KS + rank) + 4 <= p.part_bytes))
-              st_cluster_f32(map_to_rank(local, static_cast<uint32_t>(e % KS)), v);
-          };
+      for (int nt = 0; nt < NT; ++nt) {
+        float4 part[kMmaMaxRanges];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const int m0 = nt * 8 + 2 * t4;
-            push(ra, m0, acc[nt][0]);
-            push(ra, m0 + 1, acc[nt][1]);
-            push(rb, m0, acc[nt][2]);
-            push(rb, m0 + 1, acc[nt][3]);
-          }
+        for (int w = 0; w < kMmaMaxRanges; ++w)
+          if (w < nw) part[w] = lds_f4(red0 + static_cast<uint32_t>(((b * R + w) * NT + nt) * kPartialBytes + 16 * lane));
+        float4 ve = part[0];
+        float4 vo = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 1; w < kMmaMaxRanges; ++w)
+          if (w < nw) add4((w & 1) ? vo : ve, part[w]);
+        v[nt] = ve;
+        add4(v[nt], vo);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rempty0 + 8 * b);
+      if (KS == 1) {
+        store_block(blk0 + i, v);
+      } else {
+        const uint32_t owner = static_cast<uint32_t>(i % KS);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t off =
+              static_cast<uint32_t>((((i / KS) * NT + nt) * KS + rank) * kPartialBytes + 16 * lane);
+          if (W4A16_IN(a.status, off + 16 <= static_cast<uint32_t>(p.part_bytes)))
+            st_cluster_v4(map_to_rank(part0 + off, owner), v[nt]);
         }
       }
     }
-    if (KS > 1) {
-      cluster_sync();  // every rank's partials of the pass have arrived at their owners
-      const int per_row = 8 * NT;
-      const int total = (pe - pb) * 16 * per_row;
-      // this rank owns entries e = rank, rank + KS, ...: sum the KS slots of
-      // each in rank order (local shared memory only)
-      for (int i = ct; i * KS + rank < total; i += nct) {
-        const int e = i * KS + rank;
-        const int row = e / per_row;
-        const int m = e % per_row;
-        const int n = 16 * pb + row;
-        if (m >= a.M || n >= N) continue;
-        const uint32_t addr = part0 + 4 * static_cast<uint32_t>(i * KS);
-        float v = 0.f;
-        for (int q = 0; q < KS; ++q) v += lds_f32(addr + 4 * q);
-        store_out(a, m, n, v);
+  }
+
+  if (KS > 1) {
+    if (warp != 1) cluster_wait();
+    cluster_sync();  // every rank's partials are in their owners' slots
+    if (warp == 1) {
+      for (int i = rank; i < nblk; i += KS) {
+        float4 v[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          v[nt] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < KS; ++q)
+            add4(v[nt], lds_f4(part0 + static_cast<uint32_t>((((i / KS) * NT + nt) * KS + q) * kPartialBytes +
+                                                             16 * lane)));
+        }
+        store_block(blk0 + i, v);
       }
-      if (pe < blk_end) cluster_sync();  // the buffers may be rewritten by the next pass
     }
   }
 }
@@ -397,30 +546,50 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 namespace {
 
-// Tensor map of the packed weight as uint32 [N][K/8], box 32 words x rows,
-// 128-byte swizzle.
-bool weight_tensor_map(CUtensorMap* m, const uint32_t* qweight, int N, int K, int box_rows) {
+// Tensor maps of the packed weight (uint32 [N][K/8]).  view3: the two-group
+// ranges of each row as [N][K/256][32 words], box 32 words x rb ranges x 16
+// rows, 128-byte swizzle (ranges past the row's last two-group range read as
+// zeros).  tail: [N][K/8] with a box of 16 words x 16 rows, no swizzle (the
+// one-group range at the end of a row when K/128 is odd).
+bool weight_tensor_maps(CUtensorMap* view3, CUtensorMap* tail, const uint32_t* qweight, int N, int K, int rb) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 8) * 4};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBoxWords), static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(qweight), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const int G = K / 128;
+  *view3 = CUtensorMap{};
+  *tail = CUtensorMap{};
+  if (G / 2 > 0) {
+    const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(G / 2), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(K / 2)};
+    const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(rb), 16};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(view3, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(qweight), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  if (G & 1) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    const cuuint32_t box[2] = {16, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(tail, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(qweight), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
 }
 
-// How many clusters of `ks` CTAs of this kernel the GPU holds at once
-// (clusters must fit inside one GPC, so large clusters can leave SMs idle).
-// Cached per device: the query is not free.
+// How many clusters of `ks` CTAs of this kernel (threads, smem bytes each)
+// the GPU holds at once.  A cluster must fit inside one GPC, so large
+// clusters can leave SMs idle.  Cached per device: the query is not free.
 template <int NT>
-int max_active_clusters(int ks, int smem) {
+int max_active_clusters(int ks, int threads, int smem) {
   static std::mutex mu;
-  static std::map<std::pair<int, int>, int> cache;  // (device * 16 + ks, smem) -> clusters
+  static std::map<std::tuple<int, int, int, int>, int> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  const std::pair<int, int> key(dev * 16 + ks, smem);
+  const auto key = std::make_tuple(dev, ks, threads, smem);
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -428,7 +597,7 @@ int max_active_clusters(int ks, int smem) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ks * 64);
-  cfg.blockDim = dim3(kMmaThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -448,60 +617,55 @@ int max_active_clusters(int ks, int smem) {
 }
 
 struct MmaPlan {
-  int KS = 0, clusters = 0, W = 0, S = 0, pass_blocks = 0, x_bytes = 0, part_bytes = 0, sc_bytes = 0, smem = 0;
+  int KS = 0, clusters = 0, R = 0, Rb = 0, S = 0, stage_bytes = 0, red_bytes = 0, part_bytes = 0, smem = 0;
 };
 
-// Choose the K split (cluster size): every rank's x slice must fit next to a
-// ring of at least 3 stages; among those, keep the most SMs streaming with
-// enough warps (clusters x ranks x min(8, blocks per cluster)), then the
-// smaller split.
+// Choose the K split (cluster size).  Each split gives the ranks
+// R = ceil(ranges / KS) ranges (at most kMmaMaxRanges warps; the last rank
+// the rest, at least one), and as many
+// clusters as the GPU holds at once share the 16-row blocks.  The critical
+// path is the bytes the busiest CTA streams: blocks per cluster x (its
+// ranges' weights + the blocks' scale rows); the smallest wins, ties going
+// to the smaller split.  Every split needs a ring of at least 2 stages.
 template <int NT>
 MmaPlan make_mma_plan(const GemvArgs& a, const DeviceInfo& d) {
   MmaPlan best{};
-  int64_t best_score = -1;
-  const int T16 = (a.N + 15) / 16;
+  int64_t best_cost = -1;
   const int G = a.K / 128;
-  const int smem_cap = d.max_smem_optin;
-  // any cluster size up to the portable 8: a GPC holds a whole number of
-  // clusters, so sizes that are not powers of two can cover more SMs
-  for (int ks = 1; ks <= 8 && ks <= G; ++ks) {
-    const int x_bytes = ((G + ks - 1) / ks) * NT * 4 * 32 * 16;
-    const int active = max_active_clusters<NT>(ks, smem_cap);
+  const int nr = (G + 1) / 2;
+  const int T16 = (a.N + 15) / 16;
+  const int cap = d.max_smem_optin;
+  const int sc_row_block = 16 * G * 2;  // scale bytes of a 16-row block
+  for (int ks = 1; ks <= kMmaMaxCluster && ks <= nr; ++ks) {
+    const int R = (nr + ks - 1) / ks;
+    if (R > kMmaMaxRanges || (ks - 1) * R >= nr) continue;
+    const int Rb = R < G / 2 ? R : G / 2;
+    const int stage = (Rb * kRangeBytes + ((G & 1) ? static_cast<int>(kTailBytes) : 0) + sc_row_block + 1023) & ~1023;
+    const int red = kRedBufs * R * NT * kPartialBytes;
+    const int threads = 32 * (2 + R);
+    const int active = max_active_clusters<NT>(ks, threads, cap);
     if (active <= 0) continue;
     const int clusters = T16 < active ? T16 : active;
-    const int blocks = (T16 + clusters - 1) / clusters;  // per cluster (upper bound)
-    const int W = blocks < kMmaMaxW ? blocks : kMmaMaxW;
-    const int stage = 16 * W * 128;
-    // partials of one pass: pass_blocks x 16 rows x 8 NT floats (KS > 1)
-    int pass_blocks = ks > 1 ? blocks : 0;
-    int avail = smem_cap - kMmaBarrierBytes - 1024 - x_bytes;
-    if (ks > 1) {
-      const int per_block = 16 * 8 * NT * 4;
-      const int max_pb = (avail - 3 * stage - ks * 4) / per_block;
-      if (max_pb < W) continue;
-      if (pass_blocks > max_pb) pass_blocks = max_pb / W * W;
-    }
-    // owner slots: ceil(entries / ks) x ks floats
-    const int part_bytes = ((pass_blocks * 16 * 8 * NT + ks - 1) / ks) * ks * 4;
-    const int sc_bytes = (W * 16 * ((G + ks - 1) / ks) * 2 + 15) & ~15;
-    avail -= part_bytes + sc_bytes;
+    const int nb = (T16 + clusters - 1) / clusters;  // blocks of the largest cluster
+    const int part = ks > 1 ? ((nb + ks - 1) / ks) * NT * ks * kPartialBytes : 0;
+    const int corr = R * 64 * NT;  // the consumer warps' odd-lane corrections
+    const int avail = cap - kMmaBarrierBytes - red - corr - part - 1023;
     int S = avail / stage;
     if (S > kMmaMaxStages) S = kMmaMaxStages;
-    if (S < 3) continue;
-    // SMs streaming, each with up to 8 busy warps (enough to keep its share
-    // of the bandwidth); ties go to the smaller split
-    const int64_t score = static_cast<int64_t>(clusters) * ks * (W < 8 ? W : 8);
-    if (score > best_score) {
-      best_score = score;
+    if (S > nb) S = nb > 2 ? nb : 2;
+    if (S < 2 || 16 * S + 16 * kRedBufs > kMmaBarrierBytes || avail < 2 * stage) continue;
+    const int64_t cost = static_cast<int64_t>(nb) * (R * kRangeBytes + sc_row_block);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
       best.KS = ks;
       best.clusters = clusters;
-      best.W = W;
+      best.R = R;
+      best.Rb = Rb;
       best.S = S;
-      best.pass_blocks = pass_blocks;
-      best.x_bytes = x_bytes;
-      best.part_bytes = part_bytes;
-      best.sc_bytes = sc_bytes;
-      best.smem = kMmaBarrierBytes + x_bytes + part_bytes + sc_bytes + 1023 + S * stage;
+      best.stage_bytes = stage;
+      best.red_bytes = red;
+      best.part_bytes = part;
+      best.smem = kMmaBarrierBytes + red + corr + part + 1023 + S * stage;
     }
   }
   return best;
@@ -511,20 +675,20 @@ template <int NT>
 cudaError_t launch_mma_nt(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
   const MmaPlan pl = make_mma_plan<NT>(a, d);
   if (pl.KS == 0) return cudaErrorInvalidConfiguration;
-  CUtensorMap tmap;
-  if (!weight_tensor_map(&tmap, a.qweight, a.N, a.K, 16 * pl.W)) return cudaErrorInvalidValue;
+  CUtensorMap tmap, tmap_tail;
+  if (!weight_tensor_maps(&tmap, &tmap_tail, a.qweight, a.N, a.K, pl.Rb)) return cudaErrorInvalidValue;
   MmaParams p;
   p.a = a;
   p.KS = pl.KS;
-  p.W = pl.W;
+  p.R = pl.R;
+  p.Rb = pl.Rb;
   p.S = pl.S;
-  p.pass_blocks = pl.pass_blocks;
-  p.x_bytes = pl.x_bytes;
+  p.stage_bytes = pl.stage_bytes;
+  p.red_bytes = pl.red_bytes;
   p.part_bytes = pl.part_bytes;
-  p.sc_bytes = pl.sc_bytes;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.clusters * pl.KS);
-  cfg.blockDim = dim3(32 * (pl.W + 1));
+  cfg.blockDim = dim3(32 * (2 + pl.R));
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -536,12 +700,17 @@ cudaError_t launch_mma_nt(const GemvArgs& a, const DeviceInfo& d, cudaStream_t s
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<NT>, tmap, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<NT>, tmap, tmap_tail, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
+
+bool gemv_mma_supported(int K) {
+  // ranges of a row split over at most kMmaMaxCluster ranks of kMmaMaxRanges
+  return K > 0 && K % 128 == 0 && (K / 128 + 1) / 2 <= kMmaMaxCluster * kMmaMaxRanges;
+}
 
 cudaError_t launch_gemv_mma(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
   if (a.M <= 8) return launch_mma_nt<1>(a, d, st);
@@ -552,8 +721,10 @@ cudaError_t prepare_gemv_mma(const DeviceInfo& d) {
   if (tensor_map_encoder() == nullptr) return cudaErrorNotSupported;
   const int limit = d.max_smem_optin;
   cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemv_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_mma_kernel<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_mma_kernel<2>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
 }
 
 }  // namespace w4a16

@@ -149,7 +149,9 @@ bool gemv_m1_tasks_fit(const M1Task* tasks, int n, bool a8, const DeviceInfo& d)
 int gemv_m1_split_tasks(const M1Task& t, bool a8, const DeviceInfo& d, M1Task* out);
 // M = 1..7 (any K): warp-per-row-block CUDA-core kernel.
 cudaError_t launch_gemv_rows(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
-// M = 8..16: mma.sync tensor-core kernel with cluster split-K.
+// M = 2..16: mma.sync tensor-core kernel with cluster split-K, for every K
+// that gemv_mma_supported accepts.
+bool gemv_mma_supported(int K);
 cudaError_t launch_gemv_mma(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 // Decode attention (attn_decode.cu): head dimension 128, at most 16 query
 // heads per KV head; arguments checked by the caller.

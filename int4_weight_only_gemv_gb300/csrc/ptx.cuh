@@ -106,10 +106,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// 3-D form of tma_load_2d: coordinates x (innermost, same alignment rule), y, z.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // L2 policy for data read exactly once (streamed weights).
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// L2 policy for data that other CTAs read soon after (kept at normal priority).
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 
@@ -135,6 +152,15 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// The two halves of cluster_sync, for a thread that has work to do in
+// between.  Each thread alternates them (arrive, wait, arrive, ...).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -145,6 +171,12 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
 // Store to shared memory of another CTA of the cluster (a mapa'd address).
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
@@ -161,6 +193,11 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
   return v;
 }
 __device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
@@ -279,6 +316,20 @@ __device__ __forceinline__ Unpacked unpack_biased(uint32_t w) {
   u.h2 = lop3_and_xor(w8, 0x000F000Fu, 0x64086408u);
   u.h3 = lop3_and_xor(w8, 0x00F000F0u, 0x64806480u);
   return u;
+}
+
+// For a tensor-core contraction: exact q in h0 = {q0,q4}, h2 = {q2,q6}, and
+// h1 = {1152 + 16 q1, 1152 + 16 q5}, h3 = {1152 + 16 q3, 1152 + 16 q7} left
+// as unpack_biased gives them (all exact in fp16).  Multiplied by x / 16,
+// an odd lane gives q x + 72 x: the caller takes 72 x off once per group.
+__device__ __forceinline__ Unpacked unpack_mma(uint32_t w) {
+  Unpacked b = unpack_biased(w);
+  const __half2 bias_lo = __half2half2(__ushort_as_half(0x6408));  // 1032
+  __half2 t = __hsub2(*reinterpret_cast<__half2*>(&b.h0), bias_lo);
+  b.h0 = *reinterpret_cast<uint32_t*>(&t);
+  t = __hsub2(*reinterpret_cast<__half2*>(&b.h2), bias_lo);
+  b.h2 = *reinterpret_cast<uint32_t*>(&t);
+  return b;
 }
 
 // Exact q as fp16 pairs: {q0,q4}, {q1,q5}, {q2,q6}, {q3,q7}.
