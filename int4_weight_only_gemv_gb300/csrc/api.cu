@@ -112,10 +112,12 @@ w4a16_status enqueue(const DeviceState& d, GemvArgs a, cudaStream_t st) {
   cudaError_t e;
   if (a.M == 1 && gemv_m1_supported(a.K))
     e = launch_gemv_m1(a, d.info, st);
-  else if (a.M >= 2 && gemv_mma_supported(a.K))
+  else if (a.M == 1)
+    e = launch_gemv_rows(a, d.info, st);
+  else if (gemv_mma_supported(a.K))
     e = launch_gemv_mma(a, d.info, st);
   else
-    e = launch_gemv_rows(a, d.info, st);
+    e = cudaErrorInvalidValue;
   if (e != cudaSuccess) {
     cudaGetLastError();
     return W4A16_ERR_CUDA;

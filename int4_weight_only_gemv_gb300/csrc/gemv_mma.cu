@@ -31,15 +31,19 @@
 //   warps 2..   consumers.  Warp w, lane (g, t) reads the 16 bytes at word
 //               4 t of each group of its range in its rows pi(g) and
 //               pi(g) + 8.  Rows pi(2q), pi(2q + 1) of a quarter-warp are d
-//               apart with d R = 4 (mod 8): their 128-byte lines then differ
+//               apart with d Rb = 4 (mod 8): their 128-byte lines then differ
 //               in bit 2 of the swizzle and the 8 lanes of every 16-byte load
 //               hit 8 distinct chunks (no bank conflicts; R a multiple of 8
 //               leaves a 2-way conflict).  Word j of those 16 bytes gives
-//               two mma k-steps: exact-q halves {q0,q4},{q2,q6} are the A
+//               two mma k-steps: halves {q0,q4},{q2,q6} (exact q) are the A
 //               registers of one and {q1,q5},{q3,q7} of the other (the order
 //               of k inside a contraction is free; the B fragments follow
-//               it).  The two groups' mma chains are interleaved; each
-//               group's partial is scaled by its scales and summed.
+//               it).  The second k-step's weights are left as the unpack's
+//               1152 + 16 q, exact in fp16, against x / 16: each product is
+//               q x + 72 x, and the chain starts from minus 72 x summed over
+//               the group (FP32, computed once per warp), which saves two
+//               instructions a word.  The groups' and n-tiles' mma chains are
+//               interleaved; each group's partial is scaled by its scale.
 // Split-K (KS > 1): owner rank of the cluster's i-th block is i mod KS; each
 // rank's partial lands in its own slot of the owner's shared memory, and
 // after one cluster barrier at the end the owners add the KS slots in rank

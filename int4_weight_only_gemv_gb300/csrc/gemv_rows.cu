@@ -1,9 +1,11 @@
-// gemv_rows.cu -- small-batch GEMV on the CUDA cores, M = 1..7 activation rows.
+// gemv_rows.cu -- GEMV on the CUDA cores for one activation row (M = 1) when K
+// is beyond the pipelined M = 1 kernel's range (gemv_m1.cu); the kernel is
+// written for M rows and instantiated for M = 1.
 //
 // Same operation as gemv_m1.cu (INT4 group-128 weights x FP16 activations,
 // FP32 accumulation; "Costruire un runtime di inference LLM da zero",
-// "Tre bug che insegnano"), for small-batch decode: every packed weight is
-// read from HBM once and multiplied by all M activation rows.
+// "Tre bug che insegnano"): every packed weight is read from HBM once and
+// multiplied by all M activation rows.
 //
 // Mapping: a CTA of 8 warps owns a block of R rows.  The 8 warps split K:
 // warp w, lane l walks the 16-k units u = 32 w + l + 256 i (two packed words
@@ -13,8 +15,7 @@
 // every CTA).  Nibbles are unpacked to exact fp16 q (ptx.cuh), multiplied in
 // f16 x f16 -> f32 FMAs and scaled per unit.  The R x M sums are reduced in a
 // fixed order (warp butterflies, then the 8 warps through shared memory), so
-// results are deterministic.  This kernel also serves M = 1 when K is beyond
-// the pipelined kernel's range.
+// results are deterministic.
 #include <cuda_fp16.h>
 
 #include "kernels.h"
@@ -175,16 +176,8 @@ cudaError_t launch_rows_m(const GemvArgs& a, cudaStream_t st) {
 
 cudaError_t launch_gemv_rows(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
   (void)d;
-  switch (a.M) {
-    case 1: return launch_rows_m<1>(a, st);
-    case 2: return launch_rows_m<2>(a, st);
-    case 3: return launch_rows_m<3>(a, st);
-    case 4: return launch_rows_m<4>(a, st);
-    case 5: return launch_rows_m<5>(a, st);
-    case 6: return launch_rows_m<6>(a, st);
-    case 7: return launch_rows_m<7>(a, st);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.M != 1) return cudaErrorInvalidValue;
+  return launch_rows_m<1>(a, st);
 }
 
 }  // namespace w4a16

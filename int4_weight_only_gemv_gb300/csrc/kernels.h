@@ -147,7 +147,8 @@ bool gemv_m1_tasks_fit(const M1Task* tasks, int n, bool a8, const DeviceInfo& d)
 // Writes 1 or 2 tasks to out and returns the count; dep and publish are
 // copied to both.
 int gemv_m1_split_tasks(const M1Task& t, bool a8, const DeviceInfo& d, M1Task* out);
-// M = 1..7 (any K): warp-per-row-block CUDA-core kernel.
+// M = 1 (any K; used when K is beyond the M = 1 kernel's range): CUDA-core
+// kernel with 8 warps per row block.
 cudaError_t launch_gemv_rows(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 // M = 2..16: mma.sync tensor-core kernel with cluster split-K, for every K
 // that gemv_mma_supported accepts.
