@@ -103,11 +103,29 @@ struct TaskPlan {
   int red_stride;    // floats per row in a partial slot (U + 1)
 };
 
+// a / b for a >= 0, b >= 1, computed at task starts.  On the device, below
+// a = 2^21, through the approximate float reciprocal: (a + 0.5) / b lies at
+// least 0.5 / b from an integer, and the reciprocal's and the product's
+// rounding (relative 2^-22 together) move it by less than (a + 0.5) / b x
+// 2^-22, under that margin while a < 2^21.  It keeps a long integer-division
+// sequence off the producer's and consumers' path between two tasks.
+// Integer division elsewhere.
+__host__ __device__ inline int small_div(int a, int b) {
+#ifdef __CUDA_ARCH__
+  if (a >= (1 << 21)) return a / b;
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(static_cast<float>(b)));
+  return static_cast<int>((static_cast<float>(a) + 0.5f) * r);
+#else
+  return a / b;
+#endif
+}
+
 __host__ __device__ inline TaskPlan task_plan(int K, int fmt, int parts = 1) {
   TaskPlan p;
   const int cons = max_consumers(fmt);
   p.U = K / unit_k(fmt);
-  p.RL = p.U >= cons ? 1 : cons / p.U;
+  p.RL = p.U >= cons ? 1 : small_div(cons, p.U);
   p.RB = p.RL * rows_per_thread(fmt);
   p.T = p.U * p.RL;
   // Q4_K: 144 bytes per 256 weights (a multiple of 16), no separate scales
@@ -770,7 +788,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     const TaskPlan tp = task_plan(tk.K, kFmt, task_parts(tk));
     int64_t row_begin;
     const int rows = cta_rows(tk, &row_begin);
-    const int ntiles = (rows + tp.RB - 1) / tp.RB;
+    const int ntiles = small_div(rows + tp.RB - 1, tp.RB);
     if (ntiles == 0) continue;
 
     // Consecutive threads take consecutive units of one row, so a warp reads
@@ -792,8 +810,9 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         c < tp.T && W4A16_IN(p.status, (c / tp.U + (kR - 1) * tp.RL + 1) * tp.row_bytes <= tp.RB * tp.row_bytes &&
                                            4 * ((c / tp.U + (kR - 1) * tp.RL) * tp.red_stride + c % tp.U + 1) <= p.red_bytes &&
                                            (kFmt != kFmtW4A16 || !staged(tk, i) || tp.U * 260 <= p.xslot));
-    const int u = active ? c % tp.U : 0;
-    const int rl = active ? c / tp.U : 0;
+    const int cq = small_div(c, tp.U);
+    const int u = active ? c - cq * tp.U : 0;
+    const int rl = active ? cq : 0;
     const int rot = ((u >> 2) & 1) * 16;
     const int f = (u >> 1) & 3;
 
