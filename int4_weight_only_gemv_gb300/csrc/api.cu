@@ -105,12 +105,23 @@ w4a16_status check_gemv(const uint32_t* qweight, const uint16_t* scales, const u
   return W4A16_OK;
 }
 
+// Standalone M = 1 GEMVs with short rows and at most this many bytes of
+// packed weights run on the warp-per-row kernel (the same bits as the task
+// kernel); larger ones stream through the task kernel's ring.  Measured in
+// graphs of back-to-back calls (cold L2): 512 x 1024 4.55 -> 3.41 us; at
+// 512 x 3584 (0.9 MB) the two are even (4.63 / 4.72 us) and from 3584 x 3584
+// on the ring is faster (5.0 / 6.2 us).
+constexpr int64_t kShortMaxWeightBytes = 512 << 10;
+
 // Enqueue one checked GEMV (M, N > 0) whose output rows go to the segments
 // of `a` (pointers, sizes, strides and segments already filled in).
 w4a16_status enqueue(const DeviceState& d, GemvArgs a, cudaStream_t st) {
   a.status = d.status;
   cudaError_t e;
-  if (a.M == 1 && gemv_m1_supported(a.K))
+  if (a.M == 1 && gemv_m1_short_supported(a.K) &&
+      static_cast<int64_t>(a.N) * (a.K / 2) <= kShortMaxWeightBytes)
+    e = launch_gemv_m1_short(a, d.info, st);
+  else if (a.M == 1 && gemv_m1_supported(a.K))
     e = launch_gemv_m1(a, d.info, st);
   else if (a.M == 1)
     e = launch_gemv_rows(a, d.info, st);

@@ -1146,10 +1146,120 @@ bool plan_tasks(M1Params<MAXT>& p, const M1Task* tasks, int ntasks, int fmt, con
   return true;
 }
 
+// ---------------------------------------------------------------- short rows
+// A standalone M = 1 GEMV with K <= 4096 (at most 32 units of 128 k per row)
+// and few bytes is bound by the task kernel's fixed costs (its ring, its
+// roles, its one CTA per SM).  This kernel computes the same bits with a
+// short latency: one warp per row, lane u < U owns unit u.  Each lane does
+// what a consumer thread of gemv_m1_kernel does for the unit -- the 16 words
+// in the rotated order f = (u / 2) mod 4, the 128 activations paired and
+// their bias sum C in the same order, (dot - C) x scale -- and lanes 0..3
+// form the task kernel's reducer for such a row (one lane per row when
+// K <= 4096): four running sums over the units u = q (mod 4), the units
+// past the last whole four added to the first, combined as
+// (s0 + s1) + (s2 + s3), then the bias and one rounding.  So a call gives
+// the same bits here as inside a layer sequence.
+constexpr int kShortWarps = 8;
+
+__global__ void __launch_bounds__(32 * kShortWarps) gemv_m1_short_kernel(const GemvArgs a) {
+  __shared__ float part[kShortWarps][32];
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int U = a.K / 128;
+  const int G = a.K / 128;
+  const int u = lane;
+  const bool act = u < U;
+  const int f = (u >> 1) & 3;
+  const int64_t N = a.N;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kShortWarps;
+  int64_t n = static_cast<int64_t>(blockIdx.x) * kShortWarps + warp;
+
+  // this lane's 16 words of row `row` (chunk (j + f) mod 4 into words
+  // 4 j .. 4 j + 3, as load_unit128 reads a stage) and its scale
+  auto load_row = [&](int64_t row, uint32_t (&w)[16], float& sc) {
+    if (act && row < N) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.qweight + row * (a.K / 8) + 16 * u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 v = ld_stream_u4(src + ((j + f) & 3));
+        w[4 * j] = v.x;
+        w[4 * j + 1] = v.y;
+        w[4 * j + 2] = v.z;
+        w[4 * j + 3] = v.w;
+      }
+      sc = __half2float(__ushort_as_half(ld_nc_u16(a.scales + row * G + u)));
+    }
+  };
+  uint32_t w[16] = {};
+  float sc = 0.f;
+  load_row(n, w, sc);  // weights and scales are constant: before the dependency wait
+  pdl_wait();          // x may be the previous kernel's output; y may still be read by it
+
+  // the lane's 128 activations, paired as the task kernel's consumers pair
+  // them (X[4 j + i] with word 4 ((j + f) mod 4) + i), and their bias sum
+  XPairs X[16];
+  float C = 0.f;
+  if (act) {
+    const uint16_t* xp = a.x + u * 128;
+    float es[4], os[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ch = (j + f) & 3;
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) X[4 * j + i4] = pair_activations(ld_u4(xp + 32 * ch + 8 * i4));
+      chunk_bias(&X[4 * j], es[j], os[j]);
+    }
+    float e[4], o[4];
+    unrotate4(es, f, e);
+    unrotate4(os, f, o);
+    C = unit_bias(e, o);
+  }
+  const int u4 = U & ~3;  // units in whole fours
+  for (; n < N; n += step) {
+    const float res = act ? (dot_unit128(w, X) - C) * sc : 0.f;
+    load_row(n + step, w, sc);  // the next row's words, in flight during the sum
+    part[warp][lane] = res;
+    __syncwarp();
+    float s = 0.f;
+    if (lane < 4) {
+      for (int v = lane; v < u4; v += 4) s += part[warp][v];
+      if (lane == 0)
+        for (int v = u4; v < U; ++v) s += part[warp][v];
+    }
+    const float s1 = __shfl_sync(0xffffffffu, s, 1);
+    const float s2 = __shfl_sync(0xffffffffu, s, 2);
+    const float s3 = __shfl_sync(0xffffffffu, s, 3);
+    if (lane == 0) store_out(a, 0, n, (s + s1) + (s2 + s3));
+    __syncwarp();
+  }
+}
+
 }  // namespace
 
 bool gemv_m1_supported(int K) {
   return K > 0 && K % 128 == 0 && K / 64 <= kM1MaxConsumers;
+}
+
+bool gemv_m1_short_supported(int K) { return K > 0 && K % 128 == 0 && K / 128 <= 32; }
+
+cudaError_t launch_gemv_m1_short(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
+  if (a.M != 1 || a.a8 || !gemv_m1_short_supported(a.K)) return cudaErrorInvalidValue;
+  const int64_t rows_per_cta = kShortWarps;
+  int64_t grid = (static_cast<int64_t>(a.N) + rows_per_cta - 1) / rows_per_cta;
+  if (grid > 2 * d.sms) grid = 2 * d.sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(32 * kShortWarps);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_m1_short_kernel, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 int gemv_m1_split_tasks(const M1Task& t, bool a8, const DeviceInfo& d, M1Task* out) {

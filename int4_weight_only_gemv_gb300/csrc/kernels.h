@@ -126,6 +126,11 @@ struct DeviceInfo {
 // M = 1, K within the pipelined kernel's limit (see gemv_m1_supported).
 bool gemv_m1_supported(int K);
 cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
+// M = 1 with K <= 4096: a warp-per-row kernel with the task kernel's exact
+// per-unit arithmetic and row-sum order (the same bits as gemv_m1_kernel), for
+// standalone GEMVs whose launch the task kernel's fixed costs would dominate.
+bool gemv_m1_short_supported(int K);
+cudaError_t launch_gemv_m1_short(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st);
 // The same kernel on GGUF Q4_K blocks (K a multiple of 256, blocks 16-byte
 // aligned, one CTA per SM).
 bool gemv_m1_q4k_supported(int K);

@@ -29,11 +29,11 @@ def note(name, ok):
         report["fail"].append(name)
 
 
-# GEMV kernels: M = 1 (task kernel, K split at 19456; CUDA-core rows kernel
-# past K = 28672), M = 3, 5, 9, 16 (tensor cores: an odd group count at
+# GEMV kernels: M = 1 (warp-per-row kernel for a small 300 x 1024, task
+# kernel, K split at 19456; CUDA-core rows kernel past K = 28672), M = 3, 5, 9, 16 (tensor cores: an odd group count at
 # K = 640 takes the half-range box, K = 32768 a cluster of more than 8 CTAs),
 # ragged N
-for (M, N, K) in ((1, 1000, 3584), (1, 37, 19456), (1, 153, 18944), (1, 64, 32768), (3, 333, 1024),
+for (M, N, K) in ((1, 300, 1024), (1, 1000, 3584), (1, 37, 19456), (1, 153, 18944), (1, 64, 32768), (3, 333, 1024),
                   (4, 50, 640), (9, 100, 3584), (16, 777, 2048), (5, 64, 32768)):
     c = Case(N, K, M, seed=300 + M + N)
     note(f"packed {M}x{N}x{K}", c.packed_equal())
