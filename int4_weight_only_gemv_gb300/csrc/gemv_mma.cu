@@ -632,17 +632,18 @@ struct MmaPlan {
 // ranges' weights + the blocks' scale rows); the smallest wins, ties going
 // to the smaller split.  Every split needs a ring of at least 2 stages.
 template <int NT>
-MmaPlan make_mma_plan(const GemvArgs& a, const DeviceInfo& d) {
+MmaPlan make_mma_plan(const GemvArgs& a, const DeviceInfo& d, bool two_per_sm = false) {
   MmaPlan best{};
   int64_t best_cost = -1;
   const int G = a.K / 128;
   const int nr = (G + 1) / 2;
   const int T16 = (a.N + 15) / 16;
-  const int cap = d.max_smem_optin;
+  const int cap = two_per_sm ? d.max_smem_optin / 2 - 1024 : d.max_smem_optin;
+  const int rmax = two_per_sm ? kMmaMaxRanges / 2 : kMmaMaxRanges;
   const int sc_row_block = 16 * G * 2;  // scale bytes of a 16-row block
   for (int ks = 1; ks <= kMmaMaxCluster && ks <= nr; ++ks) {
     const int R = (nr + ks - 1) / ks;
-    if (R > kMmaMaxRanges || (ks - 1) * R >= nr) continue;
+    if (R > rmax || (ks - 1) * R >= nr) continue;
     const int Rb = R < G / 2 ? R : G / 2;
     const int stage = (Rb * kRangeBytes + ((G & 1) ? static_cast<int>(kTailBytes) : 0) + sc_row_block + 1023) & ~1023;
     const int red = kRedBufs * R * NT * kPartialBytes;
@@ -677,7 +678,18 @@ MmaPlan make_mma_plan(const GemvArgs& a, const DeviceInfo& d) {
 
 template <int NT>
 cudaError_t launch_mma_nt(const GemvArgs& a, const DeviceInfo& d, cudaStream_t st) {
-  const MmaPlan pl = make_mma_plan<NT>(a, d);
+  MmaPlan pl = make_mma_plan<NT>(a, d);
+  // One n-tile (96 registers a thread): when K needs a cluster of ranks of
+  // more than 7 ranges anyway (down, K = 18944: 6 ranks of 13), two CTAs of
+  // half the warps and half the shared memory per SM, so that consecutive
+  // launches overlap one's start with the other's end.  Measured (cold L2,
+  // graphs of back-to-back calls): down M = 2, 4, 8 12.2, 12.4, 13.3 ->
+  // 11.8, 11.9, 12.3 us; [gate;up] (one rank) and q (ranks of 5 ranges) were
+  // slower that way and keep one CTA per SM.
+  if (NT == 1 && pl.KS > 1 && pl.R > kMmaMaxRanges / 2) {
+    const MmaPlan p2 = make_mma_plan<NT>(a, d, true);
+    if (p2.KS != 0) pl = p2;
+  }
   if (pl.KS == 0) return cudaErrorInvalidConfiguration;
   CUtensorMap tmap, tmap_tail;
   if (!weight_tensor_maps(&tmap, &tmap_tail, a.qweight, a.N, a.K, pl.Rb)) return cudaErrorInvalidValue;
