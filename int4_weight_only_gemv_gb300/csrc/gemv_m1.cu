@@ -153,13 +153,19 @@ __host__ __device__ inline int xslot_bytes(int U) { return (U * 260 + 15) & ~15;
 // Units the stager converts in one pass (one per lane 1..31).
 constexpr int kStagers = 31;
 
-// W4A16: whether the stager may stage task i of a list (its activations come
-// through the shared-memory slot), given whether it is the first task with
-// rows on the CTA.  SwiGLU tasks never are: their elementwise work is spread
-// over the consumer threads.  The first task is only when one pass of the
-// stager converts it: nothing runs before it to hide a longer staging.
-__host__ __device__ inline bool may_stage(const M1Task& tk, int U, bool first) {
-  return tk.x2 == nullptr && (!first || U <= kStagers);
+// W4A16: whether the stager may stage task i (its activations come through
+// the shared-memory slot), given whether it is the first task with rows on
+// the CTA and whether the launch runs a task list (the layer sequence's
+// kernel instantiation) or one GEMV.  SwiGLU tasks never are: their
+// elementwise work is spread over the consumer threads.  In a single-GEMV
+// launch the first task is staged only when one pass of the stager converts
+// it (nothing runs before it to hide a longer staging: a standalone down,
+// 148 units, is 0.7 us faster on the consumers' own loads).  In a list every
+// other task is: measured, the step took 0.676 ms with the list's first
+// task held to the same rule and 0.670 ms without it (its first task is
+// [gate; up], staged either way; the simpler test is what differs).
+__host__ __device__ inline bool may_stage(const M1Task& tk, int U, bool first, bool list) {
+  return tk.x2 == nullptr && (list || !first || U <= kStagers);
 }
 
 // Sizes shared by every task of a launch.
@@ -182,7 +188,7 @@ constexpr int kPartBytes = 4 * kM1PartRows;
 
 // Shared layout: barriers | K-split partial sums | xslots | S partial slots |
 // S stages (128-aligned).
-RingPlan make_ring_plan(const M1Task* tasks, int n, int smem_limit, int fmt) {
+RingPlan make_ring_plan(const M1Task* tasks, int n, int smem_limit, int fmt, bool list) {
   RingPlan r{};
   for (int i = 0; i < n; ++i) {
     const TaskPlan tp = task_plan(tasks[i].K, fmt, task_parts(tasks[i]));
@@ -190,7 +196,7 @@ RingPlan make_ring_plan(const M1Task* tasks, int n, int smem_limit, int fmt) {
     const int rb = tp.RB * tp.red_stride * 4;
     const int cw = (tp.T + 31) / 32;
     // any task but the list's first may be some CTA's first with rows
-    const int xs = fmt == kFmtW4A16 && may_stage(tasks[i], tp.U, i == 0) ? xslot_bytes(tp.U) : 0;
+    const int xs = fmt == kFmtW4A16 && may_stage(tasks[i], tp.U, i == 0, list) ? xslot_bytes(tp.U) : 0;
     if (st > r.stage_bytes) r.stage_bytes = st;
     if (rb > r.red_bytes) r.red_bytes = rb;
     if (cw > r.CW) r.CW = cw;
@@ -499,7 +505,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
   int first_task = 0;
   while (first_task < p.ntasks && !cta_has_rows(p.task[first_task])) ++first_task;
   auto staged = [&](const M1Task& tk, int i) {
-    return kFmt == kFmtW4A16 && may_stage(tk, tk.K / unit_k(kFmt), i == first_task);
+    return kFmt == kFmtW4A16 && may_stage(tk, tk.K / unit_k(kFmt), i == first_task, MAXT > 2);
   };
 
   if (warp == 0 && lane == 0) {
@@ -1136,7 +1142,7 @@ cudaError_t launch_tasks(const M1Params<MAXT>& p, const RingPlan& rp, int grid, 
 // Shared checks and plan of a task list; fills the launch fields of p.
 template <int MAXT>
 bool plan_tasks(M1Params<MAXT>& p, const M1Task* tasks, int ntasks, int fmt, const DeviceInfo& d, RingPlan* rp) {
-  *rp = make_ring_plan(tasks, ntasks, d.max_smem_optin, fmt);
+  *rp = make_ring_plan(tasks, ntasks, d.max_smem_optin, fmt, MAXT > 2);
   if (rp->S < 2) return false;
   p.S = rp->S;
   p.stage_bytes = rp->stage_bytes;
@@ -1381,7 +1387,7 @@ bool gemv_m1_tasks_fit(const M1Task* tasks, int n, bool a8, const DeviceInfo& d)
     if (!gemv_m1_supported(tasks[i].K * task_parts(tasks[i]))) return false;
   // a table's plan takes the largest stage of its tasks: the plan over all of
   // them bounds every subset's
-  return make_ring_plan(tasks, n, d.max_smem_optin, a8 ? kFmtW4A8 : kFmtW4A16).S >= 2;
+  return make_ring_plan(tasks, n, d.max_smem_optin, a8 ? kFmtW4A8 : kFmtW4A16, true).S >= 2;
 }
 
 cudaError_t prepare_gemv_m1(const DeviceInfo& d) {
