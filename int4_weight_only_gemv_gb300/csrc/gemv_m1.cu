@@ -251,11 +251,13 @@ __device__ __forceinline__ bool cta_has_rows(const M1Task& tk) {
 }
 
 // Bounded wait until *counter >= target (acquire).  False if the bound ran out.
+// Polls every 64 ns (the 28-layer step: 0.659 ms at 256 ns, 0.658 at 128,
+// 0.657 at 64; 0.788 ms at 2 us).
 __device__ __forceinline__ bool wait_count(const int* counter, int target, uint64_t limit_ns) {
   if (ld_acquire_gpu(counter) >= target) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
-    __nanosleep(256);
+    __nanosleep(64);
     if (ld_acquire_gpu(counter) >= target) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
