@@ -563,7 +563,7 @@ def pin_q4k_fp32_and_gemv(L):
 
 # --------------------------------------------------------------------------- tolerance machinery
 #
-# Every GPU parity test is judged by the GEMV bound (per activation row m,
+# Every GPU parity test is checked against the GEMV bound (per activation row m,
 # max_n |y - y_ref| <= 2e-3 ||x_m||_2 max_n ||w_hat_n||_2 + 1e-3, and the
 # relative L2 error over the whole output <= 1e-3) and by the attention bound
 # (per query head, max_d |o - o_ref| <= 2e-3 max|v| + 1e-5 over the keys t < T
