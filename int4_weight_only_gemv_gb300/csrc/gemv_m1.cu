@@ -1189,7 +1189,8 @@ __global__ void __launch_bounds__(32 * kShortWarps) gemv_m1_short_kernel(const G
   // this lane's 16 words of row `row` (chunk (j + f) mod 4 into words
   // 4 j .. 4 j + 3, as load_unit128 reads a stage) and its scale
   auto load_row = [&](int64_t row, uint32_t (&w)[16], float& sc) {
-    if (act && row < N) {
+    // checked build: the unit's 16 words and its scale inside the row
+    if (act && row < N && W4A16_IN(a.status, 16 * u + 16 <= a.K / 8 && u < G)) {
       const uint4* src = reinterpret_cast<const uint4*>(a.qweight + row * (a.K / 8) + 16 * u);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -1211,7 +1212,7 @@ __global__ void __launch_bounds__(32 * kShortWarps) gemv_m1_short_kernel(const G
   // them (X[4 j + i] with word 4 ((j + f) mod 4) + i), and their bias sum
   XPairs X[16];
   float C = 0.f;
-  if (act) {
+  if (act && W4A16_IN(a.status, 128 * u + 128 <= a.K)) {
     const uint16_t* xp = a.x + u * 128;
     float es[4], os[4];
 #pragma unroll
@@ -1241,7 +1242,7 @@ __global__ void __launch_bounds__(32 * kShortWarps) gemv_m1_short_kernel(const G
     const float s1 = __shfl_sync(0xffffffffu, s, 1);
     const float s2 = __shfl_sync(0xffffffffu, s, 2);
     const float s3 = __shfl_sync(0xffffffffu, s, 3);
-    if (lane == 0) store_out(a, 0, n, (s + s1) + (s2 + s3));
+    if (lane == 0 && W4A16_IN(a.status, n < N)) store_out(a, 0, n, (s + s1) + (s2 + s3));
     __syncwarp();
   }
 }

@@ -305,3 +305,39 @@ def test_layer_seq_task_lists_split_between_layers():
         assert torch.equal(v.view(torch.int16), io[k].view(torch.int16)), k
     assert w4.w4a16_device_status(clear=True) == 0
     seq.close()
+
+
+@pytest.mark.parametrize("h,kv,ffn", [(640, 128, 1280), (1024, 256, 2048)])
+def test_short_rows_kernel_matches_sequence(h, kv, ffn):
+    """A standalone M = 1 GEMV small enough for the warp-per-row kernel (at
+    most 512 KB of packed weights, K <= 4096) gives the same bits as the same
+    projection inside a layer sequence (the task kernel).  h = 640: five
+    units of 128 k per row, so the row sum's units past the last whole four
+    are exercised."""
+    n = 2
+    layers = []
+    for l in range(n):
+        lw = {}
+        for pj, name in enumerate(synth.PROJ_NAMES):
+            NN, KK = {"q": (h, h), "k": (kv, h), "v": (kv, h), "o": (h, h), "gate": (ffn, h), "up": (ffn, h),
+                      "down": (h, ffn)}[name]
+            lw[name] = w4.w4a16_quantize(synth.weights(NN, KK, 92000 + 8 * l + pj).to(DEV))
+        layers.append(lw)
+    io = {"x": synth.activations(n, h, 92999).view(n, 1, h).to(DEV)}
+    for name, width in (("y_q", h), ("y_k", kv), ("y_v", kv), ("y_o", h), ("y_gu", 2 * ffn), ("y_down", h)):
+        io[name] = torch.full((n, 1, width), float("nan"), dtype=torch.float16, device=DEV)
+    seq = w4.LayerSeq(layers, io, 1, h, kv, ffn)
+    seq.run()
+    seq.sync()
+    small = 0
+    for l in range(n):
+        x = io["x"][l]
+        for name, xin, yout in (("q", x, io["y_q"][l]), ("k", x, io["y_k"][l]), ("v", x, io["y_v"][l]),
+                                ("o", io["y_q"][l], io["y_o"][l]),
+                                ("down", io["y_gu"][l][:, :ffn].contiguous(), io["y_down"][l])):
+            qw = layers[l][name][0]
+            small += qw.numel() * 4 <= 512 * 1024 and qw.shape[1] * 8 <= 4096
+            y = w4.w4a16_gemv(*layers[l][name], xin)
+            assert torch.equal(y.view(torch.int16), yout.view(torch.int16)), (h, l, name)
+    seq.close()
+    assert small >= 4 * n  # q, k, v, o of each layer took the warp-per-row kernel
