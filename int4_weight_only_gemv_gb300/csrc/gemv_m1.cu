@@ -1020,8 +1020,10 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       }
     }
 
+    // whether tile t's stage was already seen full, at the end of tile t - 1
+    bool full_seen = false;
     for (int t = 0; t < ntiles; ++t) {
-      if (!mbar_wait_bounded(full0 + 8 * s, phase, kWaitLimitNs)) {
+      if (!full_seen && !mbar_wait_bounded(full0 + 8 * s, phase, kWaitLimitNs)) {
         if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
         return;
       }
@@ -1121,6 +1123,10 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
         base = stage0;
         rs = red0;
       }
+      // A non-blocking look at the next tile's stage (acquire): when it has
+      // landed, the next tile starts without the blocking wait.  Measured on
+      // the 28-layer step (same box): 0.6640 -> 0.6580 ms.
+      full_seen = t + 1 < ntiles && mbar_try_wait(full0 + 8 * s, phase);
     }
   }
 }
