@@ -310,15 +310,16 @@ __device__ __forceinline__ float unit_bias(const float (&e)[4], const float (&o)
   return fmaf(0.0625f, (o[0] + o[1]) + (o[2] + o[3]), (e[0] + e[1]) + (e[2] + e[3]));
 }
 
-// The stager's conversion of one W4A16 unit in shared memory: its 128 raw
-// activations at dst become pairs as dot_unit128 uses them, word w of the
-// unit (activations 8 w .. 8 w + 7) at 16-byte slot w ^ (u mod 16) of the
-// same 256 bytes (so that the consumers' rotated reads of consecutive units
-// hit distinct bank groups).  Returns the unit's bias sum.
+// The stager's conversion of one W4A16 unit in shared memory, in place: word
+// w of the unit (activations 8 w .. 8 w + 7) sits at 16-byte slot
+// w ^ (u mod 16) of its 256 bytes both raw (the copies land there) and as
+// the pairs dot_unit128 uses.  The swizzle puts the same word of eight
+// consecutive units in eight distinct bank groups, for the stager's reads
+// here and for the consumers' rotated reads.  Returns the unit's bias sum.
 __device__ __forceinline__ float convert_unit128(uint32_t dst, int u) {
   uint4 v[16];
 #pragma unroll
-  for (int w = 0; w < 16; ++w) v[w] = lds_u4(dst + 16 * w);
+  for (int w = 0; w < 16; ++w) v[w] = lds_u4(dst + ((w ^ (u & 15)) << 4));
   float e[4], o[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -659,7 +660,9 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       if (!same) {
         const int chunks = tp.U * 16;  // 16-byte chunks of the task's activations
         for (int q = sl0; q < chunks; q += kStagers)
-          if (W4A16_IN(p.status, 16 * q + 16 <= p.xslot && 8 * q + 8 <= tk.K)) cp_async_16(xs + 16 * q, tk.x + 8 * q);
+          // chunk q = word q mod 16 of unit q / 16, to its swizzled slot
+          if (W4A16_IN(p.status, 16 * q + 16 <= p.xslot && 8 * q + 8 <= tk.K))
+            cp_async_16(xs + 16 * ((q & ~15) | ((q ^ (q >> 4)) & 15)), tk.x + 8 * q);
         cp_async_wait_all();
         __syncwarp(kStagerMask);
         // the producer shares this warp: after the launch's first task, a
