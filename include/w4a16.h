@@ -264,12 +264,13 @@ typedef struct {
 /*
  * w4a16_layer_seq_create with epilogues: biases (n_layers entries, or NULL
  * for none) and flags (W4A16_SEQ_SWIGLU, W4A16_SEQ_ACT_INT8 or both; other
- * bits return W4A16_ERR_SHAPE).  At M = 1 (every K within the M = 1 kernel's range) the
- * SwiGLU is computed inside the down tasks as they load their activations, so
- * h is never written to memory; otherwise a separate kernel writes h to a
- * device buffer of n_layers x M x ffn fp16 values that the object allocates
- * and frees.  Everything else as w4a16_layer_seq_create (which is this call
- * with no biases and no flags).
+ * bits return W4A16_ERR_SHAPE).  With SwiGLU, h goes to a device buffer of
+ * n_layers x M x ffn fp16 values that the object allocates and frees, and
+ * down reads it.  At M = 1 (every K within the M = 1 kernel's range) gate
+ * and up run as two GEMVs of the layer's one task list and up's epilogue
+ * writes h as each row of y_up is rounded; otherwise a separate kernel
+ * writes h after the [gate; up] GEMV.  Everything else as
+ * w4a16_layer_seq_create (which is this call with no biases and no flags).
  */
 w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4a16_layer_bias* biases,
                                      unsigned flags, int n_layers, int M, int hidden, int kv_dim, int ffn,

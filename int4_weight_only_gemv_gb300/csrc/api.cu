@@ -537,14 +537,15 @@ struct ActOp {
 // The GEMVs of a checked layer sequence, in order.  Per layer: [q; k; v] as
 // one GEMV when the three weights are stacked in one allocation (outputs
 // still go to y_q, y_k, y_v), o, [gate; up] as one GEMV when stacked, down.
-// dep[i] is the GEMV whose output GEMV i reads (o reads y_q, down the gate
-// half of y_gu, or with SwiGLU both halves: then dep2[i] is the other of gate
-// and up when they are separate GEMVs), or -1;
-// x2[i] is the SwiGLU partner of GEMV i's x (the up half) when the sequence
-// fuses SwiGLU into the M = 1 task, else null; act[i] the separate SwiGLU
-// step before GEMV i (unfused path); layer_first[l] is the index of layer l's
-// first GEMV (layer_first[n_layers] = number of GEMVs).  Biases go to the
-// output segments.
+// With SwiGLU fused into the M = 1 task lists (fuse_swiglu): up then gate as
+// two GEMVs, up carrying the epilogue that writes h, and down reading h.
+// dep[i] is the GEMV whose output GEMV i reads (o reads y_q; down the gate
+// half of y_gu, or h: written by up's epilogue, or by a separate step after
+// both halves, when dep2[i] is the other of gate and up if they are separate
+// GEMVs), or -1; x2[i] a second activation input of GEMV i (none here: null);
+// act[i] the separate SwiGLU step before GEMV i (unfused path);
+// layer_first[l] is the index of layer l's first GEMV (layer_first[n_layers]
+// = number of GEMVs).  Biases go to the output segments.
 void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, int n_layers, int M,
                      int hidden, int kv_dim, int ffn, const w4a16_seq_io* io, bool fuse_swiglu,
                      std::vector<GemvArgs>* gemvs, std::vector<int>* dep, std::vector<int>* dep2,
@@ -613,7 +614,24 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
     int ilast;       // the GEMV down waits for
     int ialso = -1;  // and, with SwiGLU over separate gate and up, the other one
     const int64_t ldgu = 2 * static_cast<int64_t>(ffn);
-    if (stacked(w, W4A16_GATE, W4A16_UP, ffn)) {
+    uint16_t* const hl = swiglu ? opt.hbuf + static_cast<int64_t>(l) * M * ffn : nullptr;
+    if (swiglu && fuse_swiglu) {
+      // The task lists: gate and up as two GEMVs over the same rows of the
+      // same CTAs; up's epilogue forms h from its own rounded output and the
+      // gate output this CTA wrote earlier, and down reads h.  up is added
+      // first: a table emits a layer's GEMVs that read x in reverse order,
+      // so gate runs before up.
+      GemvArgs u = plain_args(w.qweight[W4A16_UP], w.scales[W4A16_UP], xl, ygu + ffn, M, ffn, hidden, hidden,
+                              ldgu);
+      u.seg[0].bias = b(W4A16_UP);
+      u.epi_g = ygu;
+      u.epi_h = hl;
+      ilast = add(u, -1);
+      GemvArgs g = plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, ffn, hidden, hidden,
+                              ldgu);
+      g.seg[0].bias = b(W4A16_GATE);
+      add(g, -1);
+    } else if (stacked(w, W4A16_GATE, W4A16_UP, ffn)) {
       GemvArgs a = plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, 2 * ffn, hidden,
                               hidden, ldgu);
       a.nseg = 2;
@@ -640,14 +658,14 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
                               hidden, ffn, ldgu, hidden);
       a.seg[0].bias = b(W4A16_DOWN);
       ActOp op;
-      if (swiglu && !fuse_swiglu) {
-        op = ActOp{ygu, ygu + ffn, ldgu, opt.hbuf + static_cast<int64_t>(l) * M * ffn, M, ffn};
-        a.x = op.h;
+      if (swiglu) {
+        // down reads h (written by up's epilogue, or by a separate step)
+        if (!fuse_swiglu) op = ActOp{ygu, ygu + ffn, ldgu, hl, M, ffn};
+        a.x = hl;
         a.ldx = ffn;
       }
       const int id = add(a, ilast);
       (*dep2)[id] = ialso;
-      if (swiglu && fuse_swiglu) (*x2)[id] = ygu + ffn;
       (*act)[id] = op;
     }
   }
@@ -694,6 +712,11 @@ void seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs, const s
       tk.dep = dep[i] < 0 ? -1 : slot[dep[i]];
       if (dep2[i] >= 0 && slot[dep2[i]] > tk.dep) tk.dep = slot[dep2[i]];
       for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = M1Seg{a.seg[g].y, a.seg[g].bias, a.seg[g].n_end};
+      if (a.epi_h != nullptr) {
+        tk.epi = 1;
+        tk.seg[1].y = a.epi_h;
+        tk.seg[2].y = const_cast<uint16_t*>(a.epi_g);
+      }
       M1Task parts[2];
       const int np = gemv_m1_split_tasks(tk, a8, d.info, parts);
       for (int q = 0; q < np; ++q) tasks->push_back(parts[q]);
@@ -828,9 +851,9 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != W4A16_OK) return st;
 
-  // M = 1 with every K in the M = 1 kernel's range: task lists, SwiGLU fused
-  // into the down tasks; otherwise one launch per GEMV and, with SwiGLU, a
-  // separate activation step into a buffer this object owns
+  // M = 1 with every K in the M = 1 kernel's range: task lists, SwiGLU in
+  // up's epilogue; otherwise one launch per GEMV and, with SwiGLU, a separate
+  // activation step.  Either way h goes to a buffer this object owns.
   const bool tasks = M == 1 && gemv_m1_supported(hidden) && gemv_m1_supported(ffn);
   const bool swiglu = (flags & W4A16_SEQ_SWIGLU) != 0;
   const bool a8 = (flags & W4A16_SEQ_ACT_INT8) != 0;
@@ -849,7 +872,7 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
   s->io = *io;
   if (cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&s->done, cudaEventDisableTiming) != cudaSuccess ||
-      (swiglu && !tasks &&
+      (swiglu &&
        cudaMalloc(&s->hbuf, sizeof(uint16_t) * static_cast<size_t>(n_layers) * M * ffn) != cudaSuccess)) {
     cudaGetLastError();
     seq_free(s);

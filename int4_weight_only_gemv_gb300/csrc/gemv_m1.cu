@@ -288,6 +288,14 @@ __device__ __forceinline__ uint4 swiglu8(uint4 g, uint4 u) {
   return make_uint4(hw[0], hw[1], hw[2], hw[3]);
 }
 
+// One element of the same: fp16_RN(silu(g) u) from fp16 bits, with the same
+// operations as each lane of swiglu8, so either gives the same bits.
+__device__ __forceinline__ uint16_t swiglu1(uint16_t g, uint16_t u) {
+  const float g0 = __half2float(__ushort_as_half(g));
+  const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * __half2float(__ushort_as_half(u));
+  return __half_as_ushort(__float2half_rn(h0));
+}
+
 // Bias sums of a W4A16 unit, C = 1032 sum x(k even) + 72 sum x(k odd) (the
 // dot product of its activations with a word of zero nibbles), in one
 // canonical order: each 4-word chunk (32 activations, words in natural
@@ -788,7 +796,15 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
                 if (b != nullptr) sum += __half2float(__ushort_as_half(__ldg(b + j)));
               }
               uint16_t* y = seg == 0 ? y0 : (seg == 1 ? y1 : y2);
-              y[j] = __half_as_ushort(__float2half_rn(sum));
+              const uint16_t yb = __half_as_ushort(__float2half_rn(sum));
+              y[j] = yb;
+              if (kAct && tk.epi) {
+                // SwiGLU epilogue: the gate output of row j was written by
+                // this warp in an earlier task (the __syncwarp of each tile
+                // orders it before this read, through L2)
+                const uint16_t g = __ldcg(reinterpret_cast<const unsigned short*>(tk.seg[2].y) + j);
+                tk.seg[1].y[j] = swiglu1(g, yb);
+              }
             }
           }
         }
@@ -1409,7 +1425,7 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
   bool act = false;
   for (int i = 0; i < ntasks; ++i) {
     if (tasks[i].dep >= 0) p.task[tasks[i].dep].publish = 1;
-    act = act || tasks[i].x2 != nullptr;
+    act = act || tasks[i].x2 != nullptr || tasks[i].epi != 0;
   }
   p.ntasks = ntasks;
   p.done = done;

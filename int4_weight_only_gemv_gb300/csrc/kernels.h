@@ -43,6 +43,11 @@ struct GemvArgs {
   // W4A8: int8 activations quantised per 64-element unit inside the M = 1
   // kernel (gemv_m1.cu); only that kernel supports it.
   bool a8;
+  // M = 1 layer sequences only: a SwiGLU epilogue h[n] = fp16_RN(silu(g[n])
+  // y[n]) on this GEMV's output (null: none), g the gate output of the same
+  // rows, produced earlier in the same task list.
+  const uint16_t* epi_g;
+  uint16_t* epi_h;
 };
 
 #ifdef __CUDACC__
@@ -96,6 +101,11 @@ struct M1Task {
   // the bias and the rounding; qweight, scales, x and x2 point at the half).
   // 0 = a whole GEMV.
   uint8_t split;
+  // 1: a SwiGLU epilogue (one output segment, a whole or second-half GEMV):
+  // after y[n] is rounded, h[n] = fp16_RN(silu(g[n]) y[n]) is written too,
+  // g = seg[2].y (the gate output of the same rows, written by this CTA in an
+  // earlier task of the list) and h = seg[1].y; 0: none
+  uint8_t epi;
   M1Seg seg[kMaxSegs];
 };
 static_assert(sizeof(M1Task) == 128, "a task record is 128 bytes (the table is kernel parameters)");
