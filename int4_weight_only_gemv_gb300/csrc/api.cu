@@ -542,19 +542,17 @@ struct ActOp {
 // dep[i] is the GEMV whose output GEMV i reads (o reads y_q; down the gate
 // half of y_gu, or h: written by up's epilogue, or by a separate step after
 // both halves, when dep2[i] is the other of gate and up if they are separate
-// GEMVs), or -1; x2[i] a second activation input of GEMV i (none here: null);
-// act[i] the separate SwiGLU step before GEMV i (unfused path);
+// GEMVs), or -1; act[i] the separate SwiGLU step before GEMV i (unfused path);
 // layer_first[l] is the index of layer l's first GEMV (layer_first[n_layers]
 // = number of GEMVs).  Biases go to the output segments.
 void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, int n_layers, int M,
                      int hidden, int kv_dim, int ffn, const w4a16_seq_io* io, bool fuse_swiglu,
                      std::vector<GemvArgs>* gemvs, std::vector<int>* dep, std::vector<int>* dep2,
-                     std::vector<const uint16_t*>* x2, std::vector<ActOp>* act,
+                     std::vector<ActOp>* act,
                      std::vector<int>* layer_first) {
   gemvs->clear();
   dep->clear();
   dep2->clear();
-  x2->clear();
   act->clear();
   layer_first->clear();
   const int64_t Mh = static_cast<int64_t>(M) * hidden, Mkv = static_cast<int64_t>(M) * kv_dim,
@@ -569,7 +567,6 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
     gemvs->push_back(a);
     dep->push_back(d);
     dep2->push_back(-1);
-    x2->push_back(nullptr);
     act->push_back(ActOp{});
     return static_cast<int>(gemvs->size()) - 1;
   };
@@ -691,8 +688,7 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
 // whose K the M = 1 kernel splits becomes two consecutive tasks; a GEMV that
 // reads its output depends on the second.
 void seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs, const std::vector<int>& dep,
-               const std::vector<int>& dep2, const std::vector<const uint16_t*>& x2,
-               const std::vector<int>& layer_first, int l0, int l1, bool a8, std::vector<M1Task>* tasks) {
+               const std::vector<int>& dep2, const std::vector<int>& layer_first, int l0, int l1, bool a8, std::vector<M1Task>* tasks) {
   tasks->clear();
   static thread_local std::vector<int> slot;  // table slot of each emitted GEMV (capacity kept)
   slot.assign(gemvs.size(), -1);
@@ -703,7 +699,7 @@ void seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs, const s
       tk.qweight = a.qweight;
       tk.scales = a.scales;
       tk.x = a.x;
-      tk.x2 = x2[i];
+      tk.epi_g = a.epi_g;
       tk.N = a.N;
       tk.K = a.K;
       tk.nseg = static_cast<uint8_t>(a.nseg);
@@ -712,11 +708,7 @@ void seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs, const s
       tk.dep = dep[i] < 0 ? -1 : slot[dep[i]];
       if (dep2[i] >= 0 && slot[dep2[i]] > tk.dep) tk.dep = slot[dep2[i]];
       for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = M1Seg{a.seg[g].y, a.seg[g].bias, a.seg[g].n_end};
-      if (a.epi_h != nullptr) {
-        tk.epi = 1;
-        tk.seg[1].y = a.epi_h;
-        tk.seg[2].y = const_cast<uint16_t*>(a.epi_g);
-      }
+      if (a.epi_g != nullptr) tk.seg[1].y = a.epi_h;  // h of the SwiGLU epilogue
       M1Task parts[2];
       const int np = gemv_m1_split_tasks(tk, a8, d.info, parts);
       for (int q = 0; q < np; ++q) tasks->push_back(parts[q]);
@@ -767,7 +759,6 @@ bool seq_uses_tasks(int M, const std::vector<GemvArgs>& gemvs) {
 // scratch: the caller's buffer (its capacity is reused).
 w4a16_status check_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs,
                              const std::vector<int>& dep, const std::vector<int>& dep2,
-                             const std::vector<const uint16_t*>& x2,
                              const std::vector<int>& layer_first, bool a8, std::vector<M1Task>* scratch,
                              std::vector<int>* task_first) {
   const int n_layers = static_cast<int>(layer_first.size()) - 1;
@@ -786,7 +777,7 @@ w4a16_status check_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& 
     if (n > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
     task_first->push_back(task_first->back() + n);
   }
-  seq_tasks(d, gemvs, dep, dep2, x2, layer_first, 0, n_layers, a8, scratch);
+  seq_tasks(d, gemvs, dep, dep2, layer_first, 0, n_layers, a8, scratch);
   return gemv_m1_tasks_fit(scratch->data(), static_cast<int>(scratch->size()), a8, d.info) ? W4A16_OK
                                                                                           : W4A16_ERR_SHAPE;
 }
@@ -799,7 +790,6 @@ w4a16_status check_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& 
 // capacity is reused).  Returns the launch count through *launches.
 w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs,
                                const std::vector<int>& dep, const std::vector<int>& dep2,
-                               const std::vector<const uint16_t*>& x2,
                                const std::vector<int>& layer_first, const std::vector<int>& task_first,
                                int* done, bool a8, cudaStream_t st, std::vector<M1Task>* tasks, int* launches) {
   const int n_layers = static_cast<int>(layer_first.size()) - 1;
@@ -810,7 +800,7 @@ w4a16_status enqueue_seq_tasks(const DeviceState& d, const std::vector<GemvArgs>
     while (l1 < n_layers && task_first[l1 + 1] - task_first[l0] <= kM1MaxTasks) ++l1;
     const int t0 = task_first[l0], t1 = task_first[l1];
     if (t1 - t0 > kM1MaxTasks) return W4A16_ERR_SHAPE;  // one layer beyond a task table
-    seq_tasks(d, gemvs, dep, dep2, x2, layer_first, l0, l1, a8, tasks);
+    seq_tasks(d, gemvs, dep, dep2, layer_first, l0, l1, a8, tasks);
     const cudaError_t e =
         launch_gemv_m1_tasks(tasks->data(), t1 - t0, done + t0, d.status, *launches > 0, a8, d.info, st);
     if (e != cudaSuccess) {
@@ -881,14 +871,13 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
   opt.hbuf = s->hbuf;
   std::vector<GemvArgs> gemvs;
   std::vector<int> dep, dep2, layer_first;
-  std::vector<const uint16_t*> x2;
   std::vector<ActOp> act;
-  build_seq_gemvs(layers, opt, n_layers, M, hidden, kv_dim, ffn, io, tasks, &gemvs, &dep, &dep2, &x2, &act,
+  build_seq_gemvs(layers, opt, n_layers, M, hidden, kv_dim, ffn, io, tasks, &gemvs, &dep, &dep2, &act,
                   &layer_first);
   // M = 1: the task lists, checked on the host before anything is captured
   std::vector<M1Task> table;
   std::vector<int> task_first;
-  if (tasks && (st = check_seq_tasks(*d, gemvs, dep, dep2, x2, layer_first, a8, &table, &task_first)) != W4A16_OK) {
+  if (tasks && (st = check_seq_tasks(*d, gemvs, dep, dep2, layer_first, a8, &table, &task_first)) != W4A16_OK) {
     seq_free(s);
     return st;
   }
@@ -915,7 +904,7 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
     if (cudaMemsetAsync(s->task_done, 0, sizeof(int) * ntasks, s->capture_stream) != cudaSuccess)
       cap = W4A16_ERR_CUDA;
     else
-      cap = enqueue_seq_tasks(*d, gemvs, dep, dep2, x2, layer_first, task_first, s->task_done, a8,
+      cap = enqueue_seq_tasks(*d, gemvs, dep, dep2, layer_first, task_first, s->task_done, a8,
                               s->capture_stream, &table, &launches);
   } else {
     for (size_t i = 0; i < gemvs.size() && cap == W4A16_OK; ++i) {
@@ -1009,11 +998,10 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
   // host tables: thread-local, their capacity kept from call to call
   static thread_local std::vector<GemvArgs> gemvs;
   static thread_local std::vector<int> dep, dep2, layer_first;
-  static thread_local std::vector<const uint16_t*> x2;
   static thread_local std::vector<ActOp> act;
   static thread_local std::vector<M1Task> tasks;
   static thread_local std::vector<int> task_first;
-  build_seq_gemvs(layers, SeqOptions{}, n_layers, 1, hidden, kv_dim, ffn, io, true, &gemvs, &dep, &dep2, &x2,
+  build_seq_gemvs(layers, SeqOptions{}, n_layers, 1, hidden, kv_dim, ffn, io, true, &gemvs, &dep, &dep2,
                   &act, &layer_first);
   if (!seq_uses_tasks(1, gemvs)) return W4A16_ERR_LIMIT;
 
@@ -1023,7 +1011,7 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
   if ((st = static_task_done(&done)) != W4A16_OK) return st;
 
   // every task table is checked on the host before anything is enqueued
-  if ((st = check_seq_tasks(*d, gemvs, dep, dep2, x2, layer_first, false, &tasks, &task_first)) != W4A16_OK)
+  if ((st = check_seq_tasks(*d, gemvs, dep, dep2, layer_first, false, &tasks, &task_first)) != W4A16_OK)
     return st;
   const int n = task_first.back();  // one counter per task
   if (n > W4A16_STATIC_MAX_GEMVS) return W4A16_ERR_LIMIT;
@@ -1034,7 +1022,7 @@ extern "C" w4a16_status w4a16_layer_seq_run_static(const w4a16_layer_weights* la
     return W4A16_ERR_CUDA;
   }
   int launches = 0;
-  return enqueue_seq_tasks(*d, gemvs, dep, dep2, x2, layer_first, task_first, done, false, s, &tasks, &launches);
+  return enqueue_seq_tasks(*d, gemvs, dep, dep2, layer_first, task_first, done, false, s, &tasks, &launches);
 }
 
 extern "C" {

@@ -154,18 +154,22 @@ __host__ __device__ inline int xslot_bytes(int U) { return (U * 260 + 15) & ~15;
 constexpr int kStagers = 31;
 
 // W4A16: whether the stager may stage task i (its activations come through
-// the shared-memory slot), given whether it is the first task with rows on
-// the CTA and whether the launch runs a task list (the layer sequence's
-// kernel instantiation) or one GEMV.  SwiGLU tasks never are: their
-// elementwise work is spread over the consumer threads.  In a single-GEMV
-// launch the first task is staged only when one pass of the stager converts
-// it (nothing runs before it to hide a longer staging: a standalone down,
-// 148 units, is 0.7 us faster on the consumers' own loads).  In a list every
-// other task is: measured, the step took 0.676 ms with the list's first
-// task held to the same rule and 0.670 ms without it (its first task is
-// [gate; up], staged either way; the simpler test is what differs).
-__host__ __device__ inline bool may_stage(const M1Task& tk, int U, bool first, bool list) {
-  return tk.x2 == nullptr && (list || !first || U <= kStagers);
+// the shared-memory slot), given its activation vector x, whether it is the
+// first task with rows on the CTA and whether the launch runs a task list
+// (the layer sequence's kernel instantiation) or one GEMV.  The stager's
+// 16-byte copies need x 16-byte aligned (the ABI asks for it; an unaligned
+// x is loaded by the consumers instead).  In a single-GEMV launch the first
+// task is staged only when one pass of the stager converts it (nothing runs
+// before it to hide a longer staging: a standalone down, 148 units, is
+// 0.7 us faster on the consumers' own loads).  In a list every other task
+// is: measured, the step took 0.676 ms with the list's first task held to
+// the same rule and 0.670 ms without it (its first task is [gate; up],
+// staged either way; the simpler test is what differs).  The test runs on
+// the device too, so the list kernel keeps the consumers' own-load path:
+// with staging known at compile time the compiler's schedule of the list
+// kernel ran the step 3 % slower.
+__host__ __device__ inline bool may_stage(const uint16_t* x, int U, bool first, bool list) {
+  return (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (list || !first || U <= kStagers);
 }
 
 // Sizes shared by every task of a launch.
@@ -207,7 +211,7 @@ RingPlan make_ring_plan(const M1Task* tasks, int n, int smem_limit, int fmt, boo
     const int rb = tp.RB * tp.red_stride * 4;
     const int cw = (tp.T + 31) / 32;
     // any task but the list's first may be some CTA's first with rows
-    const int xs = fmt == kFmtW4A16 && may_stage(tasks[i], tp.U, i == 0, list) ? xslot_bytes(tp.U) : 0;
+    const int xs = fmt == kFmtW4A16 && may_stage(tasks[i].x, tp.U, i == 0, list) ? xslot_bytes(tp.U) : 0;
     if (st > r.stage_bytes) r.stage_bytes = st;
     if (rb > r.red_bytes) r.red_bytes = rb;
     if (cw > r.CW) r.CW = cw;
@@ -272,24 +276,9 @@ __device__ __forceinline__ bool wait_count(const int* counter, int target, uint6
   }
 }
 
-// SwiGLU of 8 packed fp16 values: fp16_RN(silu(g) u), silu(g) = g / (1 + e^-g),
+// SwiGLU of one element: fp16_RN(silu(g) u), silu(g) = g / (1 + e^-g),
 // computed in FP32 from the fp16 inputs with the fast exponential and
 // division (relative error ~1e-6, far below the fp16 result's 2^-11).
-__device__ __forceinline__ uint4 swiglu8(uint4 g, uint4 u) {
-  uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w}, hw[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float g0 = half_lo(gw[i]), g1 = half_hi(gw[i]);
-    const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * half_lo(uw[i]);
-    const float h1 = __fdividef(g1, 1.f + __expf(-g1)) * half_hi(uw[i]);
-    hw[i] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(h0))) |
-            (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(h1))) << 16);
-  }
-  return make_uint4(hw[0], hw[1], hw[2], hw[3]);
-}
-
-// One element of the same: fp16_RN(silu(g) u) from fp16 bits, with the same
-// operations as each lane of swiglu8, so either gives the same bits.
 __device__ __forceinline__ uint16_t swiglu1(uint16_t g, uint16_t u) {
   const float g0 = __half2float(__ushort_as_half(g));
   const float h0 = __fdividef(g0, 1.f + __expf(-g0)) * __half2float(__ushort_as_half(u));
@@ -468,7 +457,7 @@ __device__ __forceinline__ void load_row(uint32_t addr, int rot, uint32_t (&w)[8
   w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
 }
 
-// kAct: some task of the list takes SwiGLU activations (x2 set).  The
+// kAct: some task of the list has a SwiGLU epilogue (epi_g set).  The
 // instantiation without it carries no trace of that path, so the plain task
 // lists compile exactly as they would without the feature.  kFmt: the
 // weight format (kFmtW4A16, kFmtW4A8, kFmtQ4K).
@@ -528,7 +517,7 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
   int first_task = 0;
   while (first_task < p.ntasks && !cta_has_rows(p.task[first_task])) ++first_task;
   auto staged = [&](const M1Task& tk, int i) {
-    return kFmt == kFmtW4A16 && may_stage(tk, tk.K / unit_k(kFmt), i == first_task, MAXT > 2);
+    return kFmt == kFmtW4A16 && may_stage(tk.x, tk.K / unit_k(kFmt), i == first_task, MAXT > 2);
   };
 
   if (warp == 0 && lane == 0) {
@@ -798,11 +787,11 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
               uint16_t* y = seg == 0 ? y0 : (seg == 1 ? y1 : y2);
               const uint16_t yb = __half_as_ushort(__float2half_rn(sum));
               y[j] = yb;
-              if (kAct && tk.epi) {
+              if (kAct && tk.epi_g != nullptr) {
                 // SwiGLU epilogue: the gate output of row j was written by
                 // this warp in an earlier task (the __syncwarp of each tile
                 // orders it before this read, through L2)
-                const uint16_t g = __ldcg(reinterpret_cast<const unsigned short*>(tk.seg[2].y) + j);
+                const uint16_t g = __ldcg(reinterpret_cast<const unsigned short*>(tk.epi_g) + j);
                 tk.seg[1].y[j] = swiglu1(g, yb);
               }
             }
@@ -877,27 +866,23 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     // rows here has one, in order)
     const int sig = tk.dep >= 0 && p.done != nullptr ? nwait++ : -1;
     if constexpr (kFmt == kFmtW4A16) if (!staged(tk, i)) {
-      // this thread's own 128 activations (or their SwiGLU), loaded from
-      // global memory: X[4 j + i] pairs with word 4 ((j + f) mod 4) + i of
-      // the unit, the order in which the tiles' words are read.  Plain loads
-      // through L1: x of a dependent task is read after the reducer's
-      // acquire.
+      // this thread's own 128 activations, loaded from global memory:
+      // X[4 j + i] pairs with word 4 ((j + f) mod 4) + i of the unit, the
+      // order in which the tiles' words are read.  Plain loads through L1:
+      // x of a dependent task is read after the reducer's acquire.
       if (sig >= 0 && !mbar_wait_bounded(xready0 + 8 * (sig % kXReady), (sig / kXReady) & 1, kWaitLimitNs)) {
         if (lane == 0) atomicOr(p.status, W4A16_DEV_PIPE_TIMEOUT);
         return;
       }
       if (wact) {
         const uint16_t* xp = tk.x + u * 128;
-        const uint16_t* x2p = kAct && tk.x2 != nullptr ? tk.x2 + u * 128 : nullptr;
         float es[4], os[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int ch = (j + f) & 3;
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4) {
-            uint4 v = ld_u4(xp + 32 * ch + 8 * i4);
-            if (kAct && x2p != nullptr) v = swiglu8(v, ld_u4(x2p + 32 * ch + 8 * i4));
-            X[4 * j + i4] = pair_activations(v);
+            X[4 * j + i4] = pair_activations(ld_u4(xp + 32 * ch + 8 * i4));
           }
           chunk_bias(&X[4 * j], es[j], os[j]);
         }
@@ -951,7 +936,6 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       for (int j = 0; j < 8; ++j) {
         const int jj = rot ? (j ^ 4) : j;
         v[j] = ld_u4(xp + 8 * jj);
-        if (kAct && tk.x2 != nullptr) v[j] = swiglu8(v[j], ld_u4(tk.x2 + u * 64 + 8 * jj));
       }
       // max |x| with packed fp16 operations (exact), as a tree
       __half2 m2[8];
@@ -1027,13 +1011,10 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
     while (inext < p.ntasks && !cta_has_rows(p.task[inext])) ++inext;
     const uint16_t* xnext = nullptr;
     bool pending = false;
-    const uint16_t* x2next = nullptr;
     if (kFmt != kFmtW4A16 && inext < p.ntasks && c < (p.task[inext].K >> 6)) {
       xnext = p.task[inext].x + c * 64;
-      if (kAct && p.task[inext].x2 != nullptr) x2next = p.task[inext].x2 + c * 64;
       if (p.task[inext].dep < 0 || p.done == nullptr) {
         prefetch_l1(xnext);
-        if (kAct && x2next != nullptr) prefetch_l1(x2next);
       } else {
         pending = true;
       }
@@ -1049,7 +1030,6 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
       const int nr = rows - t * tp.RB;  // rows of this tile (may exceed RB)
       if (pending && mbar_try_wait(xready0 + 8 * (nwait % kXReady), (nwait / kXReady) & 1)) {
         prefetch_l1(xnext);
-        if (kAct && x2next != nullptr) prefetch_l1(x2next);
         pending = false;
       }
       float res[kR];
@@ -1338,7 +1318,7 @@ int gemv_m1_split_tasks(const M1Task& t, bool a8, const DeviceInfo& d, M1Task* o
   out[1].qweight = t.qweight + h / 8;
   out[1].scales = t.scales + h / 128;
   out[1].x = t.x + h;
-  out[1].x2 = t.x2 != nullptr ? t.x2 + h : nullptr;
+  out[0].epi_g = nullptr;  // the first half writes nothing
   return 2;
 }
 
@@ -1350,7 +1330,7 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   t.x = a.x;
   t.N = a.N;
   t.K = a.K;
-  t.x2 = nullptr;
+  t.epi_g = nullptr;
   t.nseg = static_cast<uint8_t>(a.nseg);
   t.dep = -1;
   t.publish = 0;
@@ -1388,7 +1368,7 @@ cudaError_t launch_gemv_m1_q4k(const uint8_t* blocks, const uint16_t* x, uint16_
   tk.x = x;
   tk.N = N;
   tk.K = K;
-  tk.x2 = nullptr;
+  tk.epi_g = nullptr;
   tk.nseg = 1;
   tk.dep = -1;
   tk.publish = 0;
@@ -1425,7 +1405,7 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
   bool act = false;
   for (int i = 0; i < ntasks; ++i) {
     if (tasks[i].dep >= 0) p.task[tasks[i].dep].publish = 1;
-    act = act || tasks[i].x2 != nullptr || tasks[i].epi != 0;
+    act = act || tasks[i].epi_g != nullptr;
   }
   p.ntasks = ntasks;
   p.done = done;

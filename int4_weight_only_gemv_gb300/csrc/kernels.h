@@ -86,10 +86,11 @@ struct M1Task {
   const uint32_t* qweight;  // [N][K/8]
   const uint16_t* scales;   // [N][K/128] fp16 bits
   const uint16_t* x;        // [K] fp16 bits
-  // With x2, the activations are h[k] = fp16_RN(silu(x[k]) x2[k]) computed
-  // in FP32 from the fp16 inputs (SwiGLU: x the gate, x2 the up output);
-  // null: x itself.
-  const uint16_t* x2;
+  // SwiGLU epilogue (one output segment; a whole GEMV or the second half of
+  // a K split): after y[n] is rounded, h[n] = fp16_RN(silu(g[n]) y[n]) is
+  // written to seg[1].y[n], g = epi_g the gate output of the same rows,
+  // written by this CTA in an earlier task of the list.  Null: none.
+  const uint16_t* epi_g;
   int N, K;
   int dep;                  // index of the task whose output x is, or -1
   int rq, rr;               // rows per CTA (set by the launcher): rq, one more for CTAs < rr
@@ -98,14 +99,9 @@ struct M1Task {
   // K-split of one GEMV into two consecutive tasks over the halves of each
   // row's K (rows of pitch 2 K): 1 = the first half (its row sums wait in
   // shared memory, nothing is written), 2 = the second half (adds them, then
-  // the bias and the rounding; qweight, scales, x and x2 point at the half).
+  // the bias and the rounding; qweight, scales and x point at the half).
   // 0 = a whole GEMV.
   uint8_t split;
-  // 1: a SwiGLU epilogue (one output segment, a whole or second-half GEMV):
-  // after y[n] is rounded, h[n] = fp16_RN(silu(g[n]) y[n]) is written too,
-  // g = seg[2].y (the gate output of the same rows, written by this CTA in an
-  // earlier task of the list) and h = seg[1].y; 0: none
-  uint8_t epi;
   M1Seg seg[kMaxSegs];
 };
 static_assert(sizeof(M1Task) == 128, "a task record is 128 bytes (the table is kernel parameters)");
