@@ -621,12 +621,13 @@ void build_seq_gemvs(const w4a16_layer_weights* layers, const SeqOptions& opt, i
       GemvArgs u = plain_args(w.qweight[W4A16_UP], w.scales[W4A16_UP], xl, ygu + ffn, M, ffn, hidden, hidden,
                               ldgu);
       u.seg[0].bias = b(W4A16_UP);
-      u.epi_g = ygu;
+      u.swiglu = 2;
       u.epi_h = hl;
       ilast = add(u, -1);
       GemvArgs g = plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, ffn, hidden, hidden,
                               ldgu);
       g.seg[0].bias = b(W4A16_GATE);
+      g.swiglu = 1;
       add(g, -1);
     } else if (stacked(w, W4A16_GATE, W4A16_UP, ffn)) {
       GemvArgs a = plain_args(w.qweight[W4A16_GATE], w.scales[W4A16_GATE], xl, ygu, M, 2 * ffn, hidden,
@@ -699,7 +700,7 @@ void seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs, const s
       tk.qweight = a.qweight;
       tk.scales = a.scales;
       tk.x = a.x;
-      tk.epi_g = a.epi_g;
+      tk.swiglu = static_cast<uint8_t>(a.swiglu);
       tk.N = a.N;
       tk.K = a.K;
       tk.nseg = static_cast<uint8_t>(a.nseg);
@@ -708,7 +709,7 @@ void seq_tasks(const DeviceState& d, const std::vector<GemvArgs>& gemvs, const s
       tk.dep = dep[i] < 0 ? -1 : slot[dep[i]];
       if (dep2[i] >= 0 && slot[dep2[i]] > tk.dep) tk.dep = slot[dep2[i]];
       for (int g = 0; g < kMaxSegs; ++g) tk.seg[g] = M1Seg{a.seg[g].y, a.seg[g].bias, a.seg[g].n_end};
-      if (a.epi_g != nullptr) tk.seg[1].y = a.epi_h;  // h of the SwiGLU epilogue
+      tk.epi_h = a.epi_h;  // h of the SwiGLU epilogue (up tasks)
       M1Task parts[2];
       const int np = gemv_m1_split_tasks(tk, a8, d.info, parts);
       for (int q = 0; q < np; ++q) tasks->push_back(parts[q]);
@@ -844,9 +845,11 @@ w4a16_status w4a16_layer_seq_create2(const w4a16_layer_weights* layers, const w4
   // M = 1 with every K in the M = 1 kernel's range: task lists, SwiGLU in
   // up's epilogue; otherwise one launch per GEMV and, with SwiGLU, a separate
   // activation step.  Either way h goes to a buffer this object owns.
-  const bool tasks = M == 1 && gemv_m1_supported(hidden) && gemv_m1_supported(ffn);
   const bool swiglu = (flags & W4A16_SEQ_SWIGLU) != 0;
+  const bool tasks = M == 1 && gemv_m1_supported(hidden) && gemv_m1_supported(ffn) &&
+                     (!swiglu || gemv_m1_swiglu_fits(ffn, d->info));
   const bool a8 = (flags & W4A16_SEQ_ACT_INT8) != 0;
+  if (a8 && !tasks) return W4A16_ERR_SHAPE;  // W4A8 runs only in the task lists
   SeqOptions opt;
   opt.biases = biases;
   opt.flags = flags;

@@ -201,11 +201,17 @@ constexpr int kPartBytes = 4 * kM1PartRows;
 // (0.8x and 1.25x this rate: 11.7 / 15.7 and 11.5 / 15.7 us).
 constexpr float kPaceBytesPerUs = 6800.f * 1000.f;
 
+// Bytes of the kept gate outputs (one fp16 per row of a CTA) of a list with
+// SwiGLU, after the stages.
+constexpr int kGateBytes = 2 * kM1PartRows;
+
 // Shared layout: barriers | K-split partial sums | xslots | S partial slots |
-// S stages (128-aligned).
+// S stages (128-aligned) | kept gate outputs (lists with SwiGLU).
 RingPlan make_ring_plan(const M1Task* tasks, int n, int smem_limit, int fmt, bool list) {
   RingPlan r{};
+  int gate = 0;
   for (int i = 0; i < n; ++i) {
+    if (tasks[i].swiglu != 0) gate = kGateBytes;
     const TaskPlan tp = task_plan(tasks[i].K, fmt, task_parts(tasks[i]));
     const int st = tp.RB * tp.row_bytes + sc_window_cap(tp);
     const int rb = tp.RB * tp.red_stride * 4;
@@ -220,7 +226,7 @@ RingPlan make_ring_plan(const M1Task* tasks, int n, int smem_limit, int fmt, boo
   r.stage_bytes = (r.stage_bytes + 127) & ~127;
   r.red_bytes = (r.red_bytes + 15) & ~15;
   const int per_stage = r.stage_bytes + r.red_bytes;
-  const int fixed = kBarrierBytes + kPartBytes + kXSlots * r.xslot + 128;  // 128: stage alignment slack
+  const int fixed = kBarrierBytes + kPartBytes + kXSlots * r.xslot + 128 + gate;  // 128: stage alignment slack
   const int budget = (smem_limit < kM1SmemBudget ? smem_limit : kM1SmemBudget) - fixed;
   r.S = budget / per_stage;
   if (r.S > kM1MaxStages) r.S = kM1MaxStages;
@@ -457,7 +463,7 @@ __device__ __forceinline__ void load_row(uint32_t addr, int rot, uint32_t (&w)[8
   w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
 }
 
-// kAct: some task of the list has a SwiGLU epilogue (epi_g set).  The
+// kAct: some task of the list takes part in a SwiGLU (swiglu set).  The
 // instantiation without it carries no trace of that path, so the plain task
 // lists compile exactly as they would without the feature.  kFmt: the
 // weight format (kFmtW4A16, kFmtW4A8, kFmtQ4K).
@@ -787,12 +793,18 @@ __global__ void __launch_bounds__(kM1MaxThreads, 1)
               uint16_t* y = seg == 0 ? y0 : (seg == 1 ? y1 : y2);
               const uint16_t yb = __half_as_ushort(__float2half_rn(sum));
               y[j] = yb;
-              if (kAct && tk.epi_g != nullptr) {
-                // SwiGLU epilogue: the gate output of row j was written by
-                // this warp in an earlier task (the __syncwarp of each tile
-                // orders it before this read, through L2)
-                const uint16_t g = __ldcg(reinterpret_cast<const unsigned short*>(tk.epi_g) + j);
-                tk.seg[1].y[j] = swiglu1(g, yb);
+              if (kAct && tk.swiglu != 0) {
+                // SwiGLU: the gate task keeps its rounded outputs after the
+                // stages, one per row of this CTA; the up task's epilogue
+                // reads the same row's (this warp wrote it in an earlier
+                // task: the __syncwarp of each tile orders the two)
+                const uint32_t ga = stage0 + static_cast<uint32_t>(S * p.stage_bytes + 2 * (lr0 + row));
+                if (W4A16_IN(p.status, lr0 + row < kM1PartRows)) {
+                  if (tk.swiglu == 1)
+                    sts_u16(ga, yb);
+                  else
+                    tk.epi_h[j] = swiglu1(lds_u16(ga), yb);
+                }
               }
             }
           }
@@ -1318,7 +1330,7 @@ int gemv_m1_split_tasks(const M1Task& t, bool a8, const DeviceInfo& d, M1Task* o
   out[1].qweight = t.qweight + h / 8;
   out[1].scales = t.scales + h / 128;
   out[1].x = t.x + h;
-  out[0].epi_g = nullptr;  // the first half writes nothing
+  out[0].swiglu = 0;  // the first half writes nothing
   return 2;
 }
 
@@ -1330,7 +1342,7 @@ cudaError_t launch_gemv_m1(const GemvArgs& a, const DeviceInfo& d, cudaStream_t 
   t.x = a.x;
   t.N = a.N;
   t.K = a.K;
-  t.epi_g = nullptr;
+  t.swiglu = 0;
   t.nseg = static_cast<uint8_t>(a.nseg);
   t.dep = -1;
   t.publish = 0;
@@ -1368,7 +1380,7 @@ cudaError_t launch_gemv_m1_q4k(const uint8_t* blocks, const uint16_t* x, uint16_
   tk.x = x;
   tk.N = N;
   tk.K = K;
-  tk.epi_g = nullptr;
+  tk.swiglu = 0;
   tk.nseg = 1;
   tk.dep = -1;
   tk.publish = 0;
@@ -1393,6 +1405,9 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
     if (t.dep >= i || (t.dep >= 0 && done == nullptr)) return cudaErrorInvalidValue;
     // a K split is two consecutive halves of one GEMV, small enough per CTA
     if (t.split > 2 || (t.split != 0 && (a8 || (t.N + d.sms - 1) / d.sms > kM1PartRows))) return cudaErrorInvalidValue;
+    // a SwiGLU pair keeps one gate output per row of a CTA
+    if (t.swiglu > 2 || (t.swiglu != 0 && (t.nseg != 1 || (t.N + d.sms - 1) / d.sms > kM1PartRows)))
+      return cudaErrorInvalidValue;
     if (t.split == 1 && (i + 1 >= ntasks || tasks[i + 1].split != 2 || tasks[i + 1].N != t.N ||
                          tasks[i + 1].K != t.K))
       return cudaErrorInvalidValue;
@@ -1405,7 +1420,7 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
   bool act = false;
   for (int i = 0; i < ntasks; ++i) {
     if (tasks[i].dep >= 0) p.task[tasks[i].dep].publish = 1;
-    act = act || tasks[i].epi_g != nullptr;
+    act = act || tasks[i].swiglu != 0;
   }
   p.ntasks = ntasks;
   p.done = done;
@@ -1416,6 +1431,8 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
   // one CTA per SM: every CTA must be resident for the dependency counts
   return launch_tasks(p, rp, d.sms, pdl, act, fmt, st);
 }
+
+bool gemv_m1_swiglu_fits(int ffn, const DeviceInfo& d) { return (ffn + d.sms - 1) / d.sms <= kM1PartRows; }
 
 bool gemv_m1_tasks_fit(const M1Task* tasks, int n, bool a8, const DeviceInfo& d) {
   if (tasks == nullptr || n <= 0) return false;

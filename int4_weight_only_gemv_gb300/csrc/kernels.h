@@ -43,10 +43,9 @@ struct GemvArgs {
   // W4A8: int8 activations quantised per 64-element unit inside the M = 1
   // kernel (gemv_m1.cu); only that kernel supports it.
   bool a8;
-  // M = 1 layer sequences only: a SwiGLU epilogue h[n] = fp16_RN(silu(g[n])
-  // y[n]) on this GEMV's output (null: none), g the gate output of the same
-  // rows, produced earlier in the same task list.
-  const uint16_t* epi_g;
+  // M = 1 layer sequences only: the task's SwiGLU role (M1Task::swiglu) and,
+  // for the up projection (2), where h goes.
+  int swiglu;
   uint16_t* epi_h;
 };
 
@@ -86,11 +85,7 @@ struct M1Task {
   const uint32_t* qweight;  // [N][K/8]
   const uint16_t* scales;   // [N][K/128] fp16 bits
   const uint16_t* x;        // [K] fp16 bits
-  // SwiGLU epilogue (one output segment; a whole GEMV or the second half of
-  // a K split): after y[n] is rounded, h[n] = fp16_RN(silu(g[n]) y[n]) is
-  // written to seg[1].y[n], g = epi_g the gate output of the same rows,
-  // written by this CTA in an earlier task of the list.  Null: none.
-  const uint16_t* epi_g;
+  uint16_t* epi_h;          // SwiGLU up task (swiglu = 2): where h goes; else null
   int N, K;
   int dep;                  // index of the task whose output x is, or -1
   int rq, rr;               // rows per CTA (set by the launcher): rq, one more for CTAs < rr
@@ -102,6 +97,12 @@ struct M1Task {
   // the bias and the rounding; qweight, scales and x point at the half).
   // 0 = a whole GEMV.
   uint8_t split;
+  // SwiGLU across two tasks over the same rows (one output segment each):
+  // 1 = the gate, whose rounded outputs the CTA also keeps in shared memory;
+  // 2 = the up projection, whose epilogue writes h[n] = fp16_RN(silu(g) y[n])
+  // to epi_h[n] after y[n] is rounded, g the value the last gate task kept
+  // for the same row; 0 = neither (set by the sequence builder).
+  uint8_t swiglu;
   M1Seg seg[kMaxSegs];
 };
 static_assert(sizeof(M1Task) == 128, "a task record is 128 bytes (the table is kernel parameters)");
@@ -153,6 +154,9 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
 // tables of up to kM1MaxTasks) pass launch_gemv_m1_tasks's own checks of K
 // and the shared-memory plan on this device.
 bool gemv_m1_tasks_fit(const M1Task* tasks, int n, bool a8, const DeviceInfo& d);
+// Whether a SwiGLU over ffn-row gate and up tasks fits the task lists (the
+// CTA keeps one gate output per row of its share).
+bool gemv_m1_swiglu_fits(int ffn, const DeviceInfo& d);
 // Host-only: the tasks of one M = 1 GEMV (its K, N, pointers in t, split 0):
 // one task, or (W4A16 only, when split_parts says so) its two K halves.
 // Writes 1 or 2 tasks to out and returns the count; dep and publish are
