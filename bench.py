@@ -616,7 +616,7 @@ def epilogue_step(layers, dev, reps, bias_on, act_int8=False):
     seq.close()
     b = config_block()["bytes_per_step"] + 2 * sum(width[n] for n in bias_on) * len(layers)
     note = ("W4A8: every GEMV with int8 activations quantised in-kernel" if act_int8 else
-            "biases on " + "/".join(bias_on) + ", SwiGLU fused into down")
+            "biases on " + "/".join(bias_on) + ", SwiGLU in the up projection's epilogue")
     return {"M": 1, "layers": len(layers), "ms_per_step": round(ms, 4), "GBps": round(b / ms / 1e6, 1),
             "bytes": b, "note": note}
 
