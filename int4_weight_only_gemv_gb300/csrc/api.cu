@@ -422,7 +422,7 @@ struct w4a16_layer_seq {
   cudaGraphExec_t exec = nullptr;
   cudaEvent_t done = nullptr;
   int* task_done = nullptr;  // per-GEMV completion counters of the task lists (M = 1)
-  uint16_t* hbuf = nullptr;  // SwiGLU activations of the unfused path
+  uint16_t* hbuf = nullptr;  // SwiGLU activations h (sequences with SwiGLU)
 };
 
 namespace {
@@ -520,11 +520,11 @@ w4a16_status check_seq_biases(const w4a16_layer_bias* biases, int n_layers, int 
 struct SeqOptions {
   const w4a16_layer_bias* biases = nullptr;  // n_layers entries or null
   unsigned flags = 0;                        // W4A16_SEQ_*
-  uint16_t* hbuf = nullptr;  // SwiGLU activations [n_layers][M][ffn] (unfused path), or null
+  uint16_t* hbuf = nullptr;  // SwiGLU activations h [n_layers][M][ffn], or null
 };
 
-// The SwiGLU step before a down GEMV when it is not fused into the M = 1
-// task: h[m][j] = fp16_RN(silu(g[m][j]) u[m][j]) for j < n (rows of g, u have
+// The SwiGLU step before a down GEMV outside the M = 1 task lists (there
+// up's epilogue writes h): h[m][j] = fp16_RN(silu(g[m][j]) u[m][j]) for j < n (rows of g, u have
 // stride ld, rows of h stride n).
 struct ActOp {
   const uint16_t* g = nullptr;
