@@ -524,8 +524,8 @@ struct SeqOptions {
 };
 
 // The SwiGLU step before a down GEMV outside the M = 1 task lists (there
-// up's epilogue writes h): h[m][j] = fp16_RN(silu(g[m][j]) u[m][j]) for j < n (rows of g, u have
-// stride ld, rows of h stride n).
+// up's epilogue writes h): h[m][j] = fp16_RN(silu(g[m][j]) u[m][j]) for
+// j < n (rows of g, u have stride ld, rows of h stride n).
 struct ActOp {
   const uint16_t* g = nullptr;
   const uint16_t* u = nullptr;
