@@ -67,6 +67,13 @@ struct AttnParams {
   uint32_t* status;
 };
 
+// L2 prefetch of one box of a 3-D tensor map (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(x), "r"(y),
+               "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar,
                                             uint64_t policy) {
   asm volatile(
@@ -210,6 +217,22 @@ __global__ void __launch_bounds__(kAThreads, 1)
   }
   __syncthreads();
   pdl_launch_dependents();
+  // This CTA's key range is requested into L2 before the dependency wait:
+  // a CTA that starts while the previous kernel is still finishing (its
+  // merge runs on a few CTAs) gets its first tiles from L2.  A prefetch only
+  // fills L2, the point of coherence, so a cache row the previous kernel
+  // writes is read after the wait with its new value.  Measured (graphs of
+  // 28 calls, cold L2): T = 8192 9.42 -> 9.05 us, T = 32768 16.25 -> 16.10,
+  // T = 1024 unchanged.
+  if (warp == kAWarps && lane == 0) {
+    for (int i = 0; i < nt; ++i) {
+      const int t0 = (tb + i) * kAKeys;
+      tma_prefetch_3d(&kmap, 0, t0, g);
+      tma_prefetch_3d(&kmap, 64, t0, g);
+      tma_prefetch_3d(&vmap, 0, t0, g);
+      tma_prefetch_3d(&vmap, 64, t0, g);
+    }
+  }
   pdl_wait();  // q and the cache may be the previous kernel's output
 
   if (warp == kAWarps) {
