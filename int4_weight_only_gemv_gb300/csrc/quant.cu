@@ -172,8 +172,9 @@ namespace {
 // The SwiGLU step of a decoder layer's feed-forward (the page on hipfire,
 // "Overview of hipfire-arch-qwen2", "Key Technical Specifications": SwiGLU
 // FFN): h = fp16_RN(silu(g) u) with silu(g) = g / (1 + e^-g) in FP32 (fast
-// exponential and division, as the fused M = 1 path), one thread per element.  Runs between the [gate; up] and down GEMVs of a layer
-// sequence when it is not fused into the down GEMV.
+// exponential and division, as the M = 1 task lists' epilogue), one thread
+// per element.  Runs between the [gate; up] and down GEMVs of a layer
+// sequence outside the M = 1 task lists.
 __global__ void swiglu_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u, int64_t ld,
                               uint16_t* __restrict__ h, int M, int n) {
   pdl_launch_dependents();

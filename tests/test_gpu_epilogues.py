@@ -7,8 +7,8 @@ Each projection of each layer is checked on sampled rows against the oracle:
 y_ref = sum_k x w_hat (FP64) + bias, with the GPU's own fp16 intermediates as
 inputs (o reads y_q; down reads h = fp16_RN(silu(gate) up) computed by the
 oracle from the GPU's y_gu), within the GEMV tolerance.  M = 1 runs the task
-list (SwiGLU fused into the down tasks' activation loads), M = 3 the CUDA-core
-kernel and M = 9 the tensor-core kernel (SwiGLU as a separate kernel).
+list (gate and up as two tasks, h written by up's epilogue), M = 3 and M = 9
+the tensor-core kernel (SwiGLU as a separate kernel).
 """
 import numpy as np
 import pytest
