@@ -1406,7 +1406,8 @@ cudaError_t launch_gemv_m1_tasks(const M1Task* tasks, int ntasks, int* done, uin
     // a K split is two consecutive halves of one GEMV, small enough per CTA
     if (t.split > 2 || (t.split != 0 && (a8 || (t.N + d.sms - 1) / d.sms > kM1PartRows))) return cudaErrorInvalidValue;
     // a SwiGLU pair keeps one gate output per row of a CTA
-    if (t.swiglu > 2 || (t.swiglu != 0 && (t.nseg != 1 || (t.N + d.sms - 1) / d.sms > kM1PartRows)))
+    if (t.swiglu > 2 || (t.swiglu != 0 && (t.nseg != 1 || (t.N + d.sms - 1) / d.sms > kM1PartRows)) ||
+        (t.swiglu == 2 && t.epi_h == nullptr))
       return cudaErrorInvalidValue;
     if (t.split == 1 && (i + 1 >= ntasks || tasks[i + 1].split != 2 || tasks[i + 1].N != t.N ||
                          tasks[i + 1].K != t.K))
