@@ -357,8 +357,9 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
       uint32_t st = stage0;
       int b = 0;         // partial buffer of block i
       uint32_t rph = 0;  // parity of its round
+      bool full_seen = false;  // block i's stage seen full at the end of block i - 1
       for (int i = 0; i < nblk; ++i) {
-        if (!warp_wait(full0 + 8 * s, ph)) {
+        if (!full_seen && !warp_wait(full0 + 8 * s, ph)) {
           if (lane == 0) atomicOr(a.status, W4A16_DEV_PIPE_TIMEOUT);
           break;
         }
@@ -459,6 +460,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
           b = 0;
           rph ^= 1u;
         }
+        full_seen = __all_sync(0xffffffffu, i + 1 < nblk && mbar_try_wait(full0 + 8 * s, ph));
       }
     };
     if (w < nwf)
