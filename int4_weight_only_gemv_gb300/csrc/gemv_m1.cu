@@ -406,7 +406,10 @@ __device__ __forceinline__ void dot_pair_a8(const uint32_t (&wa)[8], const uint3
 // high nibbles) with this thread's activations, paired as X[t] = {x(4t),
 // x(4t+2)}, {x(4t+1), x(4t+3)}, {x(32+4t), x(32+4t+2)}, {x(32+4t+1),
 // x(32+4t+3)}.  A low nibble becomes fp16 1024 + q and a high nibble, left
-// in place, 1024 + 16 q (bits 4-7 are still mantissa), one LOP3 each.
+// in place, 1024 + 16 q (bits 4-7 are still mantissa), one LOP3 each,
+// written as the explicit lop3 (the mask and the constant share no bit, so
+// the OR is the XOR).  Written as a C++ mask-and-OR, the [gate; up] GEMV
+// counted 9.2 LOP3 per packed word in ncu and took 19.6 us; as lop3, 17.8 us.
 // Returns D0 = sum (1024 + q) x over sub-block 2c and D1 = sum (1024 + 16 q) x
 // over sub-block 2c + 1.
 __device__ __forceinline__ void q4k_dot(const uint32_t (&q)[8], const XPairs (&X)[8], float& D0, float& D1) {
@@ -414,10 +417,10 @@ __device__ __forceinline__ void q4k_dot(const uint32_t (&q)[8], const XPairs (&X
 #pragma unroll
   for (int t = 0; t < 8; ++t) {
     const uint32_t v = q[t], v8 = v >> 8;
-    fma_f32_f16x2(a0, a1, (v & 0x000F000Fu) | 0x64006400u, X[t].p0);
-    fma_f32_f16x2(a0, a1, (v8 & 0x000F000Fu) | 0x64006400u, X[t].p1);
-    fma_f32_f16x2(b0, b1, (v & 0x00F000F0u) | 0x64006400u, X[t].p2);
-    fma_f32_f16x2(b0, b1, (v8 & 0x00F000F0u) | 0x64006400u, X[t].p3);
+    fma_f32_f16x2(a0, a1, lop3_and_xor(v, 0x000F000Fu, 0x64006400u), X[t].p0);
+    fma_f32_f16x2(a0, a1, lop3_and_xor(v8, 0x000F000Fu, 0x64006400u), X[t].p1);
+    fma_f32_f16x2(b0, b1, lop3_and_xor(v, 0x00F000F0u, 0x64006400u), X[t].p2);
+    fma_f32_f16x2(b0, b1, lop3_and_xor(v8, 0x00F000F0u, 0x64006400u), X[t].p3);
   }
   D0 = a0 + a1;
   D1 = b0 + b1;

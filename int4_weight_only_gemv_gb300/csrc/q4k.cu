@@ -90,10 +90,11 @@ __device__ __forceinline__ float q4k_unit(const uint4 h, const uint32_t (&q)[8],
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(xh0), "=r"(xh1) : "r"(xs + 64 + 8 * t));
     const uint32_t v = q[t];
     // {1024 + q(k), 1024 + q(k + 2)} pairs against {x(k), x(k + 2)}
-    const uint32_t l02 = (v & 0x000F000Fu) | 0x64006400u;
-    const uint32_t l13 = ((v >> 8) & 0x000F000Fu) | 0x64006400u;
-    const uint32_t h02 = ((v >> 4) & 0x000F000Fu) | 0x64006400u;
-    const uint32_t h13 = ((v >> 12) & 0x000F000Fu) | 0x64006400u;
+    // (the mask and the OR as one explicit LOP3: the two never share a bit)
+    const uint32_t l02 = lop3_and_xor(v, 0x000F000Fu, 0x64006400u);
+    const uint32_t l13 = lop3_and_xor(v >> 8, 0x000F000Fu, 0x64006400u);
+    const uint32_t h02 = lop3_and_xor(v >> 4, 0x000F000Fu, 0x64006400u);
+    const uint32_t h13 = lop3_and_xor(v >> 12, 0x000F000Fu, 0x64006400u);
     fma_f32_f16x2(dlo0, dlo1, l02, pair_halves(xl0, xl1, 0x5410u));
     fma_f32_f16x2(dlo0, dlo1, l13, pair_halves(xl0, xl1, 0x7632u));
     fma_f32_f16x2(dhi0, dhi1, h02, pair_halves(xh0, xh1, 0x5410u));
